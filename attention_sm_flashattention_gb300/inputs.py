@@ -1,0 +1,70 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests, the oracle's tests
+and the benchmark.
+
+This module holds no attention arithmetic: it only names the workloads and
+draws their tensors.  Recipe: a CPU ``torch.Generator`` seeded with the
+workload's seed draws ``q``, ``k``, ``v``, ``do`` in that order, each as
+standard-normal float32 of shape ``[Z, H, N, D]``, then rounds them to fp16
+(round-to-nearest-even).  ``scale = 1/sqrt(D)`` passed as a float32.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    Z: int
+    H: int
+    N: int
+    D: int
+    causal: bool
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def heads(self) -> int:
+        return self.Z * self.H
+
+    def describe(self) -> str:
+        kind = "causal" if self.causal else "non-causal"
+        return f"Z{self.Z} H{self.H} N{self.N} D{self.D} {kind}"
+
+
+# The five benchmark shapes (the D256 one in both masks).  Seeds: 1000 + the
+# shape's index, +10 for the causal variant of the D256 shape.
+WORKLOADS = {
+    "z1h2n128d64": Workload("z1h2n128d64", 1, 2, 128, 64, False, 1000),
+    "z4h8n1024d64": Workload("z4h8n1024d64", 4, 8, 1024, 64, False, 1001),
+    "z128h8n1024d128": Workload("z128h8n1024d128", 128, 8, 1024, 128, False, 1002),
+    "z128h8n1024d128c": Workload("z128h8n1024d128c", 128, 8, 1024, 128, True, 1003),
+    "z128h8n1024d256": Workload("z128h8n1024d256", 128, 8, 1024, 256, False, 1004),
+    "z128h8n1024d256c": Workload("z128h8n1024d256c", 128, 8, 1024, 256, True, 1014),
+}
+
+
+def make_inputs(Z: int, H: int, N: int, D: int, seed: int, device="cpu"):
+    """Draw fp16 ``(q, k, v, do)`` of shape ``[Z, H, N, D]`` from ``seed``.
+
+    The draw always happens on the CPU generator so that every device sees
+    bit-identical tensors; ``device`` only says where the result is moved.
+    """
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    shape = (Z, H, N, D)
+    out = []
+    for _ in range(4):
+        t = torch.randn(shape, generator=g, dtype=torch.float32).to(torch.float16)
+        out.append(t if device == "cpu" else t.to(device))
+    return tuple(out)
+
+
+def workload_inputs(w: Workload, device="cpu"):
+    return make_inputs(w.Z, w.H, w.N, w.D, w.seed, device=device)

@@ -1,0 +1,18 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libfa.so")
+
+
+def pytest_collection_modifyitems(config, items):
+    # GPU tests fail loudly if they run without a GPU; they are only deselected
+    # by -m "not gpu", never silently skipped.
+    pass
