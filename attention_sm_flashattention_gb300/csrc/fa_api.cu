@@ -1,0 +1,230 @@
+// C ABI of libfa.so (declared in include/fa.h): argument checks, tensor-map
+// encoding, grid sizing and dispatch to the (D, causal) kernel instantiations.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+
+#include "../../include/fa.h"
+#include "fa_kernels.h"
+#include "tma_host.h"
+
+// The library's only device state: one status word per device (0 = ok).
+__device__ int g_fa_status = 0;
+
+namespace {
+
+struct DevInfo {
+  bool init = false;
+  int sms = 0;
+  int* status = nullptr;  // device address of g_fa_status on this device
+};
+
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+
+int current_device_info(DevInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
+  DevInfo& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    if (major != 10 || minor != 3) return FA_ERR_DEVICE;
+    if (const char* env = std::getenv("FA_NUM_SMS")) {
+      const int v = std::atoi(env);
+      if (v > 0 && v < sms) sms = v;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
+    d.sms = sms;
+    d.status = static_cast<int*>(p);
+    d.init = true;
+  }
+  *out = &d;
+  return FA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Shared checks of the shape arguments.
+int check_shape(int Z, int H, int N, int D, int causal, float scale) {
+  if (Z <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  if (N % 128 != 0) return FA_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(Z) * H * N;
+  if (rows >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+bool fp16_map(CUtensorMap* m, const void* base, long long rows, int D, int box_rows) {
+  std::memset(m, 0, sizeof(*m));
+  return fa::make_tmap_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, static_cast<uint64_t>(rows),
+                          static_cast<uint64_t>(D), static_cast<uint64_t>(D), 64, static_cast<uint32_t>(box_rows),
+                          true);
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace layout of fa_bwd: [delta | lse2 | dq_acc], each 256-byte aligned.
+struct BwdWorkspace {
+  size_t delta_off, lse2_off, dq_off, total;
+  int grid;
+};
+
+BwdWorkspace bwd_workspace_layout(int Z, int H, int N, int D, int sms) {
+  BwdWorkspace w{};
+  const long long heads = static_cast<long long>(Z) * H;
+  const size_t vec = round_up(static_cast<size_t>(heads) * N * sizeof(float), 256);
+  w.grid = static_cast<int>(heads < sms ? heads : sms);
+  w.delta_off = 0;
+  w.lse2_off = vec;
+  w.dq_off = 2 * vec;
+  w.total = 2 * vec + round_up(static_cast<size_t>(w.grid) * N * D * sizeof(float), 256);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_error_string(int code) {
+  switch (code) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument (null/misaligned pointer, non-positive size, bad scale or causal flag)";
+    case FA_ERR_UNSUPPORTED: return "unsupported shape (D must be 64, 128 or 256; N a multiple of 128; Z*H*N < 2^31)";
+    case FA_ERR_WORKSPACE: return "workspace missing or smaller than fa_bwd_workspace_size()";
+    case FA_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
+    case FA_ERR_DEVICE: return "current device is not a compute capability 10.3 (sm_103a) GPU";
+    case FA_ERR_TIMEOUT: return "a device-side wait gave up; outputs since the last status check are invalid";
+    default: return "unknown error code";
+  }
+}
+
+long long fa_fwd_tile_count(int N, int D, int causal) {
+  if (N <= 0 || N % 128 != 0 || (D != 64 && D != 128 && D != 256) || (causal != 0 && causal != 1)) return -1;
+  const int bm = 128, bn = fa::fwd_block_n(D);
+  const long long nqt = N / bm, nkv = N / bn;
+  if (!causal) return nqt * nkv;
+  long long n = 0;
+  for (long long qt = 0; qt < nqt; ++qt) n += ((qt + 1) * bm) / bn;
+  return n;
+}
+
+double fa_fwd_flops(int Z, int H, int N, int D, int causal) {
+  const double heads = static_cast<double>(Z) * H, n = N, d = D;
+  return heads * (causal ? 2.0 * n * (n + 1.0) * d : 4.0 * n * n * d);
+}
+
+double fa_bwd_flops(int Z, int H, int N, int D, int causal) { return 2.5 * fa_fwd_flops(Z, H, N, D, causal); }
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int N, int D,
+           int causal, float scale, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  int rc = check_shape(Z, H, N, D, causal, scale);
+  if (rc != FA_OK) return rc;
+  DevInfo* dev = nullptr;
+  if ((rc = current_device_info(&dev)) != FA_OK) return rc;
+
+  const long long rows = static_cast<long long>(Z) * H * N;
+  const int bn = fa::fwd_block_n(D);
+  CUtensorMap tq, tk, tv;
+  if (!fp16_map(&tq, q, rows, D, 128) || !fp16_map(&tk, k, rows, D, bn) || !fp16_map(&tv, v, rows, D, bn))
+    return FA_ERR_CUDA;
+  fa::FwdParams prm{};
+  prm.o = static_cast<__half*>(o);
+  prm.lse = lse;
+  prm.heads = Z * H;
+  prm.N = N;
+  prm.scale_log2 = scale * kLog2e;
+  prm.status = dev->status;
+  const bool c = causal != 0;
+  switch (D) {
+    case 64: rc = fa::launch_fwd_d64(c, tq, tk, tv, prm, dev->sms, stream); break;
+    case 128: rc = fa::launch_fwd_d128(c, tq, tk, tv, prm, dev->sms, stream); break;
+    default: rc = fa::launch_fwd_d256(c, tq, tk, tv, prm, dev->sms, stream); break;
+  }
+  return rc == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal) {
+  if (check_shape(Z, H, N, D, causal, 1.f) != FA_OK) return 0;
+  DevInfo* dev = nullptr;
+  if (current_device_info(&dev) != FA_OK) return 0;
+  return bwd_workspace_layout(Z, H, N, D, dev->sms).total;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int Z, int H, int N, int D,
+           int causal, float scale, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  int rc = check_shape(Z, H, N, D, causal, scale);
+  if (rc != FA_OK) return rc;
+  DevInfo* dev = nullptr;
+  if ((rc = current_device_info(&dev)) != FA_OK) return rc;
+  const BwdWorkspace ws = bwd_workspace_layout(Z, H, N, D, dev->sms);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < ws.total) return FA_ERR_WORKSPACE;
+
+  const long long rows = static_cast<long long>(Z) * H * N;
+  // maps: q, k, v, dout (fp16, box rows chosen by the kernel's tiling)
+  CUtensorMap maps[4];
+  const int bq = (D == 256) ? 64 : 128;
+  if (!fp16_map(&maps[0], q, rows, D, bq) || !fp16_map(&maps[1], k, rows, D, 128) ||
+      !fp16_map(&maps[2], v, rows, D, 128) || !fp16_map(&maps[3], dout, rows, D, bq))
+    return FA_ERR_CUDA;
+  char* wsb = static_cast<char*>(workspace);
+  fa::BwdParams prm{};
+  prm.o = static_cast<const __half*>(o);
+  prm.dout = static_cast<const __half*>(dout);
+  prm.lse = lse;
+  prm.dq = static_cast<__half*>(dq);
+  prm.dk = static_cast<__half*>(dk);
+  prm.dv = static_cast<__half*>(dv);
+  prm.delta = reinterpret_cast<float*>(wsb + ws.delta_off);
+  prm.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
+  prm.dq_acc = reinterpret_cast<float*>(wsb + ws.dq_off);
+  prm.heads = Z * H;
+  prm.N = N;
+  prm.scale = scale;
+  prm.scale_log2 = scale * kLog2e;
+  prm.status = dev->status;
+  const bool c = causal != 0;
+  switch (D) {
+    case 64: rc = fa::launch_bwd_d64(c, maps, prm, ws.grid, stream); break;
+    case 128: rc = fa::launch_bwd_d128(c, maps, prm, ws.grid, stream); break;
+    default: rc = fa::launch_bwd_d256(c, maps, prm, ws.grid, stream); break;
+  }
+  return rc == 0 ? FA_OK : (rc == -2 ? FA_ERR_UNSUPPORTED : FA_ERR_CUDA);
+}
+
+int fa_device_status_raw(cudaStream_t stream, int* raw) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  DevInfo* dev = nullptr;
+  int rc = current_device_info(&dev);
+  if (rc != FA_OK) return rc;
+  int v = 0;
+  if (cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (raw) *raw = v;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+int fa_device_status(cudaStream_t stream) { return fa_device_status_raw(stream, nullptr); }
+
+}  // extern "C"

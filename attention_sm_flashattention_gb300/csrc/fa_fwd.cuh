@@ -1,0 +1,416 @@
+// FlashAttention forward for sm_103a: persistent, warp-specialised, TMA-fed,
+// tcgen05 MMAs accumulating in TMEM.
+//
+// Source: «把 FlashAttention 搬上昇腾：Triton-Ascend CV Pipeline 优化实战»,
+// §一 -- one Q tile stays on chip and streams K/V tiles; the online softmax
+// keeps the running row max m, the denominator l and the unnormalised fp32
+// accumulator, rescaling l and acc when the max moves; exp2 with log2(e)
+// folded into the scale; m, l, acc in fp32 and P rounded to fp16 before the
+// matrix unit; causal shortens the key-tile loop and masks only diagonal
+// tiles; D = 256 keeps two 128-wide accumulator halves; O is written once.
+//
+// Roles (192 threads):
+//   warps 0-3  softmax warpgroup: thread r owns query row r of the tile. It
+//              reads S from TMEM, applies the mask, updates m and l, writes
+//              P (fp16) back to TMEM, rescales O in TMEM when m moved, and
+//              runs the epilogue (O / l -> fp16, lse).
+//   warp 4     TMA producer: Q tile per work item, K/V tiles into a ring.
+//   warp 5     MMA issuer (one thread) and TMEM owner: S = Q K^T into one
+//              of two S buffers, then O += P V with P read from TMEM.
+//
+// The MMA of key tile j+1 (Q K^T) runs while the softmax of tile j works,
+// and P V of tile j runs while the softmax of tile j+1 works.
+#pragma once
+
+#include "fa_kernels.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+template <int D, bool CAUSAL>
+struct FwdTraits {
+  static constexpr int BM = 128;                    // query rows per tile
+  static constexpr int BN = (D == 256) ? 64 : 128;  // keys per tile
+  static constexpr int KV_STAGES = 2;
+  static constexpr int Q_STAGES = (D == 256) ? 1 : 2;
+  static constexpr int DSUB = D / 64;               // 64-column sub-tiles per row
+  static constexpr int Q_SUB = BM * 128;            // bytes of a [BM x 64] fp16 sub-tile
+  static constexpr int KV_SUB = BN * 128;
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int OH = (D > 128) ? 128 : D;    // width of one O accumulator half
+  static constexpr int NOH = D / OH;                // number of O halves
+  // TMEM columns (fp32 columns; 512 allocated)
+  static constexpr int S_COL = 0;       // S buffer b: [b*BN, b*BN + BN)
+  static constexpr int P_COL = 2 * BN;  // P buffer b: [2BN + b*BN/2, +BN/2) packed fp16 pairs
+  static constexpr int O_COL = 3 * BN;  // O: [3BN, 3BN + D)
+  static constexpr int TMEM_COLS = 512;
+  static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
+  // shared memory layout (offsets from a 1024-byte aligned base)
+  static constexpr int SM_Q = 0;
+  static constexpr int SM_K = SM_Q + Q_STAGES * Q_BYTES;
+  static constexpr int SM_V = SM_K + KV_STAGES * KV_BYTES;
+  static constexpr int SM_BAR = SM_V + KV_STAGES * KV_BYTES;
+  static constexpr int SM_BYTES = SM_BAR + 256;
+  // +1024 slack for the manual alignment; never below 120 KB so that a
+  // second CTA can never share the SM (each CTA takes all 512 TMEM columns).
+  static constexpr int SMEM_ALLOC = (SM_BYTES + 1024 > 120 * 1024) ? SM_BYTES + 1024 : 120 * 1024;
+  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  static constexpr int THREADS = 192;
+  static constexpr int PRODUCER_WARP = 4;
+  static constexpr int MMA_WARP = 5;
+};
+
+// Barrier slots inside the SM_BAR area.
+struct FwdBars {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t k_full[2], v_full[2], kv_empty[2];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_ready, o_free, mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(FwdBars) <= 256, "barrier area");
+
+// Static schedule.  Non-causal: one work unit per (head, query tile), head
+// major so that the CTAs running at the same time share K/V through L2.
+// Causal: one unit pairs query tiles qt and nqt-1-qt of the same head, so
+// every unit costs the same number of key tiles (nqt + 1 for square tiles)
+// and a static stride over units balances the SMs.
+template <bool CAUSAL>
+__device__ __forceinline__ int fwd_num_units(int heads, int nqt) {
+  return CAUSAL ? heads * ((nqt + 1) / 2) : heads * nqt;
+}
+
+template <bool CAUSAL>
+__device__ __forceinline__ void fwd_decode(int u, int nqt, int& head, int& qa, int& qb) {
+  if (CAUSAL) {
+    const int npair = (nqt + 1) / 2;
+    head = u / npair;
+    const int p = u - head * npair;
+    qa = nqt - 1 - p;
+    qb = (p != qa) ? p : -1;
+  } else {
+    head = u / nqt;
+    qa = u - head * nqt;
+    qb = -1;
+  }
+}
+
+template <int D, bool CAUSAL>
+__device__ __forceinline__ int fwd_num_kv(int qt, int nkv_full) {
+  using T = FwdTraits<D, CAUSAL>;
+  return CAUSAL ? ((qt + 1) * T::BM) / T::BN : nkv_full;
+}
+
+// Bounded wait that ignores the abort flag: used only while draining at exit.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_test(a, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams prm) {
+  using T = FwdTraits<D, CAUSAL>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  FwdBars* bars = reinterpret_cast<FwdBars*>(smem + T::SM_BAR);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], T::BM);
+    }
+    mbar_init(&bars->o_ready, 1);
+    mbar_init(&bars->o_free, T::BM);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == T::MMA_WARP) {
+    tmem_alloc(&bars->tmem_base, T::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == T::PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const WaitCtx wc{prm.status, &bars->abort_flag};
+  const uint32_t tmem = bars->tmem_base;
+  const int N = prm.N;
+  const int nqt = N / T::BM;
+  const int nkv_full = N / T::BN;
+  const int units = fwd_num_units<CAUSAL>(prm.heads, nqt);
+
+  if (warp == T::PRODUCER_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_policy_evict_last();
+      const uint64_t pol_q = l2_policy_evict_first();
+      uint32_t q_it = 0, kv_it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        int head, qa, qb;
+        fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+        for (int half = 0; ok && half < 2; ++half) {
+          const int qt = half ? qb : qa;
+          if (qt < 0) break;
+          const int qs = q_it % T::Q_STAGES;
+          if (!(ok = mbar_wait(&bars->q_empty[qs], ((q_it / T::Q_STAGES) & 1) ^ 1, wc, 1))) break;
+          mbar_arrive_expect_tx(&bars->q_full[qs], T::Q_BYTES);
+          uint8_t* sq = smem + T::SM_Q + qs * T::Q_BYTES;
+          for (int s = 0; s < T::DSUB; ++s)
+            tma_load_2d_hint(sq + s * T::Q_SUB, &tm_q, &bars->q_full[qs], s * 64, head * N + qt * T::BM, pol_q);
+          ++q_it;
+          const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+          for (int j = 0; j < nkv; ++j) {
+            const int st = kv_it % T::KV_STAGES;
+            if (!(ok = mbar_wait(&bars->kv_empty[st], ((kv_it / T::KV_STAGES) & 1) ^ 1, wc, 2))) break;
+            const int row = head * N + j * T::BN;
+            uint8_t* sk = smem + T::SM_K + st * T::KV_BYTES;
+            uint8_t* sv = smem + T::SM_V + st * T::KV_BYTES;
+            mbar_arrive_expect_tx(&bars->k_full[st], T::KV_BYTES);
+            for (int s = 0; s < T::DSUB; ++s)
+              tma_load_2d_hint(sk + s * T::KV_SUB, &tm_k, &bars->k_full[st], s * 64, row, pol_kv);
+            mbar_arrive_expect_tx(&bars->v_full[st], T::KV_BYTES);
+            for (int s = 0; s < T::DSUB; ++s)
+              tma_load_2d_hint(sv + s * T::KV_SUB, &tm_v, &bars->v_full[st], s * 64, row, pol_kv);
+            ++kv_it;
+          }
+        }
+      }
+      // Drain: every load issued must have landed before the CTA may exit.
+      for (uint32_t i = (kv_it > T::KV_STAGES ? kv_it - T::KV_STAGES : 0); i < kv_it; ++i) {
+        drain_wait(&bars->k_full[i % T::KV_STAGES], (i / T::KV_STAGES) & 1);
+        drain_wait(&bars->v_full[i % T::KV_STAGES], (i / T::KV_STAGES) & 1);
+      }
+      for (uint32_t i = (q_it > T::Q_STAGES ? q_it - T::Q_STAGES : 0); i < q_it; ++i)
+        drain_wait(&bars->q_full[i % T::Q_STAGES], (i / T::Q_STAGES) & 1);
+    }
+  } else if (warp == T::MMA_WARP) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_f16(128, T::BN, false, false);
+      constexpr uint32_t idesc_pv = idesc_f16(128, T::OH, false, true);
+      const uint32_t sbase = smem_u32(smem);
+      uint32_t q_it = 0, kv_it = 0, t = 0, item = 0;
+      bool ok = true;
+
+      // O += P_tile V_stage; the first tile of an item overwrites O.
+      auto issue_pv = [&](uint32_t tile, uint32_t kv_idx, bool first) -> bool {
+        const int b = tile & 1;
+        const int st = kv_idx % T::KV_STAGES;
+        if (first && item > 0 && !mbar_wait(&bars->o_free, (item - 1) & 1, wc, 10)) return false;
+        if (!mbar_wait(&bars->p_full[b], (tile >> 1) & 1, wc, 11)) return false;
+        if (!mbar_wait(&bars->v_full[st], (kv_idx / T::KV_STAGES) & 1, wc, 12)) return false;
+        tc_fence_after();
+        const uint32_t sv = sbase + T::SM_V + st * T::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < T::BN / 16; ++kk) {
+#pragma unroll
+          for (int h = 0; h < T::NOH; ++h) {
+            const uint64_t bdesc = sdesc_sw128(sv + (h * 2) * T::KV_SUB + kk * 16 * 128, T::KV_SUB, 1024);
+            mma_f16_ts(tmem + T::O_COL + h * 128, tmem + T::P_COL + b * (T::BN / 2) + kk * 8, bdesc, idesc_pv,
+                       (first && kk == 0) ? 0u : 1u);
+          }
+        }
+        mma_commit(&bars->kv_empty[st]);
+        mma_commit(&bars->o_ready);
+        return true;
+      };
+
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        int head, qa, qb;
+        fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+        for (int half = 0; ok && half < 2; ++half) {
+          const int qt = half ? qb : qa;
+          if (qt < 0) break;
+          const int qs = q_it % T::Q_STAGES;
+          if (!(ok = mbar_wait(&bars->q_full[qs], (q_it / T::Q_STAGES) & 1, wc, 3))) break;
+          tc_fence_after();
+          const uint32_t sq = sbase + T::SM_Q + qs * T::Q_BYTES;
+          const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+          for (int j = 0; j < nkv; ++j) {
+            const int st = kv_it % T::KV_STAGES;
+            if (!(ok = mbar_wait(&bars->k_full[st], (kv_it / T::KV_STAGES) & 1, wc, 4))) break;
+            tc_fence_after();
+            const uint32_t sk = sbase + T::SM_K + st * T::KV_BYTES;
+            const int b = t & 1;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t adesc = sdesc_sw128(sq + (kk / 4) * T::Q_SUB + (kk % 4) * 32, 16, 1024);
+              const uint64_t bdesc = sdesc_sw128(sk + (kk / 4) * T::KV_SUB + (kk % 4) * 32, 16, 1024);
+              mma_f16_ss(tmem + T::S_COL + b * T::BN, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars->s_full[b]);
+            if (j == nkv - 1) mma_commit(&bars->q_empty[qs]);
+            if (j > 0 && !(ok = issue_pv(t - 1, kv_it - 1, j == 1))) break;
+            ++t;
+            ++kv_it;
+          }
+          if (ok) ok = issue_pv(t - 1, kv_it - 1, nkv == 1);
+          ++q_it;
+          ++item;
+        }
+      }
+      // Drain: all MMAs issued by this thread complete before TMEM is freed.
+      mma_commit(&bars->mma_done);
+      drain_wait(&bars->mma_done, 0);
+    }
+  } else {
+    // ------------------------------------------------------ softmax warpgroup
+    const int r = threadIdx.x;  // query row inside the tile, == TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float sl2 = prm.scale_log2;
+    uint32_t t = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      int head, qa, qb;
+      fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+      for (int half = 0; ok && half < 2; ++half) {
+        const int qt = half ? qb : qa;
+        if (qt < 0) break;
+        const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+        const int qi = qt * T::BM + r;  // query index within the head
+        float m = -INFINITY, l = 0.f;
+        for (int j = 0; j < nkv; ++j) {
+          const int b = t & 1;
+          ok = mbar_wait(&bars->s_full[b], (t >> 1) & 1, wc, 5);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t sr[T::BN];
+#pragma unroll
+          for (int c = 0; c < T::BN; c += 32) tmem_ld32(lane_base + T::S_COL + b * T::BN + c, sr + c);
+          tmem_wait_ld();
+          reg_fence<T::BN>(sr);
+          float s[T::BN];
+#pragma unroll
+          for (int c = 0; c < T::BN; ++c) s[c] = __uint_as_float(sr[c]);
+          if (CAUSAL && (j + 1) * T::BN - 1 > qt * T::BM) {
+            const int k0 = j * T::BN;
+#pragma unroll
+            for (int c = 0; c < T::BN; ++c)
+              if (k0 + c > qi) s[c] = -INFINITY;
+          }
+          float pm[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) pm[i] = s[i];
+#pragma unroll
+          for (int c = 8; c < T::BN; ++c) pm[c & 7] = fmaxf(pm[c & 7], s[c]);
+          const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                 fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+          const float m_new = fmaxf(m, mx * sl2);
+          const float neg = -m_new;
+          float ps[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ps[i] = 0.f;
+          uint32_t pk[T::BN / 2];
+#pragma unroll
+          for (int c = 0; c < T::BN; c += 2) {
+            const float p0 = ex2_approx(fmaf(s[c], sl2, neg));
+            const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg));
+            ps[(c >> 1) & 7] += p0 + p1;
+            pk[c / 2] = pack_half2(p0, p1);
+          }
+          const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+          const float alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
+          l = l * alpha + rs;
+          m = m_new;
+          if (j > 0) {
+            // O holds P V of the previous tiles: wait for the last P V, then
+            // rescale rows whose max moved.
+            ok = mbar_wait(&bars->o_ready, (t - 1) & 1, wc, 6);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+              for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(lane_base + T::O_COL + c, o);
+                tmem_wait_ld();
+                reg_fence<32>(o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                tmem_st32(lane_base + T::O_COL + c, o);
+              }
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < T::BN / 2; c += 32) tmem_st32(lane_base + T::P_COL + b * (T::BN / 2) + c, pk + c);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bars->p_full[b]);
+          ++t;
+        }
+        if (!ok) break;
+        // ---- epilogue: O / l -> fp16, lse = ln2 * (m + log2 l)
+        ok = mbar_wait(&bars->o_ready, (t - 1) & 1, wc, 7);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        __half* orow = prm.o + (static_cast<size_t>(head) * N + qi) * D;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + T::O_COL + c, o);
+          tmem_wait_ld();
+          reg_fence<32>(o);
+          uint32_t h[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            h[i] = pack_half2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+        }
+        prm.lse[static_cast<size_t>(head) * N + qi] = (m + log2f(l)) * 0.69314718055994530942f;
+        tc_fence_before();
+        mbar_arrive(&bars->o_free);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == T::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, T::TMEM_COLS);
+  }
+}
+
+template <int D, bool CAUSAL>
+int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& prm,
+               int num_sms, cudaStream_t stream) {
+  using T = FwdTraits<D, CAUSAL>;
+  static bool attr_set = false;  // per process; the attribute is per function, not per device
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             T::SMEM_ALLOC) != cudaSuccess)
+      return -1;
+    attr_set = true;
+  }
+  const int nqt = prm.N / T::BM;
+  const int units = CAUSAL ? prm.heads * ((nqt + 1) / 2) : prm.heads * nqt;
+  const int grid = units < num_sms ? units : num_sms;
+  fa_fwd_kernel<D, CAUSAL><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(tq, tk, tv, prm);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace fa

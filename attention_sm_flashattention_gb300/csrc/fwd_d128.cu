@@ -1,0 +1,12 @@
+// Forward kernel instantiations for head dimension 128.
+#include "fa_fwd.cuh"
+
+namespace fa {
+
+int launch_fwd_d128(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                   const FwdParams& prm, int num_sms, cudaStream_t stream) {
+  return causal ? launch_fwd<128, true>(tq, tk, tv, prm, num_sms, stream)
+                : launch_fwd<128, false>(tq, tk, tv, prm, num_sms, stream);
+}
+
+}  // namespace fa

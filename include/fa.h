@@ -1,0 +1,149 @@
+/*
+ * fa.h -- C ABI of libfa.so: exact FlashAttention forward and backward for
+ * one NVIDIA GB300 (sm_103a), fp16 inputs/outputs, fp32 accumulation.
+ *
+ * What is computed (source: «把 FlashAttention 搬上昇腾：Triton-Ascend CV
+ * Pipeline 优化实战»):
+ *   forward  (§一)  S = Q K^T * scale,  P = softmax(S),  O = P V, computed
+ *                   tile by tile with the online softmax (running row max m,
+ *                   denominator l, unnormalised fp32 accumulator), exp2 with
+ *                   log2(e) folded into the scale; causal mode visits only
+ *                   key tiles at or below the diagonal and masks exactly only
+ *                   inside diagonal tiles (§一, §八).
+ *   backward (§二)  Delta = rowsum(O * dO), P recomputed from the saved
+ *                   log-sum-exp, dP = dO V^T, dS = scale * P * (dP - Delta),
+ *                   dQ = dS K, dK = dS^T Q, dV = P^T dO, with every gradient
+ *                   tile written by exactly one CTA and a workspace that does
+ *                   not grow with the number of heads times N^2 (§二's three
+ *                   rules, §五).
+ *
+ * Layout and types (all calls):
+ *   q, k, v, o, dout, dq, dk, dv : fp16 (IEEE binary16), contiguous
+ *                                  [Z, H, N, D] row-major, 16-byte aligned.
+ *   lse                          : fp32 [Z, H, N]; lse[z,h,i] is the natural
+ *                                  log of sum_j exp(S_ij) over the visible
+ *                                  keys j (j <= i when causal).
+ *   Every (z, h) pair is an independent head; queries and keys have the same
+ *   length N.  Causal means key j is visible to query i iff j <= i.
+ *
+ * Ownership: every pointer is device memory owned by the caller; the library
+ * keeps no pointer after a call returns and allocates no device memory on
+ * these paths.  The only library state is one device status word per device.
+ *
+ * Asynchrony: fa_fwd / fa_bwd validate their arguments on the host, enqueue
+ * kernels on `stream` and return.  A return of FA_OK means "enqueued".
+ * Results are ready when the stream reaches that point.
+ *
+ * Errors: argument problems are reported synchronously, before anything is
+ * enqueued, with a negative code (below).  A device-side wait that gives up
+ * (bounded by about one second; it never hangs the GPU) is reported through
+ * fa_device_status().  Not thread-safe with respect to concurrent first calls
+ * on the same device from several host threads.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_OK 0
+#define FA_ERR_INVALID_ARG (-1) /* null pointer, Z/H/N <= 0, non-finite or <= 0 scale, misaligned pointer */
+#define FA_ERR_UNSUPPORTED (-2) /* D not in {64, 128, 256}, N % 128 != 0, or sizes past 32-bit indexing */
+#define FA_ERR_WORKSPACE (-3)   /* workspace null or smaller than fa_bwd_workspace_size() */
+#define FA_ERR_CUDA (-4)        /* a CUDA runtime call or kernel launch failed */
+#define FA_ERR_DEVICE (-5)      /* current device is not a compute capability 10.3 GPU */
+#define FA_ERR_TIMEOUT (-6)     /* (fa_device_status) a kernel wait gave up; results invalid */
+
+/*
+ * Forward pass.  Source: «把 FlashAttention 搬上昇腾» §一 (tiled online
+ * softmax, exp2, fp32 m/l/acc, fp16 P into the matrix unit, causal loop
+ * bound + diagonal-only mask, D256 as two D128 halves).
+ *   q, k, v : inputs [Z,H,N,D] fp16.
+ *   o       : output [Z,H,N,D] fp16, O = softmax(Q K^T scale) V, rounded to
+ *             nearest from the fp32 accumulator divided by l.
+ *   lse     : output [Z,H,N] fp32 (natural-log log-sum-exp of each row of S).
+ *   Z, H, N : batch, heads, sequence length (N % 128 == 0).
+ *   D       : head dimension, 64, 128 or 256.
+ *   causal  : 0 or 1.
+ *   scale   : softmax scale applied to Q K^T (usually 1/sqrt(D)); finite, > 0.
+ *   stream  : CUDA stream the kernel is enqueued on (0 = legacy default).
+ * Returns FA_OK or a negative FA_ERR_* code.
+ */
+FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int N, int D,
+           int causal, float scale, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs on the current device: Delta and the
+ * log2-scaled lse (2 x Z*H*N fp32) plus one fp32 N x D dQ accumulator per
+ * resident CTA.  It grows with Z*H*N and with #SMs*N*D, never with N^2 over
+ * all heads (§二, third rule).  Returns 0 for unsupported arguments.
+ */
+FA_API size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal);
+
+/*
+ * Backward pass.  Source: «把 FlashAttention 搬上昇腾» §二 (equations and
+ * the three rules), §五 (persistent programs that each own whole heads, so
+ * every dQ/dK/dV tile has one writer), §七 (D256 as two D128 halves).
+ *   q, k, v, o, dout : inputs [Z,H,N,D] fp16; o must be fa_fwd's output for
+ *                      the same q, k, v, causal and scale.
+ *   lse              : input [Z,H,N] fp32 from the same fa_fwd call.
+ *   dq, dk, dv       : outputs [Z,H,N,D] fp16, overwritten (not accumulated).
+ *   workspace        : device scratch of at least workspace_bytes >=
+ *                      fa_bwd_workspace_size(Z,H,N,D,causal) bytes, 256-byte
+ *                      aligned; contents on entry are ignored, on exit
+ *                      undefined.  Must not be used by another call that runs
+ *                      concurrently on the GPU.
+ *   other arguments  : as for fa_fwd.
+ * Returns FA_OK or a negative FA_ERR_* code.
+ */
+FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int Z, int H, int N, int D,
+           int causal, float scale, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of
+ * the current device: FA_OK, FA_ERR_TIMEOUT (a kernel wait gave up; the
+ * outputs of the calls since the last check are invalid) or FA_ERR_CUDA.
+ */
+FA_API int fa_device_status(cudaStream_t stream);
+
+/*
+ * Like fa_device_status but also returns the raw status word (timeout site in
+ * bits 8 and up) through *raw when raw is not NULL.
+ */
+FA_API int fa_device_status_raw(cudaStream_t stream, int* raw);
+
+/* Static, human-readable description of an FA_* code. */
+FA_API const char* fa_error_string(int code);
+
+/*
+ * Number of (query tile, key tile) pairs one head's pass visits with the
+ * library's forward tiling (128-row query tiles, 128- or 64-key tiles): the
+ * causal loop bound of §八 (T*T tiles non-causal, 1+2+...+T causal for square
+ * tiles).  Host-only helper used for the FLOP model; -1 on bad arguments.
+ */
+FA_API long long fa_fwd_tile_count(int N, int D, int causal);
+
+/*
+ * Algorithmic FLOPs of one call over all heads (the work the method must do,
+ * not counting what it avoids): forward 4*N*N*D non-causal, 2*N*(N+1)*D
+ * causal, per head; backward 2.5x that (five GEMMs incl. the recompute of P).
+ */
+FA_API double fa_fwd_flops(int Z, int H, int N, int D, int causal);
+FA_API double fa_bwd_flops(int Z, int H, int N, int D, int causal);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every function ``include/fa.h`` declares, and
+reject bad arguments synchronously, before it touches the device.
+"""
+
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+from attention_sm_flashattention_gb300 import _native
+from oracle import attention as orc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_native.LIB_PATH):
+        from attention_sm_flashattention_gb300 import build
+        build.build()
+    return _native.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"FA_API\s+[\w\s\*]+?\b(fa_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    syms = set(declared_symbols())
+    for name in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_device_status", "fa_error_string"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    syms = declared_symbols()
+    assert syms
+    for name in syms:
+        assert hasattr(lib, name), name
+        assert name in _native.SIGNATURES, f"binding lacks a signature for {name}"
+
+
+def test_error_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert len(_native.error_string(code)) >= 2
+    assert "unknown" in _native.error_string(12345)
+
+
+FAKE = 1 << 20  # an aligned non-null address that is never dereferenced
+
+
+def call_fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, Z=1, H=1, N=128, D=64, causal=0, scale=0.125):
+    return lib.fa_fwd(q, k, v, o, lse, Z, H, N, D, causal, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), _native.FA_ERR_INVALID_ARG),
+    (dict(lse=None), _native.FA_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), _native.FA_ERR_INVALID_ARG),      # not 16-byte aligned
+    (dict(Z=0), _native.FA_ERR_INVALID_ARG),
+    (dict(H=-1), _native.FA_ERR_INVALID_ARG),
+    (dict(N=0), _native.FA_ERR_INVALID_ARG),
+    (dict(causal=2), _native.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), _native.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), _native.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), _native.FA_ERR_INVALID_ARG),
+    (dict(D=96), _native.FA_ERR_UNSUPPORTED),
+    (dict(D=32), _native.FA_ERR_UNSUPPORTED),
+    (dict(N=100), _native.FA_ERR_UNSUPPORTED),
+    (dict(Z=1 << 14, H=1 << 10, N=256), _native.FA_ERR_UNSUPPORTED),  # rows >= 2^31
+])
+def test_fwd_rejects_bad_arguments(lib, kw, code):
+    assert call_fwd(lib, **kw) == code
+
+
+def call_bwd(lib, ws=FAKE, ws_bytes=1 << 40, dq=FAKE, D=64, N=128, scale=0.125):
+    return lib.fa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, dq, FAKE, FAKE, ws, ws_bytes,
+                      1, 1, N, D, 0, scale, None)
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    assert call_bwd(lib, dq=None) == _native.FA_ERR_INVALID_ARG
+    assert call_bwd(lib, D=80) == _native.FA_ERR_UNSUPPORTED
+    assert call_bwd(lib, N=130) == _native.FA_ERR_UNSUPPORTED
+    assert call_bwd(lib, scale=-1.0) == _native.FA_ERR_INVALID_ARG
+
+
+def test_workspace_size_rejects_bad_shapes(lib):
+    assert lib.fa_bwd_workspace_size(1, 1, 100, 64, 0) == 0
+    assert lib.fa_bwd_workspace_size(1, 1, 128, 48, 0) == 0
+
+
+def test_tile_count_matches_pages_and_oracle(lib):
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "causal_tiles.json")))
+    n = g["n_tiles"] * 128
+    assert lib.fa_fwd_tile_count(n, 128, 0) == g["non_causal_tiles"]
+    assert lib.fa_fwd_tile_count(n, 128, 1) == g["causal_tiles"]
+    for N in (128, 256, 1024, 2048):
+        t = N // 128
+        assert lib.fa_fwd_tile_count(N, 64, 1) == orc.causal_tile_count(t, True)
+        assert lib.fa_fwd_tile_count(N, 128, 0) == orc.causal_tile_count(t, False)
+        # 64-key tiles for D = 256: twice as many key tiles, causal bound 2(qt+1)
+        assert lib.fa_fwd_tile_count(N, 256, 0) == 2 * t * t
+        assert lib.fa_fwd_tile_count(N, 256, 1) == t * (t + 1)
+    assert lib.fa_fwd_tile_count(100, 64, 0) == -1
+
+
+def test_flop_model(lib):
+    assert lib.fa_fwd_flops(128, 8, 1024, 128, 0) == pytest.approx(4 * 1024 * 1024 * 128 * 1024)
+    assert lib.fa_fwd_flops(1, 1, 1024, 128, 1) == pytest.approx(2 * 1024 * 1025 * 128)
+    assert lib.fa_bwd_flops(2, 3, 256, 64, 1) == pytest.approx(2.5 * lib.fa_fwd_flops(2, 3, 256, 64, 1))
