@@ -1,0 +1,363 @@
+"""Benchmark: attention fwd + bwd TFLOP/s on one GB300 (Z128 H8 N1024 D128).
+
+One step = one pass of the whole hot path over one batch: fa_fwd (O, lse)
+then fa_bwd (Delta preprocess + main kernel -> dQ, dK, dV), fp16 in, fp32
+accumulate.  FLOPs are the algorithmic count (forward 4 N^2 D per head, the
+backward 2.5x that); the work the method avoids is not counted.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  --impl reference times the fp64 CPU oracle (the only
+reference this method has) on a bounded sample of the same workload.
+Under torchrun each rank runs its own replica of the workload on its GPU (the
+heads are independent: no data-path collective); rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+Z, H, N, D, CAUSAL = 128, 8, 1024, 128, False
+WORKLOAD = "attention fwd+bwd, Z128 H8 N1024 D128 non-causal, fp16 inputs ~N(0,1), scale 1/sqrt(D)"
+METRIC = "attention fwd / fwd+bwd TFLOP/s at Z128 H8 N1024 D128 on 1 GB300; % of FP16 peak"
+UNIT = "TFLOP/s"
+SEED = 1002
+
+
+def set_workload(z, h, n, d, causal):
+    global Z, H, N, D, CAUSAL, WORKLOAD
+    Z, H, N, D, CAUSAL = z, h, n, d, bool(causal)
+    WORKLOAD = (f"attention fwd+bwd, Z{Z} H{H} N{N} D{D} {'causal' if CAUSAL else 'non-causal'}, "
+                "fp16 inputs ~N(0,1), scale 1/sqrt(D)")
+
+
+def flops_fwd(z, h, n, d, causal):
+    return z * h * (2.0 * n * (n + 1) * d if causal else 4.0 * n * n * d)
+
+
+def flops_step(z=None, h=None, n=None, d=None, causal=None):
+    return 3.5 * flops_fwd(Z if z is None else z, H if h is None else h, N if n is None else n,
+                           D if d is None else d, CAUSAL if causal is None else causal)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            js = json.load(f)
+        return {"tflops": js.get("bf16_tflops"), "tflops_sustained": js.get("bf16_tflops_sustained"),
+                "hbm_gbs": js.get("hbm_gbs"), "source": "measured"}
+    return {"tflops": 1900.0, "tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+
+def cpu_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            try:
+                return int(os.environ[var])
+            except ValueError:
+                pass
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(budget_s=12.0, max_heads=256):
+    """Time the fp64 oracle, forward + backward, head by head on the host
+    cores until the budget is spent (at least two heads)."""
+    from attention_sm_flashattention_gb300.inputs import make_inputs
+    from oracle import attention as orc
+
+    q, k, v, do = make_inputs(1, max_heads, N, D, seed=SEED)
+    scale = 1.0 / math.sqrt(D)
+    done, t0 = 0, time.perf_counter()
+    while done < max_heads and (done < 2 or time.perf_counter() - t0 < budget_s):
+        qh, kh, vh, dh = (t[0, done] for t in (q, k, v, do))
+        orc.attn_fwd_head(qh, kh, vh, CAUSAL, scale)
+        orc.attn_bwd_head(qh, kh, vh, dh, CAUSAL, scale)
+        done += 1
+    el = time.perf_counter() - t0
+    fl = flops_step(1, done, N, D, CAUSAL)
+    return {"value": fl / el / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"{done} of the {Z * H} heads (N{N} D{D} non-causal), fp64 numpy forward+backward, "
+                      f"{el:.1f} s wall"}
+
+
+# -------------------------------------------------------------- clock sampler
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                mx.append(float(row[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, row[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- GPU bench
+
+
+def gpu_bench(args, rank, world, local_rank):
+    import torch
+
+    import attention_sm_flashattention_gb300 as fa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device=dev).manual_seed(SEED + rank)
+    q, k, v, do = (torch.randn((Z, H, N, D), device=dev, dtype=torch.float16, generator=gen) for _ in range(4))
+    scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q)
+    lse = torch.empty((Z, H, N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(fa.bwd_workspace_size(Z, H, N, D, CAUSAL), device=dev, dtype=torch.uint8)
+
+    def step():
+        fa.fwd(q, k, v, causal=CAUSAL, scale=scale, out=(o, lse))
+        fa.bwd(q, k, v, o, do, lse, causal=CAUSAL, scale=scale, workspace=ws, out=(dq, dk, dv))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.device_status() != 0:
+        raise RuntimeError("device status reports a kernel wait timeout during warm-up")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                           os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank])
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    # per-call events on the launching stream: forward kernel and backward call
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        fa.fwd(q, k, v, causal=CAUSAL, scale=scale, out=(o, lse))
+        ev[i][1].record(stream)
+        fa.bwd(q, k, v, o, do, lse, causal=CAUSAL, scale=scale, workspace=ws, out=(dq, dk, dv))
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    if fa.device_status() != 0:
+        raise RuntimeError("device status reports a kernel wait timeout in the timed region")
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+
+    # ---- end to end through the public API: pinned host in, host out
+    hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
+    ho, hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(4))
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if fa.device_status() != 0:
+        raise RuntimeError("device status reports a kernel wait timeout in the end-to-end leg")
+    nbytes = q.numel() * q.element_size()
+    return {"total_ms": total_ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "e2e_ms": e2e_ms,
+            "h2d": 4 * nbytes, "d2h": 4 * nbytes, "clocks": clocks}
+
+
+def reduce_max(vals, world):
+    if world == 1:
+        return vals
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(vals, dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def load_traffic():
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        return json.load(f)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    # Workload overrides, for profiling the same step on a smaller case; the
+    # default is the benchmark workload above.
+    ap.add_argument("--z", type=int, default=Z)
+    ap.add_argument("--h", type=int, default=H)
+    ap.add_argument("--n", type=int, default=N)
+    ap.add_argument("--d", type=int, default=D)
+    ap.add_argument("--causal", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    set_workload(args.z, args.h, args.n, args.d, args.causal)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    config = {"workload": WORKLOAD, "Z": Z, "H": H, "N": N, "D": D, "causal": CAUSAL,
+              "global_batch": Z * world, "seq_len": N, "parallelism": f"replicas{world}",
+              "l2": f"inputs larger than L2 ({4 * Z * H * N * D * 2 / 1e6:.0f} MB fp16 per step), no flush needed"}
+
+    if args.impl == "reference":
+        # The oracle as it stands, on the host cores: each step is one head of
+        # the workload (forward + backward in fp64); warm-up steps untimed.
+        if rank != 0:
+            return
+        from attention_sm_flashattention_gb300.inputs import make_inputs
+        from oracle import attention as orc
+
+        nh = args.warmup + args.steps
+        q, k, v, do = make_inputs(1, min(nh, Z * H), N, D, seed=SEED)
+        scale = 1.0 / math.sqrt(D)
+        times = []
+        for i in range(nh):
+            hh = i % q.shape[1]
+            t0 = time.perf_counter()
+            orc.attn_fwd_head(q[0, hh], k[0, hh], v[0, hh], CAUSAL, scale)
+            orc.attn_bwd_head(q[0, hh], k[0, hh], v[0, hh], do[0, hh], CAUSAL, scale)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        per_head = flops_step(1, 1, N, D, CAUSAL)
+        el = sum(times)
+        val = per_head * len(times) / el / 1e12
+        ms = flops_step() / (val * 1e12) * 1e3
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": val, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                                 "sample": f"{len(times)} heads of the workload, one per step, fp64 numpy "
+                                           f"forward+backward, {el:.1f} s; ms_per_step extrapolates to all "
+                                           f"{Z * H} heads"},
+                "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+
+    r = gpu_bench(args, rank, world, local_rank)
+    total_ms, e2e_ms = reduce_max([r["total_ms"], r["e2e_ms"]], world)
+    ms_per_step = total_ms / args.steps
+    value = world * flops_step() / (ms_per_step * 1e-3) / 1e12
+    e2e_value = world * flops_step() / (e2e_ms * 1e-3) / 1e12
+    peaks = measured_peaks()
+    fwd_tf = flops_fwd(Z, H, N, D, CAUSAL) / (r["fwd_ms"] * 1e-3) / 1e12
+    bwd_tf = 2.5 * flops_fwd(Z, H, N, D, CAUSAL) / (r["bwd_ms"] * 1e-3) / 1e12
+    traffic = load_traffic()
+    bwd_traffic = traffic.get(f"fa_bwd_d{D}{'c' if CAUSAL else ''}") if traffic else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": config,
+        "fwd_ms": r["fwd_ms"], "bwd_ms": r["bwd_ms"], "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+        "pct_of_peak": {"fwd": fwd_tf / peaks["tflops"], "fwd_bwd": value / world / peaks["tflops"],
+                        "bwd": bwd_tf / peaks["tflops"], "peak_tflops": peaks["tflops"],
+                        "peak_source": peaks["source"]},
+        "roofline": {"bound": "tensor", "kernel": f"fa_bwd (Delta preprocess + fa_bwd_kernel<{D},{str(CAUSAL).lower()}>)",
+                     "achieved": bwd_tf, "peak": peaks["tflops"], "unit": "TFLOP/s",
+                     "frac": bwd_tf / peaks["tflops"], "peak_kind": "burst bf16 cuBLAS (" + peaks["source"] + ")",
+                     "traffic": bwd_traffic},
+        "clocks": r["clocks"],
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
