@@ -21,6 +21,7 @@ FA_ERR_WORKSPACE = -3
 FA_ERR_CUDA = -4
 FA_ERR_DEVICE = -5
 FA_ERR_TIMEOUT = -6
+FA_ERR_SCRATCH_LIMIT = -7
 
 # Every symbol include/fa.h declares, with its ctypes signature.
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -28,6 +29,7 @@ SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _f, _vp]),
+    "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_device_status": (_i, [_vp]),
     "fa_device_status_raw": (_i, [_vp, ctypes.POINTER(ctypes.c_int)]),
     "fa_error_string": (ctypes.c_char_p, [_i]),

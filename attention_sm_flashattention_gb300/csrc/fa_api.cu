@@ -104,6 +104,7 @@ const char* fa_error_string(int code) {
     case FA_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
     case FA_ERR_DEVICE: return "current device is not a compute capability 10.3 (sm_103a) GPU";
     case FA_ERR_TIMEOUT: return "a device-side wait gave up; outputs since the last status check are invalid";
+    case FA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than fa_bwd_noalloc's built-in 64 MiB buffer";
     default: return "unknown error code";
   }
 }
@@ -228,3 +229,84 @@ int fa_device_status_raw(cudaStream_t stream, int* raw) {
 int fa_device_status(cudaStream_t stream) { return fa_device_status_raw(stream, nullptr); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// fa_bwd_noalloc: the backward for callers that cannot allocate device
+// memory.  Its scratch is this file-scope buffer instead of a caller
+// workspace.  In host code `g_fa_noalloc_scratch` names a host-side shadow,
+// not the device buffer, so the device address is looked up once per device
+// with cudaGetSymbolAddress and only that address is handed to the kernels.
+static __device__ __align__(256) unsigned char g_fa_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the built-in buffer on the current device (first call on
+// a device looks it up).  Returns nullptr on failure.
+void* noalloc_scratch_on_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_noalloc_scratch) != cudaSuccess) return nullptr;
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
+}  // namespace
+
+extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                              const float* lse, void* dq, void* dk, void* dv, int Z, int H, int N, int D,
+                              int causal, float scale, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  int rc = check_shape(Z, H, N, D, causal, scale);
+  if (rc != FA_OK) return rc;
+  DevInfo* dev = nullptr;
+  if ((rc = current_device_info(&dev)) != FA_OK) return rc;
+
+  // Scratch layout [delta | lse2 | grid dQ accumulators], as fa_bwd's
+  // workspace, with the grid cut to the accumulators that fit.
+  const long long heads = static_cast<long long>(Z) * H;
+  const size_t vec = round_up(static_cast<size_t>(heads) * N * sizeof(float), 256);
+  const size_t acc_one = round_up(static_cast<size_t>(N) * D * sizeof(float), 256);
+  if (2 * vec + acc_one > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+  long long grid = static_cast<long long>((FA_NOALLOC_SCRATCH_BYTES - 2 * vec) / (static_cast<size_t>(N) * D * sizeof(float)));
+  if (grid > dev->sms) grid = dev->sms;
+  if (grid > heads) grid = heads;
+
+  char* scratch = static_cast<char*>(noalloc_scratch_on_current_device());
+  if (scratch == nullptr) return FA_ERR_CUDA;
+
+  const long long rows = heads * N;
+  CUtensorMap maps[4];
+  const int bq = (D == 256) ? 64 : 128;
+  if (!fp16_map(&maps[0], q, rows, D, bq) || !fp16_map(&maps[1], k, rows, D, 128) ||
+      !fp16_map(&maps[2], v, rows, D, 128) || !fp16_map(&maps[3], dout, rows, D, bq))
+    return FA_ERR_CUDA;
+  fa::BwdParams prm{};
+  prm.o = static_cast<const __half*>(o);
+  prm.dout = static_cast<const __half*>(dout);
+  prm.lse = lse;
+  prm.dq = static_cast<__half*>(dq);
+  prm.dk = static_cast<__half*>(dk);
+  prm.dv = static_cast<__half*>(dv);
+  prm.delta = reinterpret_cast<float*>(scratch);
+  prm.lse2 = reinterpret_cast<float*>(scratch + vec);
+  prm.dq_acc = reinterpret_cast<float*>(scratch + 2 * vec);
+  prm.heads = Z * H;
+  prm.N = N;
+  prm.scale = scale;
+  prm.scale_log2 = scale * kLog2e;
+  prm.status = dev->status;
+  const bool c = causal != 0;
+  const int g = static_cast<int>(grid);
+  switch (D) {
+    case 64: rc = fa::launch_bwd_d64(c, maps, prm, g, stream); break;
+    case 128: rc = fa::launch_bwd_d128(c, maps, prm, g, stream); break;
+    default: rc = fa::launch_bwd_d256(c, maps, prm, g, stream); break;
+  }
+  return rc == 0 ? FA_OK : FA_ERR_CUDA;
+}

@@ -63,6 +63,7 @@ extern "C" {
 #define FA_ERR_CUDA (-4)        /* a CUDA runtime call or kernel launch failed */
 #define FA_ERR_DEVICE (-5)      /* current device is not a compute capability 10.3 GPU */
 #define FA_ERR_TIMEOUT (-6)     /* (fa_device_status) a kernel wait gave up; results invalid */
+#define FA_ERR_SCRATCH_LIMIT (-7) /* (fa_bwd_noalloc) problem needs more than the built-in scratch buffer */
 
 /*
  * Forward pass.  Source: «把 FlashAttention 搬上昇腾» §一 (tiled online
@@ -109,6 +110,42 @@ FA_API size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal);
 FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
            void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int Z, int H, int N, int D,
            int causal, float scale, cudaStream_t stream);
+
+/*
+ * Backward pass that allocates nothing and takes no workspace.
+ *
+ * The attention pages have no counterpart to this call; it exists for
+ * callers that cannot allocate device memory when they run the backward --
+ * for example code that runs inside a fixed memory pool or arena it does not
+ * own, a stream that is being recorded where allocation calls are not
+ * allowed, or an embedding host whose allocator must not be re-entered.
+ *
+ * It computes exactly what fa_bwd computes (same kernels, same arguments
+ * without workspace/workspace_bytes, same outputs bit for bit), but the
+ * scratch that fa_bwd takes from the caller (Delta, the log2-scaled lse and
+ * the per-CTA fp32 dQ accumulators) lives in one static device buffer of
+ * FA_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into libfa.so.  Every GPU on
+ * which the library is used holds that buffer until the process exits.
+ *
+ *   Limit  : 2*Z*H*N*4 bytes plus at least one N*D*4-byte dQ accumulator must
+ *            fit in the buffer; otherwise FA_ERR_SCRATCH_LIMIT is returned
+ *            before anything is enqueued.  When the buffer holds fewer
+ *            accumulators than the GPU has SMs, fewer persistent CTAs run
+ *            (slower, same result).
+ *   Set-up : the first call on a device (with that device current) looks up
+ *            the buffer's device address; make that first call before any
+ *            stream capture.
+ *   Sharing: all calls share the one buffer and it keeps the last call's
+ *            contents.  Nothing in it needs clearing -- each call writes
+ *            every scratch element it reads -- but calls whose kernels may
+ *            overlap on the GPU (different streams, other host threads)
+ *            race on it: serialise them.
+ * Returns FA_OK or a negative FA_ERR_* code.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+FA_API int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* lse, void* dq, void* dk, void* dv, int Z, int H, int N, int D, int causal,
+                          float scale, cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the device status word of
