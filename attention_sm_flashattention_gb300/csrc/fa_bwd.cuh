@@ -34,7 +34,8 @@
 //
 // Roles (320 threads): warps 0-7 compute (warpgroup w handles half the
 // columns; warp%4 selects the TMEM lane quarter), warp 8 TMA producer,
-// warp 9 MMA issuer and TMEM owner.
+// warp 9 MMA issuer (converged warp, one elected lane per MMA) and TMEM
+// owner.
 #pragma once
 
 #include "fa_kernels.h"
@@ -245,7 +246,7 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == T::MMA_WARP) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {  // the whole warp runs the loop; one elected lane issues each MMA
       constexpr uint32_t id_s = idesc_f16(128, T::BM, false, false);   // S^T, dP^T: M keys, N queries
       constexpr uint32_t id_kv = idesc_f16(128, T::DH, false, true);   // dV, dK: N = DH, B MN-major
       constexpr uint32_t id_dq = T::DQ_T ? idesc_f16(128, T::BM, true, true)  // dQ^T: M = d, N = queries
@@ -256,58 +257,58 @@ __global__ void __launch_bounds__(320, 1)
       bool ok = true;
       for (int head = blockIdx.x; ok && head < prm.heads; head += gridDim.x) {
         for (int j = 0; ok && j < nkv; ++j) {
-          if (!(ok = mbar_wait(&bars->kv_full, kc & 1, wc, 31))) break;
+          if (!(ok = warp_wait(&bars->kv_full, kc & 1, wc, 31))) break;
           tc_fence_after();
           for (int h = 0; ok && h < T::NPASS; ++h) {
             const int i0 = bwd_first_qtile<D, CAUSAL>(j);
             for (int i = i0; i < nqt; ++i) {
               const bool first = (i == i0);
               const int st = t % T::Q_STAGES;
-              if (!(ok = mbar_wait(&bars->q_full[st], (t / T::Q_STAGES) & 1, wc, 32))) break;
+              if (!(ok = warp_wait(&bars->q_full[st], (t / T::Q_STAGES) & 1, wc, 32))) break;
               tc_fence_after();
               const uint32_t sQ = sb + T::SM_Q + st * T::Q_BYTES;
               const uint32_t sO = sb + T::SM_DO + st * T::Q_BYTES;
               // S^T = K Q^T (the S region still holds P^T of the previous tile
               // until that tile's dV MMA has completed)
-              if (t > 0 && !(ok = mbar_wait(&bars->dv_done, (t - 1) & 1, wc, 33))) break;
+              if (t > 0 && !(ok = warp_wait(&bars->dv_done, (t - 1) & 1, wc, 33))) break;
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t a = sdesc_sw128(sK + (kk / 4) * T::KV_SUB + (kk % 4) * 32, 16, 1024);
                 const uint64_t b = sdesc_sw128(sQ + (kk / 4) * T::Q_SUB + (kk % 4) * 32, 16, 1024);
-                mma_f16_ss(tmem + T::S_COL, a, b, id_s, kk > 0 ? 1u : 0u);
+                mma_f16_ss_warp(tmem + T::S_COL, a, b, id_s, kk > 0 ? 1u : 0u);
               }
-              mma_commit(&bars->s_full);
+              mma_commit_warp(&bars->s_full);
               // dP^T = V dO^T (the dP region holds the previous dQ until drained)
-              if (t > 0 && !(ok = mbar_wait(&bars->dq_free, (t - 1) & 1, wc, 34))) break;
+              if (t > 0 && !(ok = warp_wait(&bars->dq_free, (t - 1) & 1, wc, 34))) break;
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t a = sdesc_sw128(sV + (kk / 4) * T::KV_SUB + (kk % 4) * 32, 16, 1024);
                 const uint64_t b = sdesc_sw128(sO + (kk / 4) * T::Q_SUB + (kk % 4) * 32, 16, 1024);
-                mma_f16_ss(tmem + T::DP_COL, a, b, id_s, kk > 0 ? 1u : 0u);
+                mma_f16_ss_warp(tmem + T::DP_COL, a, b, id_s, kk > 0 ? 1u : 0u);
               }
-              mma_commit(&bars->dp_full);
+              mma_commit_warp(&bars->dp_full);
               // dV += P^T dO (P^T from TMEM); the first tile of a sweep
               // overwrites the accumulators, so the previous sweep's
               // write-out must have read them.
-              if (first && pc > 0 && !(ok = mbar_wait(&bars->dkv_free, (pc - 1) & 1, wc, 35))) break;
-              if (!(ok = mbar_wait(&bars->p_full, t & 1, wc, 36))) break;
+              if (first && pc > 0 && !(ok = warp_wait(&bars->dkv_free, (pc - 1) & 1, wc, 35))) break;
+              if (!(ok = warp_wait(&bars->p_full, t & 1, wc, 36))) break;
               tc_fence_after();
 #pragma unroll
               for (int kk = 0; kk < T::BM / 16; ++kk) {
                 const int q = kk * 16, wg = q / T::QC;
                 const uint32_t a_t = tmem + T::S_COL + wg * T::QC + (q - wg * T::QC) / 2;
                 const uint64_t b = sdesc_sw128(sO + h * (T::DH / 64) * T::Q_SUB + kk * 2048, T::Q_SUB, 1024);
-                mma_f16_ts(tmem + T::DV_COL, a_t, b, id_kv, (first && kk == 0) ? 0u : 1u);
+                mma_f16_ts_warp(tmem + T::DV_COL, a_t, b, id_kv, (first && kk == 0) ? 0u : 1u);
               }
-              mma_commit(&bars->dv_done);
+              mma_commit_warp(&bars->dv_done);
               // dK += dS^T Q and dQ (dS^T from shared memory)
-              if (!(ok = mbar_wait(&bars->ds_full, t & 1, wc, 37))) break;
+              if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 37))) break;
               tc_fence_after();
 #pragma unroll
               for (int kk = 0; kk < T::BM / 16; ++kk) {
                 const uint64_t a = sdesc_sw128(sDS + ((kk * 16) / 64) * T::DS_SUB + (kk % 4) * 32, 16, 1024);
                 const uint64_t b = sdesc_sw128(sQ + h * (T::DH / 64) * T::Q_SUB + kk * 2048, T::Q_SUB, 1024);
-                mma_f16_ss(tmem + T::DK_COL, a, b, id_kv, (first && kk == 0) ? 0u : 1u);
+                mma_f16_ss_warp(tmem + T::DK_COL, a, b, id_kv, (first && kk == 0) ? 0u : 1u);
               }
 #pragma unroll
               for (int kk = 0; kk < T::BN / 16; ++kk) {
@@ -315,29 +316,29 @@ __global__ void __launch_bounds__(320, 1)
                   // dQ^T[h half] = K[:, h half]^T dS^T : A = K (MN-major), B = dS^T (MN-major)
                   const uint64_t a = sdesc_sw128(sK + h * 2 * T::KV_SUB + kk * 2048, T::KV_SUB, 1024);
                   const uint64_t b = sdesc_sw128(sDS + kk * 2048, T::DS_SUB, 1024);
-                  mma_f16_ss(tmem + T::DQ_COL, a, b, id_dq, kk > 0 ? 1u : 0u);
+                  mma_f16_ss_warp(tmem + T::DQ_COL, a, b, id_dq, kk > 0 ? 1u : 0u);
                 } else {
                   // dQ = dS K : A = dS (dS^T buffer read MN-major), B = K (MN-major)
                   const uint64_t a = sdesc_sw128(sDS + kk * 2048, T::DS_SUB, 1024);
                   const uint64_t b = sdesc_sw128(sK + kk * 2048, T::KV_SUB, 1024);
-                  mma_f16_ss(tmem + T::DQ_COL, a, b, id_dq, kk > 0 ? 1u : 0u);
+                  mma_f16_ss_warp(tmem + T::DQ_COL, a, b, id_dq, kk > 0 ? 1u : 0u);
                 }
               }
-              mma_commit(&bars->q_empty[st]);
-              mma_commit(&bars->ds_free);
-              mma_commit(&bars->dq_full);
+              mma_commit_warp(&bars->q_empty[st]);
+              mma_commit_warp(&bars->ds_free);
+              mma_commit_warp(&bars->dq_full);
               ++t;
             }
             if (!ok) break;
-            mma_commit(&bars->dkv_full);
+            mma_commit_warp(&bars->dkv_full);
             ++pc;
           }
           if (!ok) break;
-          mma_commit(&bars->kv_empty);
+          mma_commit_warp(&bars->kv_empty);
           ++kc;
         }
       }
-      mma_commit(&bars->mma_done);
+      mma_commit_warp(&bars->mma_done);
       bwd_drain_wait(&bars->mma_done, 0);
     }
   } else {

@@ -9,14 +9,16 @@
 // matrix unit; causal shortens the key-tile loop and masks only diagonal
 // tiles; D = 256 keeps two 128-wide accumulator halves; O is written once.
 //
-// Roles (192 threads):
+// Roles (224 threads):
 //   warps 0-3  softmax warpgroup: thread r owns query row r of the tile. It
 //              reads S from TMEM, applies the mask, updates m and l, writes
 //              P (fp16) back to TMEM, rescales O in TMEM when m moved, and
 //              runs the epilogue (O / l -> fp16, lse).
-//   warp 4     TMA producer: Q tile per work item, K/V tiles into a ring.
-//   warp 5     MMA issuer (one thread) and TMEM owner: S = Q K^T into one
-//              of two S buffers, then O += P V with P read from TMEM.
+//   warp 4     TMA producer: Q tile per work item, K tiles into a ring.
+//   warp 6     TMA producer: V tiles into their own ring.
+//   warp 5     MMA issuer (converged warp, one elected lane per MMA) and
+//              TMEM owner: S = Q K^T into one of two S buffers, then
+//              O += P V with P read from TMEM.
 //
 // The MMA of key tile j+1 (Q K^T) runs while the softmax of tile j works,
 // and P V of tile j runs while the softmax of tile j+1 works.
@@ -31,7 +33,10 @@ template <int D, bool CAUSAL>
 struct FwdTraits {
   static constexpr int BM = 128;                    // query rows per tile
   static constexpr int BN = (D == 256) ? 64 : 128;  // keys per tile
-  static constexpr int KV_STAGES = 2;
+  // K is released right after Q K^T, V only after P V (a softmax later), so
+  // the two tiles travel in separate rings, each with its own producer warp.
+  static constexpr int K_STAGES = (D == 64) ? 4 : 3;
+  static constexpr int V_STAGES = (D == 64) ? 4 : 2;
   static constexpr int Q_STAGES = (D == 256) ? 1 : 2;
   static constexpr int DSUB = D / 64;               // 64-column sub-tiles per row
   static constexpr int Q_SUB = BM * 128;            // bytes of a [BM x 64] fp16 sub-tile
@@ -49,22 +54,26 @@ struct FwdTraits {
   // shared memory layout (offsets from a 1024-byte aligned base)
   static constexpr int SM_Q = 0;
   static constexpr int SM_K = SM_Q + Q_STAGES * Q_BYTES;
-  static constexpr int SM_V = SM_K + KV_STAGES * KV_BYTES;
-  static constexpr int SM_BAR = SM_V + KV_STAGES * KV_BYTES;
+  static constexpr int SM_V = SM_K + K_STAGES * KV_BYTES;
+  static constexpr int SM_BAR = SM_V + V_STAGES * KV_BYTES;
   static constexpr int SM_BYTES = SM_BAR + 256;
   // +1024 slack for the manual alignment; never below 120 KB so that a
   // second CTA can never share the SM (each CTA takes all 512 TMEM columns).
   static constexpr int SMEM_ALLOC = (SM_BYTES + 1024 > 120 * 1024) ? SM_BYTES + 1024 : 120 * 1024;
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-  static constexpr int THREADS = 192;
-  static constexpr int PRODUCER_WARP = 4;
+  static constexpr int THREADS = 224;
+  static constexpr int PRODUCER_WARP = 4;  // Q and K
   static constexpr int MMA_WARP = 5;
+  static constexpr int V_PRODUCER_WARP = 6;
 };
+
+// Threshold (log2 units) of the lazy online-softmax rescale.
+constexpr float kRescaleLog2 = 8.0f;
 
 // Barrier slots inside the SM_BAR area.
 struct FwdBars {
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[2], v_full[2], kv_empty[2];
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2];
   uint64_t o_ready, o_free, mma_done;
   uint32_t tmem_base;
@@ -113,7 +122,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams prm) {
   using T = FwdTraits<D, CAUSAL>;
@@ -127,11 +136,14 @@ __global__ void __launch_bounds__(192, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
-      mbar_init(&bars->k_full[i], 1);
-      mbar_init(&bars->v_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], T::BM);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
     }
     mbar_init(&bars->o_ready, 1);
     mbar_init(&bars->o_free, T::BM);
@@ -160,11 +172,11 @@ __global__ void __launch_bounds__(192, 1)
   const int units = fwd_num_units<CAUSAL>(prm.heads, nqt);
 
   if (warp == T::PRODUCER_WARP) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------ producer: Q and K tiles
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_last();
       const uint64_t pol_q = l2_policy_evict_first();
-      uint32_t q_it = 0, kv_it = 0;
+      uint32_t q_it = 0, k_it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         int head, qa, qb;
@@ -181,32 +193,52 @@ __global__ void __launch_bounds__(192, 1)
           ++q_it;
           const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
           for (int j = 0; j < nkv; ++j) {
-            const int st = kv_it % T::KV_STAGES;
-            if (!(ok = mbar_wait(&bars->kv_empty[st], ((kv_it / T::KV_STAGES) & 1) ^ 1, wc, 2))) break;
-            const int row = head * N + j * T::BN;
+            const int st = k_it % T::K_STAGES;
+            if (!(ok = mbar_wait(&bars->k_empty[st], ((k_it / T::K_STAGES) & 1) ^ 1, wc, 2))) break;
             uint8_t* sk = smem + T::SM_K + st * T::KV_BYTES;
-            uint8_t* sv = smem + T::SM_V + st * T::KV_BYTES;
             mbar_arrive_expect_tx(&bars->k_full[st], T::KV_BYTES);
             for (int s = 0; s < T::DSUB; ++s)
-              tma_load_2d_hint(sk + s * T::KV_SUB, &tm_k, &bars->k_full[st], s * 64, row, pol_kv);
-            mbar_arrive_expect_tx(&bars->v_full[st], T::KV_BYTES);
-            for (int s = 0; s < T::DSUB; ++s)
-              tma_load_2d_hint(sv + s * T::KV_SUB, &tm_v, &bars->v_full[st], s * 64, row, pol_kv);
-            ++kv_it;
+              tma_load_2d_hint(sk + s * T::KV_SUB, &tm_k, &bars->k_full[st], s * 64, head * N + j * T::BN, pol_kv);
+            ++k_it;
           }
         }
       }
       // Drain: every load issued must have landed before the CTA may exit.
-      for (uint32_t i = (kv_it > T::KV_STAGES ? kv_it - T::KV_STAGES : 0); i < kv_it; ++i) {
-        drain_wait(&bars->k_full[i % T::KV_STAGES], (i / T::KV_STAGES) & 1);
-        drain_wait(&bars->v_full[i % T::KV_STAGES], (i / T::KV_STAGES) & 1);
-      }
+      for (uint32_t i = (k_it > T::K_STAGES ? k_it - T::K_STAGES : 0); i < k_it; ++i)
+        drain_wait(&bars->k_full[i % T::K_STAGES], (i / T::K_STAGES) & 1);
       for (uint32_t i = (q_it > T::Q_STAGES ? q_it - T::Q_STAGES : 0); i < q_it; ++i)
         drain_wait(&bars->q_full[i % T::Q_STAGES], (i / T::Q_STAGES) & 1);
     }
+  } else if (warp == T::V_PRODUCER_WARP) {
+    // ------------------------------------------------------ producer: V tiles
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_policy_evict_last();
+      uint32_t v_it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        int head, qa, qb;
+        fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+        for (int half = 0; ok && half < 2; ++half) {
+          const int qt = half ? qb : qa;
+          if (qt < 0) break;
+          const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+          for (int j = 0; j < nkv; ++j) {
+            const int st = v_it % T::V_STAGES;
+            if (!(ok = mbar_wait(&bars->v_empty[st], ((v_it / T::V_STAGES) & 1) ^ 1, wc, 8))) break;
+            uint8_t* sv = smem + T::SM_V + st * T::KV_BYTES;
+            mbar_arrive_expect_tx(&bars->v_full[st], T::KV_BYTES);
+            for (int s = 0; s < T::DSUB; ++s)
+              tma_load_2d_hint(sv + s * T::KV_SUB, &tm_v, &bars->v_full[st], s * 64, head * N + j * T::BN, pol_kv);
+            ++v_it;
+          }
+        }
+      }
+      for (uint32_t i = (v_it > T::V_STAGES ? v_it - T::V_STAGES : 0); i < v_it; ++i)
+        drain_wait(&bars->v_full[i % T::V_STAGES], (i / T::V_STAGES) & 1);
+    }
   } else if (warp == T::MMA_WARP) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {  // the whole warp runs the loop; one elected lane issues each MMA
       constexpr uint32_t idesc_qk = idesc_f16(128, T::BN, false, false);
       constexpr uint32_t idesc_pv = idesc_f16(128, T::OH, false, true);
       const uint32_t sbase = smem_u32(smem);
@@ -216,10 +248,10 @@ __global__ void __launch_bounds__(192, 1)
       // O += P_tile V_stage; the first tile of an item overwrites O.
       auto issue_pv = [&](uint32_t tile, uint32_t kv_idx, bool first) -> bool {
         const int b = tile & 1;
-        const int st = kv_idx % T::KV_STAGES;
-        if (first && item > 0 && !mbar_wait(&bars->o_free, (item - 1) & 1, wc, 10)) return false;
-        if (!mbar_wait(&bars->p_full[b], (tile >> 1) & 1, wc, 11)) return false;
-        if (!mbar_wait(&bars->v_full[st], (kv_idx / T::KV_STAGES) & 1, wc, 12)) return false;
+        const int st = kv_idx % T::V_STAGES;
+        if (first && item > 0 && !warp_wait(&bars->o_free, (item - 1) & 1, wc, 10)) return false;
+        if (!warp_wait(&bars->p_full[b], (tile >> 1) & 1, wc, 11)) return false;
+        if (!warp_wait(&bars->v_full[st], (kv_idx / T::V_STAGES) & 1, wc, 12)) return false;
         tc_fence_after();
         const uint32_t sv = sbase + T::SM_V + st * T::KV_BYTES;
 #pragma unroll
@@ -227,12 +259,12 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int h = 0; h < T::NOH; ++h) {
             const uint64_t bdesc = sdesc_sw128(sv + (h * 2) * T::KV_SUB + kk * 16 * 128, T::KV_SUB, 1024);
-            mma_f16_ts(tmem + T::O_COL + h * 128, tmem + T::P_COL + b * (T::BN / 2) + kk * 8, bdesc, idesc_pv,
+            mma_f16_ts_warp(tmem + T::O_COL + h * 128, tmem + T::P_COL + b * (T::BN / 2) + kk * 8, bdesc, idesc_pv,
                        (first && kk == 0) ? 0u : 1u);
           }
         }
-        mma_commit(&bars->kv_empty[st]);
-        mma_commit(&bars->o_ready);
+        mma_commit_warp(&bars->v_empty[st]);
+        mma_commit_warp(&bars->o_ready);
         return true;
       };
 
@@ -243,13 +275,13 @@ __global__ void __launch_bounds__(192, 1)
           const int qt = half ? qb : qa;
           if (qt < 0) break;
           const int qs = q_it % T::Q_STAGES;
-          if (!(ok = mbar_wait(&bars->q_full[qs], (q_it / T::Q_STAGES) & 1, wc, 3))) break;
+          if (!(ok = warp_wait(&bars->q_full[qs], (q_it / T::Q_STAGES) & 1, wc, 3))) break;
           tc_fence_after();
           const uint32_t sq = sbase + T::SM_Q + qs * T::Q_BYTES;
           const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
           for (int j = 0; j < nkv; ++j) {
-            const int st = kv_it % T::KV_STAGES;
-            if (!(ok = mbar_wait(&bars->k_full[st], (kv_it / T::KV_STAGES) & 1, wc, 4))) break;
+            const int st = kv_it % T::K_STAGES;
+            if (!(ok = warp_wait(&bars->k_full[st], (kv_it / T::K_STAGES) & 1, wc, 4))) break;
             tc_fence_after();
             const uint32_t sk = sbase + T::SM_K + st * T::KV_BYTES;
             const int b = t & 1;
@@ -257,10 +289,11 @@ __global__ void __launch_bounds__(192, 1)
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint64_t adesc = sdesc_sw128(sq + (kk / 4) * T::Q_SUB + (kk % 4) * 32, 16, 1024);
               const uint64_t bdesc = sdesc_sw128(sk + (kk / 4) * T::KV_SUB + (kk % 4) * 32, 16, 1024);
-              mma_f16_ss(tmem + T::S_COL + b * T::BN, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+              mma_f16_ss_warp(tmem + T::S_COL + b * T::BN, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
             }
-            mma_commit(&bars->s_full[b]);
-            if (j == nkv - 1) mma_commit(&bars->q_empty[qs]);
+            mma_commit_warp(&bars->s_full[b]);
+            mma_commit_warp(&bars->k_empty[st]);
+            if (j == nkv - 1) mma_commit_warp(&bars->q_empty[qs]);
             if (j > 0 && !(ok = issue_pv(t - 1, kv_it - 1, j == 1))) break;
             ++t;
             ++kv_it;
@@ -270,8 +303,8 @@ __global__ void __launch_bounds__(192, 1)
           ++item;
         }
       }
-      // Drain: all MMAs issued by this thread complete before TMEM is freed.
-      mma_commit(&bars->mma_done);
+      // Drain: all MMAs issued by this warp complete before TMEM is freed.
+      mma_commit_warp(&bars->mma_done);
       drain_wait(&bars->mma_done, 0);
     }
   } else {
@@ -316,7 +349,13 @@ __global__ void __launch_bounds__(192, 1)
           for (int c = 8; c < T::BN; ++c) pm[c & 7] = fmaxf(pm[c & 7], s[c]);
           const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                                  fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-          const float m_new = fmaxf(m, mx * sl2);
+          // The running max m only moves when this tile's max exceeds it by
+          // more than kRescaleLog2: below that the stale m keeps every P value
+          // under 2^kRescaleLog2 (exact range for fp16 P and fp32 l), so O and
+          // l need no rescaling.  O / l and lse use the max actually applied,
+          // which gives the same result as always tracking the exact max.
+          const float m_tile = mx * sl2;
+          const float m_new = (m_tile > m + kRescaleLog2) ? m_tile : m;
           const float neg = -m_new;
           float ps[8];
 #pragma unroll
