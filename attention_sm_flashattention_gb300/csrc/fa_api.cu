@@ -79,15 +79,22 @@ struct BwdWorkspace {
   int grid;
 };
 
+// D <= 128 needs only Delta and lse2 (the dQ kernel owns its tiles); D = 256
+// also needs one fp32 N x D dQ accumulator per persistent CTA.
 BwdWorkspace bwd_workspace_layout(int Z, int H, int N, int D, int sms) {
   BwdWorkspace w{};
   const long long heads = static_cast<long long>(Z) * H;
   const size_t vec = round_up(static_cast<size_t>(heads) * N * sizeof(float), 256);
-  w.grid = static_cast<int>(heads < sms ? heads : sms);
   w.delta_off = 0;
   w.lse2_off = vec;
   w.dq_off = 2 * vec;
-  w.total = 2 * vec + round_up(static_cast<size_t>(w.grid) * N * D * sizeof(float), 256);
+  if (D == 256) {
+    w.grid = static_cast<int>(heads < sms ? heads : sms);
+    w.total = 2 * vec + round_up(static_cast<size_t>(w.grid) * N * D * sizeof(float), 256);
+  } else {
+    w.grid = sms;
+    w.total = 2 * vec;
+  }
   return w;
 }
 
@@ -267,15 +274,20 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   DevInfo* dev = nullptr;
   if ((rc = current_device_info(&dev)) != FA_OK) return rc;
 
-  // Scratch layout [delta | lse2 | grid dQ accumulators], as fa_bwd's
-  // workspace, with the grid cut to the accumulators that fit.
+  // Scratch layout [delta | lse2 | dQ accumulators], as fa_bwd's workspace;
+  // for D = 256 the grid is cut to the accumulators that fit.
   const long long heads = static_cast<long long>(Z) * H;
   const size_t vec = round_up(static_cast<size_t>(heads) * N * sizeof(float), 256);
-  const size_t acc_one = round_up(static_cast<size_t>(N) * D * sizeof(float), 256);
-  if (2 * vec + acc_one > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
-  long long grid = static_cast<long long>((FA_NOALLOC_SCRATCH_BYTES - 2 * vec) / (static_cast<size_t>(N) * D * sizeof(float)));
-  if (grid > dev->sms) grid = dev->sms;
-  if (grid > heads) grid = heads;
+  long long grid = dev->sms;
+  if (D == 256) {
+    const size_t acc_one = round_up(static_cast<size_t>(N) * D * sizeof(float), 256);
+    if (2 * vec + acc_one > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+    grid = static_cast<long long>((FA_NOALLOC_SCRATCH_BYTES - 2 * vec) / (static_cast<size_t>(N) * D * sizeof(float)));
+    if (grid > dev->sms) grid = dev->sms;
+    if (grid > heads) grid = heads;
+  } else if (2 * vec > FA_NOALLOC_SCRATCH_BYTES) {
+    return FA_ERR_SCRATCH_LIMIT;
+  }
 
   char* scratch = static_cast<char*>(noalloc_scratch_on_current_device());
   if (scratch == nullptr) return FA_ERR_CUDA;

@@ -1,0 +1,762 @@
+// FlashAttention backward for D = 64 and D = 128 on sm_103a: two persistent
+// kernels, each gradient tile written by exactly one CTA, no atomics and no
+// accumulator in global memory.
+//
+// Source: «把 FlashAttention 搬上昇腾：Triton-Ascend CV Pipeline 优化实战»,
+// §二 -- the backward equations (Delta = rowsum(O * dO), P recomputed from
+// the saved log-sum-exp, dP = dO V^T, dS = scale * P * (dP - Delta),
+// dQ = dS K, dK = dS^T Q, dV = P^T dO) and the rules "recompute P, never
+// store it", "one writer per gradient tile", "scratch does not grow with N^2
+// over all heads"; §七 (D128: dK and dV fused into one sweep over the query
+// tiles).
+//
+//  fa_bwd_dkdv_kernel: one work unit per (head, key tile j).  K_j and V_j stay
+//    in shared memory; the query tiles i stream through a two-stage ring
+//    (Q_i, dO_i, and the tile's lse2 and Delta).  Per tile, with M = keys:
+//      S^T  = K_j Q_i^T                 -> TMEM
+//      P^T  = exp2(S^T * c - lse2)      -> fp16, shared memory
+//      dP^T = V_j dO_i^T                -> TMEM
+//      dS^T = P^T * (dP^T - Delta)      -> fp16, TMEM (over dP^T)
+//      dV_j += P^T dO_i                 (A from shared memory)
+//      dK_j += dS^T Q_i                 (A from TMEM)
+//    and dK_j (times scale), dV_j are written once at the end of the unit.
+//  fa_bwd_dq_kernel: one work unit per (head, query tile i).  Q_i and dO_i
+//    stay in shared memory; K_j and V_j stream through separate rings.  Per
+//    tile, with M = queries: S = Q_i K_j^T (double-buffered in TMEM),
+//    P = exp2(S * c - lse2_i), dP = dO_i V_j^T, dS = P * (dP - Delta_i)
+//    (fp16 into TMEM over dP), dQ_i += dS K_j (A from TMEM); dQ_i (times
+//    scale) is written once at the end of the unit.
+//
+// The second kernel recomputes S and dP (7 GEMMs instead of 5) in exchange
+// for having no cross-tile reduction at all.  Scale is applied to dK and dQ
+// at write-out (dS is kept as P * (dP - Delta) in fp16).
+#pragma once
+
+#include "fa_kernels.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+template <int D>
+struct Bwd2Traits {
+  static_assert(D == 64 || D == 128, "two-kernel backward covers D = 64 and 128");
+  static constexpr int BM = 128;  // queries per tile
+  static constexpr int BN = 128;  // keys per tile
+  static constexpr int DSUB = D / 64;
+  static constexpr int SUB = 128 * 128;    // bytes of a [128 x 64] fp16 sub-tile
+  static constexpr int TILE = 128 * D * 2; // bytes of a [128 x D] fp16 tile
+  static constexpr int QC = 64;            // columns per compute warpgroup
+  static constexpr int MIN_SMEM = 120 * 1024;  // keeps one CTA per SM (512 TMEM columns each)
+
+  // ---- dK/dV kernel
+  static constexpr int A_DV = 0, A_DK = D, A_S = 2 * D, A_DP = 2 * D + BM;
+  static constexpr int A_SM_K = 0, A_SM_V = TILE, A_SM_Q = 2 * TILE, A_SM_DO = 4 * TILE, A_SM_PT = 6 * TILE;
+  static constexpr int A_SM_LD = A_SM_PT + BN * BM * 2;  // 2 stages x (lse2[128], delta[128]) fp32
+  static constexpr int A_SM_BAR = A_SM_LD + 2 * 1024;
+  static constexpr int A_SM_BYTES = A_SM_BAR + 256;
+  static constexpr int A_SMEM = A_SM_BYTES > MIN_SMEM ? A_SM_BYTES : MIN_SMEM;
+  static_assert(A_SMEM <= 232448, "dK/dV kernel shared memory budget");
+  static_assert(A_DP + BM <= 512, "dK/dV kernel TMEM budget");
+
+  // ---- dQ kernel
+  static constexpr int B_K_STAGES = (D == 64) ? 4 : 3;
+  static constexpr int B_V_STAGES = (D == 64) ? 4 : 2;
+  static constexpr int B_DQ = 0, B_S = D, B_DP = D + 2 * BN;
+  static constexpr int B_SM_Q = 0, B_SM_DO = TILE, B_SM_K = 2 * TILE;
+  static constexpr int B_SM_V = B_SM_K + B_K_STAGES * TILE;
+  static constexpr int B_SM_BAR = B_SM_V + B_V_STAGES * TILE;
+  static constexpr int B_SM_BYTES = B_SM_BAR + 256;
+  static constexpr int B_SMEM = B_SM_BYTES > MIN_SMEM ? B_SM_BYTES : MIN_SMEM;
+  static_assert(B_SMEM <= 232448, "dQ kernel shared memory budget");
+  static_assert(B_DP + BN <= 512, "dQ kernel TMEM budget");
+};
+
+// Work units of the two kernels.  Non-causal: one unit per (head, tile),
+// head-major.  Causal: tiles t and n-1-t of a head form one unit so that all
+// units cost the same number of tile pairs (n + 1).
+template <bool CAUSAL>
+__device__ __forceinline__ int bwd2_units(int heads, int ntiles) {
+  return CAUSAL ? heads * ((ntiles + 1) / 2) : heads * ntiles;
+}
+
+template <bool CAUSAL>
+__device__ __forceinline__ void bwd2_decode(int u, int ntiles, int& head, int& ta, int& tb) {
+  if (CAUSAL) {
+    const int npair = (ntiles + 1) / 2;
+    head = u / npair;
+    const int p = u - head * npair;
+    ta = ntiles - 1 - p;
+    tb = (p != ta) ? p : -1;
+  } else {
+    head = u / ntiles;
+    ta = u - head * ntiles;
+    tb = -1;
+  }
+}
+
+__device__ __forceinline__ void bwd2_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_test(a, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Site code reported when the dynamic shared memory base is not 1024-byte
+// aligned (the 128-byte-swizzled tiles need it); the kernel then does nothing.
+constexpr int kSiteSmemAlign = 99;
+
+// ===================================================================== dK, dV
+
+struct DkdvBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full, s_free, dp_full, p_full, dv_done, ds_full, dk_done;
+  uint64_t dkv_full, dkv_free, mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(DkdvBars) <= 256, "barrier area");
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdParams prm) {
+  using T = Bwd2Traits<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) record_timeout(prm.status, kSiteSmemAlign);
+    return;
+  }
+  DkdvBars* bars = reinterpret_cast<DkdvBars*>(smem + T::A_SM_BAR);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, NCOMPUTE = 256;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, NCOMPUTE);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_full, NCOMPUTE);
+    mbar_init(&bars->dv_done, 1);
+    mbar_init(&bars->ds_full, NCOMPUTE);
+    mbar_init(&bars->dk_done, 1);
+    mbar_init(&bars->dkv_full, 1);
+    mbar_init(&bars->dkv_free, NCOMPUTE);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const WaitCtx wc{prm.status, &bars->abort_flag};
+  const uint32_t tmem = bars->tmem_base;
+  const int N = prm.N;
+  const int nqt = N / T::BM, nkv = N / T::BN;
+  const int units = bwd2_units<CAUSAL>(prm.heads, nkv);
+
+  if (warp == PRODUCER_WARP) {
+    // --------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol_q = l2_policy_evict_last();
+      const uint64_t pol_kv = l2_policy_evict_first();
+      uint32_t t = 0, kc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        int head, ja, jb;
+        bwd2_decode<CAUSAL>(u, nkv, head, ja, jb);
+        for (int half = 0; ok && half < 2; ++half) {
+          const int j = half ? jb : ja;
+          if (j < 0) break;
+          if (!(ok = mbar_wait(&bars->kv_empty, (kc & 1) ^ 1, wc, 51))) break;
+          mbar_arrive_expect_tx(&bars->kv_full, 2 * T::TILE);
+          for (int s = 0; s < T::DSUB; ++s) {
+            tma_load_2d_hint(smem + T::A_SM_K + s * T::SUB, &tm_k, &bars->kv_full, s * 64, head * N + j * T::BN, pol_kv);
+            tma_load_2d_hint(smem + T::A_SM_V + s * T::SUB, &tm_v, &bars->kv_full, s * 64, head * N + j * T::BN, pol_kv);
+          }
+          ++kc;
+          for (int i = CAUSAL ? j : 0; i < nqt; ++i) {
+            const int st = t & 1;
+            if (!(ok = mbar_wait(&bars->q_empty[st], ((t >> 1) & 1) ^ 1, wc, 52))) break;
+            mbar_arrive_expect_tx(&bars->q_full[st], 2 * T::TILE + 1024);
+            const int row = head * N + i * T::BM;
+            for (int s = 0; s < T::DSUB; ++s) {
+              tma_load_2d_hint(smem + T::A_SM_Q + st * T::TILE + s * T::SUB, &tm_q, &bars->q_full[st], s * 64, row, pol_q);
+              tma_load_2d_hint(smem + T::A_SM_DO + st * T::TILE + s * T::SUB, &tm_do, &bars->q_full[st], s * 64, row,
+                               pol_q);
+            }
+            bulk_load(smem + T::A_SM_LD + st * 1024, prm.lse2 + row, 512, &bars->q_full[st]);
+            bulk_load(smem + T::A_SM_LD + st * 1024 + 512, prm.delta + row, 512, &bars->q_full[st]);
+            ++t;
+          }
+        }
+      }
+      if (kc > 0) bwd2_drain(&bars->kv_full, (kc - 1) & 1);
+      for (uint32_t i = (t > 2 ? t - 2 : 0); i < t; ++i) bwd2_drain(&bars->q_full[i & 1], (i >> 1) & 1);
+    }
+  } else if (warp == MMA_WARP) {
+    // ----------------------------------------------------- MMA issuer (warp)
+    constexpr uint32_t id_s = idesc_f16(128, T::BM, false, false);  // S^T, dP^T: M keys, N queries
+    constexpr uint32_t id_g = idesc_f16(128, D, false, true);       // dV, dK: N = D, B MN-major
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t sK = sb + T::A_SM_K, sV = sb + T::A_SM_V, sPT = sb + T::A_SM_PT;
+    uint32_t t = 0, kc = 0;
+    bool ok = true;
+    auto issue_s = [&](uint32_t tile) {
+      const uint32_t sQ = sb + T::A_SM_Q + (tile & 1) * T::TILE;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t a = sdesc_sw128(sK + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
+        const uint64_t b = sdesc_sw128(sQ + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
+        mma_f16_ss_warp(tmem + T::A_S, a, b, id_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_warp(&bars->s_full);
+    };
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      int head, ja, jb;
+      bwd2_decode<CAUSAL>(u, nkv, head, ja, jb);
+      for (int half = 0; ok && half < 2; ++half) {
+        const int j = half ? jb : ja;
+        if (j < 0) break;
+        const int i0 = CAUSAL ? j : 0;
+        if (!(ok = warp_wait(&bars->kv_full, kc & 1, wc, 61))) break;
+        tc_fence_after();
+        // first S^T of the unit (the S region is free once the previous tile's
+        // S^T was read)
+        if (!(ok = warp_wait(&bars->q_full[t & 1], (t >> 1) & 1, wc, 62))) break;
+        if (t > 0 && !(ok = warp_wait(&bars->s_free, (t - 1) & 1, wc, 63))) break;
+        tc_fence_after();
+        issue_s(t);
+        for (int i = i0; i < nqt; ++i) {
+          const bool first = (i == i0), last = (i == nqt - 1);
+          const int st = t & 1;
+          const uint32_t sQ = sb + T::A_SM_Q + st * T::TILE;
+          const uint32_t sO = sb + T::A_SM_DO + st * T::TILE;
+          // dP^T = V dO^T; the dP region holds dS^T of the previous tile until
+          // that tile's dK MMA has read it
+          if (t > 0 && !(ok = warp_wait(&bars->dk_done, (t - 1) & 1, wc, 64))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = sdesc_sw128(sV + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
+            const uint64_t b = sdesc_sw128(sO + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
+            mma_f16_ss_warp(tmem + T::A_DP, a, b, id_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_warp(&bars->dp_full);
+          if (last) mma_commit_warp(&bars->kv_empty);  // K_j, V_j are not read again
+          // next S^T as soon as this tile's S^T has been read
+          if (!last) {
+            if (!(ok = warp_wait(&bars->q_full[(t + 1) & 1], ((t + 1) >> 1) & 1, wc, 65))) break;
+            if (!(ok = warp_wait(&bars->s_free, t & 1, wc, 66))) break;
+            tc_fence_after();
+            issue_s(t + 1);
+          }
+          // dV += P^T dO (P^T in shared memory); the first tile of a unit
+          // overwrites the accumulators, which the previous unit's write-out
+          // must have read
+          if (first && kc > 0 && !(ok = warp_wait(&bars->dkv_free, (kc - 1) & 1, wc, 67))) break;
+          if (!(ok = warp_wait(&bars->p_full, t & 1, wc, 68))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < T::BM / 16; ++kk) {
+            const uint64_t a = sdesc_sw128(sPT + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
+            const uint64_t b = sdesc_sw128(sO + kk * 2048, T::SUB, 1024);
+            mma_f16_ss_warp(tmem + T::A_DV, a, b, id_g, (first && kk == 0) ? 0u : 1u);
+          }
+          mma_commit_warp(&bars->dv_done);
+          // dK += dS^T Q (dS^T in TMEM over dP^T)
+          if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 69))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < T::BM / 16; ++kk) {
+            const uint32_t a_t = tmem + T::A_DP + (kk / 4) * T::QC + (kk % 4) * 8;
+            const uint64_t b = sdesc_sw128(sQ + kk * 2048, T::SUB, 1024);
+            mma_f16_ts_warp(tmem + T::A_DK, a_t, b, id_g, (first && kk == 0) ? 0u : 1u);
+          }
+          mma_commit_warp(&bars->dk_done);
+          mma_commit_warp(&bars->q_empty[st]);
+          if (last) mma_commit_warp(&bars->dkv_full);
+          ++t;
+        }
+        ++kc;
+      }
+    }
+    mma_commit_warp(&bars->mma_done);
+    bwd2_drain(&bars->mma_done, 0);
+  } else {
+    // ------------------------------------------------------------ compute
+    const int wg = warp >> 2, quad = warp & 3;
+    const int row = quad * 32 + lane;  // TMEM lane = key row of the tile
+    const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const float sl2 = prm.scale_log2;
+    const uint32_t sPT = smem_u32(smem + T::A_SM_PT);
+    uint32_t t = 0, kc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      int head, ja, jb;
+      bwd2_decode<CAUSAL>(u, nkv, head, ja, jb);
+      for (int half = 0; ok && half < 2; ++half) {
+        const int j = half ? jb : ja;
+        if (j < 0) break;
+        const int key = j * T::BN + row;
+        for (int i = CAUSAL ? j : 0; i < nqt; ++i) {
+          const int st = t & 1;
+          const int q0 = i * T::BM + wg * T::QC;
+          // ---- P^T = exp2(S^T * c - lse2), fp16 into shared memory
+          ok = mbar_wait(&bars->q_full[st], (t >> 1) & 1, wc, 71) && mbar_wait(&bars->s_full, t & 1, wc, 72);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t sr[T::QC];
+          tmem_ld32(lb + T::A_S + wg * T::QC, sr);
+          tmem_ld32(lb + T::A_S + wg * T::QC + 32, sr + 32);
+          tmem_wait_ld();
+          reg_fence<T::QC>(sr);
+          tc_fence_before();
+          mbar_arrive(&bars->s_free);
+          const float4* l4 = reinterpret_cast<const float4*>(smem + T::A_SM_LD + st * 1024) + wg * (T::QC / 4);
+          float p[T::QC];
+#pragma unroll
+          for (int c = 0; c < T::QC; c += 4) {
+            const float4 L = l4[c / 4];
+            p[c + 0] = ex2_approx(fmaf(__uint_as_float(sr[c + 0]), sl2, -L.x));
+            p[c + 1] = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -L.y));
+            p[c + 2] = ex2_approx(fmaf(__uint_as_float(sr[c + 2]), sl2, -L.z));
+            p[c + 3] = ex2_approx(fmaf(__uint_as_float(sr[c + 3]), sl2, -L.w));
+          }
+          if (CAUSAL && i == j) {
+#pragma unroll
+            for (int c = 0; c < T::QC; ++c)
+              if (key > q0 + c) p[c] = 0.f;
+          }
+          if (t > 0) {  // the P^T buffer is free once the previous tile's dV read it
+            ok = mbar_wait(&bars->dv_done, (t - 1) & 1, wc, 73);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          }
+#pragma unroll
+          for (int c = 0; c < T::QC; c += 8) {
+            const uint32_t addr = sPT + wg * T::SUB + row * 128 + (((c / 8) ^ (row & 7)) * 16);
+            st_shared_v4(addr, pack_half2(p[c], p[c + 1]), pack_half2(p[c + 2], p[c + 3]),
+                         pack_half2(p[c + 4], p[c + 5]), pack_half2(p[c + 6], p[c + 7]));
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&bars->p_full);
+          // ---- dS^T = P^T * (dP^T - Delta), fp16 into TMEM over dP^T
+          ok = mbar_wait(&bars->dp_full, t & 1, wc, 74);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          tmem_ld32(lb + T::A_DP + wg * T::QC, sr);
+          tmem_ld32(lb + T::A_DP + wg * T::QC + 32, sr + 32);
+          tmem_wait_ld();
+          reg_fence<T::QC>(sr);
+          const float4* d4 = reinterpret_cast<const float4*>(smem + T::A_SM_LD + st * 1024 + 512) + wg * (T::QC / 4);
+          uint32_t pk[T::QC / 2];
+#pragma unroll
+          for (int c = 0; c < T::QC; c += 4) {
+            const float4 Dl = d4[c / 4];
+            pk[c / 2] = pack_half2(p[c] * (__uint_as_float(sr[c]) - Dl.x), p[c + 1] * (__uint_as_float(sr[c + 1]) - Dl.y));
+            pk[c / 2 + 1] =
+                pack_half2(p[c + 2] * (__uint_as_float(sr[c + 2]) - Dl.z), p[c + 3] * (__uint_as_float(sr[c + 3]) - Dl.w));
+          }
+          tmem_st32(lb + T::A_DP + wg * T::QC, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bars->ds_full);
+          ++t;
+        }
+        if (!ok) break;
+        // ---- write dV_j and dK_j (times scale) once
+        ok = mbar_wait(&bars->dkv_full, kc & 1, wc, 75);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        const size_t orow = (static_cast<size_t>(head) * N + key) * D + wg * (D / 2);
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t col = (which == 0 ? T::A_DV : T::A_DK) + wg * (D / 2);
+          const float mul = which == 0 ? 1.f : prm.scale;
+          __half* out = (which == 0 ? prm.dv : prm.dk) + orow;
+#pragma unroll
+          for (int c = 0; c < D / 2; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(lb + col + c, v);
+            tmem_wait_ld();
+            reg_fence<32>(v);
+            uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_uint4(pack_half2(__uint_as_float(v[8 * e]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
+                                  pack_half2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
+                                  pack_half2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
+                                  pack_half2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->dkv_free);
+        ++kc;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ========================================================================= dQ
+
+struct DqBars {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], s_free[2];
+  uint64_t dp_full, ds_full, dq_done, dq_full, dq_free, mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(DqBars) <= 256, "barrier area");
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(352, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdParams prm) {
+  using T = Bwd2Traits<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) record_timeout(prm.status, kSiteSmemAlign);
+    return;
+  }
+  DqBars* bars = reinterpret_cast<DqBars*>(smem + T::B_SM_BAR);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, V_PRODUCER_WARP = 10, NCOMPUTE = 256;
+  constexpr int KS = T::B_K_STAGES, VS = T::B_V_STAGES;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_free[i], NCOMPUTE);
+    }
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->ds_full, NCOMPUTE);
+    mbar_init(&bars->dq_done, 1);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, NCOMPUTE);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const WaitCtx wc{prm.status, &bars->abort_flag};
+  const uint32_t tmem = bars->tmem_base;
+  const int N = prm.N;
+  const int nqt = N / T::BM, nkv = N / T::BN;
+  const int units = bwd2_units<CAUSAL>(prm.heads, nqt);
+  auto num_kv = [&](int i) { return CAUSAL ? i + 1 : nkv; };
+
+  if (warp == PRODUCER_WARP) {
+    // ------------------------------------------------ producer: Q, dO and K
+    if (lane == 0) {
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      uint32_t qc = 0, k_it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        int head, ia, ib;
+        bwd2_decode<CAUSAL>(u, nqt, head, ia, ib);
+        for (int half = 0; ok && half < 2; ++half) {
+          const int i = half ? ib : ia;
+          if (i < 0) break;
+          if (!(ok = mbar_wait(&bars->q_empty, (qc & 1) ^ 1, wc, 81))) break;
+          mbar_arrive_expect_tx(&bars->q_full, 2 * T::TILE);
+          for (int s = 0; s < T::DSUB; ++s) {
+            tma_load_2d_hint(smem + T::B_SM_Q + s * T::SUB, &tm_q, &bars->q_full, s * 64, head * N + i * T::BM, pol_q);
+            tma_load_2d_hint(smem + T::B_SM_DO + s * T::SUB, &tm_do, &bars->q_full, s * 64, head * N + i * T::BM, pol_q);
+          }
+          ++qc;
+          for (int j = 0; j < num_kv(i); ++j) {
+            const int ks = k_it % KS;
+            if (!(ok = mbar_wait(&bars->k_empty[ks], ((k_it / KS) & 1) ^ 1, wc, 82))) break;
+            mbar_arrive_expect_tx(&bars->k_full[ks], T::TILE);
+            for (int s = 0; s < T::DSUB; ++s)
+              tma_load_2d_hint(smem + T::B_SM_K + ks * T::TILE + s * T::SUB, &tm_k, &bars->k_full[ks], s * 64,
+                               head * N + j * T::BN, pol_kv);
+            ++k_it;
+          }
+        }
+      }
+      if (qc > 0) bwd2_drain(&bars->q_full, (qc - 1) & 1);
+      for (uint32_t i = (k_it > KS ? k_it - KS : 0); i < k_it; ++i) bwd2_drain(&bars->k_full[i % KS], (i / KS) & 1);
+    }
+  } else if (warp == V_PRODUCER_WARP) {
+    // --------------------------------------------------------- producer: V
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_policy_evict_last();
+      uint32_t v_it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        int head, ia, ib;
+        bwd2_decode<CAUSAL>(u, nqt, head, ia, ib);
+        for (int half = 0; ok && half < 2; ++half) {
+          const int i = half ? ib : ia;
+          if (i < 0) break;
+          for (int j = 0; j < num_kv(i); ++j) {
+            const int vs = v_it % VS;
+            if (!(ok = mbar_wait(&bars->v_empty[vs], ((v_it / VS) & 1) ^ 1, wc, 83))) break;
+            mbar_arrive_expect_tx(&bars->v_full[vs], T::TILE);
+            for (int s = 0; s < T::DSUB; ++s)
+              tma_load_2d_hint(smem + T::B_SM_V + vs * T::TILE + s * T::SUB, &tm_v, &bars->v_full[vs], s * 64,
+                               head * N + j * T::BN, pol_kv);
+            ++v_it;
+          }
+        }
+      }
+      for (uint32_t i = (v_it > VS ? v_it - VS : 0); i < v_it; ++i) bwd2_drain(&bars->v_full[i % VS], (i / VS) & 1);
+    }
+  } else if (warp == MMA_WARP) {
+    // ----------------------------------------------------- MMA issuer (warp)
+    constexpr uint32_t id_s = idesc_f16(128, T::BN, false, false);  // S, dP: M queries, N keys
+    constexpr uint32_t id_q = idesc_f16(128, D, false, true);       // dQ: N = D, B = K MN-major
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t sQ = sb + T::B_SM_Q, sO = sb + T::B_SM_DO;
+    uint32_t t = 0, k_it = 0, v_it = 0, qc = 0;
+    bool ok = true;
+    // S(tile) = Q K^T into S buffer tile & 1, from K stage `ks`
+    auto issue_s = [&](uint32_t tile, uint32_t kidx) -> bool {
+      const int b = tile & 1, ks = kidx % KS;
+      if (!warp_wait(&bars->k_full[ks], (kidx / KS) & 1, wc, 91)) return false;
+      if (tile >= 2 && !warp_wait(&bars->s_free[b], ((tile - 2) >> 1) & 1, wc, 92)) return false;
+      tc_fence_after();
+      const uint32_t sK = sb + T::B_SM_K + ks * T::TILE;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t a = sdesc_sw128(sQ + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(sK + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
+        mma_f16_ss_warp(tmem + T::B_S + b * T::BN, a, bd, id_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_warp(&bars->s_full[b]);
+      return true;
+    };
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      int head, ia, ib;
+      bwd2_decode<CAUSAL>(u, nqt, head, ia, ib);
+      for (int half = 0; ok && half < 2; ++half) {
+        const int i = half ? ib : ia;
+        if (i < 0) break;
+        const int nj = num_kv(i);
+        if (!(ok = warp_wait(&bars->q_full, qc & 1, wc, 93))) break;
+        tc_fence_after();
+        if (!(ok = issue_s(t, k_it))) break;
+        for (int j = 0; j < nj; ++j) {
+          const bool first = (j == 0), last = (j == nj - 1);
+          const int ks = k_it % KS, vs = v_it % VS;
+          // dP = dO V^T; the dP region holds dS of the previous tile until that
+          // tile's dQ MMA has read it
+          if (!(ok = warp_wait(&bars->v_full[vs], (v_it / VS) & 1, wc, 94))) break;
+          if (t > 0 && !(ok = warp_wait(&bars->dq_done, (t - 1) & 1, wc, 95))) break;
+          tc_fence_after();
+          const uint32_t sV = sb + T::B_SM_V + vs * T::TILE;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = sdesc_sw128(sO + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sV + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
+            mma_f16_ss_warp(tmem + T::B_DP, a, bd, id_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_warp(&bars->dp_full);
+          mma_commit_warp(&bars->v_empty[vs]);
+          if (last) mma_commit_warp(&bars->q_empty);  // Q_i, dO_i are not read again
+          // next S while the compute warps work on this tile
+          if (!last && !(ok = issue_s(t + 1, k_it + 1))) break;
+          // dQ += dS K (dS in TMEM over dP); the first tile overwrites dQ, which
+          // the previous unit's write-out must have read
+          if (first && qc > 0 && !(ok = warp_wait(&bars->dq_free, (qc - 1) & 1, wc, 96))) break;
+          if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 97))) break;
+          tc_fence_after();
+          const uint32_t sK = sb + T::B_SM_K + ks * T::TILE;
+#pragma unroll
+          for (int kk = 0; kk < T::BN / 16; ++kk) {
+            const uint32_t a_t = tmem + T::B_DP + (kk / 4) * T::QC + (kk % 4) * 8;
+            const uint64_t bd = sdesc_sw128(sK + kk * 2048, T::SUB, 1024);
+            mma_f16_ts_warp(tmem + T::B_DQ, a_t, bd, id_q, (first && kk == 0) ? 0u : 1u);
+          }
+          mma_commit_warp(&bars->dq_done);
+          mma_commit_warp(&bars->k_empty[ks]);
+          if (last) mma_commit_warp(&bars->dq_full);
+          ++t;
+          ++k_it;
+          ++v_it;
+        }
+        ++qc;
+      }
+    }
+    mma_commit_warp(&bars->mma_done);
+    bwd2_drain(&bars->mma_done, 0);
+  } else {
+    // ------------------------------------------------------------ compute
+    const int wg = warp >> 2, quad = warp & 3;
+    const int row = quad * 32 + lane;  // TMEM lane = query row of the tile
+    const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const float sl2 = prm.scale_log2;
+    uint32_t t = 0, qc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      int head, ia, ib;
+      bwd2_decode<CAUSAL>(u, nqt, head, ia, ib);
+      for (int half = 0; ok && half < 2; ++half) {
+        const int i = half ? ib : ia;
+        if (i < 0) break;
+        const int query = i * T::BM + row;
+        const size_t grow = static_cast<size_t>(head) * N + query;
+        const float lse2 = __ldg(prm.lse2 + grow);
+        const float delta = __ldg(prm.delta + grow);
+        for (int j = 0; j < num_kv(i); ++j) {
+          const int b = t & 1;
+          const int k0 = j * T::BN + wg * T::QC;  // first key column of this warpgroup
+          // ---- P = exp2(S * c - lse2)
+          ok = mbar_wait(&bars->s_full[b], (t >> 1) & 1, wc, 101);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t sr[T::QC];
+          tmem_ld32(lb + T::B_S + b * T::BN + wg * T::QC, sr);
+          tmem_ld32(lb + T::B_S + b * T::BN + wg * T::QC + 32, sr + 32);
+          tmem_wait_ld();
+          reg_fence<T::QC>(sr);
+          tc_fence_before();
+          mbar_arrive(&bars->s_free[b]);
+          float p[T::QC];
+#pragma unroll
+          for (int c = 0; c < T::QC; ++c) p[c] = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
+          if (CAUSAL && j == i) {
+#pragma unroll
+            for (int c = 0; c < T::QC; ++c)
+              if (k0 + c > query) p[c] = 0.f;
+          }
+          // ---- dS = P * (dP - Delta), fp16 into TMEM over dP
+          ok = mbar_wait(&bars->dp_full, t & 1, wc, 102);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          tmem_ld32(lb + T::B_DP + wg * T::QC, sr);
+          tmem_ld32(lb + T::B_DP + wg * T::QC + 32, sr + 32);
+          tmem_wait_ld();
+          reg_fence<T::QC>(sr);
+          uint32_t pk[T::QC / 2];
+#pragma unroll
+          for (int c = 0; c < T::QC; c += 2)
+            pk[c / 2] = pack_half2(p[c] * (__uint_as_float(sr[c]) - delta), p[c + 1] * (__uint_as_float(sr[c + 1]) - delta));
+          tmem_st32(lb + T::B_DP + wg * T::QC, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bars->ds_full);
+          ++t;
+        }
+        if (!ok) break;
+        // ---- write dQ_i (times scale) once
+        ok = mbar_wait(&bars->dq_full, qc & 1, wc, 103);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        __half* out = prm.dq + grow * D + wg * (D / 2);
+#pragma unroll
+        for (int c = 0; c < D / 2; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(lb + T::B_DQ + wg * (D / 2) + c, v);
+          tmem_wait_ld();
+          reg_fence<32>(v);
+          const float sc = prm.scale;
+          uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(pack_half2(__uint_as_float(v[8 * e]) * sc, __uint_as_float(v[8 * e + 1]) * sc),
+                                pack_half2(__uint_as_float(v[8 * e + 2]) * sc, __uint_as_float(v[8 * e + 3]) * sc),
+                                pack_half2(__uint_as_float(v[8 * e + 4]) * sc, __uint_as_float(v[8 * e + 5]) * sc),
+                                pack_half2(__uint_as_float(v[8 * e + 6]) * sc, __uint_as_float(v[8 * e + 7]) * sc));
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->dq_free);
+        ++qc;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Delta/lse2 preprocess, then the dK/dV and dQ kernels on the same stream.
+// `max_ctas` caps each persistent grid (normally the SM count).
+template <int D, bool CAUSAL>
+int launch_bwd2(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, cudaStream_t stream) {
+  using T = Bwd2Traits<D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::A_SMEM) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(fa_bwd_dq_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::B_SMEM) !=
+            cudaSuccess)
+      return -1;
+    attr_set = true;
+  }
+  const int rows = prm.heads * prm.N;
+  constexpr int RPB = 256 / (D / 8);
+  fa_bwd_prep_kernel<D><<<(rows + RPB - 1) / RPB, 256, 0, stream>>>(prm.o, prm.dout, prm.lse, prm.delta, prm.lse2,
+                                                                     rows);
+  if (cudaGetLastError() != cudaSuccess) return -1;
+  const int nt = prm.N / 128;
+  const int units = CAUSAL ? prm.heads * ((nt + 1) / 2) : prm.heads * nt;
+  const int grid = units < max_ctas ? units : max_ctas;
+  fa_bwd_dkdv_kernel<D, CAUSAL><<<grid, 320, T::A_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  if (cudaGetLastError() != cudaSuccess) return -1;
+  fa_bwd_dq_kernel<D, CAUSAL><<<grid, 352, T::B_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace fa

@@ -28,7 +28,7 @@ struct BwdParams {
   __half* dv;
   float* delta;        // workspace [heads, N]: rowsum(O * dO)
   float* lse2;         // workspace [heads, N]: lse * log2(e)
-  float* dq_acc;       // workspace [grid, N, D]: per-CTA fp32 dQ accumulator
+  float* dq_acc;       // workspace [grid, N, D]: per-CTA fp32 dQ accumulator (D = 256 only)
   int heads;
   int N;
   float scale;         // softmax scale
@@ -36,7 +36,10 @@ struct BwdParams {
   int* status;
 };
 
-// One launcher per (D, causal) instantiation; return 0 on success.
+// One launcher per (D, causal) instantiation; return 0 on success.  For the
+// backward, `grid` caps the persistent grid: for D = 256 it is the number of
+// per-CTA dQ accumulators in the workspace, for D <= 128 (no accumulators)
+// the SM count.
 #define FA_DECLARE_LAUNCHERS(D)                                                                      \
   int launch_fwd_d##D(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, \
                       const FwdParams& prm, int num_sms, cudaStream_t stream);                        \
