@@ -22,10 +22,12 @@
 //    and dK_j (times scale), dV_j are written once at the end of the unit.
 //  fa_bwd_dq_kernel: one work unit per (head, query tile i).  Q_i and dO_i
 //    stay in shared memory; K_j and V_j stream through separate rings.  Per
-//    tile, with M = queries: S = Q_i K_j^T (double-buffered in TMEM),
-//    P = exp2(S * c - lse2_i), dP = dO_i V_j^T, dS = P * (dP - Delta_i)
-//    (fp16 into TMEM over dP), dQ_i += dS K_j (A from TMEM); dQ_i (times
-//    scale) is written once at the end of the unit.
+//    tile, with M = queries: S = Q_i K_j^T, P = exp2(S * c - lse2_i),
+//    dP = dO_i V_j^T (double-buffered in TMEM), dS = P * (dP - Delta_i)
+//    (fp16 into TMEM over its dP), dQ_i += dS K_j (A from TMEM); dQ_i (times
+//    scale) is written once at the end of the unit.  S is released as soon
+//    as it is read, so the next S overlaps this tile's dS work, and the two
+//    dP/dS buffers let dP of the next tile run before dQ of this one ends.
 //
 // The second kernel recomputes S and dP (7 GEMMs instead of 5) in exchange
 // for having no cross-tile reduction at all.  Scale is applied to dK and dQ
@@ -61,14 +63,14 @@ struct Bwd2Traits {
   // ---- dQ kernel
   static constexpr int B_K_STAGES = (D == 64) ? 4 : 3;
   static constexpr int B_V_STAGES = (D == 64) ? 4 : 2;
-  static constexpr int B_DQ = 0, B_S = D, B_DP = D + 2 * BN;
+  static constexpr int B_DQ = 0, B_S = D, B_DP = D + BN;  // dP/dS buffer b at B_DP + b * BN
   static constexpr int B_SM_Q = 0, B_SM_DO = TILE, B_SM_K = 2 * TILE;
   static constexpr int B_SM_V = B_SM_K + B_K_STAGES * TILE;
   static constexpr int B_SM_BAR = B_SM_V + B_V_STAGES * TILE;
   static constexpr int B_SM_BYTES = B_SM_BAR + 256;
   static constexpr int B_SMEM = B_SM_BYTES > MIN_SMEM ? B_SM_BYTES : MIN_SMEM;
   static_assert(B_SMEM <= 232448, "dQ kernel shared memory budget");
-  static_assert(B_DP + BN <= 512, "dQ kernel TMEM budget");
+  static_assert(B_DP + 2 * BN <= 512, "dQ kernel TMEM budget");
 };
 
 // Work units of the two kernels.  Non-causal: one unit per (head, tile),
@@ -227,13 +229,14 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t sK = sb + T::A_SM_K, sV = sb + T::A_SM_V, sPT = sb + T::A_SM_PT;
     uint32_t t = 0, kc = 0;
     bool ok = true;
+    const uint64_t kdesc = sdesc_sw128(sK, 16, 1024), vdesc = sdesc_sw128(sV, 16, 1024);
+    const uint64_t ptdesc = sdesc_sw128(sPT, 16, 1024);
     auto issue_s = [&](uint32_t tile) {
-      const uint32_t sQ = sb + T::A_SM_Q + (tile & 1) * T::TILE;
+      const uint64_t qdesc = sdesc_sw128(sb + T::A_SM_Q + (tile & 1) * T::TILE, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t a = sdesc_sw128(sK + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
-        const uint64_t b = sdesc_sw128(sQ + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
-        mma_f16_ss_warp(tmem + T::A_S, a, b, id_s, kk > 0 ? 1u : 0u);
+        const uint32_t off = (kk / 4) * T::SUB + (kk % 4) * 32;
+        mma_f16_ss_warp(tmem + T::A_S, sdesc_add(kdesc, off), sdesc_add(qdesc, off), id_s, kk > 0 ? 1u : 0u);
       }
       mma_commit_warp(&bars->s_full);
     };
@@ -255,17 +258,17 @@ __global__ void __launch_bounds__(320, 1)
         for (int i = i0; i < nqt; ++i) {
           const bool first = (i == i0), last = (i == nqt - 1);
           const int st = t & 1;
-          const uint32_t sQ = sb + T::A_SM_Q + st * T::TILE;
-          const uint32_t sO = sb + T::A_SM_DO + st * T::TILE;
+          const uint64_t qdesc_mn = sdesc_sw128(sb + T::A_SM_Q + st * T::TILE, T::SUB, 1024);
+          const uint64_t odesc = sdesc_sw128(sb + T::A_SM_DO + st * T::TILE, 16, 1024);
+          const uint64_t odesc_mn = sdesc_sw128(sb + T::A_SM_DO + st * T::TILE, T::SUB, 1024);
           // dP^T = V dO^T; the dP region holds dS^T of the previous tile until
           // that tile's dK MMA has read it
           if (t > 0 && !(ok = warp_wait(&bars->dk_done, (t - 1) & 1, wc, 64))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(sV + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
-            const uint64_t b = sdesc_sw128(sO + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
-            mma_f16_ss_warp(tmem + T::A_DP, a, b, id_s, kk > 0 ? 1u : 0u);
+            const uint32_t off = (kk / 4) * T::SUB + (kk % 4) * 32;
+            mma_f16_ss_warp(tmem + T::A_DP, sdesc_add(vdesc, off), sdesc_add(odesc, off), id_s, kk > 0 ? 1u : 0u);
           }
           mma_commit_warp(&bars->dp_full);
           if (last) mma_commit_warp(&bars->kv_empty);  // K_j, V_j are not read again
@@ -284,9 +287,8 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < T::BM / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(sPT + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
-            const uint64_t b = sdesc_sw128(sO + kk * 2048, T::SUB, 1024);
-            mma_f16_ss_warp(tmem + T::A_DV, a, b, id_g, (first && kk == 0) ? 0u : 1u);
+            mma_f16_ss_warp(tmem + T::A_DV, sdesc_add(ptdesc, (kk / 4) * T::SUB + (kk % 4) * 32),
+                            sdesc_add(odesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
           }
           mma_commit_warp(&bars->dv_done);
           // dK += dS^T Q (dS^T in TMEM over dP^T)
@@ -295,8 +297,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int kk = 0; kk < T::BM / 16; ++kk) {
             const uint32_t a_t = tmem + T::A_DP + (kk / 4) * T::QC + (kk % 4) * 8;
-            const uint64_t b = sdesc_sw128(sQ + kk * 2048, T::SUB, 1024);
-            mma_f16_ts_warp(tmem + T::A_DK, a_t, b, id_g, (first && kk == 0) ? 0u : 1u);
+            mma_f16_ts_warp(tmem + T::A_DK, a_t, sdesc_add(qdesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
           }
           mma_commit_warp(&bars->dk_done);
           mma_commit_warp(&bars->q_empty[st]);
@@ -434,15 +435,16 @@ __global__ void __launch_bounds__(320, 1)
 struct DqBars {
   uint64_t q_full, q_empty;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], s_free[2];
-  uint64_t dp_full, ds_full, dq_done, dq_full, dq_free, mma_done;
+  uint64_t s_full, s_free;
+  uint64_t dp_full[2], ds_full[2], dq_done[2];
+  uint64_t dq_full, dq_free, mma_done[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(DqBars) <= 256, "barrier area");
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const BwdParams prm) {
@@ -454,7 +456,9 @@ __global__ void __launch_bounds__(352, 1)
   }
   DqBars* bars = reinterpret_cast<DqBars*>(smem + T::B_SM_BAR);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, V_PRODUCER_WARP = 10, NCOMPUTE = 256;
+  // Two MMA warps: warp 9 issues S and dP, warp 11 issues dQ, so that one
+  // can issue while the other waits on the compute warps.
+  constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, V_PRODUCER_WARP = 10, DQ_MMA_WARP = 11, NCOMPUTE = 256;
   constexpr int KS = T::B_K_STAGES, VS = T::B_V_STAGES;
 
   if (threadIdx.x == 0) {
@@ -466,16 +470,17 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, NCOMPUTE);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_free[i], NCOMPUTE);
+      mbar_init(&bars->dp_full[i], 1);
+      mbar_init(&bars->ds_full[i], NCOMPUTE);
+      mbar_init(&bars->dq_done[i], 1);
     }
-    mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->ds_full, NCOMPUTE);
-    mbar_init(&bars->dq_done, 1);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, NCOMPUTE);
-    mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->mma_done[0], 1);
+    mbar_init(&bars->mma_done[1], 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -560,27 +565,26 @@ __global__ void __launch_bounds__(352, 1)
       for (uint32_t i = (v_it > VS ? v_it - VS : 0); i < v_it; ++i) bwd2_drain(&bars->v_full[i % VS], (i / VS) & 1);
     }
   } else if (warp == MMA_WARP) {
-    // ----------------------------------------------------- MMA issuer (warp)
+    // ------------------------------------------- MMA warp: S = Q K^T, dP = dO V^T
     constexpr uint32_t id_s = idesc_f16(128, T::BN, false, false);  // S, dP: M queries, N keys
-    constexpr uint32_t id_q = idesc_f16(128, D, false, true);       // dQ: N = D, B = K MN-major
     const uint32_t sb = smem_u32(smem);
-    const uint32_t sQ = sb + T::B_SM_Q, sO = sb + T::B_SM_DO;
+    const uint64_t qdesc = sdesc_sw128(sb + T::B_SM_Q, 16, 1024), odesc = sdesc_sw128(sb + T::B_SM_DO, 16, 1024);
     uint32_t t = 0, k_it = 0, v_it = 0, qc = 0;
     bool ok = true;
-    // S(tile) = Q K^T into S buffer tile & 1, from K stage `ks`
+    // S(tile) = Q K^T from K stage `kidx`; the S buffer is free once the
+    // compute warps have read the previous tile's S (right at its start)
     auto issue_s = [&](uint32_t tile, uint32_t kidx) -> bool {
-      const int b = tile & 1, ks = kidx % KS;
+      const int ks = kidx % KS;
       if (!warp_wait(&bars->k_full[ks], (kidx / KS) & 1, wc, 91)) return false;
-      if (tile >= 2 && !warp_wait(&bars->s_free[b], ((tile - 2) >> 1) & 1, wc, 92)) return false;
+      if (tile >= 1 && !warp_wait(&bars->s_free, (tile - 1) & 1, wc, 92)) return false;
       tc_fence_after();
-      const uint32_t sK = sb + T::B_SM_K + ks * T::TILE;
+      const uint64_t kdesc = sdesc_sw128(sb + T::B_SM_K + ks * T::TILE, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t a = sdesc_sw128(sQ + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(sK + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
-        mma_f16_ss_warp(tmem + T::B_S + b * T::BN, a, bd, id_s, kk > 0 ? 1u : 0u);
+        const uint32_t off = (kk / 4) * T::SUB + (kk % 4) * 32;
+        mma_f16_ss_warp(tmem + T::B_S, sdesc_add(qdesc, off), sdesc_add(kdesc, off), id_s, kk > 0 ? 1u : 0u);
       }
-      mma_commit_warp(&bars->s_full[b]);
+      mma_commit_warp(&bars->s_full);
       return true;
     };
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
@@ -594,40 +598,26 @@ __global__ void __launch_bounds__(352, 1)
         tc_fence_after();
         if (!(ok = issue_s(t, k_it))) break;
         for (int j = 0; j < nj; ++j) {
-          const bool first = (j == 0), last = (j == nj - 1);
-          const int ks = k_it % KS, vs = v_it % VS;
-          // dP = dO V^T; the dP region holds dS of the previous tile until that
-          // tile's dQ MMA has read it
+          const bool last = (j == nj - 1);
+          const int vs = v_it % VS;
+          // dP = dO V^T into dP buffer t & 1; that buffer holds dS of tile t-2
+          // until tile t-2's dQ MMA has read it
+          const int pb = t & 1;
           if (!(ok = warp_wait(&bars->v_full[vs], (v_it / VS) & 1, wc, 94))) break;
-          if (t > 0 && !(ok = warp_wait(&bars->dq_done, (t - 1) & 1, wc, 95))) break;
+          if (t >= 2 && !(ok = warp_wait(&bars->dq_done[pb], ((t - 2) >> 1) & 1, wc, 95))) break;
           tc_fence_after();
-          const uint32_t sV = sb + T::B_SM_V + vs * T::TILE;
+          const uint64_t vdesc = sdesc_sw128(sb + T::B_SM_V + vs * T::TILE, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(sO + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sV + (kk / 4) * T::SUB + (kk % 4) * 32, 16, 1024);
-            mma_f16_ss_warp(tmem + T::B_DP, a, bd, id_s, kk > 0 ? 1u : 0u);
+            const uint32_t off = (kk / 4) * T::SUB + (kk % 4) * 32;
+            mma_f16_ss_warp(tmem + T::B_DP + pb * T::BN, sdesc_add(odesc, off), sdesc_add(vdesc, off), id_s,
+                            kk > 0 ? 1u : 0u);
           }
-          mma_commit_warp(&bars->dp_full);
+          mma_commit_warp(&bars->dp_full[pb]);
           mma_commit_warp(&bars->v_empty[vs]);
           if (last) mma_commit_warp(&bars->q_empty);  // Q_i, dO_i are not read again
           // next S while the compute warps work on this tile
           if (!last && !(ok = issue_s(t + 1, k_it + 1))) break;
-          // dQ += dS K (dS in TMEM over dP); the first tile overwrites dQ, which
-          // the previous unit's write-out must have read
-          if (first && qc > 0 && !(ok = warp_wait(&bars->dq_free, (qc - 1) & 1, wc, 96))) break;
-          if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 97))) break;
-          tc_fence_after();
-          const uint32_t sK = sb + T::B_SM_K + ks * T::TILE;
-#pragma unroll
-          for (int kk = 0; kk < T::BN / 16; ++kk) {
-            const uint32_t a_t = tmem + T::B_DP + (kk / 4) * T::QC + (kk % 4) * 8;
-            const uint64_t bd = sdesc_sw128(sK + kk * 2048, T::SUB, 1024);
-            mma_f16_ts_warp(tmem + T::B_DQ, a_t, bd, id_q, (first && kk == 0) ? 0u : 1u);
-          }
-          mma_commit_warp(&bars->dq_done);
-          mma_commit_warp(&bars->k_empty[ks]);
-          if (last) mma_commit_warp(&bars->dq_full);
           ++t;
           ++k_it;
           ++v_it;
@@ -635,8 +625,48 @@ __global__ void __launch_bounds__(352, 1)
         ++qc;
       }
     }
-    mma_commit_warp(&bars->mma_done);
-    bwd2_drain(&bars->mma_done, 0);
+    mma_commit_warp(&bars->mma_done[0]);
+    bwd2_drain(&bars->mma_done[0], 0);
+  } else if (warp == DQ_MMA_WARP) {
+    // ------------------------------------------------- MMA warp: dQ += dS K
+    constexpr uint32_t id_q = idesc_f16(128, D, false, true);  // dQ: N = D, B = K MN-major
+    const uint32_t sb = smem_u32(smem);
+    uint32_t t = 0, k_it = 0, qc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      int head, ia, ib;
+      bwd2_decode<CAUSAL>(u, nqt, head, ia, ib);
+      for (int half = 0; ok && half < 2; ++half) {
+        const int i = half ? ib : ia;
+        if (i < 0) break;
+        const int nj = num_kv(i);
+        for (int j = 0; j < nj; ++j) {
+          const bool first = (j == 0), last = (j == nj - 1);
+          const int ks = k_it % KS, pb = t & 1;
+          // the first tile overwrites dQ, which the previous unit's write-out
+          // must have read; dS of this tile is in TMEM over its dP buffer
+          if (first && qc > 0 && !(ok = warp_wait(&bars->dq_free, (qc - 1) & 1, wc, 96))) break;
+          if (!(ok = warp_wait(&bars->ds_full[pb], (t >> 1) & 1, wc, 97))) break;
+          tc_fence_after();
+          const uint64_t kdesc_mn = sdesc_sw128(sb + T::B_SM_K + ks * T::TILE, T::SUB, 1024);
+#pragma unroll
+          for (int kk = 0; kk < T::BN / 16; ++kk) {
+            const uint32_t a_t = tmem + T::B_DP + pb * T::BN + (kk / 4) * T::QC + (kk % 4) * 8;
+            mma_f16_ts_warp(tmem + T::B_DQ, a_t, sdesc_add(kdesc_mn, kk * 2048), id_q, (first && kk == 0) ? 0u : 1u);
+          }
+          mma_commit_warp(&bars->dq_done[pb]);
+          // K_j is free: S of this tile completed before the compute warps
+          // could signal ds_full
+          mma_commit_warp(&bars->k_empty[ks]);
+          if (last) mma_commit_warp(&bars->dq_full);
+          ++t;
+          ++k_it;
+        }
+        ++qc;
+      }
+    }
+    mma_commit_warp(&bars->mma_done[1]);
+    bwd2_drain(&bars->mma_done[1], 0);
   } else {
     // ------------------------------------------------------------ compute
     const int wg = warp >> 2, quad = warp & 3;
@@ -656,19 +686,19 @@ __global__ void __launch_bounds__(352, 1)
         const float lse2 = __ldg(prm.lse2 + grow);
         const float delta = __ldg(prm.delta + grow);
         for (int j = 0; j < num_kv(i); ++j) {
-          const int b = t & 1;
+          const int pb = t & 1;
           const int k0 = j * T::BN + wg * T::QC;  // first key column of this warpgroup
           // ---- P = exp2(S * c - lse2)
-          ok = mbar_wait(&bars->s_full[b], (t >> 1) & 1, wc, 101);
+          ok = mbar_wait(&bars->s_full, t & 1, wc, 101);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
           uint32_t sr[T::QC];
-          tmem_ld32(lb + T::B_S + b * T::BN + wg * T::QC, sr);
-          tmem_ld32(lb + T::B_S + b * T::BN + wg * T::QC + 32, sr + 32);
+          tmem_ld32(lb + T::B_S + wg * T::QC, sr);
+          tmem_ld32(lb + T::B_S + wg * T::QC + 32, sr + 32);
           tmem_wait_ld();
           reg_fence<T::QC>(sr);
           tc_fence_before();
-          mbar_arrive(&bars->s_free[b]);
+          mbar_arrive(&bars->s_free);
           float p[T::QC];
 #pragma unroll
           for (int c = 0; c < T::QC; ++c) p[c] = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
@@ -678,21 +708,22 @@ __global__ void __launch_bounds__(352, 1)
               if (k0 + c > query) p[c] = 0.f;
           }
           // ---- dS = P * (dP - Delta), fp16 into TMEM over dP
-          ok = mbar_wait(&bars->dp_full, t & 1, wc, 102);
+          ok = mbar_wait(&bars->dp_full[pb], (t >> 1) & 1, wc, 102);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
-          tmem_ld32(lb + T::B_DP + wg * T::QC, sr);
-          tmem_ld32(lb + T::B_DP + wg * T::QC + 32, sr + 32);
+          const uint32_t dpc = T::B_DP + pb * T::BN + wg * T::QC;
+          tmem_ld32(lb + dpc, sr);
+          tmem_ld32(lb + dpc + 32, sr + 32);
           tmem_wait_ld();
           reg_fence<T::QC>(sr);
           uint32_t pk[T::QC / 2];
 #pragma unroll
           for (int c = 0; c < T::QC; c += 2)
             pk[c / 2] = pack_half2(p[c] * (__uint_as_float(sr[c]) - delta), p[c + 1] * (__uint_as_float(sr[c + 1]) - delta));
-          tmem_st32(lb + T::B_DP + wg * T::QC, pk);
+          tmem_st32(lb + dpc, pk);
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(&bars->ds_full);
+          mbar_arrive(&bars->ds_full[pb]);
           ++t;
         }
         if (!ok) break;
@@ -755,7 +786,7 @@ int launch_bwd2(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, cud
   const int grid = units < max_ctas ? units : max_ctas;
   fa_bwd_dkdv_kernel<D, CAUSAL><<<grid, 320, T::A_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
   if (cudaGetLastError() != cudaSuccess) return -1;
-  fa_bwd_dq_kernel<D, CAUSAL><<<grid, 352, T::B_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  fa_bwd_dq_kernel<D, CAUSAL><<<grid, 384, T::B_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

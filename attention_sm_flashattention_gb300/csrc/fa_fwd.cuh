@@ -253,14 +253,14 @@ __global__ void __launch_bounds__(224, 1)
         if (!warp_wait(&bars->p_full[b], (tile >> 1) & 1, wc, 11)) return false;
         if (!warp_wait(&bars->v_full[st], (kv_idx / T::V_STAGES) & 1, wc, 12)) return false;
         tc_fence_after();
-        const uint32_t sv = sbase + T::SM_V + st * T::KV_BYTES;
+        const uint64_t vdesc = sdesc_sw128(sbase + T::SM_V + st * T::KV_BYTES, T::KV_SUB, 1024);
 #pragma unroll
         for (int kk = 0; kk < T::BN / 16; ++kk) {
 #pragma unroll
           for (int h = 0; h < T::NOH; ++h) {
-            const uint64_t bdesc = sdesc_sw128(sv + (h * 2) * T::KV_SUB + kk * 16 * 128, T::KV_SUB, 1024);
-            mma_f16_ts_warp(tmem + T::O_COL + h * 128, tmem + T::P_COL + b * (T::BN / 2) + kk * 8, bdesc, idesc_pv,
-                       (first && kk == 0) ? 0u : 1u);
+            mma_f16_ts_warp(tmem + T::O_COL + h * 128, tmem + T::P_COL + b * (T::BN / 2) + kk * 8,
+                            sdesc_add(vdesc, (h * 2) * T::KV_SUB + kk * 16 * 128), idesc_pv,
+                            (first && kk == 0) ? 0u : 1u);
           }
         }
         mma_commit_warp(&bars->v_empty[st]);
@@ -277,19 +277,18 @@ __global__ void __launch_bounds__(224, 1)
           const int qs = q_it % T::Q_STAGES;
           if (!(ok = warp_wait(&bars->q_full[qs], (q_it / T::Q_STAGES) & 1, wc, 3))) break;
           tc_fence_after();
-          const uint32_t sq = sbase + T::SM_Q + qs * T::Q_BYTES;
+          const uint64_t qdesc = sdesc_sw128(sbase + T::SM_Q + qs * T::Q_BYTES, 16, 1024);
           const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
           for (int j = 0; j < nkv; ++j) {
             const int st = kv_it % T::K_STAGES;
             if (!(ok = warp_wait(&bars->k_full[st], (kv_it / T::K_STAGES) & 1, wc, 4))) break;
             tc_fence_after();
-            const uint32_t sk = sbase + T::SM_K + st * T::KV_BYTES;
+            const uint64_t kdesc = sdesc_sw128(sbase + T::SM_K + st * T::KV_BYTES, 16, 1024);
             const int b = t & 1;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t adesc = sdesc_sw128(sq + (kk / 4) * T::Q_SUB + (kk % 4) * 32, 16, 1024);
-              const uint64_t bdesc = sdesc_sw128(sk + (kk / 4) * T::KV_SUB + (kk % 4) * 32, 16, 1024);
-              mma_f16_ss_warp(tmem + T::S_COL + b * T::BN, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+              mma_f16_ss_warp(tmem + T::S_COL + b * T::BN, sdesc_add(qdesc, (kk / 4) * T::Q_SUB + (kk % 4) * 32),
+                              sdesc_add(kdesc, (kk / 4) * T::KV_SUB + (kk % 4) * 32), idesc_qk, kk > 0 ? 1u : 0u);
             }
             mma_commit_warp(&bars->s_full[b]);
             mma_commit_warp(&bars->k_empty[st]);

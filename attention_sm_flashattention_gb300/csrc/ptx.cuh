@@ -278,6 +278,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Descriptor of the same operand `bytes` further on (bytes a multiple of 16,
+// the result still inside shared memory): only the start-address field moves.
+// Build a stage's descriptor once and step through its k-blocks with this
+// (one add) instead of re-encoding every descriptor in the MMA issue loop.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor, kind::f16: fp16 A and B, fp32 D, dense.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4)                                   // D = f32
