@@ -121,14 +121,14 @@ struct DkdvBars {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full, s_free, dp_full, p_full, dv_done, ds_full, dk_done;
-  uint64_t dkv_full, dkv_free, mma_done;
+  uint64_t dkv_full, dkv_free, mma_done[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(DkdvBars) <= 256, "barrier area");
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const BwdParams prm) {
@@ -140,7 +140,10 @@ __global__ void __launch_bounds__(320, 1)
   }
   DkdvBars* bars = reinterpret_cast<DkdvBars*>(smem + T::A_SM_BAR);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, NCOMPUTE = 256;
+  // Two MMA warps: warp 9 issues S^T and dP^T, warp 10 issues dV and dK, so
+  // that waiting for the next query tile's data never holds back the
+  // gradient MMAs of the current one.
+  constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, GRAD_MMA_WARP = 10, NCOMPUTE = 256;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
@@ -158,7 +161,8 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(&bars->dk_done, 1);
     mbar_init(&bars->dkv_full, 1);
     mbar_init(&bars->dkv_free, NCOMPUTE);
-    mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->mma_done[0], 1);
+    mbar_init(&bars->mma_done[1], 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -222,16 +226,18 @@ __global__ void __launch_bounds__(320, 1)
       for (uint32_t i = (t > 2 ? t - 2 : 0); i < t; ++i) bwd2_drain(&bars->q_full[i & 1], (i >> 1) & 1);
     }
   } else if (warp == MMA_WARP) {
-    // ----------------------------------------------------- MMA issuer (warp)
+    // ----------------------------------- MMA warp: S^T = K Q^T, dP^T = V dO^T
     constexpr uint32_t id_s = idesc_f16(128, T::BM, false, false);  // S^T, dP^T: M keys, N queries
-    constexpr uint32_t id_g = idesc_f16(128, D, false, true);       // dV, dK: N = D, B MN-major
     const uint32_t sb = smem_u32(smem);
-    const uint32_t sK = sb + T::A_SM_K, sV = sb + T::A_SM_V, sPT = sb + T::A_SM_PT;
+    const uint64_t kdesc = sdesc_sw128(sb + T::A_SM_K, 16, 1024), vdesc = sdesc_sw128(sb + T::A_SM_V, 16, 1024);
     uint32_t t = 0, kc = 0;
     bool ok = true;
-    const uint64_t kdesc = sdesc_sw128(sK, 16, 1024), vdesc = sdesc_sw128(sV, 16, 1024);
-    const uint64_t ptdesc = sdesc_sw128(sPT, 16, 1024);
-    auto issue_s = [&](uint32_t tile) {
+    // S^T(tile): needs the tile's Q and the S region, free once the compute
+    // warps have read the previous S^T
+    auto issue_s = [&](uint32_t tile) -> bool {
+      if (!warp_wait(&bars->q_full[tile & 1], (tile >> 1) & 1, wc, 62)) return false;
+      if (tile > 0 && !warp_wait(&bars->s_free, (tile - 1) & 1, wc, 63)) return false;
+      tc_fence_after();
       const uint64_t qdesc = sdesc_sw128(sb + T::A_SM_Q + (tile & 1) * T::TILE, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -239,6 +245,7 @@ __global__ void __launch_bounds__(320, 1)
         mma_f16_ss_warp(tmem + T::A_S, sdesc_add(kdesc, off), sdesc_add(qdesc, off), id_s, kk > 0 ? 1u : 0u);
       }
       mma_commit_warp(&bars->s_full);
+      return true;
     };
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
       int head, ja, jb;
@@ -249,18 +256,10 @@ __global__ void __launch_bounds__(320, 1)
         const int i0 = CAUSAL ? j : 0;
         if (!(ok = warp_wait(&bars->kv_full, kc & 1, wc, 61))) break;
         tc_fence_after();
-        // first S^T of the unit (the S region is free once the previous tile's
-        // S^T was read)
-        if (!(ok = warp_wait(&bars->q_full[t & 1], (t >> 1) & 1, wc, 62))) break;
-        if (t > 0 && !(ok = warp_wait(&bars->s_free, (t - 1) & 1, wc, 63))) break;
-        tc_fence_after();
-        issue_s(t);
+        if (!(ok = issue_s(t))) break;
         for (int i = i0; i < nqt; ++i) {
-          const bool first = (i == i0), last = (i == nqt - 1);
-          const int st = t & 1;
-          const uint64_t qdesc_mn = sdesc_sw128(sb + T::A_SM_Q + st * T::TILE, T::SUB, 1024);
-          const uint64_t odesc = sdesc_sw128(sb + T::A_SM_DO + st * T::TILE, 16, 1024);
-          const uint64_t odesc_mn = sdesc_sw128(sb + T::A_SM_DO + st * T::TILE, T::SUB, 1024);
+          const bool last = (i == nqt - 1);
+          const uint64_t odesc = sdesc_sw128(sb + T::A_SM_DO + (t & 1) * T::TILE, 16, 1024);
           // dP^T = V dO^T; the dP region holds dS^T of the previous tile until
           // that tile's dK MMA has read it
           if (t > 0 && !(ok = warp_wait(&bars->dk_done, (t - 1) & 1, wc, 64))) break;
@@ -272,17 +271,37 @@ __global__ void __launch_bounds__(320, 1)
           }
           mma_commit_warp(&bars->dp_full);
           if (last) mma_commit_warp(&bars->kv_empty);  // K_j, V_j are not read again
-          // next S^T as soon as this tile's S^T has been read
-          if (!last) {
-            if (!(ok = warp_wait(&bars->q_full[(t + 1) & 1], ((t + 1) >> 1) & 1, wc, 65))) break;
-            if (!(ok = warp_wait(&bars->s_free, t & 1, wc, 66))) break;
-            tc_fence_after();
-            issue_s(t + 1);
-          }
-          // dV += P^T dO (P^T in shared memory); the first tile of a unit
-          // overwrites the accumulators, which the previous unit's write-out
-          // must have read
+          if (!last && !(ok = issue_s(t + 1))) break;
+          ++t;
+        }
+        ++kc;
+      }
+    }
+    mma_commit_warp(&bars->mma_done[0]);
+    bwd2_drain(&bars->mma_done[0], 0);
+  } else if (warp == GRAD_MMA_WARP) {
+    // ---------------------------- MMA warp: dV += P^T dO, dK += dS^T Q
+    constexpr uint32_t id_g = idesc_f16(128, D, false, true);  // dV, dK: N = D, B MN-major
+    const uint32_t sb = smem_u32(smem);
+    const uint64_t ptdesc = sdesc_sw128(sb + T::A_SM_PT, 16, 1024);
+    uint32_t t = 0, kc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      int head, ja, jb;
+      bwd2_decode<CAUSAL>(u, nkv, head, ja, jb);
+      for (int half = 0; ok && half < 2; ++half) {
+        const int j = half ? jb : ja;
+        if (j < 0) break;
+        const int i0 = CAUSAL ? j : 0;
+        for (int i = i0; i < nqt; ++i) {
+          const bool first = (i == i0), last = (i == nqt - 1);
+          const int st = t & 1;
+          const uint64_t qdesc_mn = sdesc_sw128(sb + T::A_SM_Q + st * T::TILE, T::SUB, 1024);
+          const uint64_t odesc_mn = sdesc_sw128(sb + T::A_SM_DO + st * T::TILE, T::SUB, 1024);
+          // the first tile of a unit overwrites the accumulators, which the
+          // previous unit's write-out must have read
           if (first && kc > 0 && !(ok = warp_wait(&bars->dkv_free, (kc - 1) & 1, wc, 67))) break;
+          if (!(ok = warp_wait(&bars->q_full[st], (t >> 1) & 1, wc, 60))) break;
           if (!(ok = warp_wait(&bars->p_full, t & 1, wc, 68))) break;
           tc_fence_after();
 #pragma unroll
@@ -291,7 +310,6 @@ __global__ void __launch_bounds__(320, 1)
                             sdesc_add(odesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
           }
           mma_commit_warp(&bars->dv_done);
-          // dK += dS^T Q (dS^T in TMEM over dP^T)
           if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 69))) break;
           tc_fence_after();
 #pragma unroll
@@ -300,6 +318,8 @@ __global__ void __launch_bounds__(320, 1)
             mma_f16_ts_warp(tmem + T::A_DK, a_t, sdesc_add(qdesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
           }
           mma_commit_warp(&bars->dk_done);
+          // stage t is free: S^T(t) and dP^T(t) completed before the compute
+          // warps could signal p_full / ds_full
           mma_commit_warp(&bars->q_empty[st]);
           if (last) mma_commit_warp(&bars->dkv_full);
           ++t;
@@ -307,8 +327,8 @@ __global__ void __launch_bounds__(320, 1)
         ++kc;
       }
     }
-    mma_commit_warp(&bars->mma_done);
-    bwd2_drain(&bars->mma_done, 0);
+    mma_commit_warp(&bars->mma_done[1]);
+    bwd2_drain(&bars->mma_done[1], 0);
   } else {
     // ------------------------------------------------------------ compute
     const int wg = warp >> 2, quad = warp & 3;
@@ -784,7 +804,7 @@ int launch_bwd2(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, cud
   const int nt = prm.N / 128;
   const int units = CAUSAL ? prm.heads * ((nt + 1) / 2) : prm.heads * nt;
   const int grid = units < max_ctas ? units : max_ctas;
-  fa_bwd_dkdv_kernel<D, CAUSAL><<<grid, 320, T::A_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  fa_bwd_dkdv_kernel<D, CAUSAL><<<grid, 352, T::A_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
   if (cudaGetLastError() != cudaSuccess) return -1;
   fa_bwd_dq_kernel<D, CAUSAL><<<grid, 384, T::B_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
