@@ -145,8 +145,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
   const long long rows = static_cast<long long>(Z) * H * N;
   const int bn = fa::fwd_block_n(D);
-  CUtensorMap tq, tk, tv;
-  if (!fp16_map(&tq, q, rows, D, 128) || !fp16_map(&tk, k, rows, D, bn) || !fp16_map(&tv, v, rows, D, bn))
+  CUtensorMap maps[4];  // q, k, v, o
+  if (!fp16_map(&maps[0], q, rows, D, 128) || !fp16_map(&maps[1], k, rows, D, bn) ||
+      !fp16_map(&maps[2], v, rows, D, bn) || !fp16_map(&maps[3], o, rows, D, 128))
     return FA_ERR_CUDA;
   fa::FwdParams prm{};
   prm.o = static_cast<__half*>(o);
@@ -157,9 +158,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   prm.status = dev->status;
   const bool c = causal != 0;
   switch (D) {
-    case 64: rc = fa::launch_fwd_d64(c, tq, tk, tv, prm, dev->sms, stream); break;
-    case 128: rc = fa::launch_fwd_d128(c, tq, tk, tv, prm, dev->sms, stream); break;
-    default: rc = fa::launch_fwd_d256(c, tq, tk, tv, prm, dev->sms, stream); break;
+    case 64: rc = fa::launch_fwd_d64(c, maps, prm, dev->sms, stream); break;
+    case 128: rc = fa::launch_fwd_d128(c, maps, prm, dev->sms, stream); break;
+    default: rc = fa::launch_fwd_d256(c, maps, prm, dev->sms, stream); break;
   }
   return rc == 0 ? FA_OK : FA_ERR_CUDA;
 }

@@ -9,13 +9,16 @@
 // matrix unit; causal shortens the key-tile loop and masks only diagonal
 // tiles; D = 256 keeps two 128-wide accumulator halves; O is written once.
 //
-// Roles (224 threads):
+// Roles (256 threads):
 //   warps 0-3  softmax warpgroup: thread r owns query row r of the tile. It
 //              reads S from TMEM, applies the mask, updates m and l, writes
 //              P (fp16) back to TMEM, rescales O in TMEM when m moved, and
 //              runs the epilogue (O / l -> fp16, lse).
 //   warp 4     TMA producer: Q tile per work item, K tiles into a ring.
 //   warp 6     TMA producer: V tiles into their own ring.
+//   warp 7     O store: the softmax warpgroup writes the normalised O tile
+//              into the item's (now unused) Q buffer; this warp stores it
+//              with TMA and then releases the buffer.
 //   warp 5     MMA issuer (converged warp, one elected lane per MMA) and
 //              TMEM owner: S = Q K^T into one of two S buffers, then
 //              O += P V with P read from TMEM.
@@ -61,10 +64,11 @@ struct FwdTraits {
   // second CTA can never share the SM (each CTA takes all 512 TMEM columns).
   static constexpr int SMEM_ALLOC = (SM_BYTES + 1024 > 120 * 1024) ? SM_BYTES + 1024 : 120 * 1024;
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-  static constexpr int THREADS = 224;
+  static constexpr int THREADS = 256;
   static constexpr int PRODUCER_WARP = 4;  // Q and K
   static constexpr int MMA_WARP = 5;
   static constexpr int V_PRODUCER_WARP = 6;
+  static constexpr int STORE_WARP = 7;
 };
 
 // Threshold (log2 units) of the lazy online-softmax rescale.
@@ -76,6 +80,7 @@ struct FwdBars {
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2];
   uint64_t o_ready, o_free, mma_done;
+  uint64_t epi_full[2];  // O tile written into Q buffer b
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -122,9 +127,10 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(224, 1)
+__global__ void __launch_bounds__(256, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdParams prm) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FwdParams prm) {
   using T = FwdTraits<D, CAUSAL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -135,9 +141,12 @@ __global__ void __launch_bounds__(224, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1);
-      mbar_init(&bars->q_empty[i], 1);
+      // a Q buffer is free once its last Q K^T completed (MMA commit) and the
+      // O tile written into it has been stored (store warp)
+      mbar_init(&bars->q_empty[i], 2);
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], T::BM);
+      mbar_init(&bars->epi_full[i], T::BM);
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars->k_full[i], 1);
@@ -159,6 +168,7 @@ __global__ void __launch_bounds__(224, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -236,6 +246,29 @@ __global__ void __launch_bounds__(224, 1)
       for (uint32_t i = (v_it > T::V_STAGES ? v_it - T::V_STAGES : 0); i < v_it; ++i)
         drain_wait(&bars->v_full[i % T::V_STAGES], (i / T::V_STAGES) & 1);
     }
+  } else if (warp == T::STORE_WARP) {
+    // ------------------------------------------------ O store (TMA, async)
+    if (lane == 0) {
+      uint32_t q_it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        int head, qa, qb;
+        fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+        for (int half = 0; ok && half < 2; ++half) {
+          const int qt = half ? qb : qa;
+          if (qt < 0) break;
+          const int qs = q_it % T::Q_STAGES;
+          if (!(ok = mbar_wait(&bars->epi_full[qs], (q_it / T::Q_STAGES) & 1, wc, 13))) break;
+          const uint8_t* so = smem + T::SM_Q + qs * T::Q_BYTES;
+          for (int s = 0; s < T::DSUB; ++s) tma_store_2d(&tm_o, so + s * T::Q_SUB, s * 64, head * N + qt * T::BM);
+          bulk_commit();
+          bulk_wait_read<0>();  // the buffer may be refilled once TMA has read it
+          mbar_arrive(&bars->q_empty[qs]);
+          ++q_it;
+        }
+      }
+      bulk_wait<0>();  // all O stores complete before the CTA exits
+    }
   } else if (warp == T::MMA_WARP) {
     // ------------------------------------------------------------- MMA issuer
     {  // the whole warp runs the loop; one elected lane issues each MMA
@@ -311,7 +344,7 @@ __global__ void __launch_bounds__(224, 1)
     const int r = threadIdx.x;  // query row inside the tile, == TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const float sl2 = prm.scale_log2;
-    uint32_t t = 0;
+    uint32_t t = 0, q_item = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
       int head, qa, qb;
@@ -398,12 +431,13 @@ __global__ void __launch_bounds__(224, 1)
           ++t;
         }
         if (!ok) break;
-        // ---- epilogue: O / l -> fp16, lse = ln2 * (m + log2 l)
+        // ---- epilogue: O / l -> fp16 into this item's Q buffer (swizzled
+        // like a Q tile; the store warp writes it out with TMA), lse direct
         ok = mbar_wait(&bars->o_ready, (t - 1) & 1, wc, 7);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         const float inv_l = 1.f / l;
-        __half* orow = prm.o + (static_cast<size_t>(head) * N + qi) * D;
+        const uint32_t so = smem_u32(smem + T::SM_Q + (q_item % T::Q_STAGES) * T::Q_BYTES) + r * 128;
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           uint32_t o[32];
@@ -414,13 +448,19 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             h[i] = pack_half2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          uint4* dst = reinterpret_cast<uint4*>(orow + c);
+          const uint32_t sub = so + (c / 64) * T::Q_SUB;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+          for (int i = 0; i < 4; ++i) {
+            const int ch = ((c % 64) / 8 + i) ^ (r & 7);
+            st_shared_v4(sub + ch * 16, h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+          }
         }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->epi_full[q_item % T::Q_STAGES]);
         prm.lse[static_cast<size_t>(head) * N + qi] = (m + log2f(l)) * 0.69314718055994530942f;
         tc_fence_before();
         mbar_arrive(&bars->o_free);
+        ++q_item;
       }
     }
   }
@@ -434,8 +474,7 @@ __global__ void __launch_bounds__(224, 1)
 }
 
 template <int D, bool CAUSAL>
-int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& prm,
-               int num_sms, cudaStream_t stream) {
+int launch_fwd(const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaStream_t stream) {
   using T = FwdTraits<D, CAUSAL>;
   static bool attr_set = false;  // per process; the attribute is per function, not per device
   if (!attr_set) {
@@ -447,7 +486,7 @@ int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
   const int nqt = prm.N / T::BM;
   const int units = CAUSAL ? prm.heads * ((nqt + 1) / 2) : prm.heads * nqt;
   const int grid = units < num_sms ? units : num_sms;
-  fa_fwd_kernel<D, CAUSAL><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(tq, tk, tv, prm);
+  fa_fwd_kernel<D, CAUSAL><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -11,7 +11,7 @@
 namespace fa {
 
 struct FwdParams {
-  __half* o;         // [heads, N, D]
+  __half* o;         // [heads, N, D] (written through the O tensor map)
   float* lse;        // [heads, N]
   int heads;         // Z * H
   int N;             // sequence length (multiple of 128)
@@ -41,8 +41,8 @@ struct BwdParams {
 // per-CTA dQ accumulators in the workspace, for D <= 128 (no accumulators)
 // the SM count.
 #define FA_DECLARE_LAUNCHERS(D)                                                                      \
-  int launch_fwd_d##D(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, \
-                      const FwdParams& prm, int num_sms, cudaStream_t stream);                        \
+  int launch_fwd_d##D(bool causal, const CUtensorMap* maps, const FwdParams& prm, int num_sms,      \
+                      cudaStream_t stream);                                                           \
   int launch_bwd_d##D(bool causal, const CUtensorMap* maps, const BwdParams& prm, int grid,          \
                       cudaStream_t stream);
 

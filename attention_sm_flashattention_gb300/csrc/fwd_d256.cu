@@ -3,10 +3,8 @@
 
 namespace fa {
 
-int launch_fwd_d256(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                   const FwdParams& prm, int num_sms, cudaStream_t stream) {
-  return causal ? launch_fwd<256, true>(tq, tk, tv, prm, num_sms, stream)
-                : launch_fwd<256, false>(tq, tk, tv, prm, num_sms, stream);
+int launch_fwd_d256(bool causal, const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaStream_t stream) {
+  return causal ? launch_fwd<256, true>(maps, prm, num_sms, stream) : launch_fwd<256, false>(maps, prm, num_sms, stream);
 }
 
 }  // namespace fa

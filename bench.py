@@ -250,6 +250,18 @@ def reduce_max(vals, world):
     return t.tolist()
 
 
+def bwd_kernel_names(d, causal):
+    c = str(bool(causal)).lower()
+    if d == 256:
+        return f"fa_bwd call: fa_bwd_prep_kernel<{d}> + fa_bwd_kernel<{d},{c}>"
+    return f"fa_bwd call: fa_bwd_prep_kernel<{d}> + fa_bwd_dkdv_kernel<{d},{c}> + fa_bwd_dq_kernel<{d},{c}>"
+
+
+def bwd_launches(d):
+    """Kernels one fa_bwd call launches (Delta preprocess + main kernel(s))."""
+    return 2 if d == 256 else 3
+
+
 def load_traffic():
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
@@ -341,14 +353,14 @@ def main():
         "pct_of_peak": {"fwd": fwd_tf / peaks["tflops"], "fwd_bwd": value / world / peaks["tflops"],
                         "bwd": bwd_tf / peaks["tflops"], "peak_tflops": peaks["tflops"],
                         "peak_source": peaks["source"]},
-        "roofline": {"bound": "tensor", "kernel": f"fa_bwd (Delta preprocess + fa_bwd_kernel<{D},{str(CAUSAL).lower()}>)",
+        "roofline": {"bound": "tensor", "kernel": bwd_kernel_names(D, CAUSAL),
                      "achieved": bwd_tf, "peak": peaks["tflops"], "unit": "TFLOP/s",
                      "frac": bwd_tf / peaks["tflops"], "peak_kind": "burst bf16 cuBLAS (" + peaks["source"] + ")",
                      "traffic": bwd_traffic},
         "clocks": r["clocks"],
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "ms_per_step": e2e_ms},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (1 + bwd_launches(D)) * args.steps,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample()
