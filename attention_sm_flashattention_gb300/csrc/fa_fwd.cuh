@@ -9,19 +9,23 @@
 // matrix unit; causal shortens the key-tile loop and masks only diagonal
 // tiles; D = 256 keeps two 128-wide accumulator halves; O is written once.
 //
-// Roles (256 threads):
-//   warps 0-3  softmax warpgroup: thread r owns query row r of the tile. It
-//              reads S from TMEM, applies the mask, updates m and l, writes
-//              P (fp16) back to TMEM, rescales O in TMEM when m moved, and
-//              runs the epilogue (O / l -> fp16, lse).
-//   warp 4     TMA producer: Q tile per work item, K tiles into a ring.
-//   warp 6     TMA producer: V tiles into their own ring.
-//   warp 7     O store: the softmax warpgroup writes the normalised O tile
-//              into the item's (now unused) Q buffer; this warp stores it
-//              with TMA and then releases the buffer.
-//   warp 5     MMA issuer (converged warp, one elected lane per MMA) and
+// Roles (384 threads):
+//   warps 0-7  softmax: two warpgroups split the columns of each tile; thread
+//              (g, r) owns query row r and half g of the key columns of S
+//              (and of the O columns).  Both halves of a row read the whole
+//              S row to take the same row max (TMEM reads are cheap), then
+//              each exponentiates its own half and keeps its own partial l;
+//              the partial sums are combined once, in the epilogue.  They
+//              write P (fp16) back to TMEM, rescale O when m moved, and run
+//              the epilogue.
+//   warp 8     TMA producer: Q tile per work item, K tiles into a ring.
+//   warp 9     MMA issuer (converged warp, one elected lane per MMA) and
 //              TMEM owner: S = Q K^T into one of two S buffers, then
 //              O += P V with P read from TMEM.
+//   warp 10    TMA producer: V tiles into their own ring.
+//   warp 11    O store: the softmax warps write the normalised O tile into
+//              the item's (now unused) Q buffer; this warp stores it with
+//              TMA and then releases the buffer.
 //
 // The MMA of key tile j+1 (Q K^T) runs while the softmax of tile j works,
 // and P V of tile j runs while the softmax of tile j+1 works.
@@ -58,17 +62,19 @@ struct FwdTraits {
   static constexpr int SM_Q = 0;
   static constexpr int SM_K = SM_Q + Q_STAGES * Q_BYTES;
   static constexpr int SM_V = SM_K + K_STAGES * KV_BYTES;
-  static constexpr int SM_BAR = SM_V + V_STAGES * KV_BYTES;
-  static constexpr int SM_BYTES = SM_BAR + 256;
-  // +1024 slack for the manual alignment; never below 120 KB so that a
-  // second CTA can never share the SM (each CTA takes all 512 TMEM columns).
-  static constexpr int SMEM_ALLOC = (SM_BYTES + 1024 > 120 * 1024) ? SM_BYTES + 1024 : 120 * 1024;
+  static constexpr int SM_XCH = SM_V + V_STAGES * KV_BYTES;  // [2][2][128] fp32 row partials
+  static constexpr int SM_BAR = SM_XCH + 2 * 2 * BM * 4;
+  static constexpr int SM_BYTES = SM_BAR + 512;
+  // never below 120 KB so that a second CTA can never share the SM (each
+  // CTA takes all 512 TMEM columns)
+  static constexpr int SMEM_ALLOC = (SM_BYTES > 120 * 1024) ? SM_BYTES : 120 * 1024;
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-  static constexpr int THREADS = 256;
-  static constexpr int PRODUCER_WARP = 4;  // Q and K
-  static constexpr int MMA_WARP = 5;
-  static constexpr int V_PRODUCER_WARP = 6;
-  static constexpr int STORE_WARP = 7;
+  static constexpr int THREADS = 384;
+  static constexpr int SOFTMAX_THREADS = 256;
+  static constexpr int PRODUCER_WARP = 8;  // Q and K
+  static constexpr int MMA_WARP = 9;
+  static constexpr int V_PRODUCER_WARP = 10;
+  static constexpr int STORE_WARP = 11;
 };
 
 // Threshold (log2 units) of the lazy online-softmax rescale.
@@ -80,11 +86,13 @@ struct FwdBars {
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2];
   uint64_t o_ready, o_free, mma_done;
+  uint64_t pv_done[2];   // P V of a tile that used P buffer b completed
   uint64_t epi_full[2];  // O tile written into Q buffer b
+  uint64_t pair[4];      // row-partial exchange between warps q and q + 4
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(FwdBars) <= 256, "barrier area");
+static_assert(sizeof(FwdBars) <= 512, "barrier area");
 
 // Static schedule.  Non-causal: one work unit per (head, query tile), head
 // major so that the CTAs running at the same time share K/V through L2.
@@ -127,13 +135,16 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams prm) {
   using T = FwdTraits<D, CAUSAL>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // the 128-byte-swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) record_timeout(prm.status, 99);
+    return;
+  }
   FwdBars* bars = reinterpret_cast<FwdBars*>(smem + T::SM_BAR);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -145,9 +156,10 @@ __global__ void __launch_bounds__(256, 1)
       // O tile written into it has been stored (store warp)
       mbar_init(&bars->q_empty[i], 2);
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], T::BM);
-      mbar_init(&bars->epi_full[i], T::BM);
+      mbar_init(&bars->p_full[i], T::SOFTMAX_THREADS);
+      mbar_init(&bars->epi_full[i], T::SOFTMAX_THREADS);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(&bars->pair[i], 64);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
@@ -155,7 +167,9 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&bars->v_empty[i], 1);
     }
     mbar_init(&bars->o_ready, 1);
-    mbar_init(&bars->o_free, T::BM);
+    mbar_init(&bars->pv_done[0], 1);
+    mbar_init(&bars->pv_done[1], 1);
+    mbar_init(&bars->o_free, T::SOFTMAX_THREADS);
     mbar_init(&bars->mma_done, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -298,6 +312,7 @@ __global__ void __launch_bounds__(256, 1)
         }
         mma_commit_warp(&bars->v_empty[st]);
         mma_commit_warp(&bars->o_ready);
+        mma_commit_warp(&bars->pv_done[b]);
         return true;
       };
 
@@ -340,12 +355,30 @@ __global__ void __launch_bounds__(256, 1)
       drain_wait(&bars->mma_done, 0);
     }
   } else {
-    // ------------------------------------------------------ softmax warpgroup
-    const int r = threadIdx.x;  // query row inside the tile, == TMEM lane
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // ----------------------------------------------------- softmax warps
+    constexpr int HC = T::BN / 2;  // S columns per thread
+    constexpr int HD = D / 2;      // O columns per thread
+    const int wg = warp >> 2;      // column half
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // query row inside the tile, == TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    float* xch = reinterpret_cast<float*>(smem + T::SM_XCH);
+    uint64_t* pair = &bars->pair[quad];
     const float sl2 = prm.scale_log2;
-    uint32_t t = 0, q_item = 0;
+    uint32_t t = 0, q_item = 0, xc = 0;
     bool ok = true;
+    // Swap a per-row value with the other half of the row (same row, other
+    // column half).  Double-buffered by exchange parity: a slot is rewritten
+    // two exchanges later, after the partner passed the next exchange.
+    auto exchange = [&](float v, float& other) -> bool {
+      float* buf = xch + (xc & 1) * (2 * T::BM);
+      buf[wg * T::BM + r] = v;
+      mbar_arrive(pair);
+      const bool w = mbar_wait(pair, xc & 1, wc, 14);
+      other = buf[(wg ^ 1) * T::BM + r];
+      ++xc;
+      return __all_sync(0xffffffffu, w);
+    };
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
       int head, qa, qb;
       fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
@@ -354,47 +387,66 @@ __global__ void __launch_bounds__(256, 1)
         if (qt < 0) break;
         const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
         const int qi = qt * T::BM + r;  // query index within the head
-        float m = -INFINITY, l = 0.f;
+        float m = -INFINITY, l = 0.f;   // l: this half's partial row sum
         for (int j = 0; j < nkv; ++j) {
           const int b = t & 1;
           ok = mbar_wait(&bars->s_full[b], (t >> 1) & 1, wc, 5);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
-          uint32_t sr[T::BN];
-#pragma unroll
-          for (int c = 0; c < T::BN; c += 32) tmem_ld32(lane_base + T::S_COL + b * T::BN + c, sr + c);
-          tmem_wait_ld();
-          reg_fence<T::BN>(sr);
-          float s[T::BN];
-#pragma unroll
-          for (int c = 0; c < T::BN; ++c) s[c] = __uint_as_float(sr[c]);
-          if (CAUSAL && (j + 1) * T::BN - 1 > qt * T::BM) {
-            const int k0 = j * T::BN;
-#pragma unroll
-            for (int c = 0; c < T::BN; ++c)
-              if (k0 + c > qi) s[c] = -INFINITY;
-          }
+          // other half of the row: only its max is needed
+          uint32_t sr[HC];
           float pm[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) pm[i] = s[i];
+          for (int c = 0; c < HC; c += 32) tmem_ld32(lane_base + T::S_COL + b * T::BN + (wg ^ 1) * HC + c, sr + c);
+          tmem_wait_ld();
+          reg_fence<HC>(sr);
+          if (CAUSAL && (j + 1) * T::BN - 1 > qt * T::BM) {
+            const int k0 = j * T::BN + (wg ^ 1) * HC;
 #pragma unroll
-          for (int c = 8; c < T::BN; ++c) pm[c & 7] = fmaxf(pm[c & 7], s[c]);
-          const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                 fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+            for (int c = 0; c < HC; ++c)
+              if (k0 + c > qi) sr[c] = __float_as_uint(-INFINITY);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) pm[i] = fmaxf(__uint_as_float(sr[i]), __uint_as_float(sr[i + 8]));
+#pragma unroll
+          for (int c = 16; c < HC; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pm[i] = fmax3(pm[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
+          // own half
+#pragma unroll
+          for (int c = 0; c < HC; c += 32) tmem_ld32(lane_base + T::S_COL + b * T::BN + wg * HC + c, sr + c);
+          tmem_wait_ld();
+          reg_fence<HC>(sr);
+          float s[HC];
+#pragma unroll
+          for (int c = 0; c < HC; ++c) s[c] = __uint_as_float(sr[c]);
+          if (CAUSAL && (j + 1) * T::BN - 1 > qt * T::BM) {
+            const int k0 = j * T::BN + wg * HC;
+#pragma unroll
+            for (int c = 0; c < HC; ++c)
+              if (k0 + c > qi) s[c] = -INFINITY;
+          }
+#pragma unroll
+          for (int c = 0; c < HC; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pm[i] = fmax3(pm[i], s[c + i], s[c + 8 + i]);
+          const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
           // The running max m only moves when this tile's max exceeds it by
           // more than kRescaleLog2: below that the stale m keeps every P value
           // under 2^kRescaleLog2 (exact range for fp16 P and fp32 l), so O and
           // l need no rescaling.  O / l and lse use the max actually applied,
           // which gives the same result as always tracking the exact max.
+          // Both halves of a row compute the same row max, so they take the
+          // same decision.
           const float m_tile = mx * sl2;
           const float m_new = (m_tile > m + kRescaleLog2) ? m_tile : m;
           const float neg = -m_new;
           float ps[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) ps[i] = 0.f;
-          uint32_t pk[T::BN / 2];
+          uint32_t pk[HC / 2];
 #pragma unroll
-          for (int c = 0; c < T::BN; c += 2) {
+          for (int c = 0; c < HC; c += 2) {
             const float p0 = ex2_approx(fmaf(s[c], sl2, neg));
             const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg));
             ps[(c >> 1) & 7] += p0 + p1;
@@ -404,27 +456,42 @@ __global__ void __launch_bounds__(256, 1)
           const float alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
           l = l * alpha + rs;
           m = m_new;
-          if (j > 0) {
+          // With two 128-column O halves (D = 256), letting P V of this tile
+          // start while the previous P V still runs gave wrong O on GB300
+          // (the MMAs alternate between the two accumulators); there the
+          // softmax always waits for the previous P V before releasing P.
+          constexpr bool kSerialPV = (T::NOH > 1);
+          if (j > 0 && (kSerialPV || __any_sync(0xffffffffu, alpha != 1.f))) {
             // O holds P V of the previous tiles: wait for the last P V, then
-            // rescale rows whose max moved.
+            // rescale (this half's columns of) rows whose max moved.
             ok = mbar_wait(&bars->o_ready, (t - 1) & 1, wc, 6);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-              for (int c = 0; c < D; c += 32) {
+              for (int c = 0; c < HD; c += 32) {
                 uint32_t o[32];
-                tmem_ld32(lane_base + T::O_COL + c, o);
+                tmem_ld32(lane_base + T::O_COL + wg * HD + c, o);
                 tmem_wait_ld();
                 reg_fence<32>(o);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                tmem_st32(lane_base + T::O_COL + c, o);
+                tmem_st32(lane_base + T::O_COL + wg * HD + c, o);
               }
             }
           }
-#pragma unroll
-          for (int c = 0; c < T::BN / 2; c += 32) tmem_st32(lane_base + T::P_COL + b * (T::BN / 2) + c, pk + c);
+          // P buffer b was last read by the P V of tile t - 2
+          if (t >= 2) {
+            ok = mbar_wait(&bars->pv_done[b], ((t - 2) >> 1) & 1, wc, 15);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+          }
+          const uint32_t pcol = lane_base + T::P_COL + b * (T::BN / 2) + wg * (HC / 2);
+          if (HC / 2 == 32) {
+            tmem_st32(pcol, pk);
+          } else {
+            tmem_st16(pcol, pk);
+          }
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->p_full[b]);
@@ -436,28 +503,32 @@ __global__ void __launch_bounds__(256, 1)
         ok = mbar_wait(&bars->o_ready, (t - 1) & 1, wc, 7);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        const float inv_l = 1.f / l;
+        float l_other;
+        if (!(ok = exchange(l, l_other))) break;
+        const float l_row = l + l_other;
+        const float inv_l = 1.f / l_row;
         const uint32_t so = smem_u32(smem + T::SM_Q + (q_item % T::Q_STAGES) * T::Q_BYTES) + r * 128;
 #pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
+        for (int c = 0; c < HD; c += 32) {
           uint32_t o[32];
-          tmem_ld32(lane_base + T::O_COL + c, o);
+          tmem_ld32(lane_base + T::O_COL + wg * HD + c, o);
           tmem_wait_ld();
           reg_fence<32>(o);
           uint32_t h[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             h[i] = pack_half2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          const uint32_t sub = so + (c / 64) * T::Q_SUB;
+          const int col0 = wg * HD + c;
+          const uint32_t sub = so + (col0 / 64) * T::Q_SUB;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int ch = ((c % 64) / 8 + i) ^ (r & 7);
+            const int ch = ((col0 % 64) / 8 + i) ^ (r & 7);
             st_shared_v4(sub + ch * 16, h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
           }
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars->epi_full[q_item % T::Q_STAGES]);
-        prm.lse[static_cast<size_t>(head) * N + qi] = (m + log2f(l)) * 0.69314718055994530942f;
+        if (wg == 0) prm.lse[static_cast<size_t>(head) * N + qi] = (m + log2f(l_row)) * 0.69314718055994530942f;
         tc_fence_before();
         mbar_arrive(&bars->o_free);
         ++q_item;
