@@ -33,6 +33,7 @@ SIGNATURES = {
     "fa_device_status": (_i, [_vp]),
     "fa_device_status_raw": (_i, [_vp, ctypes.POINTER(ctypes.c_int)]),
     "fa_error_string": (ctypes.c_char_p, [_i]),
+    "fa_selftest_wait_timeout": (_i, [_vp]),
     "fa_fwd_tile_count": (ctypes.c_longlong, [_i, _i, _i]),
     "fa_fwd_flops": (ctypes.c_double, [_i, _i, _i, _i, _i]),
     "fa_bwd_flops": (ctypes.c_double, [_i, _i, _i, _i, _i]),

@@ -11,6 +11,24 @@
 // The library's only device state: one status word per device (0 = ok).
 __device__ int g_fa_status = 0;
 
+#include "ptx.cuh"
+
+// Waits on a barrier that is never signalled: exercises the bounded wait,
+// the status report and the clean exit of a kernel that gave up.
+__global__ void fa_selftest_wait_kernel(int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    fa::mbar_init(&bar, 1);
+    abort_flag = 0;
+    fa::fence_barrier_init();
+  }
+  __syncthreads();
+  const fa::WaitCtx wc{status, &abort_flag};
+  if (threadIdx.x == 0) fa::mbar_wait(&bar, 0, wc, 200);
+  __syncthreads();
+}
+
 namespace {
 
 struct DevInfo {
@@ -322,4 +340,12 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
     default: rc = fa::launch_bwd_d256(c, maps, prm, g, stream); break;
   }
   return rc == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" int fa_selftest_wait_timeout(cudaStream_t stream) {
+  DevInfo* dev = nullptr;
+  int rc = current_device_info(&dev);
+  if (rc != FA_OK) return rc;
+  fa_selftest_wait_kernel<<<1, 32, 0, stream>>>(dev->status);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -160,6 +160,17 @@ FA_API int fa_device_status(cudaStream_t stream);
  */
 FA_API int fa_device_status_raw(cudaStream_t stream, int* raw);
 
+/*
+ * Self-test of the failure-detection path: enqueues one tiny kernel on
+ * `stream` that waits on a shared-memory barrier nothing ever signals, using
+ * the same bounded wait as every kernel of the library.  The wait gives up
+ * after about one second, records FA_ERR_TIMEOUT with site code 200 in the
+ * device status word and the kernel returns normally, so the context stays
+ * usable.  Callers then see FA_ERR_TIMEOUT from fa_device_status().
+ * Returns FA_OK once enqueued, FA_ERR_CUDA or FA_ERR_DEVICE otherwise.
+ */
+FA_API int fa_selftest_wait_timeout(cudaStream_t stream);
+
 /* Static, human-readable description of an FA_* code. */
 FA_API const char* fa_error_string(int code);
 
