@@ -11,13 +11,13 @@
 // tiles).
 //
 //  fa_bwd_dkdv_kernel: one work unit per (head, key tile j).  K_j and V_j stay
-//    in shared memory; the query tiles i stream through a two-stage ring
-//    (Q_i, dO_i, and the tile's lse2 and Delta).  Per tile, with M = keys:
+//    in shared memory; Q_i (with the tile's lse2) and dO_i (with its Delta)
+//    stream through two separate rings.  Per tile, with M = keys:
 //      S^T  = K_j Q_i^T                 -> TMEM
-//      P^T  = exp2(S^T * c - lse2)      -> fp16, shared memory
+//      P^T  = exp2(S^T * c - lse2)      -> fp16, TMEM (over S^T)
 //      dP^T = V_j dO_i^T                -> TMEM
 //      dS^T = P^T * (dP^T - Delta)      -> fp16, TMEM (over dP^T)
-//      dV_j += P^T dO_i                 (A from shared memory)
+//      dV_j += P^T dO_i                 (A from TMEM)
 //      dK_j += dS^T Q_i                 (A from TMEM)
 //    and dK_j (times scale), dV_j are written once at the end of the unit.
 //  fa_bwd_dq_kernel: one work unit per (head, query tile i).  Q_i and dO_i
@@ -50,11 +50,16 @@ struct Bwd2Traits {
   static constexpr int QC = 64;            // columns per compute warpgroup
   static constexpr int MIN_SMEM = 120 * 1024;  // keeps one CTA per SM (512 TMEM columns each)
 
-  // ---- dK/dV kernel
+  // ---- dK/dV kernel: Q ring of A_QS stages, dO ring of A_OS stages; each
+  // Q stage carries the tile's lse2, each dO stage its Delta
+  static constexpr int A_QS = (D == 64) ? 4 : 3;
+  static constexpr int A_OS = (D == 64) ? 4 : 2;
   static constexpr int A_DV = 0, A_DK = D, A_S = 2 * D, A_DP = 2 * D + BM;
-  static constexpr int A_SM_K = 0, A_SM_V = TILE, A_SM_Q = 2 * TILE, A_SM_DO = 4 * TILE, A_SM_PT = 6 * TILE;
-  static constexpr int A_SM_LD = A_SM_PT + BN * BM * 2;  // 2 stages x (lse2[128], delta[128]) fp32
-  static constexpr int A_SM_BAR = A_SM_LD + 2 * 1024;
+  static constexpr int A_SM_K = 0, A_SM_V = TILE, A_SM_Q = 2 * TILE;
+  static constexpr int A_SM_DO = A_SM_Q + A_QS * TILE;
+  static constexpr int A_SM_L2 = A_SM_DO + A_OS * TILE;       // lse2[128] per Q stage
+  static constexpr int A_SM_DL = A_SM_L2 + A_QS * BM * 4;     // Delta[128] per dO stage
+  static constexpr int A_SM_BAR = A_SM_DL + A_OS * BM * 4;
   static constexpr int A_SM_BYTES = A_SM_BAR + 256;
   static constexpr int A_SMEM = A_SM_BYTES > MIN_SMEM ? A_SM_BYTES : MIN_SMEM;
   static_assert(A_SMEM <= 232448, "dK/dV kernel shared memory budget");
@@ -119,14 +124,19 @@ constexpr int kSiteSmemAlign = 99;
 
 struct DkdvBars {
   uint64_t kv_full, kv_empty;
-  uint64_t q_full[2], q_empty[2];
-  uint64_t s_full, s_free, dp_full, p_full, dv_done, ds_full, dk_done;
+  uint64_t q_full[4], q_empty[4], o_full[4], o_empty[4];
+  uint64_t s_full, dp_full, p_full, dv_done, ds_full, dk_done;
   uint64_t dkv_full, dkv_free, mma_done[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(DkdvBars) <= 256, "barrier area");
 
+// TMEM use per key tile j: dV_j, dK_j accumulators; S^T of the current query
+// tile, overwritten in place by P^T (fp16, the A operand of dV += P^T dO);
+// dP^T, overwritten in place by dS^T (fp16, the A operand of dK += dS^T Q).
+// The next S^T waits for the dV MMA that reads P^T, the next dP^T for the dK
+// MMA that reads dS^T.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(352, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -141,19 +151,21 @@ __global__ void __launch_bounds__(352, 1)
   DkdvBars* bars = reinterpret_cast<DkdvBars*>(smem + T::A_SM_BAR);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // Two MMA warps: warp 9 issues S^T and dP^T, warp 10 issues dV and dK, so
-  // that waiting for the next query tile's data never holds back the
-  // gradient MMAs of the current one.
+  // that waiting for the next query tile never holds back the gradient MMAs
+  // of the current one.
   constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, GRAD_MMA_WARP = 10, NCOMPUTE = 256;
+  constexpr int QS = T::A_QS, OS = T::A_OS;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
     mbar_init(&bars->kv_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
+      mbar_init(&bars->o_full[i], 1);
+      mbar_init(&bars->o_empty[i], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, NCOMPUTE);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_full, NCOMPUTE);
     mbar_init(&bars->dv_done, 1);
@@ -207,23 +219,26 @@ __global__ void __launch_bounds__(352, 1)
           }
           ++kc;
           for (int i = CAUSAL ? j : 0; i < nqt; ++i) {
-            const int st = t & 1;
-            if (!(ok = mbar_wait(&bars->q_empty[st], ((t >> 1) & 1) ^ 1, wc, 52))) break;
-            mbar_arrive_expect_tx(&bars->q_full[st], 2 * T::TILE + 1024);
             const int row = head * N + i * T::BM;
-            for (int s = 0; s < T::DSUB; ++s) {
-              tma_load_2d_hint(smem + T::A_SM_Q + st * T::TILE + s * T::SUB, &tm_q, &bars->q_full[st], s * 64, row, pol_q);
-              tma_load_2d_hint(smem + T::A_SM_DO + st * T::TILE + s * T::SUB, &tm_do, &bars->q_full[st], s * 64, row,
+            const int qs = t % QS, os = t % OS;
+            if (!(ok = mbar_wait(&bars->q_empty[qs], ((t / QS) & 1) ^ 1, wc, 52))) break;
+            mbar_arrive_expect_tx(&bars->q_full[qs], T::TILE + 512);
+            for (int s = 0; s < T::DSUB; ++s)
+              tma_load_2d_hint(smem + T::A_SM_Q + qs * T::TILE + s * T::SUB, &tm_q, &bars->q_full[qs], s * 64, row, pol_q);
+            bulk_load(smem + T::A_SM_L2 + qs * 512, prm.lse2 + row, 512, &bars->q_full[qs]);
+            if (!(ok = mbar_wait(&bars->o_empty[os], ((t / OS) & 1) ^ 1, wc, 53))) break;
+            mbar_arrive_expect_tx(&bars->o_full[os], T::TILE + 512);
+            for (int s = 0; s < T::DSUB; ++s)
+              tma_load_2d_hint(smem + T::A_SM_DO + os * T::TILE + s * T::SUB, &tm_do, &bars->o_full[os], s * 64, row,
                                pol_q);
-            }
-            bulk_load(smem + T::A_SM_LD + st * 1024, prm.lse2 + row, 512, &bars->q_full[st]);
-            bulk_load(smem + T::A_SM_LD + st * 1024 + 512, prm.delta + row, 512, &bars->q_full[st]);
+            bulk_load(smem + T::A_SM_DL + os * 512, prm.delta + row, 512, &bars->o_full[os]);
             ++t;
           }
         }
       }
       if (kc > 0) bwd2_drain(&bars->kv_full, (kc - 1) & 1);
-      for (uint32_t i = (t > 2 ? t - 2 : 0); i < t; ++i) bwd2_drain(&bars->q_full[i & 1], (i >> 1) & 1);
+      for (uint32_t i = (t > QS ? t - QS : 0); i < t; ++i) bwd2_drain(&bars->q_full[i % QS], (i / QS) & 1);
+      for (uint32_t i = (t > OS ? t - OS : 0); i < t; ++i) bwd2_drain(&bars->o_full[i % OS], (i / OS) & 1);
     }
   } else if (warp == MMA_WARP) {
     // ----------------------------------- MMA warp: S^T = K Q^T, dP^T = V dO^T
@@ -232,38 +247,35 @@ __global__ void __launch_bounds__(352, 1)
     const uint64_t kdesc = sdesc_sw128(sb + T::A_SM_K, 16, 1024), vdesc = sdesc_sw128(sb + T::A_SM_V, 16, 1024);
     uint32_t t = 0, kc = 0;
     bool ok = true;
-    // S^T(tile): needs the tile's Q and the S region, free once the compute
-    // warps have read the previous S^T
-    auto issue_s = [&](uint32_t tile) -> bool {
-      if (!warp_wait(&bars->q_full[tile & 1], (tile >> 1) & 1, wc, 62)) return false;
-      if (tile > 0 && !warp_wait(&bars->s_free, (tile - 1) & 1, wc, 63)) return false;
-      tc_fence_after();
-      const uint64_t qdesc = sdesc_sw128(sb + T::A_SM_Q + (tile & 1) * T::TILE, 16, 1024);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * T::SUB + (kk % 4) * 32;
-        mma_f16_ss_warp(tmem + T::A_S, sdesc_add(kdesc, off), sdesc_add(qdesc, off), id_s, kk > 0 ? 1u : 0u);
-      }
-      mma_commit_warp(&bars->s_full);
-      return true;
-    };
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
       int head, ja, jb;
       bwd2_decode<CAUSAL>(u, nkv, head, ja, jb);
       for (int half = 0; ok && half < 2; ++half) {
         const int j = half ? jb : ja;
         if (j < 0) break;
-        const int i0 = CAUSAL ? j : 0;
         if (!(ok = warp_wait(&bars->kv_full, kc & 1, wc, 61))) break;
         tc_fence_after();
-        if (!(ok = issue_s(t))) break;
-        for (int i = i0; i < nqt; ++i) {
+        for (int i = CAUSAL ? j : 0; i < nqt; ++i) {
           const bool last = (i == nqt - 1);
-          const uint64_t odesc = sdesc_sw128(sb + T::A_SM_DO + (t & 1) * T::TILE, 16, 1024);
+          const int qs = t % QS, os = t % OS;
+          // S^T = K Q^T; the S region holds P^T of the previous tile until
+          // that tile's dV MMA has read it
+          if (!(ok = warp_wait(&bars->q_full[qs], (t / QS) & 1, wc, 62))) break;
+          if (t > 0 && !(ok = warp_wait(&bars->dv_done, (t - 1) & 1, wc, 63))) break;
+          tc_fence_after();
+          const uint64_t qdesc = sdesc_sw128(sb + T::A_SM_Q + qs * T::TILE, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * T::SUB + (kk % 4) * 32;
+            mma_f16_ss_warp(tmem + T::A_S, sdesc_add(kdesc, off), sdesc_add(qdesc, off), id_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_warp(&bars->s_full);
           // dP^T = V dO^T; the dP region holds dS^T of the previous tile until
           // that tile's dK MMA has read it
-          if (t > 0 && !(ok = warp_wait(&bars->dk_done, (t - 1) & 1, wc, 64))) break;
+          if (!(ok = warp_wait(&bars->o_full[os], (t / OS) & 1, wc, 64))) break;
+          if (t > 0 && !(ok = warp_wait(&bars->dk_done, (t - 1) & 1, wc, 65))) break;
           tc_fence_after();
+          const uint64_t odesc = sdesc_sw128(sb + T::A_SM_DO + os * T::TILE, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * T::SUB + (kk % 4) * 32;
@@ -271,7 +283,6 @@ __global__ void __launch_bounds__(352, 1)
           }
           mma_commit_warp(&bars->dp_full);
           if (last) mma_commit_warp(&bars->kv_empty);  // K_j, V_j are not read again
-          if (!last && !(ok = issue_s(t + 1))) break;
           ++t;
         }
         ++kc;
@@ -283,7 +294,6 @@ __global__ void __launch_bounds__(352, 1)
     // ---------------------------- MMA warp: dV += P^T dO, dK += dS^T Q
     constexpr uint32_t id_g = idesc_f16(128, D, false, true);  // dV, dK: N = D, B MN-major
     const uint32_t sb = smem_u32(smem);
-    const uint64_t ptdesc = sdesc_sw128(sb + T::A_SM_PT, 16, 1024);
     uint32_t t = 0, kc = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
@@ -295,21 +305,22 @@ __global__ void __launch_bounds__(352, 1)
         const int i0 = CAUSAL ? j : 0;
         for (int i = i0; i < nqt; ++i) {
           const bool first = (i == i0), last = (i == nqt - 1);
-          const int st = t & 1;
-          const uint64_t qdesc_mn = sdesc_sw128(sb + T::A_SM_Q + st * T::TILE, T::SUB, 1024);
-          const uint64_t odesc_mn = sdesc_sw128(sb + T::A_SM_DO + st * T::TILE, T::SUB, 1024);
+          const int qs = t % QS, os = t % OS;
+          const uint64_t qdesc_mn = sdesc_sw128(sb + T::A_SM_Q + qs * T::TILE, T::SUB, 1024);
+          const uint64_t odesc_mn = sdesc_sw128(sb + T::A_SM_DO + os * T::TILE, T::SUB, 1024);
           // the first tile of a unit overwrites the accumulators, which the
           // previous unit's write-out must have read
           if (first && kc > 0 && !(ok = warp_wait(&bars->dkv_free, (kc - 1) & 1, wc, 67))) break;
-          if (!(ok = warp_wait(&bars->q_full[st], (t >> 1) & 1, wc, 60))) break;
+          if (!(ok = warp_wait(&bars->o_full[os], (t / OS) & 1, wc, 60))) break;
           if (!(ok = warp_wait(&bars->p_full, t & 1, wc, 68))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < T::BM / 16; ++kk) {
-            mma_f16_ss_warp(tmem + T::A_DV, sdesc_add(ptdesc, (kk / 4) * T::SUB + (kk % 4) * 32),
-                            sdesc_add(odesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
+            const uint32_t a_t = tmem + T::A_S + (kk / 4) * T::QC + (kk % 4) * 8;
+            mma_f16_ts_warp(tmem + T::A_DV, a_t, sdesc_add(odesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
           }
           mma_commit_warp(&bars->dv_done);
+          if (!(ok = warp_wait(&bars->q_full[qs], (t / QS) & 1, wc, 59))) break;
           if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 69))) break;
           tc_fence_after();
 #pragma unroll
@@ -318,9 +329,10 @@ __global__ void __launch_bounds__(352, 1)
             mma_f16_ts_warp(tmem + T::A_DK, a_t, sdesc_add(qdesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
           }
           mma_commit_warp(&bars->dk_done);
-          // stage t is free: S^T(t) and dP^T(t) completed before the compute
-          // warps could signal p_full / ds_full
-          mma_commit_warp(&bars->q_empty[st]);
+          // Q_i and dO_i are free: S^T and dP^T of this tile completed before
+          // the compute warps could signal p_full and ds_full
+          mma_commit_warp(&bars->q_empty[qs]);
+          mma_commit_warp(&bars->o_empty[os]);
           if (last) mma_commit_warp(&bars->dkv_full);
           ++t;
         }
@@ -329,13 +341,12 @@ __global__ void __launch_bounds__(352, 1)
     }
     mma_commit_warp(&bars->mma_done[1]);
     bwd2_drain(&bars->mma_done[1], 0);
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ compute
     const int wg = warp >> 2, quad = warp & 3;
     const int row = quad * 32 + lane;  // TMEM lane = key row of the tile
     const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const float sl2 = prm.scale_log2;
-    const uint32_t sPT = smem_u32(smem + T::A_SM_PT);
     uint32_t t = 0, kc = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
@@ -346,10 +357,10 @@ __global__ void __launch_bounds__(352, 1)
         if (j < 0) break;
         const int key = j * T::BN + row;
         for (int i = CAUSAL ? j : 0; i < nqt; ++i) {
-          const int st = t & 1;
+          const int qs = t % QS, os = t % OS;
           const int q0 = i * T::BM + wg * T::QC;
-          // ---- P^T = exp2(S^T * c - lse2), fp16 into shared memory
-          ok = mbar_wait(&bars->q_full[st], (t >> 1) & 1, wc, 71) && mbar_wait(&bars->s_full, t & 1, wc, 72);
+          // ---- P^T = exp2(S^T * c - lse2), fp16 into TMEM over S^T
+          ok = mbar_wait(&bars->q_full[qs], (t / QS) & 1, wc, 71) && mbar_wait(&bars->s_full, t & 1, wc, 72);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
           uint32_t sr[T::QC];
@@ -357,9 +368,7 @@ __global__ void __launch_bounds__(352, 1)
           tmem_ld32(lb + T::A_S + wg * T::QC + 32, sr + 32);
           tmem_wait_ld();
           reg_fence<T::QC>(sr);
-          tc_fence_before();
-          mbar_arrive(&bars->s_free);
-          const float4* l4 = reinterpret_cast<const float4*>(smem + T::A_SM_LD + st * 1024) + wg * (T::QC / 4);
+          const float4* l4 = reinterpret_cast<const float4*>(smem + T::A_SM_L2 + qs * 512) + wg * (T::QC / 4);
           float p[T::QC];
 #pragma unroll
           for (int c = 0; c < T::QC; c += 4) {
@@ -374,28 +383,22 @@ __global__ void __launch_bounds__(352, 1)
             for (int c = 0; c < T::QC; ++c)
               if (key > q0 + c) p[c] = 0.f;
           }
-          if (t > 0) {  // the P^T buffer is free once the previous tile's dV read it
-            ok = mbar_wait(&bars->dv_done, (t - 1) & 1, wc, 73);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          }
+          uint32_t pk[T::QC / 2];
 #pragma unroll
-          for (int c = 0; c < T::QC; c += 8) {
-            const uint32_t addr = sPT + wg * T::SUB + row * 128 + (((c / 8) ^ (row & 7)) * 16);
-            st_shared_v4(addr, pack_half2(p[c], p[c + 1]), pack_half2(p[c + 2], p[c + 3]),
-                         pack_half2(p[c + 4], p[c + 5]), pack_half2(p[c + 6], p[c + 7]));
-          }
-          fence_proxy_async_smem();
+          for (int c = 0; c < T::QC / 2; ++c) pk[c] = pack_half2(p[2 * c], p[2 * c + 1]);
+          tmem_st32(lb + T::A_S + wg * T::QC, pk);
+          tmem_wait_st();
+          tc_fence_before();
           mbar_arrive(&bars->p_full);
           // ---- dS^T = P^T * (dP^T - Delta), fp16 into TMEM over dP^T
-          ok = mbar_wait(&bars->dp_full, t & 1, wc, 74);
+          ok = mbar_wait(&bars->o_full[os], (t / OS) & 1, wc, 73) && mbar_wait(&bars->dp_full, t & 1, wc, 74);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
           tmem_ld32(lb + T::A_DP + wg * T::QC, sr);
           tmem_ld32(lb + T::A_DP + wg * T::QC + 32, sr + 32);
           tmem_wait_ld();
           reg_fence<T::QC>(sr);
-          const float4* d4 = reinterpret_cast<const float4*>(smem + T::A_SM_LD + st * 1024 + 512) + wg * (T::QC / 4);
-          uint32_t pk[T::QC / 2];
+          const float4* d4 = reinterpret_cast<const float4*>(smem + T::A_SM_DL + os * 512) + wg * (T::QC / 4);
 #pragma unroll
           for (int c = 0; c < T::QC; c += 4) {
             const float4 Dl = d4[c / 4];
