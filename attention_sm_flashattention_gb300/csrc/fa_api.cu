@@ -205,11 +205,14 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < ws.total) return FA_ERR_WORKSPACE;
 
   const long long rows = static_cast<long long>(Z) * H * N;
-  // maps: q, k, v, dout (fp16, box rows chosen by the kernel's tiling)
-  CUtensorMap maps[4];
+  // maps: q, k, v, dout (fp16, box rows chosen by the kernel's tiling), then
+  // the outputs dq, dk, dv (written with TMA stores by the D <= 128 kernels)
+  CUtensorMap maps[7];
   const int bq = (D == 256) ? 64 : 128;
   if (!fp16_map(&maps[0], q, rows, D, bq) || !fp16_map(&maps[1], k, rows, D, 128) ||
-      !fp16_map(&maps[2], v, rows, D, 128) || !fp16_map(&maps[3], dout, rows, D, bq))
+      !fp16_map(&maps[2], v, rows, D, 128) || !fp16_map(&maps[3], dout, rows, D, bq) ||
+      !fp16_map(&maps[4], dq, rows, D, 128) || !fp16_map(&maps[5], dk, rows, D, 128) ||
+      !fp16_map(&maps[6], dv, rows, D, 128))
     return FA_ERR_CUDA;
   char* wsb = static_cast<char*>(workspace);
   fa::BwdParams prm{};
@@ -312,10 +315,12 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   if (scratch == nullptr) return FA_ERR_CUDA;
 
   const long long rows = heads * N;
-  CUtensorMap maps[4];
+  CUtensorMap maps[7];
   const int bq = (D == 256) ? 64 : 128;
   if (!fp16_map(&maps[0], q, rows, D, bq) || !fp16_map(&maps[1], k, rows, D, 128) ||
-      !fp16_map(&maps[2], v, rows, D, 128) || !fp16_map(&maps[3], dout, rows, D, bq))
+      !fp16_map(&maps[2], v, rows, D, 128) || !fp16_map(&maps[3], dout, rows, D, bq) ||
+      !fp16_map(&maps[4], dq, rows, D, 128) || !fp16_map(&maps[5], dk, rows, D, 128) ||
+      !fp16_map(&maps[6], dv, rows, D, 128))
     return FA_ERR_CUDA;
   fa::BwdParams prm{};
   prm.o = static_cast<const __half*>(o);

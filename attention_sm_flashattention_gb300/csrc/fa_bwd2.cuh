@@ -116,6 +116,18 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
+// Write 32 fp16 values (16 packed words) of row `row`, columns col0..col0+31
+// (col0 a multiple of 32) into a [128 x D] tile laid out as 128-byte-swizzled
+// [128 x 64] sub-tiles -- the layout a TMA store of 64 x 128 boxes reads.
+__device__ __forceinline__ void stage_row32(uint32_t tile, int row, int col0, const uint32_t* h) {
+  const uint32_t base = tile + (col0 / 64) * (128 * 128) + row * 128;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int ch = ((col0 % 64) / 8 + i) ^ (row & 7);
+    st_shared_v4(base + ch * 16, h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+  }
+}
+
 // Site code reported when the dynamic shared memory base is not 1024-byte
 // aligned (the 128-byte-swizzled tiles need it); the kernel then does nothing.
 constexpr int kSiteSmemAlign = 99;
@@ -125,22 +137,34 @@ constexpr int kSiteSmemAlign = 99;
 struct DkdvBars {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[4], q_empty[4], o_full[4], o_empty[4];
-  uint64_t s_full, dp_full, p_full, dv_done, ds_full, dk_done;
-  uint64_t dkv_full, dkv_free, mma_done[2];
+  uint64_t s_full, s_free, dp_full, p_full, ds_full, dk_done;
+  uint64_t dkv_full, dkv_free, epi_full, mma_done[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(DkdvBars) <= 256, "barrier area");
 
 // TMEM use per key tile j: dV_j, dK_j accumulators; S^T of the current query
-// tile, overwritten in place by P^T (fp16, the A operand of dV += P^T dO);
-// dP^T, overwritten in place by dS^T (fp16, the A operand of dK += dS^T Q).
-// The next S^T waits for the dV MMA that reads P^T, the next dP^T for the dK
-// MMA that reads dS^T.
+// tile (read into registers at once, so the next S^T can be computed while
+// this tile is still being worked on); dP^T, overwritten in place by P^T and
+// dS^T in fp16 (the A operands of dV += P^T dO and dK += dS^T Q).  Per
+// warpgroup half of the 128 query columns, P^T takes the first 32 TMEM
+// columns and dS^T the next 32.  The next dP^T waits for the dK MMA of this
+// tile (issued after its dV MMA), the next S^T only for the compute warps to
+// have read this one; warp 9 issues S^T of tile i+1 right after dP^T of tile
+// i, so that it runs while the compute warps turn dP^T into P^T and dS^T.
+//
+// Unit boundaries: K_j and V_j are released after the last dP^T of the unit,
+// so the next unit's K, V load overlaps the unit's last dV, dK MMAs and its
+// write-out.  dK_j and dV_j are staged in the Q and dO ring slots of the
+// unit's last query tile (free once its dK and dV MMAs completed) and written
+// with TMA stores by warp 11, which then hands those two slots back to the
+// producer.
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                        const BwdParams prm) {
   using T = Bwd2Traits<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -150,10 +174,7 @@ __global__ void __launch_bounds__(352, 1)
   }
   DkdvBars* bars = reinterpret_cast<DkdvBars*>(smem + T::A_SM_BAR);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Two MMA warps: warp 9 issues S^T and dP^T, warp 10 issues dV and dK, so
-  // that waiting for the next query tile never holds back the gradient MMAs
-  // of the current one.
-  constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, GRAD_MMA_WARP = 10, NCOMPUTE = 256;
+  constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, GRAD_MMA_WARP = 10, STORE_WARP = 11, NCOMPUTE = 256;
   constexpr int QS = T::A_QS, OS = T::A_OS;
 
   if (threadIdx.x == 0) {
@@ -166,13 +187,14 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(&bars->o_empty[i], 1);
     }
     mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, NCOMPUTE);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_full, NCOMPUTE);
-    mbar_init(&bars->dv_done, 1);
     mbar_init(&bars->ds_full, NCOMPUTE);
     mbar_init(&bars->dk_done, 1);
     mbar_init(&bars->dkv_full, 1);
     mbar_init(&bars->dkv_free, NCOMPUTE);
+    mbar_init(&bars->epi_full, NCOMPUTE);
     mbar_init(&bars->mma_done[0], 1);
     mbar_init(&bars->mma_done[1], 1);
     bars->abort_flag = 0;
@@ -187,6 +209,9 @@ __global__ void __launch_bounds__(352, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+  } else if (warp == STORE_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_dk);
+    tma_prefetch_desc(&tm_dv);
   }
   tc_fence_before();
   __syncthreads();
@@ -247,6 +272,22 @@ __global__ void __launch_bounds__(352, 1)
     const uint64_t kdesc = sdesc_sw128(sb + T::A_SM_K, 16, 1024), vdesc = sdesc_sw128(sb + T::A_SM_V, 16, 1024);
     uint32_t t = 0, kc = 0;
     bool ok = true;
+    // S^T(tile) = K Q^T into the S region, free once the compute warps have
+    // read the previous tile's S^T
+    auto issue_s = [&](uint32_t tile) -> bool {
+      const int qs = tile % QS;
+      if (!warp_wait(&bars->q_full[qs], (tile / QS) & 1, wc, 62)) return false;
+      if (tile > 0 && !warp_wait(&bars->s_free, (tile - 1) & 1, wc, 63)) return false;
+      tc_fence_after();
+      const uint64_t qdesc = sdesc_sw128(sb + T::A_SM_Q + qs * T::TILE, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * T::SUB + (kk % 4) * 32;
+        mma_f16_ss_warp(tmem + T::A_S, sdesc_add(kdesc, off), sdesc_add(qdesc, off), id_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_warp(&bars->s_full);
+      return true;
+    };
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
       int head, ja, jb;
       bwd2_decode<CAUSAL>(u, nkv, head, ja, jb);
@@ -255,23 +296,12 @@ __global__ void __launch_bounds__(352, 1)
         if (j < 0) break;
         if (!(ok = warp_wait(&bars->kv_full, kc & 1, wc, 61))) break;
         tc_fence_after();
+        if (!(ok = issue_s(t))) break;
         for (int i = CAUSAL ? j : 0; i < nqt; ++i) {
           const bool last = (i == nqt - 1);
-          const int qs = t % QS, os = t % OS;
-          // S^T = K Q^T; the S region holds P^T of the previous tile until
-          // that tile's dV MMA has read it
-          if (!(ok = warp_wait(&bars->q_full[qs], (t / QS) & 1, wc, 62))) break;
-          if (t > 0 && !(ok = warp_wait(&bars->dv_done, (t - 1) & 1, wc, 63))) break;
-          tc_fence_after();
-          const uint64_t qdesc = sdesc_sw128(sb + T::A_SM_Q + qs * T::TILE, 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * T::SUB + (kk % 4) * 32;
-            mma_f16_ss_warp(tmem + T::A_S, sdesc_add(kdesc, off), sdesc_add(qdesc, off), id_s, kk > 0 ? 1u : 0u);
-          }
-          mma_commit_warp(&bars->s_full);
-          // dP^T = V dO^T; the dP region holds dS^T of the previous tile until
-          // that tile's dK MMA has read it
+          const int os = t % OS;
+          // dP^T = V dO^T; the dP region holds P^T and dS^T of the previous
+          // tile until that tile's dK MMA (issued after its dV MMA) completed
           if (!(ok = warp_wait(&bars->o_full[os], (t / OS) & 1, wc, 64))) break;
           if (t > 0 && !(ok = warp_wait(&bars->dk_done, (t - 1) & 1, wc, 65))) break;
           tc_fence_after();
@@ -282,7 +312,11 @@ __global__ void __launch_bounds__(352, 1)
             mma_f16_ss_warp(tmem + T::A_DP, sdesc_add(vdesc, off), sdesc_add(odesc, off), id_s, kk > 0 ? 1u : 0u);
           }
           mma_commit_warp(&bars->dp_full);
-          if (last) mma_commit_warp(&bars->kv_empty);  // K_j, V_j are not read again
+          if (last) {
+            mma_commit_warp(&bars->kv_empty);  // K_j, V_j are not read again
+          } else if (!(ok = issue_s(t + 1))) {
+            break;
+          }
           ++t;
         }
         ++kc;
@@ -316,24 +350,29 @@ __global__ void __launch_bounds__(352, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < T::BM / 16; ++kk) {
-            const uint32_t a_t = tmem + T::A_S + (kk / 4) * T::QC + (kk % 4) * 8;
+            const uint32_t a_t = tmem + T::A_DP + (kk / 4) * T::QC + (kk % 4) * 8;
             mma_f16_ts_warp(tmem + T::A_DV, a_t, sdesc_add(odesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
           }
-          mma_commit_warp(&bars->dv_done);
           if (!(ok = warp_wait(&bars->q_full[qs], (t / QS) & 1, wc, 59))) break;
           if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 69))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < T::BM / 16; ++kk) {
-            const uint32_t a_t = tmem + T::A_DP + (kk / 4) * T::QC + (kk % 4) * 8;
+            const uint32_t a_t = tmem + T::A_DP + T::QC / 2 + (kk / 4) * T::QC + (kk % 4) * 8;
             mma_f16_ts_warp(tmem + T::A_DK, a_t, sdesc_add(qdesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
           }
+          // dV and dK of this tile (in issue order) have read P^T and dS^T
           mma_commit_warp(&bars->dk_done);
-          // Q_i and dO_i are free: S^T and dP^T of this tile completed before
-          // the compute warps could signal p_full and ds_full
-          mma_commit_warp(&bars->q_empty[qs]);
-          mma_commit_warp(&bars->o_empty[os]);
-          if (last) mma_commit_warp(&bars->dkv_full);
+          if (last) {
+            // the Q and dO slots of the last tile receive dK_j and dV_j; the
+            // store warp releases them after writing those out
+            mma_commit_warp(&bars->dkv_full);
+          } else {
+            // Q_i and dO_i are free: S^T and dP^T of this tile completed
+            // before the compute warps could signal p_full and ds_full
+            mma_commit_warp(&bars->q_empty[qs]);
+            mma_commit_warp(&bars->o_empty[os]);
+          }
           ++t;
         }
         ++kc;
@@ -341,7 +380,37 @@ __global__ void __launch_bounds__(352, 1)
     }
     mma_commit_warp(&bars->mma_done[1]);
     bwd2_drain(&bars->mma_done[1], 0);
-  } else if (warp < 8) {
+  } else if (warp == STORE_WARP) {
+    // -------------- write dK_j, dV_j (staged by the compute warps in the Q
+    // and dO slots of the unit's last tile), then release those slots
+    uint32_t t = 0, kc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      int head, ja, jb;
+      bwd2_decode<CAUSAL>(u, nkv, head, ja, jb);
+      for (int half = 0; ok && half < 2; ++half) {
+        const int j = half ? jb : ja;
+        if (j < 0) break;
+        t += nqt - (CAUSAL ? j : 0);
+        const int qs = (t - 1) % QS, os = (t - 1) % OS;
+        if (!(ok = warp_wait(&bars->epi_full, kc & 1, wc, 58))) break;
+        if (lane == 0) {
+          for (int s = 0; s < T::DSUB; ++s) {
+            tma_store_2d(&tm_dk, smem + T::A_SM_Q + qs * T::TILE + s * T::SUB, s * 64, head * N + j * T::BN);
+            tma_store_2d(&tm_dv, smem + T::A_SM_DO + os * T::TILE + s * T::SUB, s * 64, head * N + j * T::BN);
+          }
+          bulk_commit();
+          bulk_wait_read<0>();
+          mbar_arrive(&bars->q_empty[qs]);
+          mbar_arrive(&bars->o_empty[os]);
+        }
+        __syncwarp();
+        ++kc;
+      }
+    }
+    if (lane == 0) bulk_wait<0>();  // all stores complete before the CTA exits
+    __syncwarp();
+  } else {
     // ------------------------------------------------------------ compute
     const int wg = warp >> 2, quad = warp & 3;
     const int row = quad * 32 + lane;  // TMEM lane = key row of the tile
@@ -359,7 +428,7 @@ __global__ void __launch_bounds__(352, 1)
         for (int i = CAUSAL ? j : 0; i < nqt; ++i) {
           const int qs = t % QS, os = t % OS;
           const int q0 = i * T::BM + wg * T::QC;
-          // ---- P^T = exp2(S^T * c - lse2), fp16 into TMEM over S^T
+          // ---- P^T = exp2(S^T * c - lse2); S^T is free once read
           ok = mbar_wait(&bars->q_full[qs], (t / QS) & 1, wc, 71) && mbar_wait(&bars->s_full, t & 1, wc, 72);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
@@ -368,6 +437,8 @@ __global__ void __launch_bounds__(352, 1)
           tmem_ld32(lb + T::A_S + wg * T::QC + 32, sr + 32);
           tmem_wait_ld();
           reg_fence<T::QC>(sr);
+          tc_fence_before();
+          mbar_arrive(&bars->s_free);
           const float4* l4 = reinterpret_cast<const float4*>(smem + T::A_SM_L2 + qs * 512) + wg * (T::QC / 4);
           float p[T::QC];
 #pragma unroll
@@ -383,63 +454,75 @@ __global__ void __launch_bounds__(352, 1)
             for (int c = 0; c < T::QC; ++c)
               if (key > q0 + c) p[c] = 0.f;
           }
+          // ---- P^T (fp16) over the first half of dP^T once that half is
+          // read; dS^T = P^T * (dP^T - Delta) over the second half.  The
+          // halves are read one at a time to keep register pressure low.
           uint32_t pk[T::QC / 2];
 #pragma unroll
           for (int c = 0; c < T::QC / 2; ++c) pk[c] = pack_half2(p[2 * c], p[2 * c + 1]);
-          tmem_st32(lb + T::A_S + wg * T::QC, pk);
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(&bars->p_full);
-          // ---- dS^T = P^T * (dP^T - Delta), fp16 into TMEM over dP^T
           ok = mbar_wait(&bars->o_full[os], (t / OS) & 1, wc, 73) && mbar_wait(&bars->dp_full, t & 1, wc, 74);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
           tmem_ld32(lb + T::A_DP + wg * T::QC, sr);
-          tmem_ld32(lb + T::A_DP + wg * T::QC + 32, sr + 32);
           tmem_wait_ld();
-          reg_fence<T::QC>(sr);
+          reg_fence<32>(sr);
+          tmem_st32(lb + T::A_DP + wg * T::QC, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bars->p_full);
           const float4* d4 = reinterpret_cast<const float4*>(smem + T::A_SM_DL + os * 512) + wg * (T::QC / 4);
 #pragma unroll
-          for (int c = 0; c < T::QC; c += 4) {
-            const float4 Dl = d4[c / 4];
-            pk[c / 2] = pack_half2(p[c] * (__uint_as_float(sr[c]) - Dl.x), p[c + 1] * (__uint_as_float(sr[c + 1]) - Dl.y));
-            pk[c / 2 + 1] =
-                pack_half2(p[c + 2] * (__uint_as_float(sr[c + 2]) - Dl.z), p[c + 3] * (__uint_as_float(sr[c + 3]) - Dl.w));
+          for (int h = 0; h < 2; ++h) {
+            if (h == 1) {
+              tmem_ld32(lb + T::A_DP + wg * T::QC + 32, sr);
+              tmem_wait_ld();
+              reg_fence<32>(sr);
+            }
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              const float4 Dl = d4[(32 * h + c) / 4];
+              const float* ph = p + 32 * h;
+              pk[16 * h + c / 2] =
+                  pack_half2(ph[c] * (__uint_as_float(sr[c]) - Dl.x), ph[c + 1] * (__uint_as_float(sr[c + 1]) - Dl.y));
+              pk[16 * h + c / 2 + 1] = pack_half2(ph[c + 2] * (__uint_as_float(sr[c + 2]) - Dl.z),
+                                                  ph[c + 3] * (__uint_as_float(sr[c + 3]) - Dl.w));
+            }
           }
-          tmem_st32(lb + T::A_DP + wg * T::QC, pk);
+          tmem_st32(lb + T::A_DP + wg * T::QC + T::QC / 2, pk);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->ds_full);
           ++t;
         }
         if (!ok) break;
-        // ---- write dV_j and dK_j (times scale) once
+        // ---- dV_j and dK_j (times scale) -> fp16, staged in the dO and Q
+        // slots of the unit's last tile; the store warp writes them out
         ok = mbar_wait(&bars->dkv_full, kc & 1, wc, 75);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        const size_t orow = (static_cast<size_t>(head) * N + key) * D + wg * (D / 2);
+        const int ql = (t - 1) % QS, ol = (t - 1) % OS;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           const uint32_t col = (which == 0 ? T::A_DV : T::A_DK) + wg * (D / 2);
           const float mul = which == 0 ? 1.f : prm.scale;
-          __half* out = (which == 0 ? prm.dv : prm.dk) + orow;
+          const uint32_t tile = smem_u32(smem + (which == 0 ? T::A_SM_DO + ol * T::TILE : T::A_SM_Q + ql * T::TILE));
 #pragma unroll
           for (int c = 0; c < D / 2; c += 32) {
             uint32_t v[32];
             tmem_ld32(lb + col + c, v);
             tmem_wait_ld();
             reg_fence<32>(v);
-            uint4* dst = reinterpret_cast<uint4*>(out + c);
+            uint32_t h[16];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              dst[e] = make_uint4(pack_half2(__uint_as_float(v[8 * e]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
-                                  pack_half2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
-                                  pack_half2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
-                                  pack_half2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
+            for (int e = 0; e < 16; ++e)
+              h[e] = pack_half2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+            stage_row32(tile, row, wg * (D / 2) + c, h);
           }
         }
+        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bars->dkv_free);
+        mbar_arrive(&bars->epi_full);
         ++kc;
       }
     }
@@ -461,6 +544,7 @@ struct DqBars {
   uint64_t s_full, s_free;
   uint64_t dp_full[2], ds_full[2], dq_done[2];
   uint64_t dq_full, dq_free, mma_done[2];
+  uint64_t epi_full;  // dQ_i staged in the Q buffer
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -470,7 +554,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                     const BwdParams prm) {
+                     const __grid_constant__ CUtensorMap tm_dq, const BwdParams prm) {
   using T = Bwd2Traits<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
@@ -487,6 +571,7 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->epi_full, NCOMPUTE);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
@@ -678,16 +763,36 @@ __global__ void __launch_bounds__(384, 1)
             mma_f16_ts_warp(tmem + T::B_DQ, a_t, sdesc_add(kdesc_mn, kk * 2048), id_q, (first && kk == 0) ? 0u : 1u);
           }
           mma_commit_warp(&bars->dq_done[pb]);
-          // K_j is free: S of this tile completed before the compute warps
-          // could signal ds_full
-          mma_commit_warp(&bars->k_empty[ks]);
-          if (last) mma_commit_warp(&bars->dq_full);
+          if (last) {
+            // the K slot of the last tile receives dQ_i; it is released once
+            // dQ_i has been written out
+            mma_commit_warp(&bars->dq_full);
+          } else {
+            // K_j is free: S of this tile completed before the compute warps
+            // could signal ds_full
+            mma_commit_warp(&bars->k_empty[ks]);
+          }
           ++t;
           ++k_it;
         }
+        if (!ok) break;
+        // the compute warps stage dQ_i in the K slot of the last tile; store
+        // it with TMA, then release the slot for the next K load
+        if (!(ok = warp_wait(&bars->epi_full, qc & 1, wc, 98))) break;
+        if (lane == 0) {
+          const int kl = (k_it - 1) % KS;
+          for (int s = 0; s < T::DSUB; ++s)
+            tma_store_2d(&tm_dq, smem + T::B_SM_K + kl * T::TILE + s * T::SUB, s * 64, head * N + i * T::BM);
+          bulk_commit();
+          bulk_wait_read<0>();
+          mbar_arrive(&bars->k_empty[kl]);
+        }
+        __syncwarp();
         ++qc;
       }
     }
+    if (lane == 0) bulk_wait<0>();  // all stores complete before the CTA exits
+    __syncwarp();
     mma_commit_warp(&bars->mma_done[1]);
     bwd2_drain(&bars->mma_done[1], 0);
   } else {
@@ -750,11 +855,12 @@ __global__ void __launch_bounds__(384, 1)
           ++t;
         }
         if (!ok) break;
-        // ---- write dQ_i (times scale) once
+        // ---- dQ_i (times scale) -> fp16, staged in the K slot of the last
+        // tile (no longer read); the dQ MMA warp stores it
         ok = mbar_wait(&bars->dq_full, qc & 1, wc, 103);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        __half* out = prm.dq + grow * D + wg * (D / 2);
+        const uint32_t tile = smem_u32(smem + T::B_SM_K + ((t - 1) % KS) * T::TILE);
 #pragma unroll
         for (int c = 0; c < D / 2; c += 32) {
           uint32_t v[32];
@@ -762,16 +868,15 @@ __global__ void __launch_bounds__(384, 1)
           tmem_wait_ld();
           reg_fence<32>(v);
           const float sc = prm.scale;
-          uint4* dst = reinterpret_cast<uint4*>(out + c);
+          uint32_t h[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(pack_half2(__uint_as_float(v[8 * e]) * sc, __uint_as_float(v[8 * e + 1]) * sc),
-                                pack_half2(__uint_as_float(v[8 * e + 2]) * sc, __uint_as_float(v[8 * e + 3]) * sc),
-                                pack_half2(__uint_as_float(v[8 * e + 4]) * sc, __uint_as_float(v[8 * e + 5]) * sc),
-                                pack_half2(__uint_as_float(v[8 * e + 6]) * sc, __uint_as_float(v[8 * e + 7]) * sc));
+          for (int e = 0; e < 16; ++e) h[e] = pack_half2(__uint_as_float(v[2 * e]) * sc, __uint_as_float(v[2 * e + 1]) * sc);
+          stage_row32(tile, row, wg * (D / 2) + c, h);
         }
+        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bars->dq_free);
+        mbar_arrive(&bars->epi_full);
         ++qc;
       }
     }
@@ -807,9 +912,10 @@ int launch_bwd2(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, cud
   const int nt = prm.N / 128;
   const int units = CAUSAL ? prm.heads * ((nt + 1) / 2) : prm.heads * nt;
   const int grid = units < max_ctas ? units : max_ctas;
-  fa_bwd_dkdv_kernel<D, CAUSAL><<<grid, 352, T::A_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  fa_bwd_dkdv_kernel<D, CAUSAL><<<grid, 384, T::A_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[5],
+                                                                   maps[6], prm);
   if (cudaGetLastError() != cudaSuccess) return -1;
-  fa_bwd_dq_kernel<D, CAUSAL><<<grid, 384, T::B_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  fa_bwd_dq_kernel<D, CAUSAL><<<grid, 384, T::B_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

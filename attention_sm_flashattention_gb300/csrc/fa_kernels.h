@@ -43,6 +43,7 @@ struct BwdParams {
 #define FA_DECLARE_LAUNCHERS(D)                                                                      \
   int launch_fwd_d##D(bool causal, const CUtensorMap* maps, const FwdParams& prm, int num_sms,      \
                       cudaStream_t stream);                                                           \
+  /* bwd maps: q, k, v, dout, dq, dk, dv */                                                         \
   int launch_bwd_d##D(bool causal, const CUtensorMap* maps, const BwdParams& prm, int grid,          \
                       cudaStream_t stream);
 
