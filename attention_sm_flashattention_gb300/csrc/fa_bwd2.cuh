@@ -54,7 +54,7 @@ struct Bwd2Traits {
   // Q stage carries the tile's lse2, each dO stage its Delta
   static constexpr int A_QS = (D == 64) ? 4 : 3;
   static constexpr int A_OS = (D == 64) ? 4 : 2;
-  static constexpr int A_DV = 0, A_DK = D, A_S = 2 * D, A_DP = 2 * D + BM;
+  static constexpr int A_DV = 0, A_DK = D, A_R = 2 * D;  // region r of the query tiles at A_R + r * BM
   static constexpr int A_SM_K = 0, A_SM_V = TILE, A_SM_Q = 2 * TILE;
   static constexpr int A_SM_DO = A_SM_Q + A_QS * TILE;
   static constexpr int A_SM_L2 = A_SM_DO + A_OS * TILE;       // lse2[128] per Q stage
@@ -63,7 +63,7 @@ struct Bwd2Traits {
   static constexpr int A_SM_BYTES = A_SM_BAR + 256;
   static constexpr int A_SMEM = A_SM_BYTES > MIN_SMEM ? A_SM_BYTES : MIN_SMEM;
   static_assert(A_SMEM <= 232448, "dK/dV kernel shared memory budget");
-  static_assert(A_DP + BM <= 512, "dK/dV kernel TMEM budget");
+  static_assert(A_R + 2 * BM <= 512, "dK/dV kernel TMEM budget");
 
   // ---- dQ kernel
   static constexpr int B_K_STAGES = (D == 64) ? 4 : 3;
@@ -137,22 +137,22 @@ constexpr int kSiteSmemAlign = 99;
 struct DkdvBars {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[4], q_empty[4], o_full[4], o_empty[4];
-  uint64_t s_full, s_free, dp_full, p_full, ds_full, dk_done;
+  uint64_t s_full, s_free, dp_full, p_full, ds_full, dk_done[2];
   uint64_t dkv_full, dkv_free, epi_full, mma_done[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(DkdvBars) <= 256, "barrier area");
 
-// TMEM use per key tile j: dV_j, dK_j accumulators; S^T of the current query
-// tile (read into registers at once, so the next S^T can be computed while
-// this tile is still being worked on); dP^T, overwritten in place by P^T and
-// dS^T in fp16 (the A operands of dV += P^T dO and dK += dS^T Q).  Per
-// warpgroup half of the 128 query columns, P^T takes the first 32 TMEM
-// columns and dS^T the next 32.  The next dP^T waits for the dK MMA of this
-// tile (issued after its dV MMA), the next S^T only for the compute warps to
-// have read this one; warp 9 issues S^T of tile i+1 right after dP^T of tile
-// i, so that it runs while the compute warps turn dP^T into P^T and dS^T.
+// TMEM use per key tile j: the dV_j and dK_j accumulators and two 128-column
+// regions that the query tiles use in turn.  Query tile t works in region
+// t % 2 from start to end: S^T, read into registers at once; then dP^T in
+// the same columns; then P^T and dS^T in fp16 (the A operands of dV += P^T
+// dO and dK += dS^T Q; per warpgroup half of the 128 query columns, P^T
+// takes the first 32 TMEM columns and dS^T the next 32).  A region is free
+// again once the tile's dK MMA (issued after its dV MMA) completed, so the
+// MMAs of tile t+1 run in the other region while the compute warps turn dP^T
+// of tile t into P^T and dS^T, and no tile waits on the previous one's MMAs.
 //
 // Unit boundaries: K_j and V_j are released after the last dP^T of the unit,
 // so the next unit's K, V load overlaps the unit's last dV, dK MMAs and its
@@ -191,7 +191,8 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_full, NCOMPUTE);
     mbar_init(&bars->ds_full, NCOMPUTE);
-    mbar_init(&bars->dk_done, 1);
+    mbar_init(&bars->dk_done[0], 1);
+    mbar_init(&bars->dk_done[1], 1);
     mbar_init(&bars->dkv_full, 1);
     mbar_init(&bars->dkv_free, NCOMPUTE);
     mbar_init(&bars->epi_full, NCOMPUTE);
@@ -257,6 +258,8 @@ __global__ void __launch_bounds__(384, 1)
               tma_load_2d_hint(smem + T::A_SM_DO + os * T::TILE + s * T::SUB, &tm_do, &bars->o_full[os], s * 64, row,
                                pol_q);
             bulk_load(smem + T::A_SM_DL + os * 512, prm.delta + row, 512, &bars->o_full[os]);
+            // warm L2 with the tiles that will refill these slots, so their
+            // loads are short once the slots free up
             ++t;
           }
         }
@@ -272,18 +275,19 @@ __global__ void __launch_bounds__(384, 1)
     const uint64_t kdesc = sdesc_sw128(sb + T::A_SM_K, 16, 1024), vdesc = sdesc_sw128(sb + T::A_SM_V, 16, 1024);
     uint32_t t = 0, kc = 0;
     bool ok = true;
-    // S^T(tile) = K Q^T into the S region, free once the compute warps have
-    // read the previous tile's S^T
+    // S^T(tile) = K Q^T into region tile % 2, free once the dK MMA of tile
+    // - 2 completed
     auto issue_s = [&](uint32_t tile) -> bool {
-      const int qs = tile % QS;
+      const int qs = tile % QS, r = tile & 1;
       if (!warp_wait(&bars->q_full[qs], (tile / QS) & 1, wc, 62)) return false;
-      if (tile > 0 && !warp_wait(&bars->s_free, (tile - 1) & 1, wc, 63)) return false;
+      if (tile >= 2 && !warp_wait(&bars->dk_done[r], ((tile - 2) >> 1) & 1, wc, 63)) return false;
       tc_fence_after();
       const uint64_t qdesc = sdesc_sw128(sb + T::A_SM_Q + qs * T::TILE, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk / 4) * T::SUB + (kk % 4) * 32;
-        mma_f16_ss_warp(tmem + T::A_S, sdesc_add(kdesc, off), sdesc_add(qdesc, off), id_s, kk > 0 ? 1u : 0u);
+        mma_f16_ss_warp(tmem + T::A_R + r * T::BM, sdesc_add(kdesc, off), sdesc_add(qdesc, off), id_s,
+                        kk > 0 ? 1u : 0u);
       }
       mma_commit_warp(&bars->s_full);
       return true;
@@ -300,16 +304,17 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = CAUSAL ? j : 0; i < nqt; ++i) {
           const bool last = (i == nqt - 1);
           const int os = t % OS;
-          // dP^T = V dO^T; the dP region holds P^T and dS^T of the previous
-          // tile until that tile's dK MMA (issued after its dV MMA) completed
+          // dP^T = V dO^T over S^T in the tile's region, once the compute
+          // warps have read S^T
           if (!(ok = warp_wait(&bars->o_full[os], (t / OS) & 1, wc, 64))) break;
-          if (t > 0 && !(ok = warp_wait(&bars->dk_done, (t - 1) & 1, wc, 65))) break;
+          if (!(ok = warp_wait(&bars->s_free, t & 1, wc, 65))) break;
           tc_fence_after();
           const uint64_t odesc = sdesc_sw128(sb + T::A_SM_DO + os * T::TILE, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * T::SUB + (kk % 4) * 32;
-            mma_f16_ss_warp(tmem + T::A_DP, sdesc_add(vdesc, off), sdesc_add(odesc, off), id_s, kk > 0 ? 1u : 0u);
+            mma_f16_ss_warp(tmem + T::A_R + (t & 1) * T::BM, sdesc_add(vdesc, off), sdesc_add(odesc, off), id_s,
+                            kk > 0 ? 1u : 0u);
           }
           mma_commit_warp(&bars->dp_full);
           if (last) {
@@ -350,28 +355,31 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < T::BM / 16; ++kk) {
-            const uint32_t a_t = tmem + T::A_DP + (kk / 4) * T::QC + (kk % 4) * 8;
+            const uint32_t a_t = tmem + T::A_R + (t & 1) * T::BM + (kk / 4) * T::QC + (kk % 4) * 8;
             mma_f16_ts_warp(tmem + T::A_DV, a_t, sdesc_add(odesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
           }
+          // dO_i is free once this dV MMA completed (dP^T of the tile
+          // completed before the compute warps could signal p_full); the
+          // last tile's slot receives dV_j and is released by the store warp
+          if (!last) mma_commit_warp(&bars->o_empty[os]);
           if (!(ok = warp_wait(&bars->q_full[qs], (t / QS) & 1, wc, 59))) break;
           if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 69))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < T::BM / 16; ++kk) {
-            const uint32_t a_t = tmem + T::A_DP + T::QC / 2 + (kk / 4) * T::QC + (kk % 4) * 8;
+            const uint32_t a_t = tmem + T::A_R + (t & 1) * T::BM + T::QC / 2 + (kk / 4) * T::QC + (kk % 4) * 8;
             mma_f16_ts_warp(tmem + T::A_DK, a_t, sdesc_add(qdesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
           }
           // dV and dK of this tile (in issue order) have read P^T and dS^T
-          mma_commit_warp(&bars->dk_done);
+          mma_commit_warp(&bars->dk_done[t & 1]);
           if (last) {
             // the Q and dO slots of the last tile receive dK_j and dV_j; the
             // store warp releases them after writing those out
             mma_commit_warp(&bars->dkv_full);
           } else {
-            // Q_i and dO_i are free: S^T and dP^T of this tile completed
-            // before the compute warps could signal p_full and ds_full
+            // Q_i is free: S^T of this tile completed before the compute
+            // warps could signal p_full
             mma_commit_warp(&bars->q_empty[qs]);
-            mma_commit_warp(&bars->o_empty[os]);
           }
           ++t;
         }
@@ -428,13 +436,15 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = CAUSAL ? j : 0; i < nqt; ++i) {
           const int qs = t % QS, os = t % OS;
           const int q0 = i * T::BM + wg * T::QC;
-          // ---- P^T = exp2(S^T * c - lse2); S^T is free once read
+          // ---- P^T = exp2(S^T * c - lse2); the region takes dP^T once S^T
+          // has been read
           ok = mbar_wait(&bars->q_full[qs], (t / QS) & 1, wc, 71) && mbar_wait(&bars->s_full, t & 1, wc, 72);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
           uint32_t sr[T::QC];
-          tmem_ld32(lb + T::A_S + wg * T::QC, sr);
-          tmem_ld32(lb + T::A_S + wg * T::QC + 32, sr + 32);
+          const uint32_t rb = lb + T::A_R + (t & 1) * T::BM + wg * T::QC;  // this warpgroup's columns
+          tmem_ld32(rb, sr);
+          tmem_ld32(rb + 32, sr + 32);
           tmem_wait_ld();
           reg_fence<T::QC>(sr);
           tc_fence_before();
@@ -463,10 +473,10 @@ __global__ void __launch_bounds__(384, 1)
           ok = mbar_wait(&bars->o_full[os], (t / OS) & 1, wc, 73) && mbar_wait(&bars->dp_full, t & 1, wc, 74);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
-          tmem_ld32(lb + T::A_DP + wg * T::QC, sr);
+          tmem_ld32(rb, sr);
           tmem_wait_ld();
           reg_fence<32>(sr);
-          tmem_st32(lb + T::A_DP + wg * T::QC, pk);
+          tmem_st32(rb, pk);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->p_full);
@@ -474,7 +484,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             if (h == 1) {
-              tmem_ld32(lb + T::A_DP + wg * T::QC + 32, sr);
+              tmem_ld32(rb + 32, sr);
               tmem_wait_ld();
               reg_fence<32>(sr);
             }
@@ -488,7 +498,7 @@ __global__ void __launch_bounds__(384, 1)
                                                   ph[c + 3] * (__uint_as_float(sr[c + 3]) - Dl.w));
             }
           }
-          tmem_st32(lb + T::A_DP + wg * T::QC + T::QC / 2, pk);
+          tmem_st32(rb + T::QC / 2, pk);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->ds_full);
@@ -640,6 +650,7 @@ __global__ void __launch_bounds__(384, 1)
             for (int s = 0; s < T::DSUB; ++s)
               tma_load_2d_hint(smem + T::B_SM_K + ks * T::TILE + s * T::SUB, &tm_k, &bars->k_full[ks], s * 64,
                                head * N + j * T::BN, pol_kv);
+            // warm L2 with the tile that will refill this slot
             ++k_it;
           }
         }
