@@ -84,9 +84,14 @@ constexpr float kRescaleLog2 = 8.0f;
 struct FwdBars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_ready, o_free, mma_done;
-  uint64_t pv_done[2];   // P V of a tile that used P buffer b completed
+  uint64_t s_full[2], s_free[2], p_full[2];
+  uint64_t o_free, mma_done;
+  // P V of a tile that used P buffer b completed (and with it every earlier
+  // P V).  Waits name the tile's buffer and phase, never "the latest P V":
+  // Q K^T of later tiles is issued ahead of P V, so a completed S does not
+  // imply that all earlier P V completed, and one shared barrier could be
+  // two phases behind.
+  uint64_t pv_done[2];
   uint64_t epi_full[2];  // O tile written into Q buffer b
   uint64_t pair[4];      // row-partial exchange between warps q and q + 4
   uint32_t tmem_base;
@@ -156,6 +161,7 @@ __global__ void __launch_bounds__(384, 1)
       // O tile written into it has been stored (store warp)
       mbar_init(&bars->q_empty[i], 2);
       mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_free[i], T::SOFTMAX_THREADS);
       mbar_init(&bars->p_full[i], T::SOFTMAX_THREADS);
       mbar_init(&bars->epi_full[i], T::SOFTMAX_THREADS);
     }
@@ -166,7 +172,6 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
-    mbar_init(&bars->o_ready, 1);
     mbar_init(&bars->pv_done[0], 1);
     mbar_init(&bars->pv_done[1], 1);
     mbar_init(&bars->o_free, T::SOFTMAX_THREADS);
@@ -311,11 +316,34 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         mma_commit_warp(&bars->v_empty[st]);
-        mma_commit_warp(&bars->o_ready);
         mma_commit_warp(&bars->pv_done[b]);
         return true;
       };
 
+      // S = Q K^T of global tile `tile` (key tile kv_idx) into S buffer
+      // tile % 2, which the softmax of tile - 2 has read by then.
+      auto issue_s = [&](uint32_t tile, uint32_t kv_idx, uint64_t qdesc, bool last_of_item, int qs) -> bool {
+        const int st = kv_idx % T::K_STAGES;
+        const int b = tile & 1;
+        if (!warp_wait(&bars->k_full[st], (kv_idx / T::K_STAGES) & 1, wc, 4)) return false;
+        if (tile >= 2 && !warp_wait(&bars->s_free[b], ((tile - 2) >> 1) & 1, wc, 16)) return false;
+        tc_fence_after();
+        const uint64_t kdesc = sdesc_sw128(sbase + T::SM_K + st * T::KV_BYTES, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          mma_f16_ss_warp(tmem + T::S_COL + b * T::BN, sdesc_add(qdesc, (kk / 4) * T::Q_SUB + (kk % 4) * 32),
+                          sdesc_add(kdesc, (kk / 4) * T::KV_SUB + (kk % 4) * 32), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_warp(&bars->s_full[b]);
+        mma_commit_warp(&bars->k_empty[st]);
+        if (last_of_item) mma_commit_warp(&bars->q_empty[qs]);
+        return true;
+      };
+
+      // Issue order per item: S(0), S(1), then for each tile j: S(j + 2) as
+      // soon as the softmax of tile j has read S(j) (early in that softmax),
+      // then P V(j) once P(j) is in TMEM.  Q K^T thus runs two tiles ahead
+      // of the softmax and is queued on the tensor pipe ahead of P V(j).
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         int head, qa, qb;
         fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
@@ -327,25 +355,14 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
           const uint64_t qdesc = sdesc_sw128(sbase + T::SM_Q + qs * T::Q_BYTES, 16, 1024);
           const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
-          for (int j = 0; j < nkv; ++j) {
-            const int st = kv_it % T::K_STAGES;
-            if (!(ok = warp_wait(&bars->k_full[st], (kv_it / T::K_STAGES) & 1, wc, 4))) break;
-            tc_fence_after();
-            const uint64_t kdesc = sdesc_sw128(sbase + T::SM_K + st * T::KV_BYTES, 16, 1024);
-            const int b = t & 1;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              mma_f16_ss_warp(tmem + T::S_COL + b * T::BN, sdesc_add(qdesc, (kk / 4) * T::Q_SUB + (kk % 4) * 32),
-                              sdesc_add(kdesc, (kk / 4) * T::KV_SUB + (kk % 4) * 32), idesc_qk, kk > 0 ? 1u : 0u);
-            }
-            mma_commit_warp(&bars->s_full[b]);
-            mma_commit_warp(&bars->k_empty[st]);
-            if (j == nkv - 1) mma_commit_warp(&bars->q_empty[qs]);
-            if (j > 0 && !(ok = issue_pv(t - 1, kv_it - 1, j == 1))) break;
-            ++t;
-            ++kv_it;
+          const uint32_t t0 = t, k0 = kv_it;
+          for (int j = 0; ok && j < 2 && j < nkv; ++j) ok = issue_s(t0 + j, k0 + j, qdesc, j == nkv - 1, qs);
+          for (int j = 0; ok && j < nkv; ++j) {
+            if (j + 2 < nkv && !(ok = issue_s(t0 + j + 2, k0 + j + 2, qdesc, j + 2 == nkv - 1, qs))) break;
+            ok = issue_pv(t0 + j, k0 + j, j == 0);
           }
-          if (ok) ok = issue_pv(t - 1, kv_it - 1, nkv == 1);
+          t += nkv;
+          kv_it += nkv;
           ++q_it;
           ++item;
         }
@@ -417,6 +434,8 @@ __global__ void __launch_bounds__(384, 1)
           for (int c = 0; c < HC; c += 32) tmem_ld32(lane_base + T::S_COL + b * T::BN + wg * HC + c, sr + c);
           tmem_wait_ld();
           reg_fence<HC>(sr);
+          tc_fence_before();
+          mbar_arrive(&bars->s_free[b]);  // S buffer b may take the S of tile t + 2
           float s[HC];
 #pragma unroll
           for (int c = 0; c < HC; ++c) s[c] = __uint_as_float(sr[c]);
@@ -441,17 +460,25 @@ __global__ void __launch_bounds__(384, 1)
           const float m_tile = mx * sl2;
           const float m_new = (m_tile > m + kRescaleLog2) ? m_tile : m;
           const float neg = -m_new;
-          float ps[8];
+          // x = s * c - m and the row sum in packed fp32 pairs (one f32x2
+          // instruction per two columns)
+          const uint64_t c2 = f2_pack(sl2, sl2), neg2 = f2_pack(neg, neg);
+          uint64_t ps2[4];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) ps[i] = 0.f;
+          for (int i = 0; i < 4; ++i) ps2[i] = 0ull;
           uint32_t pk[HC / 2];
 #pragma unroll
           for (int c = 0; c < HC; c += 2) {
-            const float p0 = ex2_approx(fmaf(s[c], sl2, neg));
-            const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg));
-            ps[(c >> 1) & 7] += p0 + p1;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), c2, neg2), x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            ps2[(c >> 1) & 3] = f2_add(ps2[(c >> 1) & 3], f2_pack(p0, p1));
             pk[c / 2] = pack_half2(p0, p1);
           }
+          float ps[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) f2_unpack(ps2[i], ps[2 * i], ps[2 * i + 1]);
           const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
           const float alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
           l = l * alpha + rs;
@@ -464,7 +491,7 @@ __global__ void __launch_bounds__(384, 1)
           if (j > 0 && (kSerialPV || __any_sync(0xffffffffu, alpha != 1.f))) {
             // O holds P V of the previous tiles: wait for the last P V, then
             // rescale (this half's columns of) rows whose max moved.
-            ok = mbar_wait(&bars->o_ready, (t - 1) & 1, wc, 6);
+            ok = mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, wc, 6);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
@@ -500,7 +527,7 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         // ---- epilogue: O / l -> fp16 into this item's Q buffer (swizzled
         // like a Q tile; the store warp writes it out with TMA), lse direct
-        ok = mbar_wait(&bars->o_ready, (t - 1) & 1, wc, 7);
+        ok = mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, wc, 7);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         float l_other;
