@@ -79,6 +79,22 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_test, but a thread whose phase has not completed yet may be
+// suspended (for up to about `hint_ns`) until it does, instead of spinning:
+// a waiting warp then takes no issue slots from the warps that share its
+// SM sub-partition.
+__device__ __forceinline__ bool mbar_test_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed.  Gives up after
 // kWaitLimitNs, or at once when *abort is set by another thread of the CTA;
 // on giving up it records the site in the status word, raises *abort and
@@ -87,15 +103,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   const uint32_t a = smem_u32(bar);
   if (mbar_test(a, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_test(a, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*w.abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        record_timeout(w.status, site);
-        *w.abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_test_sleep(a, parity, 2000u)) return true;
+    if (*w.abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      record_timeout(w.status, site);
+      *w.abort = 1;
+      return false;
     }
   }
 }
