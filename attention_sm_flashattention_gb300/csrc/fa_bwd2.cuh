@@ -449,27 +449,33 @@ __global__ void __launch_bounds__(384, 1)
           reg_fence<T::QC>(sr);
           tc_fence_before();
           mbar_arrive(&bars->s_free);
+          // y = lse2 - S^T * c in packed fp32 pairs, P^T = exp2(-y)
           const float4* l4 = reinterpret_cast<const float4*>(smem + T::A_SM_L2 + qs * 512) + wg * (T::QC / 4);
-          float p[T::QC];
+          const uint64_t nc2 = f2_pack(-sl2, -sl2);
+          uint64_t p2[T::QC / 2];
 #pragma unroll
           for (int c = 0; c < T::QC; c += 4) {
             const float4 L = l4[c / 4];
-            p[c + 0] = ex2_approx(fmaf(__uint_as_float(sr[c + 0]), sl2, -L.x));
-            p[c + 1] = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -L.y));
-            p[c + 2] = ex2_approx(fmaf(__uint_as_float(sr[c + 2]), sl2, -L.z));
-            p[c + 3] = ex2_approx(fmaf(__uint_as_float(sr[c + 3]), sl2, -L.w));
-          }
-          if (CAUSAL && i == j) {
+            float y[4];
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), nc2, f2_pack(L.x, L.y)), y[0],
+                      y[1]);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), nc2, f2_pack(L.z, L.w)),
+                      y[2], y[3]);
+            float pv[4];
 #pragma unroll
-            for (int c = 0; c < T::QC; ++c)
-              if (key > q0 + c) p[c] = 0.f;
+            for (int e = 0; e < 4; ++e) {
+              pv[e] = ex2_approx(-y[e]);
+              if (CAUSAL && i == j && key > q0 + c + e) pv[e] = 0.f;
+            }
+            p2[c / 2] = f2_pack(pv[0], pv[1]);
+            p2[c / 2 + 1] = f2_pack(pv[2], pv[3]);
           }
           // ---- P^T (fp16) over the first half of dP^T once that half is
           // read; dS^T = P^T * (dP^T - Delta) over the second half.  The
           // halves are read one at a time to keep register pressure low.
           uint32_t pk[T::QC / 2];
 #pragma unroll
-          for (int c = 0; c < T::QC / 2; ++c) pk[c] = pack_half2(p[2 * c], p[2 * c + 1]);
+          for (int c = 0; c < T::QC / 2; ++c) pk[c] = f2_to_half2(p2[c]);
           ok = mbar_wait(&bars->o_full[os], (t / OS) & 1, wc, 73) && mbar_wait(&bars->dp_full, t & 1, wc, 74);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
@@ -491,11 +497,11 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int c = 0; c < 32; c += 4) {
               const float4 Dl = d4[(32 * h + c) / 4];
-              const float* ph = p + 32 * h;
-              pk[16 * h + c / 2] =
-                  pack_half2(ph[c] * (__uint_as_float(sr[c]) - Dl.x), ph[c + 1] * (__uint_as_float(sr[c + 1]) - Dl.y));
-              pk[16 * h + c / 2 + 1] = pack_half2(ph[c + 2] * (__uint_as_float(sr[c + 2]) - Dl.z),
-                                                  ph[c + 3] * (__uint_as_float(sr[c + 3]) - Dl.w));
+              const uint64_t d01 = f2_sub(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), f2_pack(Dl.x, Dl.y));
+              const uint64_t d23 =
+                  f2_sub(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), f2_pack(Dl.z, Dl.w));
+              pk[16 * h + c / 2] = f2_to_half2(f2_mul(p2[(32 * h + c) / 2], d01));
+              pk[16 * h + c / 2 + 1] = f2_to_half2(f2_mul(p2[(32 * h + c) / 2 + 1], d23));
             }
           }
           tmem_st32(rb + T::QC / 2, pk);
@@ -824,6 +830,7 @@ __global__ void __launch_bounds__(384, 1)
         const size_t grow = static_cast<size_t>(head) * N + query;
         const float lse2 = __ldg(prm.lse2 + grow);
         const float delta = __ldg(prm.delta + grow);
+        const uint64_t c2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2), nd2 = f2_pack(-delta, -delta);
         for (int j = 0; j < num_kv(i); ++j) {
           const int pb = t & 1;
           const int k0 = j * T::BN + wg * T::QC;  // first key column of this warpgroup
@@ -838,13 +845,18 @@ __global__ void __launch_bounds__(384, 1)
           reg_fence<T::QC>(sr);
           tc_fence_before();
           mbar_arrive(&bars->s_free);
-          float p[T::QC];
+          // x = S * c - lse2 in packed fp32 pairs, P = exp2(x)
+          uint64_t p2[T::QC / 2];
 #pragma unroll
-          for (int c = 0; c < T::QC; ++c) p[c] = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
-          if (CAUSAL && j == i) {
-#pragma unroll
-            for (int c = 0; c < T::QC; ++c)
-              if (k0 + c > query) p[c] = 0.f;
+          for (int c = 0; c < T::QC; c += 2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nl2), x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (CAUSAL && j == i) {
+              if (k0 + c > query) p0 = 0.f;
+              if (k0 + c + 1 > query) p1 = 0.f;
+            }
+            p2[c / 2] = f2_pack(p0, p1);
           }
           // ---- dS = P * (dP - Delta), fp16 into TMEM over dP
           ok = mbar_wait(&bars->dp_full[pb], (t >> 1) & 1, wc, 102);
@@ -858,7 +870,7 @@ __global__ void __launch_bounds__(384, 1)
           uint32_t pk[T::QC / 2];
 #pragma unroll
           for (int c = 0; c < T::QC; c += 2)
-            pk[c / 2] = pack_half2(p[c] * (__uint_as_float(sr[c]) - delta), p[c + 1] * (__uint_as_float(sr[c + 1]) - delta));
+            pk[c / 2] = f2_to_half2(f2_mul(p2[c / 2], f2_add(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), nd2)));
           tmem_st32(lb + dpc, pk);
           tmem_wait_st();
           tc_fence_before();
