@@ -9,26 +9,28 @@
 // matrix unit; causal shortens the key-tile loop and masks only diagonal
 // tiles; D = 256 keeps two 128-wide accumulator halves; O is written once.
 //
-// Roles (384 threads):
-//   warps 0-7  softmax: two warpgroups split the columns of each tile; thread
-//              (g, r) owns query row r and half g of the key columns of S
-//              (and of the O columns).  Both halves of a row read the whole
-//              S row to take the same row max (TMEM reads are cheap), then
-//              each exponentiates its own half and keeps its own partial l;
-//              the partial sums are combined once, in the epilogue.  They
-//              write P (fp16) back to TMEM, rescale O when m moved, and run
-//              the epilogue.
-//   warp 8     TMA producer: Q tile per work item, K tiles into a ring.
-//   warp 9     MMA issuer (converged warp, one elected lane per MMA) and
-//              TMEM owner: S = Q K^T into one of two S buffers, then
-//              O += P V with P read from TMEM.
-//   warp 10    TMA producer: V tiles into their own ring.
-//   warp 11    O store: the softmax warps write the normalised O tile into
-//              the item's (now unused) Q buffer; this warp stores it with
-//              TMA and then releases the buffer.
-//
-// The MMA of key tile j+1 (Q K^T) runs while the softmax of tile j works,
-// and P V of tile j runs while the softmax of tile j+1 works.
+// Roles (512 threads, one CTA per SM):
+//   warps 0-7   softmax: two warpgroups split the columns of each tile; thread
+//               (g, r) owns query row r and half g of the key columns of S.
+//               Both halves of a row read the whole S row to take the same
+//               row max (TMEM reads are cheap), then each exponentiates its
+//               own half and keeps its own partial l.  They write P (fp16)
+//               back to TMEM and rescale O when m moved; at the end of an
+//               item they publish l and m and go straight on to the next
+//               item.
+//   warps 8-11  epilogue: O / l -> fp16 into the item's (now unused) Q
+//               buffer, lse; this overlaps the softmax of the next item.
+//   warp 12     TMA producer: Q tile per work item, K tiles into a ring.
+//   warp 13     MMA issuer (converged warp, one elected lane per MMA) and
+//               TMEM owner.  It walks the CTA's tiles as one flat sequence
+//               (across work items) and issues S = Q K^T two tiles ahead of
+//               P V, into one of two S buffers, and O += P V (P read from
+//               TMEM) as soon as a tile's P is ready.
+//   warp 14     TMA producer: V tiles into their own ring.
+//   warp 15     O store: TMA store of the epilogue's tile, then releases the
+//               Q buffer.
+// The softmax warpgroups run with more registers than the others
+// (setmaxnreg), since they hold a whole S half-row and its P.
 #pragma once
 
 #include "fa_kernels.h"
@@ -62,19 +64,26 @@ struct FwdTraits {
   static constexpr int SM_Q = 0;
   static constexpr int SM_K = SM_Q + Q_STAGES * Q_BYTES;
   static constexpr int SM_V = SM_K + K_STAGES * KV_BYTES;
-  static constexpr int SM_XCH = SM_V + V_STAGES * KV_BYTES;  // [2][2][128] fp32 row partials
-  static constexpr int SM_BAR = SM_XCH + 2 * 2 * BM * 4;
+  // partial row sums l of both column halves and the row max m of the item
+  // the epilogue works on next
+  static constexpr int SM_LM = SM_V + V_STAGES * KV_BYTES;  // [3][128] fp32
+  static constexpr int SM_BAR = SM_LM + 3 * BM * 4;
   static constexpr int SM_BYTES = SM_BAR + 512;
   // never below 120 KB so that a second CTA can never share the SM (each
   // CTA takes all 512 TMEM columns)
   static constexpr int SMEM_ALLOC = (SM_BYTES > 120 * 1024) ? SM_BYTES : 120 * 1024;
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-  static constexpr int THREADS = 384;
+  static constexpr int THREADS = 512;
   static constexpr int SOFTMAX_THREADS = 256;
-  static constexpr int PRODUCER_WARP = 8;  // Q and K
-  static constexpr int MMA_WARP = 9;
-  static constexpr int V_PRODUCER_WARP = 10;
-  static constexpr int STORE_WARP = 11;
+  static constexpr int EPI_THREADS = 128;  // warps 8-11
+  static constexpr int PRODUCER_WARP = 12;  // Q and K
+  static constexpr int MMA_WARP = 13;
+  static constexpr int V_PRODUCER_WARP = 14;
+  static constexpr int PV_MMA_WARP = 15;
+  // registers per thread after the split (launch: 65536 / 512 = 128):
+  // 256 x 184 + 256 x 64 = 63488 <= 65536
+  static constexpr int SOFTMAX_REGS = 184;
+  static constexpr int OTHER_REGS = 64;
 };
 
 // Threshold (log2 units) of the lazy online-softmax rescale.
@@ -85,7 +94,7 @@ struct FwdBars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], s_free[2], p_full[2];
-  uint64_t o_free, mma_done;
+  uint64_t o_free, mma_done[2];
   // P V of a tile that used P buffer b completed (and with it every earlier
   // P V).  Waits name the tile's buffer and phase, never "the latest P V":
   // Q K^T of later tiles is issued ahead of P V, so a completed S does not
@@ -93,7 +102,7 @@ struct FwdBars {
   // two phases behind.
   uint64_t pv_done[2];
   uint64_t epi_full[2];  // O tile written into Q buffer b
-  uint64_t pair[4];      // row-partial exchange between warps q and q + 4
+  uint64_t lm_full, lm_empty;  // l, m of one item, handed to the epilogue warps
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -139,8 +148,54 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// The CTA's tiles in the order it processes them: work items (query tiles)
+// in schedule order, the key tiles of each item in order.  Global tile index
+// `tile` also indexes the K and V rings, which hold one tile per key tile.
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(384, 1)
+struct FwdCursor {
+  int u, half, head, qt, qb, j, nkv;
+  uint32_t item, tile;
+  bool valid;
+  int units, nqt, nkv_full;
+
+  __device__ void start(int first_unit, int units_, int nqt_, int nkv_full_) {
+    units = units_;
+    nqt = nqt_;
+    nkv_full = nkv_full_;
+    item = 0;
+    tile = 0;
+    j = 0;
+    u = first_unit;
+    half = 0;
+    load_unit();
+  }
+  __device__ void load_unit() {
+    valid = u < units;
+    if (!valid) return;
+    int qa;
+    fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+    qt = qa;
+    half = 0;
+    nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+  }
+  __device__ void advance() {
+    ++tile;
+    if (++j < nkv) return;
+    j = 0;
+    ++item;
+    if (half == 0 && qb >= 0) {
+      half = 1;
+      qt = qb;
+      nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+    } else {
+      u += gridDim.x;
+      load_unit();
+    }
+  }
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(512, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams prm) {
@@ -163,9 +218,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->s_free[i], T::SOFTMAX_THREADS);
       mbar_init(&bars->p_full[i], T::SOFTMAX_THREADS);
-      mbar_init(&bars->epi_full[i], T::SOFTMAX_THREADS);
+      mbar_init(&bars->epi_full[i], T::EPI_THREADS);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&bars->pair[i], 64);
+    mbar_init(&bars->lm_full, T::SOFTMAX_THREADS);
+    mbar_init(&bars->lm_empty, T::EPI_THREADS);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
@@ -174,8 +230,9 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(&bars->pv_done[0], 1);
     mbar_init(&bars->pv_done[1], 1);
-    mbar_init(&bars->o_free, T::SOFTMAX_THREADS);
-    mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->o_free, T::EPI_THREADS);
+    mbar_init(&bars->mma_done[0], 1);
+    mbar_init(&bars->mma_done[1], 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -192,7 +249,6 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-
   const WaitCtx wc{prm.status, &bars->abort_flag};
   const uint32_t tmem = bars->tmem_base;
   const int N = prm.N;
@@ -200,49 +256,18 @@ __global__ void __launch_bounds__(384, 1)
   const int nkv_full = N / T::BN;
   const int units = fwd_num_units<CAUSAL>(prm.heads, nqt);
 
-  if (warp == T::PRODUCER_WARP) {
-    // ------------------------------------------------ producer: Q and K tiles
-    if (lane == 0) {
-      const uint64_t pol_kv = l2_policy_evict_last();
-      const uint64_t pol_q = l2_policy_evict_first();
-      uint32_t q_it = 0, k_it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        int head, qa, qb;
-        fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
-        for (int half = 0; ok && half < 2; ++half) {
-          const int qt = half ? qb : qa;
-          if (qt < 0) break;
-          const int qs = q_it % T::Q_STAGES;
-          if (!(ok = mbar_wait(&bars->q_empty[qs], ((q_it / T::Q_STAGES) & 1) ^ 1, wc, 1))) break;
-          mbar_arrive_expect_tx(&bars->q_full[qs], T::Q_BYTES);
-          uint8_t* sq = smem + T::SM_Q + qs * T::Q_BYTES;
-          for (int s = 0; s < T::DSUB; ++s)
-            tma_load_2d_hint(sq + s * T::Q_SUB, &tm_q, &bars->q_full[qs], s * 64, head * N + qt * T::BM, pol_q);
-          ++q_it;
-          const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
-          for (int j = 0; j < nkv; ++j) {
-            const int st = k_it % T::K_STAGES;
-            if (!(ok = mbar_wait(&bars->k_empty[st], ((k_it / T::K_STAGES) & 1) ^ 1, wc, 2))) break;
-            uint8_t* sk = smem + T::SM_K + st * T::KV_BYTES;
-            mbar_arrive_expect_tx(&bars->k_full[st], T::KV_BYTES);
-            for (int s = 0; s < T::DSUB; ++s)
-              tma_load_2d_hint(sk + s * T::KV_SUB, &tm_k, &bars->k_full[st], s * 64, head * N + j * T::BN, pol_kv);
-            ++k_it;
-          }
-        }
-      }
-      // Drain: every load issued must have landed before the CTA may exit.
-      for (uint32_t i = (k_it > T::K_STAGES ? k_it - T::K_STAGES : 0); i < k_it; ++i)
-        drain_wait(&bars->k_full[i % T::K_STAGES], (i / T::K_STAGES) & 1);
-      for (uint32_t i = (q_it > T::Q_STAGES ? q_it - T::Q_STAGES : 0); i < q_it; ++i)
-        drain_wait(&bars->q_full[i % T::Q_STAGES], (i / T::Q_STAGES) & 1);
-    }
-  } else if (warp == T::V_PRODUCER_WARP) {
-    // ------------------------------------------------------ producer: V tiles
-    if (lane == 0) {
-      const uint64_t pol_kv = l2_policy_evict_last();
-      uint32_t v_it = 0;
+  if (warp < 8) {
+    reg_alloc<T::SOFTMAX_REGS>();
+      // ----------------------------------------------------- softmax warps
+      constexpr int HC = T::BN / 2;  // S columns per thread
+      constexpr int HD = D / 2;      // O columns per thread
+      const int wg = warp >> 2;      // column half
+      const int quad = warp & 3;
+      const int r = quad * 32 + lane;  // query row inside the tile, == TMEM lane
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+      float* lm = reinterpret_cast<float*>(smem + T::SM_LM);
+      const float sl2 = prm.scale_log2;
+      uint32_t t = 0, q_item = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         int head, qa, qb;
@@ -251,64 +276,252 @@ __global__ void __launch_bounds__(384, 1)
           const int qt = half ? qb : qa;
           if (qt < 0) break;
           const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+          const int qi = qt * T::BM + r;  // query index within the head
+          float m = -INFINITY, l = 0.f;   // l: this half's partial row sum
           for (int j = 0; j < nkv; ++j) {
-            const int st = v_it % T::V_STAGES;
-            if (!(ok = mbar_wait(&bars->v_empty[st], ((v_it / T::V_STAGES) & 1) ^ 1, wc, 8))) break;
-            uint8_t* sv = smem + T::SM_V + st * T::KV_BYTES;
-            mbar_arrive_expect_tx(&bars->v_full[st], T::KV_BYTES);
+            const int b = t & 1;
+            ok = mbar_wait(&bars->s_full[b], (t >> 1) & 1, wc, 5);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            // other half of the row: only its max is needed
+            uint32_t sr[HC];
+            float pm[8];
+  #pragma unroll
+            for (int c = 0; c < HC; c += 32) tmem_ld32(lane_base + T::S_COL + b * T::BN + (wg ^ 1) * HC + c, sr + c);
+            tmem_wait_ld();
+            reg_fence<HC>(sr);
+            if (CAUSAL && (j + 1) * T::BN - 1 > qt * T::BM) {
+              const int k0 = j * T::BN + (wg ^ 1) * HC;
+  #pragma unroll
+              for (int c = 0; c < HC; ++c)
+                if (k0 + c > qi) sr[c] = __float_as_uint(-INFINITY);
+            }
+  #pragma unroll
+            for (int i = 0; i < 8; ++i) pm[i] = fmaxf(__uint_as_float(sr[i]), __uint_as_float(sr[i + 8]));
+  #pragma unroll
+            for (int c = 16; c < HC; c += 16)
+  #pragma unroll
+              for (int i = 0; i < 8; ++i) pm[i] = fmax3(pm[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
+            // own half
+  #pragma unroll
+            for (int c = 0; c < HC; c += 32) tmem_ld32(lane_base + T::S_COL + b * T::BN + wg * HC + c, sr + c);
+            tmem_wait_ld();
+            reg_fence<HC>(sr);
+            tc_fence_before();
+            mbar_arrive(&bars->s_free[b]);  // S buffer b may take the S of tile t + 2
+            float s[HC];
+  #pragma unroll
+            for (int c = 0; c < HC; ++c) s[c] = __uint_as_float(sr[c]);
+            if (CAUSAL && (j + 1) * T::BN - 1 > qt * T::BM) {
+              const int k0 = j * T::BN + wg * HC;
+  #pragma unroll
+              for (int c = 0; c < HC; ++c)
+                if (k0 + c > qi) s[c] = -INFINITY;
+            }
+  #pragma unroll
+            for (int c = 0; c < HC; c += 16)
+  #pragma unroll
+              for (int i = 0; i < 8; ++i) pm[i] = fmax3(pm[i], s[c + i], s[c + 8 + i]);
+            const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+            // The running max m only moves when this tile's max exceeds it by
+            // more than kRescaleLog2: below that the stale m keeps every P value
+            // under 2^kRescaleLog2 (exact range for fp16 P and fp32 l), so O and
+            // l need no rescaling.  O / l and lse use the max actually applied,
+            // which gives the same result as always tracking the exact max.
+            // Both halves of a row compute the same row max, so they take the
+            // same decision.
+            const float m_tile = mx * sl2;
+            const float m_new = (m_tile > m + kRescaleLog2) ? m_tile : m;
+            const float neg = -m_new;
+            // x = s * c - m and the row sum in packed fp32 pairs (one f32x2
+            // instruction per two columns)
+            const uint64_t c2 = f2_pack(sl2, sl2), neg2 = f2_pack(neg, neg);
+            uint64_t ps2[4];
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) ps2[i] = 0ull;
+            uint32_t pk[HC / 2];
+  #pragma unroll
+            for (int c = 0; c < HC; c += 2) {
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), c2, neg2), x0, x1);
+              const float p0 = ex2_approx(x0);
+              const float p1 = ex2_approx(x1);
+              ps2[(c >> 1) & 3] = f2_add(ps2[(c >> 1) & 3], f2_pack(p0, p1));
+              pk[c / 2] = pack_half2(p0, p1);
+            }
+            float ps[8];
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) f2_unpack(ps2[i], ps[2 * i], ps[2 * i + 1]);
+            const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+            const float alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
+            l = l * alpha + rs;
+            m = m_new;
+            // With two 128-column O halves (D = 256), letting P V of this tile
+            // start while the previous P V still runs gave wrong O on GB300
+            // (the MMAs alternate between the two accumulators); there the
+            // softmax always waits for the previous P V before releasing P.
+            constexpr bool kSerialPV = (T::NOH > 1);
+            if (j > 0 && (kSerialPV || __any_sync(0xffffffffu, alpha != 1.f))) {
+              // O holds P V of the previous tiles: wait for the last P V, then
+              // rescale (this half's columns of) rows whose max moved.
+              ok = mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, wc, 6);
+              if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+              tc_fence_after();
+              if (__any_sync(0xffffffffu, alpha != 1.f)) {
+  #pragma unroll 1
+                for (int c = 0; c < HD; c += 32) {
+                  uint32_t o[32];
+                  tmem_ld32(lane_base + T::O_COL + wg * HD + c, o);
+                  tmem_wait_ld();
+                  reg_fence<32>(o);
+  #pragma unroll
+                  for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                  tmem_st32(lane_base + T::O_COL + wg * HD + c, o);
+                }
+              }
+            }
+            // P buffer b was last read by the P V of tile t - 2
+            if (t >= 2) {
+              ok = mbar_wait(&bars->pv_done[b], ((t - 2) >> 1) & 1, wc, 15);
+              if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+              tc_fence_after();
+            }
+            const uint32_t pcol = lane_base + T::P_COL + b * (T::BN / 2) + wg * (HC / 2);
+            if (HC / 2 == 32) {
+              tmem_st32(pcol, pk);
+            } else {
+              tmem_st16(pcol, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bars->p_full[b]);
+            ++t;
+          }
+          if (!ok) break;
+          // ---- hand l (this half's partial row sum) and m to the epilogue
+          // warps, once they have read the previous item's
+          if (q_item >= 1) {
+            ok = mbar_wait(&bars->lm_empty, (q_item - 1) & 1, wc, 14);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          }
+          lm[wg * T::BM + r] = l;
+          if (wg == 0) lm[2 * T::BM + r] = m;
+          mbar_arrive(&bars->lm_full);
+          ++q_item;
+        }
+      }
+  } else {
+    reg_dealloc<T::OTHER_REGS>();
+    if (warp == T::PRODUCER_WARP) {
+      // ------------------------------------------------ producer: Q and K tiles
+      if (lane == 0) {
+        const uint64_t pol_kv = l2_policy_evict_last();
+        const uint64_t pol_q = l2_policy_evict_first();
+        uint32_t q_it = 0, k_it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+          int head, qa, qb;
+          fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+          for (int half = 0; ok && half < 2; ++half) {
+            const int qt = half ? qb : qa;
+            if (qt < 0) break;
+            const int qs = q_it % T::Q_STAGES;
+            if (!(ok = mbar_wait(&bars->q_empty[qs], ((q_it / T::Q_STAGES) & 1) ^ 1, wc, 1))) break;
+            mbar_arrive_expect_tx(&bars->q_full[qs], T::Q_BYTES);
+            uint8_t* sq = smem + T::SM_Q + qs * T::Q_BYTES;
             for (int s = 0; s < T::DSUB; ++s)
-              tma_load_2d_hint(sv + s * T::KV_SUB, &tm_v, &bars->v_full[st], s * 64, head * N + j * T::BN, pol_kv);
-            ++v_it;
+              tma_load_2d_hint(sq + s * T::Q_SUB, &tm_q, &bars->q_full[qs], s * 64, head * N + qt * T::BM, pol_q);
+            ++q_it;
+            const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+            for (int j = 0; j < nkv; ++j) {
+              const int st = k_it % T::K_STAGES;
+              if (!(ok = mbar_wait(&bars->k_empty[st], ((k_it / T::K_STAGES) & 1) ^ 1, wc, 2))) break;
+              uint8_t* sk = smem + T::SM_K + st * T::KV_BYTES;
+              mbar_arrive_expect_tx(&bars->k_full[st], T::KV_BYTES);
+              for (int s = 0; s < T::DSUB; ++s)
+                tma_load_2d_hint(sk + s * T::KV_SUB, &tm_k, &bars->k_full[st], s * 64, head * N + j * T::BN, pol_kv);
+              ++k_it;
+            }
           }
         }
+        // Drain: every load issued must have landed before the CTA may exit.
+        for (uint32_t i = (k_it > T::K_STAGES ? k_it - T::K_STAGES : 0); i < k_it; ++i)
+          drain_wait(&bars->k_full[i % T::K_STAGES], (i / T::K_STAGES) & 1);
+        for (uint32_t i = (q_it > T::Q_STAGES ? q_it - T::Q_STAGES : 0); i < q_it; ++i)
+          drain_wait(&bars->q_full[i % T::Q_STAGES], (i / T::Q_STAGES) & 1);
       }
-      for (uint32_t i = (v_it > T::V_STAGES ? v_it - T::V_STAGES : 0); i < v_it; ++i)
-        drain_wait(&bars->v_full[i % T::V_STAGES], (i / T::V_STAGES) & 1);
-    }
-  } else if (warp == T::STORE_WARP) {
-    // ------------------------------------------------ O store (TMA, async)
-    if (lane == 0) {
-      uint32_t q_it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        int head, qa, qb;
-        fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
-        for (int half = 0; ok && half < 2; ++half) {
-          const int qt = half ? qb : qa;
-          if (qt < 0) break;
-          const int qs = q_it % T::Q_STAGES;
-          if (!(ok = mbar_wait(&bars->epi_full[qs], (q_it / T::Q_STAGES) & 1, wc, 13))) break;
-          const uint8_t* so = smem + T::SM_Q + qs * T::Q_BYTES;
-          for (int s = 0; s < T::DSUB; ++s) tma_store_2d(&tm_o, so + s * T::Q_SUB, s * 64, head * N + qt * T::BM);
-          bulk_commit();
-          bulk_wait_read<0>();  // the buffer may be refilled once TMA has read it
-          mbar_arrive(&bars->q_empty[qs]);
-          ++q_it;
+    } else if (warp == T::V_PRODUCER_WARP) {
+      // ------------------------------------------------------ producer: V tiles
+      if (lane == 0) {
+        const uint64_t pol_kv = l2_policy_evict_last();
+        uint32_t v_it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+          int head, qa, qb;
+          fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+          for (int half = 0; ok && half < 2; ++half) {
+            const int qt = half ? qb : qa;
+            if (qt < 0) break;
+            const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+            for (int j = 0; j < nkv; ++j) {
+              const int st = v_it % T::V_STAGES;
+              if (!(ok = mbar_wait(&bars->v_empty[st], ((v_it / T::V_STAGES) & 1) ^ 1, wc, 8))) break;
+              uint8_t* sv = smem + T::SM_V + st * T::KV_BYTES;
+              mbar_arrive_expect_tx(&bars->v_full[st], T::KV_BYTES);
+              for (int s = 0; s < T::DSUB; ++s)
+                tma_load_2d_hint(sv + s * T::KV_SUB, &tm_v, &bars->v_full[st], s * 64, head * N + j * T::BN, pol_kv);
+              ++v_it;
+            }
+          }
         }
+        for (uint32_t i = (v_it > T::V_STAGES ? v_it - T::V_STAGES : 0); i < v_it; ++i)
+          drain_wait(&bars->v_full[i % T::V_STAGES], (i / T::V_STAGES) & 1);
       }
-      bulk_wait<0>();  // all O stores complete before the CTA exits
-    }
-  } else if (warp == T::MMA_WARP) {
-    // ------------------------------------------------------------- MMA issuer
-    {  // the whole warp runs the loop; one elected lane issues each MMA
+    } else if (warp == T::MMA_WARP || warp == T::PV_MMA_WARP) {
+      // ------------------------------------------------------------ MMA issuers
+      // The whole warp runs the loop; one elected lane issues each MMA.
       constexpr uint32_t idesc_qk = idesc_f16(128, T::BN, false, false);
       constexpr uint32_t idesc_pv = idesc_f16(128, T::OH, false, true);
       const uint32_t sbase = smem_u32(smem);
-      uint32_t q_it = 0, kv_it = 0, t = 0, item = 0;
       bool ok = true;
 
-      // O += P_tile V_stage; the first tile of an item overwrites O.
-      auto issue_pv = [&](uint32_t tile, uint32_t kv_idx, bool first) -> bool {
-        const int b = tile & 1;
-        const int st = kv_idx % T::V_STAGES;
-        if (first && item > 0 && !warp_wait(&bars->o_free, (item - 1) & 1, wc, 10)) return false;
-        if (!warp_wait(&bars->p_full[b], (tile >> 1) & 1, wc, 11)) return false;
-        if (!warp_wait(&bars->v_full[st], (kv_idx / T::V_STAGES) & 1, wc, 12)) return false;
+      // S = Q K^T of the cursor's tile into S buffer tile % 2, which the
+      // softmax of tile - 2 has read by then.
+      auto issue_s = [&](const FwdCursor<D, CAUSAL>& c) -> bool {
+        const int qs = c.item % T::Q_STAGES;
+        const int st = c.tile % T::K_STAGES;
+        const int b = c.tile & 1;
+        if (c.j == 0 && !warp_wait(&bars->q_full[qs], (c.item / T::Q_STAGES) & 1, wc, 3)) return false;
+        if (!warp_wait(&bars->k_full[st], (c.tile / T::K_STAGES) & 1, wc, 4)) return false;
+        if (c.tile >= 2 && !warp_wait(&bars->s_free[b], ((c.tile - 2) >> 1) & 1, wc, 16)) return false;
+        tc_fence_after();
+        const uint64_t qdesc = sdesc_sw128(sbase + T::SM_Q + qs * T::Q_BYTES, 16, 1024);
+        const uint64_t kdesc = sdesc_sw128(sbase + T::SM_K + st * T::KV_BYTES, 16, 1024);
+  #pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          mma_f16_ss_warp(tmem + T::S_COL + b * T::BN, sdesc_add(qdesc, (kk / 4) * T::Q_SUB + (kk % 4) * 32),
+                          sdesc_add(kdesc, (kk / 4) * T::KV_SUB + (kk % 4) * 32), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_warp(&bars->s_full[b]);
+        mma_commit_warp(&bars->k_empty[st]);
+        if (c.j == c.nkv - 1) mma_commit_warp(&bars->q_empty[qs]);
+        return true;
+      };
+
+      // O += P V of the cursor's tile; the first tile of an item overwrites O,
+      // which the previous item's epilogue must have read.
+      auto issue_pv = [&](const FwdCursor<D, CAUSAL>& c) -> bool {
+        const int b = c.tile & 1;
+        const int st = c.tile % T::V_STAGES;
+        const bool first = (c.j == 0);
+        if (first && c.item > 0 && !warp_wait(&bars->o_free, (c.item - 1) & 1, wc, 10)) return false;
+        if (!warp_wait(&bars->p_full[b], (c.tile >> 1) & 1, wc, 11)) return false;
+        if (!warp_wait(&bars->v_full[st], (c.tile / T::V_STAGES) & 1, wc, 12)) return false;
         tc_fence_after();
         const uint64_t vdesc = sdesc_sw128(sbase + T::SM_V + st * T::KV_BYTES, T::KV_SUB, 1024);
-#pragma unroll
+  #pragma unroll
         for (int kk = 0; kk < T::BN / 16; ++kk) {
-#pragma unroll
+  #pragma unroll
           for (int h = 0; h < T::NOH; ++h) {
             mma_f16_ts_warp(tmem + T::O_COL + h * 128, tmem + T::P_COL + b * (T::BN / 2) + kk * 8,
                             sdesc_add(vdesc, (h * 2) * T::KV_SUB + kk * 16 * 128), idesc_pv,
@@ -320,246 +533,99 @@ __global__ void __launch_bounds__(384, 1)
         return true;
       };
 
-      // S = Q K^T of global tile `tile` (key tile kv_idx) into S buffer
-      // tile % 2, which the softmax of tile - 2 has read by then.
-      auto issue_s = [&](uint32_t tile, uint32_t kv_idx, uint64_t qdesc, bool last_of_item, int qs) -> bool {
-        const int st = kv_idx % T::K_STAGES;
-        const int b = tile & 1;
-        if (!warp_wait(&bars->k_full[st], (kv_idx / T::K_STAGES) & 1, wc, 4)) return false;
-        if (tile >= 2 && !warp_wait(&bars->s_free[b], ((tile - 2) >> 1) & 1, wc, 16)) return false;
-        tc_fence_after();
-        const uint64_t kdesc = sdesc_sw128(sbase + T::SM_K + st * T::KV_BYTES, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          mma_f16_ss_warp(tmem + T::S_COL + b * T::BN, sdesc_add(qdesc, (kk / 4) * T::Q_SUB + (kk % 4) * 32),
-                          sdesc_add(kdesc, (kk / 4) * T::KV_SUB + (kk % 4) * 32), idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        mma_commit_warp(&bars->s_full[b]);
-        mma_commit_warp(&bars->k_empty[st]);
-        if (last_of_item) mma_commit_warp(&bars->q_empty[qs]);
-        return true;
-      };
-
-      // Issue order per item: S(0), S(1), then for each tile j: S(j + 2) as
-      // soon as the softmax of tile j has read S(j) (early in that softmax),
-      // then P V(j) once P(j) is in TMEM.  Q K^T thus runs two tiles ahead
-      // of the softmax and is queued on the tensor pipe ahead of P V(j).
+      // Q K^T two tiles ahead of P V, across work items: S(0), S(1), then for
+      // every tile t: S(t + 2) (as soon as the softmax has read S(t)), P V(t).
+      // An item's Q is loaded into the buffer of the item Q_STAGES earlier,
+      // once that item's O has been stored, so Q K^T never runs Q_STAGES or
+      // more items ahead of P V (short causal items would otherwise deadlock:
+      // the S waiting for a Q buffer that only a later P V can release).
+      // Two issuing warps: this one issues Q K^T, bounded only by the two S
+      // buffers (S(t + 2) as soon as the softmax has read S(t)), so it runs
+      // two tiles ahead of the softmax, across work items; warp 15 issues
+      // P V as each tile's P becomes ready.  Neither waits behind the
+      // other's dependencies.
+      FwdCursor<D, CAUSAL> c;
+      c.start(blockIdx.x, units, nqt, nkv_full);
+      const bool s_side = (warp == T::MMA_WARP);
+      while (ok && c.valid) {
+        ok = s_side ? issue_s(c) : issue_pv(c);
+        c.advance();
+      }
+      // Drain: all MMAs issued by this warp complete before TMEM is freed.
+      mma_commit_warp(&bars->mma_done[s_side ? 0 : 1]);
+      drain_wait(&bars->mma_done[s_side ? 0 : 1], 0);
+    } else {
+      // -------------------------------------------- epilogue warps (8-11)
+      // (warp 8 also writes each finished O tile out with a TMA store)
+      // O / l -> fp16 into the item's Q buffer (swizzled like a Q tile; the
+      // store warp writes it out with TMA), lse direct.  Runs while the
+      // softmax warps start on the next item.
+      const int quad = warp & 3;
+      const int r = quad * 32 + lane;  // query row inside the tile, == TMEM lane
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+      const float* lm = reinterpret_cast<const float*>(smem + T::SM_LM);
+      uint32_t t = 0, q_item = 0;
+      bool ok = true;
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         int head, qa, qb;
         fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
         for (int half = 0; ok && half < 2; ++half) {
           const int qt = half ? qb : qa;
           if (qt < 0) break;
-          const int qs = q_it % T::Q_STAGES;
-          if (!(ok = warp_wait(&bars->q_full[qs], (q_it / T::Q_STAGES) & 1, wc, 3))) break;
-          tc_fence_after();
-          const uint64_t qdesc = sdesc_sw128(sbase + T::SM_Q + qs * T::Q_BYTES, 16, 1024);
-          const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
-          const uint32_t t0 = t, k0 = kv_it;
-          for (int j = 0; ok && j < 2 && j < nkv; ++j) ok = issue_s(t0 + j, k0 + j, qdesc, j == nkv - 1, qs);
-          for (int j = 0; ok && j < nkv; ++j) {
-            if (j + 2 < nkv && !(ok = issue_s(t0 + j + 2, k0 + j + 2, qdesc, j + 2 == nkv - 1, qs))) break;
-            ok = issue_pv(t0 + j, k0 + j, j == 0);
-          }
-          t += nkv;
-          kv_it += nkv;
-          ++q_it;
-          ++item;
-        }
-      }
-      // Drain: all MMAs issued by this warp complete before TMEM is freed.
-      mma_commit_warp(&bars->mma_done);
-      drain_wait(&bars->mma_done, 0);
-    }
-  } else {
-    // ----------------------------------------------------- softmax warps
-    constexpr int HC = T::BN / 2;  // S columns per thread
-    constexpr int HD = D / 2;      // O columns per thread
-    const int wg = warp >> 2;      // column half
-    const int quad = warp & 3;
-    const int r = quad * 32 + lane;  // query row inside the tile, == TMEM lane
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    float* xch = reinterpret_cast<float*>(smem + T::SM_XCH);
-    uint64_t* pair = &bars->pair[quad];
-    const float sl2 = prm.scale_log2;
-    uint32_t t = 0, q_item = 0, xc = 0;
-    bool ok = true;
-    // Swap a per-row value with the other half of the row (same row, other
-    // column half).  Double-buffered by exchange parity: a slot is rewritten
-    // two exchanges later, after the partner passed the next exchange.
-    auto exchange = [&](float v, float& other) -> bool {
-      float* buf = xch + (xc & 1) * (2 * T::BM);
-      buf[wg * T::BM + r] = v;
-      mbar_arrive(pair);
-      const bool w = mbar_wait(pair, xc & 1, wc, 14);
-      other = buf[(wg ^ 1) * T::BM + r];
-      ++xc;
-      return __all_sync(0xffffffffu, w);
-    };
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      int head, qa, qb;
-      fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
-      for (int half = 0; ok && half < 2; ++half) {
-        const int qt = half ? qb : qa;
-        if (qt < 0) break;
-        const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
-        const int qi = qt * T::BM + r;  // query index within the head
-        float m = -INFINITY, l = 0.f;   // l: this half's partial row sum
-        for (int j = 0; j < nkv; ++j) {
-          const int b = t & 1;
-          ok = mbar_wait(&bars->s_full[b], (t >> 1) & 1, wc, 5);
+          t += fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+          ok = mbar_wait(&bars->lm_full, q_item & 1, wc, 17);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          const float l_row = lm[r] + lm[T::BM + r];
+          const float m = lm[2 * T::BM + r];
+          mbar_arrive(&bars->lm_empty);
+          // the item's last P V has completed
+          ok = mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, wc, 7);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
-          // other half of the row: only its max is needed
-          uint32_t sr[HC];
-          float pm[8];
-#pragma unroll
-          for (int c = 0; c < HC; c += 32) tmem_ld32(lane_base + T::S_COL + b * T::BN + (wg ^ 1) * HC + c, sr + c);
-          tmem_wait_ld();
-          reg_fence<HC>(sr);
-          if (CAUSAL && (j + 1) * T::BN - 1 > qt * T::BM) {
-            const int k0 = j * T::BN + (wg ^ 1) * HC;
-#pragma unroll
-            for (int c = 0; c < HC; ++c)
-              if (k0 + c > qi) sr[c] = __float_as_uint(-INFINITY);
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) pm[i] = fmaxf(__uint_as_float(sr[i]), __uint_as_float(sr[i + 8]));
-#pragma unroll
-          for (int c = 16; c < HC; c += 16)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) pm[i] = fmax3(pm[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
-          // own half
-#pragma unroll
-          for (int c = 0; c < HC; c += 32) tmem_ld32(lane_base + T::S_COL + b * T::BN + wg * HC + c, sr + c);
-          tmem_wait_ld();
-          reg_fence<HC>(sr);
-          tc_fence_before();
-          mbar_arrive(&bars->s_free[b]);  // S buffer b may take the S of tile t + 2
-          float s[HC];
-#pragma unroll
-          for (int c = 0; c < HC; ++c) s[c] = __uint_as_float(sr[c]);
-          if (CAUSAL && (j + 1) * T::BN - 1 > qt * T::BM) {
-            const int k0 = j * T::BN + wg * HC;
-#pragma unroll
-            for (int c = 0; c < HC; ++c)
-              if (k0 + c > qi) s[c] = -INFINITY;
-          }
-#pragma unroll
-          for (int c = 0; c < HC; c += 16)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) pm[i] = fmax3(pm[i], s[c + i], s[c + 8 + i]);
-          const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
-          // The running max m only moves when this tile's max exceeds it by
-          // more than kRescaleLog2: below that the stale m keeps every P value
-          // under 2^kRescaleLog2 (exact range for fp16 P and fp32 l), so O and
-          // l need no rescaling.  O / l and lse use the max actually applied,
-          // which gives the same result as always tracking the exact max.
-          // Both halves of a row compute the same row max, so they take the
-          // same decision.
-          const float m_tile = mx * sl2;
-          const float m_new = (m_tile > m + kRescaleLog2) ? m_tile : m;
-          const float neg = -m_new;
-          // x = s * c - m and the row sum in packed fp32 pairs (one f32x2
-          // instruction per two columns)
-          const uint64_t c2 = f2_pack(sl2, sl2), neg2 = f2_pack(neg, neg);
-          uint64_t ps2[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) ps2[i] = 0ull;
-          uint32_t pk[HC / 2];
-#pragma unroll
-          for (int c = 0; c < HC; c += 2) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), c2, neg2), x0, x1);
-            const float p0 = ex2_approx(x0);
-            const float p1 = ex2_approx(x1);
-            ps2[(c >> 1) & 3] = f2_add(ps2[(c >> 1) & 3], f2_pack(p0, p1));
-            pk[c / 2] = pack_half2(p0, p1);
-          }
-          float ps[8];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) f2_unpack(ps2[i], ps[2 * i], ps[2 * i + 1]);
-          const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-          const float alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
-          l = l * alpha + rs;
-          m = m_new;
-          // With two 128-column O halves (D = 256), letting P V of this tile
-          // start while the previous P V still runs gave wrong O on GB300
-          // (the MMAs alternate between the two accumulators); there the
-          // softmax always waits for the previous P V before releasing P.
-          constexpr bool kSerialPV = (T::NOH > 1);
-          if (j > 0 && (kSerialPV || __any_sync(0xffffffffu, alpha != 1.f))) {
-            // O holds P V of the previous tiles: wait for the last P V, then
-            // rescale (this half's columns of) rows whose max moved.
-            ok = mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, wc, 6);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            tc_fence_after();
-            if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-              for (int c = 0; c < HD; c += 32) {
-                uint32_t o[32];
-                tmem_ld32(lane_base + T::O_COL + wg * HD + c, o);
-                tmem_wait_ld();
-                reg_fence<32>(o);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                tmem_st32(lane_base + T::O_COL + wg * HD + c, o);
-              }
+          const float inv_l = 1.f / l_row;
+          const uint32_t so = smem_u32(smem + T::SM_Q + (q_item % T::Q_STAGES) * T::Q_BYTES) + r * 128;
+  #pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + T::O_COL + c, o);
+            tmem_wait_ld();
+            reg_fence<32>(o);
+            uint32_t h[16];
+  #pragma unroll
+            for (int i = 0; i < 16; ++i)
+              h[i] = pack_half2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            const uint32_t sub = so + (c / 64) * T::Q_SUB;
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int ch = ((c % 64) / 8 + i) ^ (r & 7);
+              st_shared_v4(sub + ch * 16, h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
             }
           }
-          // P buffer b was last read by the P V of tile t - 2
-          if (t >= 2) {
-            ok = mbar_wait(&bars->pv_done[b], ((t - 2) >> 1) & 1, wc, 15);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            tc_fence_after();
-          }
-          const uint32_t pcol = lane_base + T::P_COL + b * (T::BN / 2) + wg * (HC / 2);
-          if (HC / 2 == 32) {
-            tmem_st32(pcol, pk);
-          } else {
-            tmem_st16(pcol, pk);
-          }
-          tmem_wait_st();
+          fence_proxy_async_smem();
+          mbar_arrive(&bars->epi_full[q_item % T::Q_STAGES]);
+          prm.lse[static_cast<size_t>(head) * N + qt * T::BM + r] = (m + log2f(l_row)) * 0.69314718055994530942f;
           tc_fence_before();
-          mbar_arrive(&bars->p_full[b]);
-          ++t;
-        }
-        if (!ok) break;
-        // ---- epilogue: O / l -> fp16 into this item's Q buffer (swizzled
-        // like a Q tile; the store warp writes it out with TMA), lse direct
-        ok = mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, wc, 7);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        float l_other;
-        if (!(ok = exchange(l, l_other))) break;
-        const float l_row = l + l_other;
-        const float inv_l = 1.f / l_row;
-        const uint32_t so = smem_u32(smem + T::SM_Q + (q_item % T::Q_STAGES) * T::Q_BYTES) + r * 128;
-#pragma unroll 1
-        for (int c = 0; c < HD; c += 32) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + T::O_COL + wg * HD + c, o);
-          tmem_wait_ld();
-          reg_fence<32>(o);
-          uint32_t h[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            h[i] = pack_half2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          const int col0 = wg * HD + c;
-          const uint32_t sub = so + (col0 / 64) * T::Q_SUB;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int ch = ((col0 % 64) / 8 + i) ^ (r & 7);
-            st_shared_v4(sub + ch * 16, h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+          mbar_arrive(&bars->o_free);
+          if (warp == 8) {
+            // all 128 rows are staged: store the tile with TMA, then release
+            // the Q buffer once TMA has read it
+            const int qs = q_item % T::Q_STAGES;
+            if (!(ok = warp_wait(&bars->epi_full[qs], (q_item / T::Q_STAGES) & 1, wc, 13))) break;
+            if (lane == 0) {
+              const uint8_t* so_tile = smem + T::SM_Q + qs * T::Q_BYTES;
+              for (int sub = 0; sub < T::DSUB; ++sub)
+                tma_store_2d(&tm_o, so_tile + sub * T::Q_SUB, sub * 64, head * N + qt * T::BM);
+              bulk_commit();
+              bulk_wait_read<0>();
+              mbar_arrive(&bars->q_empty[qs]);
+            }
+            __syncwarp();
           }
+          ++q_item;
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars->epi_full[q_item % T::Q_STAGES]);
-        if (wg == 0) prm.lse[static_cast<size_t>(head) * N + qi] = (m + log2f(l_row)) * 0.69314718055994530942f;
-        tc_fence_before();
-        mbar_arrive(&bars->o_free);
-        ++q_item;
       }
+      if (warp == 8 && lane == 0) bulk_wait<0>();  // all O stores complete before the CTA exits
+      __syncwarp();
     }
   }
 

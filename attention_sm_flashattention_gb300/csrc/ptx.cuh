@@ -120,6 +120,22 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, w, site));
 }
 
+// ------------------------------------------------------ register budget
+// Per-warpgroup register re-allocation (every thread of the warpgroup runs
+// it).  The block's pool is what it was launched with; the warpgroups that
+// give registers back must do so before the others can take them, and the
+// shares must add up to no more than the launch total.
+
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------- packed fp32 pairs
 // Two fp32 values in one 64-bit register, operated on by the f32x2 forms of
 // add and fma (one instruction for both lanes).
