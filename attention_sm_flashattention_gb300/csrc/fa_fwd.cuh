@@ -533,12 +533,6 @@ __global__ void __launch_bounds__(512, 1)
         return true;
       };
 
-      // Q K^T two tiles ahead of P V, across work items: S(0), S(1), then for
-      // every tile t: S(t + 2) (as soon as the softmax has read S(t)), P V(t).
-      // An item's Q is loaded into the buffer of the item Q_STAGES earlier,
-      // once that item's O has been stored, so Q K^T never runs Q_STAGES or
-      // more items ahead of P V (short causal items would otherwise deadlock:
-      // the S waiting for a Q buffer that only a later P V can release).
       // Two issuing warps: this one issues Q K^T, bounded only by the two S
       // buffers (S(t + 2) as soon as the softmax has read S(t)), so it runs
       // two tiles ahead of the softmax, across work items; warp 15 issues
