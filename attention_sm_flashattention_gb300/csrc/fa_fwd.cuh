@@ -44,9 +44,9 @@ struct FwdTraits {
   static constexpr int BN = (D == 256) ? 64 : 128;  // keys per tile
   // K is released right after Q K^T, V only after P V (a softmax later), so
   // the two tiles travel in separate rings, each with its own producer warp.
-  static constexpr int K_STAGES = (D == 64) ? 4 : 3;
+  static constexpr int K_STAGES = (D == 64) ? 4 : (D == 128) ? 2 : 3;
   static constexpr int V_STAGES = (D == 64) ? 4 : 2;
-  static constexpr int Q_STAGES = (D == 256) ? 1 : 2;
+  static constexpr int Q_STAGES = (D == 256) ? 1 : 3;
   static constexpr int DSUB = D / 64;               // 64-column sub-tiles per row
   static constexpr int Q_SUB = BM * 128;            // bytes of a [BM x 64] fp16 sub-tile
   static constexpr int KV_SUB = BN * 128;
@@ -91,7 +91,7 @@ constexpr float kRescaleLog2 = 8.0f;
 
 // Barrier slots inside the SM_BAR area.
 struct FwdBars {
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[3], q_empty[3];
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], s_free[2], p_full[2];
   uint64_t o_free, mma_done[2];
@@ -101,7 +101,7 @@ struct FwdBars {
   // imply that all earlier P V completed, and one shared barrier could be
   // two phases behind.
   uint64_t pv_done[2];
-  uint64_t epi_full[2];  // O tile written into Q buffer b
+  uint64_t epi_full[3];  // O tile written into Q buffer b
   uint64_t lm_full, lm_empty;  // l, m of one item, handed to the epilogue warps
   uint32_t tmem_base;
   int abort_flag;
@@ -210,15 +210,17 @@ __global__ void __launch_bounds__(512, 1)
   const int lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
       mbar_init(&bars->q_full[i], 1);
       // a Q buffer is free once its last Q K^T completed (MMA commit) and the
       // O tile written into it has been stored (store warp)
       mbar_init(&bars->q_empty[i], 2);
+      mbar_init(&bars->epi_full[i], T::EPI_THREADS);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->s_free[i], T::SOFTMAX_THREADS);
       mbar_init(&bars->p_full[i], T::SOFTMAX_THREADS);
-      mbar_init(&bars->epi_full[i], T::EPI_THREADS);
     }
     mbar_init(&bars->lm_full, T::SOFTMAX_THREADS);
     mbar_init(&bars->lm_empty, T::EPI_THREADS);
