@@ -642,6 +642,21 @@ __global__ void __launch_bounds__(384, 1)
         for (int half = 0; ok && half < 2; ++half) {
           const int i = half ? ib : ia;
           if (i < 0) break;
+          // The item's first K tile goes first: its ring slot frees up early
+          // (tile t-3's dQ), while the Q, dO buffer waits for the previous
+          // item's last dP, so loading K_0 first lets the two latencies
+          // overlap instead of adding up at the item boundary.
+          for (int j = 0; j < num_kv(i); ++j) {
+            if (j == 1 || num_kv(i) == 0) break;
+            const int ks = k_it % KS;
+            if (!(ok = mbar_wait(&bars->k_empty[ks], ((k_it / KS) & 1) ^ 1, wc, 82))) break;
+            mbar_arrive_expect_tx(&bars->k_full[ks], T::TILE);
+            for (int s = 0; s < T::DSUB; ++s)
+              tma_load_2d_hint(smem + T::B_SM_K + ks * T::TILE + s * T::SUB, &tm_k, &bars->k_full[ks], s * 64,
+                               head * N + j * T::BN, pol_kv);
+            ++k_it;
+          }
+          if (!ok) break;
           if (!(ok = mbar_wait(&bars->q_empty, (qc & 1) ^ 1, wc, 81))) break;
           mbar_arrive_expect_tx(&bars->q_full, 2 * T::TILE);
           for (int s = 0; s < T::DSUB; ++s) {
@@ -649,14 +664,13 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_2d_hint(smem + T::B_SM_DO + s * T::SUB, &tm_do, &bars->q_full, s * 64, head * N + i * T::BM, pol_q);
           }
           ++qc;
-          for (int j = 0; j < num_kv(i); ++j) {
+          for (int j = 1; j < num_kv(i); ++j) {
             const int ks = k_it % KS;
             if (!(ok = mbar_wait(&bars->k_empty[ks], ((k_it / KS) & 1) ^ 1, wc, 82))) break;
             mbar_arrive_expect_tx(&bars->k_full[ks], T::TILE);
             for (int s = 0; s < T::DSUB; ++s)
               tma_load_2d_hint(smem + T::B_SM_K + ks * T::TILE + s * T::SUB, &tm_k, &bars->k_full[ks], s * 64,
                                head * N + j * T::BN, pol_kv);
-            // warm L2 with the tile that will refill this slot
             ++k_it;
           }
         }

@@ -641,6 +641,13 @@ int launch_fwd(const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaS
     if (cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              T::SMEM_ALLOC) != cudaSuccess)
       return -1;
+    // the kernel splits its launch registers between warpgroups
+    // (setmaxnreg); refuse to launch if the build gave it fewer than the
+    // split needs, rather than let the raising warpgroups wait forever
+    cudaFuncAttributes fa_attr;
+    if (cudaFuncGetAttributes(&fa_attr, fa_fwd_kernel<D, CAUSAL>) != cudaSuccess ||
+        fa_attr.numRegs * T::THREADS < T::SOFTMAX_THREADS * T::SOFTMAX_REGS + (T::THREADS - T::SOFTMAX_THREADS) * T::OTHER_REGS)
+      return -1;
     attr_set = true;
   }
   const int nqt = prm.N / T::BM;
