@@ -20,13 +20,18 @@ def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
     return s.cuda_stream
 
 
-def _check_input(name: str, t: torch.Tensor, shape=None) -> None:
+_DTYPES = (torch.float16, torch.bfloat16)
+
+
+def _check_input(name: str, t: torch.Tensor, shape=None, dtype=None) -> None:
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must live on a CUDA device")
-    if t.dtype != torch.float16:
-        raise ValueError(f"{name} must be float16, got {t.dtype}")
+    if t.dtype not in _DTYPES:
+        raise ValueError(f"{name} must be float16 or bfloat16, got {t.dtype}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} is {t.dtype}, expected {dtype} like q")
     if t.dim() != 4 or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous [Z, H, N, D] tensor")
     if shape is not None and tuple(t.shape) != tuple(shape):
@@ -36,12 +41,13 @@ def _check_input(name: str, t: torch.Tensor, shape=None) -> None:
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         scale: Optional[float] = None, out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
         stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Exact attention forward.  Returns ``(o, lse)``: o fp16 [Z,H,N,D],
-    lse fp32 [Z,H,N] (natural-log log-sum-exp of each row of scale*Q K^T)."""
+    """Exact attention forward.  Returns ``(o, lse)``: o [Z,H,N,D] in q's dtype
+    (float16 or bfloat16), lse fp32 [Z,H,N] (natural-log log-sum-exp of each
+    row of scale*Q K^T)."""
     _check_input("q", q)
     Z, H, N, D = q.shape
-    _check_input("k", k, q.shape)
-    _check_input("v", v, q.shape)
+    _check_input("k", k, q.shape, q.dtype)
+    _check_input("v", v, q.shape, q.dtype)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
@@ -49,9 +55,10 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         lse = torch.empty((Z, H, N), dtype=torch.float32, device=q.device)
     else:
         o, lse = out
-    rc = _native.lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                              Z, H, N, D, int(bool(causal)), float(scale), _stream_handle(stream))
-    _native.check(rc, "fa_fwd")
+    fn = "fa_fwd_bf16" if q.dtype == torch.bfloat16 else "fa_fwd"
+    rc = getattr(_native.lib(), fn)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                    Z, H, N, D, int(bool(causal)), float(scale), _stream_handle(stream))
+    _native.check(rc, fn)
     return o, lse
 
 
@@ -63,11 +70,12 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, do: 
         lse: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
         workspace: Optional[torch.Tensor] = None, out=None,
         stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """Exact attention backward.  Returns ``(dq, dk, dv)`` fp16 [Z,H,N,D]."""
+    """Exact attention backward.  Returns ``(dq, dk, dv)`` [Z,H,N,D] in q's
+    dtype (float16 or bfloat16)."""
     _check_input("q", q)
     Z, H, N, D = q.shape
     for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
-        _check_input(name, t, q.shape)
+        _check_input(name, t, q.shape, q.dtype)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (Z, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 [Z, H, N] tensor")
     if scale is None:
@@ -79,11 +87,12 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, do: 
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     else:
         dq, dk, dv = out
-    rc = _native.lib().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                              lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                              workspace.data_ptr(), workspace.numel(), Z, H, N, D, int(bool(causal)),
-                              float(scale), _stream_handle(stream))
-    _native.check(rc, "fa_bwd")
+    fn = "fa_bwd_bf16" if q.dtype == torch.bfloat16 else "fa_bwd"
+    rc = getattr(_native.lib(), fn)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                    workspace.data_ptr(), workspace.numel(), Z, H, N, D, int(bool(causal)),
+                                    float(scale), _stream_handle(stream))
+    _native.check(rc, fn)
     return dq, dk, dv
 
 

@@ -3,8 +3,13 @@
 
 namespace fa {
 
-int launch_bwd_d256(bool causal, const CUtensorMap* maps, const BwdParams& prm, int grid, cudaStream_t stream) {
-  return causal ? launch_bwd<256, true>(maps, prm, grid, stream) : launch_bwd<256, false>(maps, prm, grid, stream);
+int launch_bwd_d256(bool causal, bool bf16, const CUtensorMap* maps, const BwdParams& prm, int grid,
+                    cudaStream_t stream) {
+  if (bf16)
+    return causal ? launch_bwd<256, true, true>(maps, prm, grid, stream)
+                  : launch_bwd<256, false, true>(maps, prm, grid, stream);
+  return causal ? launch_bwd<256, true, false>(maps, prm, grid, stream)
+                : launch_bwd<256, false, false>(maps, prm, grid, stream);
 }
 
 }  // namespace fa

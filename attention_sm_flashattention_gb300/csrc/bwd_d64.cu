@@ -5,8 +5,13 @@
 
 namespace fa {
 
-int launch_bwd_d64(bool causal, const CUtensorMap* maps, const BwdParams& prm, int grid, cudaStream_t stream) {
-  return causal ? launch_bwd2<64, true>(maps, prm, grid, stream) : launch_bwd2<64, false>(maps, prm, grid, stream);
+int launch_bwd_d64(bool causal, bool bf16, const CUtensorMap* maps, const BwdParams& prm, int grid,
+                    cudaStream_t stream) {
+  if (bf16)
+    return causal ? launch_bwd2<64, true, true>(maps, prm, grid, stream)
+                  : launch_bwd2<64, false, true>(maps, prm, grid, stream);
+  return causal ? launch_bwd2<64, true, false>(maps, prm, grid, stream)
+                : launch_bwd2<64, false, false>(maps, prm, grid, stream);
 }
 
 }  // namespace fa

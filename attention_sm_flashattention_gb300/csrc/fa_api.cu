@@ -80,9 +80,11 @@ int check_shape(int Z, int H, int N, int D, int causal, float scale) {
   return FA_OK;
 }
 
-bool fp16_map(CUtensorMap* m, const void* base, long long rows, int D, int box_rows) {
+// A [rows x D] tensor of 16-bit elements (fp16, or bf16 when `bf16`).
+bool map16(CUtensorMap* m, const void* base, long long rows, int D, int box_rows, bool bf16) {
   std::memset(m, 0, sizeof(*m));
-  return fa::make_tmap_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, static_cast<uint64_t>(rows),
+  return fa::make_tmap_2d(m, base, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                          static_cast<uint64_t>(rows),
                           static_cast<uint64_t>(D), static_cast<uint64_t>(D), 64, static_cast<uint32_t>(box_rows),
                           true);
 }
@@ -151,8 +153,12 @@ double fa_fwd_flops(int Z, int H, int N, int D, int causal) {
 
 double fa_bwd_flops(int Z, int H, int N, int D, int causal) { return 2.5 * fa_fwd_flops(Z, H, N, D, causal); }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int N, int D,
-           int causal, float scale, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int N, int D,
+             int causal, float scale, cudaStream_t stream, bool bf16) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return FA_ERR_INVALID_ARG;
@@ -164,8 +170,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   const long long rows = static_cast<long long>(Z) * H * N;
   const int bn = fa::fwd_block_n(D);
   CUtensorMap maps[4];  // q, k, v, o
-  if (!fp16_map(&maps[0], q, rows, D, 128) || !fp16_map(&maps[1], k, rows, D, bn) ||
-      !fp16_map(&maps[2], v, rows, D, bn) || !fp16_map(&maps[3], o, rows, D, 128))
+  if (!map16(&maps[0], q, rows, D, 128, bf16) || !map16(&maps[1], k, rows, D, bn, bf16) ||
+      !map16(&maps[2], v, rows, D, bn, bf16) || !map16(&maps[3], o, rows, D, 128, bf16))
     return FA_ERR_CUDA;
   fa::FwdParams prm{};
   prm.o = static_cast<__half*>(o);
@@ -176,11 +182,25 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   prm.status = dev->status;
   const bool c = causal != 0;
   switch (D) {
-    case 64: rc = fa::launch_fwd_d64(c, maps, prm, dev->sms, stream); break;
-    case 128: rc = fa::launch_fwd_d128(c, maps, prm, dev->sms, stream); break;
-    default: rc = fa::launch_fwd_d256(c, maps, prm, dev->sms, stream); break;
+    case 64: rc = fa::launch_fwd_d64(c, bf16, maps, prm, dev->sms, stream); break;
+    case 128: rc = fa::launch_fwd_d128(c, bf16, maps, prm, dev->sms, stream); break;
+    default: rc = fa::launch_fwd_d256(c, bf16, maps, prm, dev->sms, stream); break;
   }
   return rc == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int N, int D,
+           int causal, float scale, cudaStream_t stream) {
+  return fwd_impl(q, k, v, o, lse, Z, H, N, D, causal, scale, stream, false);
+}
+
+int fa_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int N, int D,
+                int causal, float scale, cudaStream_t stream) {
+  return fwd_impl(q, k, v, o, lse, Z, H, N, D, causal, scale, stream, true);
 }
 
 size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal) {
@@ -190,9 +210,13 @@ size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal) {
   return bwd_workspace_layout(Z, H, N, D, dev->sms).total;
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-           void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int Z, int H, int N, int D,
-           int causal, float scale, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int Z, int H, int N, int D,
+             int causal, float scale, cudaStream_t stream, bool bf16) {
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
@@ -209,10 +233,10 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   // the outputs dq, dk, dv (written with TMA stores by the D <= 128 kernels)
   CUtensorMap maps[7];
   const int bq = (D == 256) ? 64 : 128;
-  if (!fp16_map(&maps[0], q, rows, D, bq) || !fp16_map(&maps[1], k, rows, D, 128) ||
-      !fp16_map(&maps[2], v, rows, D, 128) || !fp16_map(&maps[3], dout, rows, D, bq) ||
-      !fp16_map(&maps[4], dq, rows, D, 128) || !fp16_map(&maps[5], dk, rows, D, 128) ||
-      !fp16_map(&maps[6], dv, rows, D, 128))
+  if (!map16(&maps[0], q, rows, D, bq, bf16) || !map16(&maps[1], k, rows, D, 128, bf16) ||
+      !map16(&maps[2], v, rows, D, 128, bf16) || !map16(&maps[3], dout, rows, D, bq, bf16) ||
+      !map16(&maps[4], dq, rows, D, 128, bf16) || !map16(&maps[5], dk, rows, D, 128, bf16) ||
+      !map16(&maps[6], dv, rows, D, 128, bf16))
     return FA_ERR_CUDA;
   char* wsb = static_cast<char*>(workspace);
   fa::BwdParams prm{};
@@ -232,11 +256,29 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   prm.status = dev->status;
   const bool c = causal != 0;
   switch (D) {
-    case 64: rc = fa::launch_bwd_d64(c, maps, prm, ws.grid, stream); break;
-    case 128: rc = fa::launch_bwd_d128(c, maps, prm, ws.grid, stream); break;
-    default: rc = fa::launch_bwd_d256(c, maps, prm, ws.grid, stream); break;
+    case 64: rc = fa::launch_bwd_d64(c, bf16, maps, prm, ws.grid, stream); break;
+    case 128: rc = fa::launch_bwd_d128(c, bf16, maps, prm, ws.grid, stream); break;
+    default: rc = fa::launch_bwd_d256(c, bf16, maps, prm, ws.grid, stream); break;
   }
   return rc == 0 ? FA_OK : (rc == -2 ? FA_ERR_UNSUPPORTED : FA_ERR_CUDA);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int Z, int H, int N, int D,
+           int causal, float scale, cudaStream_t stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, Z, H, N, D, causal, scale, stream,
+                  false);
+}
+
+int fa_bwd_bf16(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int Z, int H, int N, int D,
+                int causal, float scale, cudaStream_t stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, Z, H, N, D, causal, scale, stream,
+                  true);
 }
 
 int fa_device_status_raw(cudaStream_t stream, int* raw) {
@@ -317,10 +359,10 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   const long long rows = heads * N;
   CUtensorMap maps[7];
   const int bq = (D == 256) ? 64 : 128;
-  if (!fp16_map(&maps[0], q, rows, D, bq) || !fp16_map(&maps[1], k, rows, D, 128) ||
-      !fp16_map(&maps[2], v, rows, D, 128) || !fp16_map(&maps[3], dout, rows, D, bq) ||
-      !fp16_map(&maps[4], dq, rows, D, 128) || !fp16_map(&maps[5], dk, rows, D, 128) ||
-      !fp16_map(&maps[6], dv, rows, D, 128))
+  if (!map16(&maps[0], q, rows, D, bq, false) || !map16(&maps[1], k, rows, D, 128, false) ||
+      !map16(&maps[2], v, rows, D, 128, false) || !map16(&maps[3], dout, rows, D, bq, false) ||
+      !map16(&maps[4], dq, rows, D, 128, false) || !map16(&maps[5], dk, rows, D, 128, false) ||
+      !map16(&maps[6], dv, rows, D, 128, false))
     return FA_ERR_CUDA;
   fa::BwdParams prm{};
   prm.o = static_cast<const __half*>(o);
@@ -340,9 +382,9 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   const bool c = causal != 0;
   const int g = static_cast<int>(grid);
   switch (D) {
-    case 64: rc = fa::launch_bwd_d64(c, maps, prm, g, stream); break;
-    case 128: rc = fa::launch_bwd_d128(c, maps, prm, g, stream); break;
-    default: rc = fa::launch_bwd_d256(c, maps, prm, g, stream); break;
+    case 64: rc = fa::launch_bwd_d64(c, false, maps, prm, g, stream); break;
+    case 128: rc = fa::launch_bwd_d128(c, false, maps, prm, g, stream); break;
+    default: rc = fa::launch_bwd_d256(c, false, maps, prm, g, stream); break;
   }
   return rc == 0 ? FA_OK : FA_ERR_CUDA;
 }

@@ -45,7 +45,7 @@ namespace fa {
 
 // -------------------------------------------------------------- preprocess
 
-template <int D>
+template <int D, bool BF>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __half* __restrict__ o,
                                                           const __half* __restrict__ dout,
                                                           const float* __restrict__ lse, float* __restrict__ delta,
@@ -58,12 +58,12 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __half* __restri
   if (r < rows) {
     const uint4 a = reinterpret_cast<const uint4*>(o + static_cast<size_t>(r) * D)[part];
     const uint4 b = reinterpret_cast<const uint4*>(dout + static_cast<size_t>(r) * D)[part];
-    const __half2* ha = reinterpret_cast<const __half2*>(&a);
-    const __half2* hb = reinterpret_cast<const __half2*>(&b);
+    const uint32_t* ha = reinterpret_cast<const uint32_t*>(&a);
+    const uint32_t* hb = reinterpret_cast<const uint32_t*>(&b);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float2 fa2 = __half22float2(ha[i]);
-      const float2 fb2 = __half22float2(hb[i]);
+      const float2 fa2 = unpack2<BF>(ha[i]);
+      const float2 fb2 = unpack2<BF>(hb[i]);
       acc = fmaf(fa2.x, fb2.x, acc);
       acc = fmaf(fa2.y, fb2.y, acc);
     }
@@ -153,7 +153,7 @@ __device__ __forceinline__ int bwd_first_qtile(int j) {
   return CAUSAL ? (j * T::BN) / T::BM : 0;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BF>
 __global__ void __launch_bounds__(320, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -247,10 +247,10 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == T::MMA_WARP) {
     // ------------------------------------------------------------- MMA issuer
     {  // the whole warp runs the loop; one elected lane issues each MMA
-      constexpr uint32_t id_s = idesc_f16(128, T::BM, false, false);   // S^T, dP^T: M keys, N queries
-      constexpr uint32_t id_kv = idesc_f16(128, T::DH, false, true);   // dV, dK: N = DH, B MN-major
-      constexpr uint32_t id_dq = T::DQ_T ? idesc_f16(128, T::BM, true, true)  // dQ^T: M = d, N = queries
-                                         : idesc_f16(128, D, true, true);     // dQ: M = queries, N = D
+      constexpr uint32_t id_s = idesc_16<BF>(128, T::BM, false, false);   // S^T, dP^T: M keys, N queries
+      constexpr uint32_t id_kv = idesc_16<BF>(128, T::DH, false, true);   // dV, dK: N = DH, B MN-major
+      constexpr uint32_t id_dq = T::DQ_T ? idesc_16<BF>(128, T::BM, true, true)  // dQ^T: M = d, N = queries
+                                         : idesc_16<BF>(128, D, true, true);     // dQ: M = queries, N = D
       const uint32_t sb = smem_u32(smem);
       const uint32_t sK = sb + T::SM_K, sV = sb + T::SM_V, sDS = sb + T::SM_DS;
       uint32_t t = 0, kc = 0, pc = 0;
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(320, 1)
             }
             uint32_t pk[T::QC / 2];
 #pragma unroll
-            for (int c = 0; c < T::QC / 2; ++c) pk[c] = pack_half2(p[2 * c], p[2 * c + 1]);
+            for (int c = 0; c < T::QC / 2; ++c) pk[c] = pack2<BF>(p[2 * c], p[2 * c + 1]);
             if (T::QC / 2 == 32) {
               tmem_st32(lb + T::S_COL + wg * T::QC, pk);
             } else {
@@ -417,9 +417,9 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int c = 0; c < T::QC; c += 4) {
               const float4 Dl = __ldg(d4 + c / 4);
-              pk[c / 2] = pack_half2(p[c] * (__uint_as_float(sr[c]) - Dl.x), p[c + 1] * (__uint_as_float(sr[c + 1]) - Dl.y));
+              pk[c / 2] = pack2<BF>(p[c] * (__uint_as_float(sr[c]) - Dl.x), p[c + 1] * (__uint_as_float(sr[c + 1]) - Dl.y));
               pk[c / 2 + 1] =
-                  pack_half2(p[c + 2] * (__uint_as_float(sr[c + 2]) - Dl.z), p[c + 3] * (__uint_as_float(sr[c + 3]) - Dl.w));
+                  pack2<BF>(p[c + 2] * (__uint_as_float(sr[c + 2]) - Dl.z), p[c + 3] * (__uint_as_float(sr[c + 3]) - Dl.w));
             }
             if (t > 0) {
               ok = mbar_wait(&bars->ds_free, (t - 1) & 1, wc, 43);
@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(320, 1)
               uint32_t hv[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e)
-                hv[e] = pack_half2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+                hv[e] = pack2<BF>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
               uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
               for (int e = 0; e < 4; ++e) dst[e] = make_uint4(hv[4 * e], hv[4 * e + 1], hv[4 * e + 2], hv[4 * e + 3]);
@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(320, 1)
       uint2* dq = reinterpret_cast<uint2*>(prm.dq + static_cast<size_t>(head) * N * D);
       for (int e = threadIdx.x; e < N * D / 4; e += T::COMPUTE_THREADS) {
         const float4 v = __ldcg(src + e);
-        dq[e] = make_uint2(pack_half2(v.x * scale, v.y * scale), pack_half2(v.z * scale, v.w * scale));
+        dq[e] = make_uint2(pack2<BF>(v.x * scale, v.y * scale), pack2<BF>(v.z * scale, v.w * scale));
       }
       // the next head's first key tile overwrites the accumulator
       if (!(ok = cw_barrier(47))) break;
@@ -534,22 +534,22 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BF>
 int launch_bwd(const CUtensorMap* maps, const BwdParams& prm, int grid, cudaStream_t stream) {
   using T = BwdTraits<D, CAUSAL>;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(fa_bwd_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(fa_bwd_kernel<D, CAUSAL, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              T::SMEM_ALLOC) != cudaSuccess)
       return -1;
     attr_set = true;
   }
   const int rows = prm.heads * prm.N;
   constexpr int RPB = 256 / (D / 8);
-  fa_bwd_prep_kernel<D><<<(rows + RPB - 1) / RPB, 256, 0, stream>>>(prm.o, prm.dout, prm.lse, prm.delta, prm.lse2,
+  fa_bwd_prep_kernel<D, BF><<<(rows + RPB - 1) / RPB, 256, 0, stream>>>(prm.o, prm.dout, prm.lse, prm.delta, prm.lse2,
                                                                      rows);
   if (cudaGetLastError() != cudaSuccess) return -1;
-  fa_bwd_kernel<D, CAUSAL><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  fa_bwd_kernel<D, CAUSAL, BF><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

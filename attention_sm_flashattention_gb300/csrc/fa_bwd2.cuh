@@ -160,7 +160,7 @@ static_assert(sizeof(DkdvBars) <= 256, "barrier area");
 // unit's last query tile (free once its dK and dV MMAs completed) and written
 // with TMA stores by warp 11, which then hands those two slots back to the
 // producer.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BF>
 __global__ void __launch_bounds__(384, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == MMA_WARP) {
     // ----------------------------------- MMA warp: S^T = K Q^T, dP^T = V dO^T
-    constexpr uint32_t id_s = idesc_f16(128, T::BM, false, false);  // S^T, dP^T: M keys, N queries
+    constexpr uint32_t id_s = idesc_16<BF>(128, T::BM, false, false);  // S^T, dP^T: M keys, N queries
     const uint32_t sb = smem_u32(smem);
     const uint64_t kdesc = sdesc_sw128(sb + T::A_SM_K, 16, 1024), vdesc = sdesc_sw128(sb + T::A_SM_V, 16, 1024);
     uint32_t t = 0, kc = 0;
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(384, 1)
     bwd2_drain(&bars->mma_done[0], 0);
   } else if (warp == GRAD_MMA_WARP) {
     // ---------------------------- MMA warp: dV += P^T dO, dK += dS^T Q
-    constexpr uint32_t id_g = idesc_f16(128, D, false, true);  // dV, dK: N = D, B MN-major
+    constexpr uint32_t id_g = idesc_16<BF>(128, D, false, true);  // dV, dK: N = D, B MN-major
     const uint32_t sb = smem_u32(smem);
     uint32_t t = 0, kc = 0;
     bool ok = true;
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(384, 1)
           // halves are read one at a time to keep register pressure low.
           uint32_t pk[T::QC / 2];
 #pragma unroll
-          for (int c = 0; c < T::QC / 2; ++c) pk[c] = f2_to_half2(p2[c]);
+          for (int c = 0; c < T::QC / 2; ++c) pk[c] = f2_to_pack2<BF>(p2[c]);
           ok = mbar_wait(&bars->o_full[os], (t / OS) & 1, wc, 73) && mbar_wait(&bars->dp_full, t & 1, wc, 74);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
@@ -500,8 +500,8 @@ __global__ void __launch_bounds__(384, 1)
               const uint64_t d01 = f2_sub(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), f2_pack(Dl.x, Dl.y));
               const uint64_t d23 =
                   f2_sub(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), f2_pack(Dl.z, Dl.w));
-              pk[16 * h + c / 2] = f2_to_half2(f2_mul(p2[(32 * h + c) / 2], d01));
-              pk[16 * h + c / 2 + 1] = f2_to_half2(f2_mul(p2[(32 * h + c) / 2 + 1], d23));
+              pk[16 * h + c / 2] = f2_to_pack2<BF>(f2_mul(p2[(32 * h + c) / 2], d01));
+              pk[16 * h + c / 2 + 1] = f2_to_pack2<BF>(f2_mul(p2[(32 * h + c) / 2 + 1], d23));
             }
           }
           tmem_st32(rb + T::QC / 2, pk);
@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(384, 1)
             uint32_t h[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              h[e] = pack_half2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+              h[e] = pack2<BF>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
             stage_row32(tile, row, wg * (D / 2) + c, h);
           }
         }
@@ -566,7 +566,7 @@ struct DqBars {
 };
 static_assert(sizeof(DqBars) <= 256, "barrier area");
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BF>
 __global__ void __launch_bounds__(384, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -705,7 +705,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------- MMA warp: S = Q K^T, dP = dO V^T
-    constexpr uint32_t id_s = idesc_f16(128, T::BN, false, false);  // S, dP: M queries, N keys
+    constexpr uint32_t id_s = idesc_16<BF>(128, T::BN, false, false);  // S, dP: M queries, N keys
     const uint32_t sb = smem_u32(smem);
     const uint64_t qdesc = sdesc_sw128(sb + T::B_SM_Q, 16, 1024), odesc = sdesc_sw128(sb + T::B_SM_DO, 16, 1024);
     uint32_t t = 0, k_it = 0, v_it = 0, qc = 0;
@@ -768,7 +768,7 @@ __global__ void __launch_bounds__(384, 1)
     bwd2_drain(&bars->mma_done[0], 0);
   } else if (warp == DQ_MMA_WARP) {
     // ------------------------------------------------- MMA warp: dQ += dS K
-    constexpr uint32_t id_q = idesc_f16(128, D, false, true);  // dQ: N = D, B = K MN-major
+    constexpr uint32_t id_q = idesc_16<BF>(128, D, false, true);  // dQ: N = D, B = K MN-major
     const uint32_t sb = smem_u32(smem);
     uint32_t t = 0, k_it = 0, qc = 0;
     bool ok = true;
@@ -884,7 +884,7 @@ __global__ void __launch_bounds__(384, 1)
           uint32_t pk[T::QC / 2];
 #pragma unroll
           for (int c = 0; c < T::QC; c += 2)
-            pk[c / 2] = f2_to_half2(f2_mul(p2[c / 2], f2_add(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), nd2)));
+            pk[c / 2] = f2_to_pack2<BF>(f2_mul(p2[c / 2], f2_add(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), nd2)));
           tmem_st32(lb + dpc, pk);
           tmem_wait_st();
           tc_fence_before();
@@ -907,7 +907,7 @@ __global__ void __launch_bounds__(384, 1)
           const float sc = prm.scale;
           uint32_t h[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) h[e] = pack_half2(__uint_as_float(v[2 * e]) * sc, __uint_as_float(v[2 * e + 1]) * sc);
+          for (int e = 0; e < 16; ++e) h[e] = pack2<BF>(__uint_as_float(v[2 * e]) * sc, __uint_as_float(v[2 * e + 1]) * sc);
           stage_row32(tile, row, wg * (D / 2) + c, h);
         }
         fence_proxy_async_smem();
@@ -929,30 +929,30 @@ __global__ void __launch_bounds__(384, 1)
 
 // Delta/lse2 preprocess, then the dK/dV and dQ kernels on the same stream.
 // `max_ctas` caps each persistent grid (normally the SM count).
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BF>
 int launch_bwd2(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, cudaStream_t stream) {
   using T = Bwd2Traits<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::A_SMEM) !=
+    if (cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, CAUSAL, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::A_SMEM) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(fa_bwd_dq_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::B_SMEM) !=
+        cudaFuncSetAttribute(fa_bwd_dq_kernel<D, CAUSAL, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::B_SMEM) !=
             cudaSuccess)
       return -1;
     attr_set = true;
   }
   const int rows = prm.heads * prm.N;
   constexpr int RPB = 256 / (D / 8);
-  fa_bwd_prep_kernel<D><<<(rows + RPB - 1) / RPB, 256, 0, stream>>>(prm.o, prm.dout, prm.lse, prm.delta, prm.lse2,
+  fa_bwd_prep_kernel<D, BF><<<(rows + RPB - 1) / RPB, 256, 0, stream>>>(prm.o, prm.dout, prm.lse, prm.delta, prm.lse2,
                                                                      rows);
   if (cudaGetLastError() != cudaSuccess) return -1;
   const int nt = prm.N / 128;
   const int units = CAUSAL ? prm.heads * ((nt + 1) / 2) : prm.heads * nt;
   const int grid = units < max_ctas ? units : max_ctas;
-  fa_bwd_dkdv_kernel<D, CAUSAL><<<grid, 384, T::A_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[5],
+  fa_bwd_dkdv_kernel<D, CAUSAL, BF><<<grid, 384, T::A_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[5],
                                                                    maps[6], prm);
   if (cudaGetLastError() != cudaSuccess) return -1;
-  fa_bwd_dq_kernel<D, CAUSAL><<<grid, 384, T::B_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], prm);
+  fa_bwd_dq_kernel<D, CAUSAL, BF><<<grid, 384, T::B_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

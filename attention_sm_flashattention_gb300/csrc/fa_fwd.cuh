@@ -194,7 +194,7 @@ struct FwdCursor {
   }
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BF>
 __global__ void __launch_bounds__(512, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(512, 1)
               const float p0 = ex2_approx(x0);
               const float p1 = ex2_approx(x1);
               ps2[(c >> 1) & 3] = f2_add(ps2[(c >> 1) & 3], f2_pack(p0, p1));
-              pk[c / 2] = pack_half2(p0, p1);
+              pk[c / 2] = pack2<BF>(p0, p1);
             }
             float ps[8];
   #pragma unroll
@@ -482,8 +482,8 @@ __global__ void __launch_bounds__(512, 1)
     } else if (warp == T::MMA_WARP || warp == T::PV_MMA_WARP) {
       // ------------------------------------------------------------ MMA issuers
       // The whole warp runs the loop; one elected lane issues each MMA.
-      constexpr uint32_t idesc_qk = idesc_f16(128, T::BN, false, false);
-      constexpr uint32_t idesc_pv = idesc_f16(128, T::OH, false, true);
+      constexpr uint32_t idesc_qk = idesc_16<BF>(128, T::BN, false, false);
+      constexpr uint32_t idesc_pv = idesc_16<BF>(128, T::OH, false, true);
       const uint32_t sbase = smem_u32(smem);
       bool ok = true;
 
@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t h[16];
   #pragma unroll
             for (int i = 0; i < 16; ++i)
-              h[i] = pack_half2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+              h[i] = pack2<BF>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
             const uint32_t sub = so + (c / 64) * T::Q_SUB;
   #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -633,19 +633,19 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BF>
 int launch_fwd(const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaStream_t stream) {
   using T = FwdTraits<D, CAUSAL>;
   static bool attr_set = false;  // per process; the attribute is per function, not per device
   if (!attr_set) {
-    if (cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              T::SMEM_ALLOC) != cudaSuccess)
       return -1;
     // the kernel splits its launch registers between warpgroups
     // (setmaxnreg); refuse to launch if the build gave it fewer than the
     // split needs, rather than let the raising warpgroups wait forever
     cudaFuncAttributes fa_attr;
-    if (cudaFuncGetAttributes(&fa_attr, fa_fwd_kernel<D, CAUSAL>) != cudaSuccess ||
+    if (cudaFuncGetAttributes(&fa_attr, fa_fwd_kernel<D, CAUSAL, BF>) != cudaSuccess ||
         fa_attr.numRegs * T::THREADS < T::SOFTMAX_THREADS * T::SOFTMAX_REGS + (T::THREADS - T::SOFTMAX_THREADS) * T::OTHER_REGS)
       return -1;
     attr_set = true;
@@ -653,7 +653,7 @@ int launch_fwd(const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaS
   const int nqt = prm.N / T::BM;
   const int units = CAUSAL ? prm.heads * ((nqt + 1) / 2) : prm.heads * nqt;
   const int grid = units < num_sms ? units : num_sms;
-  fa_fwd_kernel<D, CAUSAL><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  fa_fwd_kernel<D, CAUSAL, BF><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -36,16 +36,17 @@ struct BwdParams {
   int* status;
 };
 
-// One launcher per (D, causal) instantiation; return 0 on success.  For the
-// backward, `grid` caps the persistent grid: for D = 256 it is the number of
-// per-CTA dQ accumulators in the workspace, for D <= 128 (no accumulators)
-// the SM count.
+// One launcher per head dimension; `causal` and `bf16` (bf16 instead of
+// fp16 inputs and outputs) select the instantiation.  Return 0 on success.
+// For the backward, `grid` caps the persistent grid: for D = 256 it is the
+// number of per-CTA dQ accumulators in the workspace, for D <= 128 (no
+// accumulators) the SM count.  The tensor maps carry the element type.
 #define FA_DECLARE_LAUNCHERS(D)                                                                      \
-  int launch_fwd_d##D(bool causal, const CUtensorMap* maps, const FwdParams& prm, int num_sms,      \
-                      cudaStream_t stream);                                                           \
+  int launch_fwd_d##D(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm,       \
+                      int num_sms, cudaStream_t stream);                                              \
   /* bwd maps: q, k, v, dout, dq, dk, dv */                                                         \
-  int launch_bwd_d##D(bool causal, const CUtensorMap* maps, const BwdParams& prm, int grid,          \
-                      cudaStream_t stream);
+  int launch_bwd_d##D(bool causal, bool bf16, const CUtensorMap* maps, const BwdParams& prm,       \
+                      int grid, cudaStream_t stream);
 
 FA_DECLARE_LAUNCHERS(64)
 FA_DECLARE_LAUNCHERS(128)

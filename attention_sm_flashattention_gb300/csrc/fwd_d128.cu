@@ -3,8 +3,13 @@
 
 namespace fa {
 
-int launch_fwd_d128(bool causal, const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaStream_t stream) {
-  return causal ? launch_fwd<128, true>(maps, prm, num_sms, stream) : launch_fwd<128, false>(maps, prm, num_sms, stream);
+int launch_fwd_d128(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,
+                    cudaStream_t stream) {
+  if (bf16)
+    return causal ? launch_fwd<128, true, true>(maps, prm, num_sms, stream)
+                  : launch_fwd<128, false, true>(maps, prm, num_sms, stream);
+  return causal ? launch_fwd<128, true, false>(maps, prm, num_sms, stream)
+                : launch_fwd<128, false, false>(maps, prm, num_sms, stream);
 }
 
 }  // namespace fa

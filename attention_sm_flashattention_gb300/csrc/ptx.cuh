@@ -13,6 +13,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 namespace fa {
@@ -363,6 +364,13 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, 
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// kind::f16 instruction descriptor with A and B both fp16 (BF = false) or
+// both bf16 (BF = true).
+template <bool BF>
+__host__ __device__ constexpr uint32_t idesc_16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return idesc_f16(M, N, a_mn_major, b_mn_major) | (BF ? ((1u << 7) | (1u << 10)) : 0u);
+}
+
 // ---- TMEM loads/stores (32x32b shape: thread t of warp w <-> lane 32*(w%4)+t)
 
 #define FA_R8(b) "=r"(r[b + 0]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), \
@@ -445,6 +453,36 @@ __device__ __forceinline__ uint32_t f2_to_half2(uint64_t v) {
   float a, b;
   f2_unpack(v, a, b);
   return pack_half2(a, b);
+}
+
+// The 16-bit element type of the inputs, outputs and MMA operands: fp16
+// (BF = false) or bf16 (BF = true).  Two floats -> one packed pair, round to
+// nearest even.
+template <bool BF>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    return pack_half2(lo, hi);
+  }
+}
+
+template <bool BF>
+__device__ __forceinline__ uint32_t f2_to_pack2(uint64_t v) {
+  float a, b;
+  f2_unpack(v, a, b);
+  return pack2<BF>(a, b);
+}
+
+// Two packed 16-bit values -> two floats.
+template <bool BF>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+  if constexpr (BF) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+  } else {
+    return __half22float2(*reinterpret_cast<const __half2*>(&v));
+  }
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {

@@ -5,7 +5,7 @@ This module holds no attention arithmetic: it only names the workloads and
 draws their tensors.  Recipe: a CPU ``torch.Generator`` seeded with the
 workload's seed draws ``q``, ``k``, ``v``, ``do`` in that order, each as
 standard-normal float32 of shape ``[Z, H, N, D]``, then rounds them to fp16
-(round-to-nearest-even).  ``scale = 1/sqrt(D)`` passed as a float32.
+(round-to-nearest-even), or to bf16 for the bf16 path.  ``scale = 1/sqrt(D)`` passed as a float32.
 """
 
 from __future__ import annotations
@@ -51,8 +51,9 @@ WORKLOADS = {
 }
 
 
-def make_inputs(Z: int, H: int, N: int, D: int, seed: int, device="cpu"):
-    """Draw fp16 ``(q, k, v, do)`` of shape ``[Z, H, N, D]`` from ``seed``.
+def make_inputs(Z: int, H: int, N: int, D: int, seed: int, device="cpu", dtype=torch.float16):
+    """Draw ``(q, k, v, do)`` of shape ``[Z, H, N, D]`` from ``seed``, rounded
+    to ``dtype`` (fp16 by default, or bf16; the same draw either way).
 
     The draw always happens on the CPU generator so that every device sees
     bit-identical tensors; ``device`` only says where the result is moved.
@@ -61,7 +62,7 @@ def make_inputs(Z: int, H: int, N: int, D: int, seed: int, device="cpu"):
     shape = (Z, H, N, D)
     out = []
     for _ in range(4):
-        t = torch.randn(shape, generator=g, dtype=torch.float32).to(torch.float16)
+        t = torch.randn(shape, generator=g, dtype=torch.float32).to(dtype)
         out.append(t if device == "cpu" else t.to(device))
     return tuple(out)
 

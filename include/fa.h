@@ -84,10 +84,11 @@ FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* l
            int causal, float scale, cudaStream_t stream);
 
 /*
- * Bytes of device workspace fa_bwd needs on the current device: Delta and the
- * log2-scaled lse (2 x Z*H*N fp32) plus one fp32 N x D dQ accumulator per
- * resident CTA.  It grows with Z*H*N and with #SMs*N*D, never with N^2 over
- * all heads (§二, third rule).  Returns 0 for unsupported arguments.
+ * Bytes of device workspace fa_bwd (or fa_bwd_bf16) needs on the current
+ * device: Delta and the log2-scaled lse (2 x Z*H*N fp32); for D = 256 also
+ * one fp32 N x D dQ accumulator per resident CTA.  It grows with Z*H*N (and
+ * #SMs*N*D for D = 256), never with N^2 over all heads (§二, third rule).
+ * Returns 0 for unsupported arguments.
  */
 FA_API size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal);
 
@@ -110,6 +111,21 @@ FA_API size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal);
 FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
            void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int Z, int H, int N, int D,
            int causal, float scale, cudaStream_t stream);
+
+/*
+ * bf16 forward and backward.  Source: «把 FlashAttention 搬上昇腾» §九 (every
+ * candidate version is checked for correctness in FP16 and in BF16).  Identical to fa_fwd / fa_bwd
+ * except that every [Z,H,N,D] tensor (q, k, v, o, dout, dq, dk, dv) is
+ * bf16, and P and dS are rounded to bf16 before the matrix unit; lse, Delta,
+ * the accumulators and the softmax statistics stay fp32.  Same layout,
+ * alignment, ownership, workspace (fa_bwd_workspace_size) and error codes.
+ */
+FA_API int fa_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int N,
+                       int D, int causal, float scale, cudaStream_t stream);
+
+FA_API int fa_bwd_bf16(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                       const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                       int Z, int H, int N, int D, int causal, float scale, cudaStream_t stream);
 
 /*
  * Backward pass that allocates nothing and takes no workspace.

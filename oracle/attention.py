@@ -51,9 +51,12 @@ __all__ = [
 
 
 def _f64(x) -> np.ndarray:
-    """Exact widening of fp16/fp32 host data (numpy or torch CPU) to fp64."""
+    """Exact widening of fp16/bf16/fp32 host data (numpy or torch CPU) to fp64."""
     if hasattr(x, "detach"):  # torch tensor: go through numpy without torch math
-        x = x.detach().cpu().numpy()
+        x = x.detach().cpu()
+        if str(x.dtype) == "torch.bfloat16":
+            x = x.float()  # exact: every bf16 value is an fp32 value (numpy has no bf16)
+        x = x.numpy()
     return np.asarray(x, dtype=np.float64)
 
 

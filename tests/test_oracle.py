@@ -324,3 +324,25 @@ def test_pins_catch_planted_forward_mistakes():
     p_good, _ = orc.softmax_probs(s)
     p_late, _ = orc.softmax_probs(q @ k.T)
     assert not np.allclose(p_good @ v, p_late @ v)
+
+
+def test_bf16_inputs_widen_exactly():
+    # bf16 carries 8 significant bits: these values are exact in bf16 and
+    # must reach the oracle unchanged.
+    vals = [1.0, 1.0 + 2.0 ** -7, -3.0, 2.0 ** -20, 1.5 * 2.0 ** 60]
+    t = torch.tensor(vals, dtype=torch.bfloat16)
+    assert list(orc._f64(t)) == vals
+
+
+def test_bf16_closed_form_zero_q():
+    # Q = 0 in bf16: every row of P is uniform, O_i = mean_j V_j and
+    # lse_i = ln N, whatever the (bf16) K and V.
+    n, d = 64, 16
+    g = torch.Generator().manual_seed(5)
+    q = torch.zeros(1, 1, n, d, dtype=torch.bfloat16)
+    k = torch.randn(1, 1, n, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, 1, n, d, generator=g).to(torch.bfloat16)
+    o, lse = orc.attn_fwd_ref(q, k, v, False, 0.25)
+    vm = v.float().double().numpy()[0, 0].mean(axis=0)
+    assert np.max(np.abs(o[0, 0] - vm)) < 1e-14
+    assert np.max(np.abs(lse - np.log(n))) < 1e-14
