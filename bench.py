@@ -30,6 +30,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 Z, H, N, D, CAUSAL = 128, 8, 1024, 128, False
+DTYPE = "f16"  # element type of the inputs and outputs: "f16" (benchmark) or "bf16"
 WORKLOAD = "attention fwd+bwd, Z128 H8 N1024 D128 non-causal, fp16 inputs ~N(0,1), scale 1/sqrt(D)"
 METRIC = "attention fwd / fwd+bwd TFLOP/s at Z128 H8 N1024 D128 on 1 GB300; % of FP16 peak"
 UNIT = "TFLOP/s"
@@ -157,7 +158,8 @@ def gpu_bench(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     gen = torch.Generator(device=dev).manual_seed(SEED + rank)
-    q, k, v, do = (torch.randn((Z, H, N, D), device=dev, dtype=torch.float16, generator=gen) for _ in range(4))
+    elem = torch.bfloat16 if DTYPE == "bf16" else torch.float16
+    q, k, v, do = (torch.randn((Z, H, N, D), device=dev, dtype=elem, generator=gen) for _ in range(4))
     scale = 1.0 / math.sqrt(D)
     o = torch.empty_like(q)
     lse = torch.empty((Z, H, N), device=dev, dtype=torch.float32)
@@ -284,16 +286,23 @@ def main():
     ap.add_argument("--n", type=int, default=N)
     ap.add_argument("--d", type=int, default=D)
     ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
+                    help="element type of the inputs and outputs (the benchmark is f16)")
     args = ap.parse_args()
+    global DTYPE
+    DTYPE = args.dtype
     args.warmup = max(args.warmup, 3)
     set_workload(args.z, args.h, args.n, args.d, args.causal)
+    global WORKLOAD
+    if DTYPE == "bf16":
+        WORKLOAD = WORKLOAD.replace("fp16 inputs", "bf16 inputs")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     config = {"workload": WORKLOAD, "Z": Z, "H": H, "N": N, "D": D, "causal": CAUSAL,
               "global_batch": Z * world, "seq_len": N, "parallelism": f"replicas{world}",
-              "l2": f"inputs larger than L2 ({4 * Z * H * N * D * 2 / 1e6:.0f} MB fp16 per step), no flush needed"}
+              "l2": f"inputs larger than L2 ({4 * Z * H * N * D * 2 / 1e6:.0f} MB {DTYPE} per step), no flush needed"}
 
     if args.impl == "reference":
         # The oracle as it stands, on the host cores: each step is one head of
@@ -348,7 +357,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": config,
+        "vs_baseline": None, "dtype": DTYPE, "data": "synthetic", "config": config,
         "fwd_ms": r["fwd_ms"], "bwd_ms": r["bwd_ms"], "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
         "pct_of_peak": {"fwd": fwd_tf / peaks["tflops"], "fwd_bwd": value / world / peaks["tflops"],
                         "bwd": bwd_tf / peaks["tflops"], "peak_tflops": peaks["tflops"],
