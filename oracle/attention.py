@@ -19,6 +19,14 @@ reordered:
 * causal -- same article, §一 (the causal bullet) and §八: the upper triangle
   (key index j > query index i) takes no part, i.e. it is masked to -inf
   before the softmax.
+* grouped K/V heads -- same article, the GQA Paged Attention part of the
+  contest section: the number of query heads is an integer multiple g of the
+  number of K/V heads and several query heads share one K/V head.  Query head
+  h reads K/V head ``h // g``; a shared K or V gets the sum of the gradients
+  of every query head that reads it (chain rule).
+* query and key lengths -- the same part: a query attends to the context of
+  its sequence (``context_lens``), and the last incomplete block is masked.
+  Queries and keys may have different lengths n_q and n_k, any length >= 1.
 
 Readings where the pages are silent (each is listed in the design doc):
 
@@ -27,7 +35,14 @@ Readings where the pages are silent (each is listed in the design doc):
   recomputes P (§二); the saved row statistic has to be something from which
   ``P_ij = exp(S_ij - lse_i)``, and this is the plainest one.
 * ``scale`` is the float32 value handed to the GPU, widened to fp64.
-* Layout ``[Z, H, N, D]``; every (z, h) pair is an independent head.
+* Layout ``[Z, H, N, D]``; every (z, h) pair is an independent head.  With
+  grouped heads, Q/O/dO are ``[Z, H, n_q, D]`` and K/V ``[Z, H_kv, n_k, D]``.
+* Causal with n_q != n_k: the queries are the last n_q positions of an n_k
+  long sequence (the decode reading of the contest section, where a new
+  token sees its whole context), so query i sees key j iff
+  ``j <= i + (n_k - n_q)``; for n_q == n_k this is §八's triangle.  n_q > n_k
+  would leave the first rows with no visible key and no softmax; the pages
+  never form such a row, and the oracle refuses it.
 
 Parity pins: every function here is pinned by ``tests/test_oracle.py`` against
 closed forms, invariants, brute force, central finite differences and the
@@ -47,6 +62,8 @@ __all__ = [
     "attn_fwd_head",
     "attn_bwd_head",
     "causal_tile_count",
+    "kv_head_of",
+    "sampled_kv_heads",
 ]
 
 
@@ -69,12 +86,16 @@ def scores(q_h: np.ndarray, k_h: np.ndarray, scale: float, causal: bool) -> np.n
     """S = Q K^T * scale for one head, with -inf above the diagonal if causal.
 
     §一 of «把 FlashAttention 搬上昇腾»; the mask follows §八 (upper triangle,
-    key j > query i, does not take part).
+    key j > query i, does not take part), with the diagonal moved to
+    ``j > i + (n_k - n_q)`` when the query block is the end of a longer
+    sequence (module docstring).
     """
     s = (q_h @ k_h.T) * _scale64(scale)
     if causal:
         n_q, n_k = s.shape
-        mask = np.arange(n_k)[None, :] > np.arange(n_q)[:, None]
+        if n_q > n_k:
+            raise ValueError("causal attention needs n_q <= n_k (every query sees at least one key)")
+        mask = np.arange(n_k)[None, :] > np.arange(n_q)[:, None] + (n_k - n_q)
         s = np.where(mask, -np.inf, s)
     return s
 
@@ -121,43 +142,92 @@ def attn_bwd_head(q_h, k_h, v_h, do_h, causal: bool, scale: float):
     return dq, dk, dv
 
 
-def attn_fwd_ref(q, k, v, causal: bool, scale: float, heads=None):
-    """Forward over ``[Z, H, N, D]`` inputs.  Returns fp64 ``(O, lse)``.
+def _group(q, k) -> int:
+    """Query heads per K/V head (the GQA ratio g); K/V must divide Q's heads."""
+    h, h_kv = q.shape[1], k.shape[1]
+    if q.shape[0] != k.shape[0] or h % h_kv != 0 or q.shape[3] != k.shape[3]:
+        raise ValueError(f"incompatible q {tuple(q.shape)} and k {tuple(k.shape)}")
+    return h // h_kv
 
-    ``heads``: optional iterable of flat head indices ``z * H + h``; when given
-    only those heads are computed and the result has shape ``[len(heads), N, D]``
-    / ``[len(heads), N]`` (used to sample the full-size workloads).
+
+def kv_head_of(head: int, group: int) -> int:
+    """Flat K/V head read by flat query head ``z * H + h``: ``z * H_kv + h // g``.
+
+    Since ``H = g * H_kv`` this is the flat query head divided by g.
     """
-    z, h, n, d = q.shape
-    qf = q.reshape(z * h, n, d)
-    kf = k.reshape(z * h, n, d)
-    vf = v.reshape(z * h, n, d)
+    return head // group
+
+
+def attn_fwd_ref(q, k, v, causal: bool, scale: float, heads=None):
+    """Forward over ``[Z, H, n_q, D]`` queries and ``[Z, H_kv, n_k, D]`` keys
+    and values.  Returns fp64 ``(O, lse)`` shaped like q and ``[Z, H, n_q]``.
+
+    ``heads``: optional iterable of flat query-head indices ``z * H + h``; when
+    given only those heads are computed and the result has shape
+    ``[len(heads), n_q, D]`` / ``[len(heads), n_q]`` (used to sample the
+    full-size workloads).
+    """
+    g = _group(q, k)
+    z, h, n_q, d = q.shape
+    n_k = k.shape[2]
+    qf = q.reshape(z * h, n_q, d)
+    kf = k.reshape(z * h // g, n_k, d)
+    vf = v.reshape(z * h // g, n_k, d)
     idx = range(z * h) if heads is None else list(heads)
-    o = np.empty((len(idx), n, d))
-    lse = np.empty((len(idx), n))
+    o = np.empty((len(idx), n_q, d))
+    lse = np.empty((len(idx), n_q))
     for out_i, hi in enumerate(idx):
-        o[out_i], lse[out_i] = attn_fwd_head(qf[hi], kf[hi], vf[hi], causal, scale)
+        kv = kv_head_of(hi, g)
+        o[out_i], lse[out_i] = attn_fwd_head(qf[hi], kf[kv], vf[kv], causal, scale)
     if heads is None:
-        return o.reshape(z, h, n, d), lse.reshape(z, h, n)
+        return o.reshape(z, h, n_q, d), lse.reshape(z, h, n_q)
     return o, lse
 
 
 def attn_bwd_ref(q, k, v, do, causal: bool, scale: float, heads=None):
-    """Backward over ``[Z, H, N, D]`` inputs.  Returns fp64 ``(dQ, dK, dV)``.
+    """Backward over ``[Z, H, n_q, D]`` q, do and ``[Z, H_kv, n_k, D]`` k, v.
+    Returns fp64 ``(dQ, dK, dV)`` shaped like q, k, v.
 
-    ``heads`` has the same meaning as in :func:`attn_fwd_ref`.
+    dK and dV of a K/V head sum the per-head gradients of the g query heads
+    that read it.  ``heads``: optional flat query-head indices; dQ is then
+    returned for those heads (``[len(heads), n_q, D]``) and dK, dV for
+    ``sampled_kv_heads(heads, g)`` (each summed over its whole group).
     """
-    z, h, n, d = q.shape
-    flat = [t.reshape(z * h, n, d) for t in (q, k, v, do)]
-    idx = range(z * h) if heads is None else list(heads)
-    outs = [np.empty((len(idx), n, d)) for _ in range(3)]
-    for out_i, hi in enumerate(idx):
-        g = attn_bwd_head(*(t[hi] for t in flat), causal, scale)
-        for o_arr, g_arr in zip(outs, g):
-            o_arr[out_i] = g_arr
+    g = _group(q, k)
+    z, h, n_q, d = q.shape
+    n_k = k.shape[2]
+    qf, dof = q.reshape(z * h, n_q, d), do.reshape(z * h, n_q, d)
+    kf, vf = k.reshape(z * h // g, n_k, d), v.reshape(z * h // g, n_k, d)
     if heads is None:
-        return tuple(o.reshape(z, h, n, d) for o in outs)
-    return tuple(outs)
+        q_idx, kv_idx = list(range(z * h)), list(range(z * h // g))
+    else:
+        q_idx, kv_idx = list(heads), sampled_kv_heads(heads, g)
+    dq = np.empty((len(q_idx), n_q, d))
+    dk = np.zeros((len(kv_idx), n_k, d))
+    dv = np.zeros((len(kv_idx), n_k, d))
+    kv_pos = {kvh: i for i, kvh in enumerate(kv_idx)}
+    need = sorted(set(q_idx) | {kvh * g + r for kvh in kv_idx for r in range(g)})
+    for hi in need:
+        kv = kv_head_of(hi, g)
+        gq, gk, gv = attn_bwd_head(qf[hi], kf[kv], vf[kv], dof[hi], causal, scale)
+        if hi in q_idx:
+            dq[q_idx.index(hi)] = gq
+        if kv in kv_pos:
+            dk[kv_pos[kv]] += gk
+            dv[kv_pos[kv]] += gv
+    if heads is None:
+        return dq.reshape(z, h, n_q, d), dk.reshape(z, h // g, n_k, d), dv.reshape(z, h // g, n_k, d)
+    return dq, dk, dv
+
+
+def sampled_kv_heads(heads, group: int) -> list:
+    """The K/V heads read by the query heads ``heads``, in first-use order."""
+    out = []
+    for hi in heads:
+        kv = kv_head_of(hi, group)
+        if kv not in out:
+            out.append(kv)
+    return out
 
 
 def causal_tile_count(n_tiles: int, causal: bool) -> int:

@@ -346,3 +346,145 @@ def test_bf16_closed_form_zero_q():
     vm = v.float().double().numpy()[0, 0].mean(axis=0)
     assert np.max(np.abs(o[0, 0] - vm)) < 1e-14
     assert np.max(np.abs(lse - np.log(n))) < 1e-14
+
+
+# ------------------------------------ grouped K/V heads, unequal/ragged lengths
+
+
+def rand_gqa(z, h, h_kv, n_q, n_k, d, seed):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((z, h, n_q, d))
+    k = rng.standard_normal((z, h_kv, n_k, d))
+    v = rng.standard_normal((z, h_kv, n_k, d))
+    do = rng.standard_normal((z, h, n_q, d))
+    return q, k, v, do
+
+
+def brute_force_fwd_offset(q, k, v, causal, scale):
+    """Pure-Python loops: query i is position len(k) - len(q) + i of the sequence."""
+    n_q, n_k, d = len(q), len(k), len(q[0])
+    o, lse = [], []
+    for i in range(n_q):
+        pos = n_k - n_q + i
+        s = [(j, scale * sum(q[i][t] * k[j][t] for t in range(d))) for j in range(n_k) if not (causal and j > pos)]
+        mx = max(x for _, x in s)
+        w = [(j, math.exp(x - mx)) for j, x in s]
+        tot = sum(x for _, x in w)
+        o.append([sum(x * v[j][t] for j, x in w) / tot for t in range(d)])
+        lse.append(mx + math.log(tot))
+    return o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n_q,n_k,d", [(1, 1, 2), (1, 7, 3), (3, 8, 2), (5, 6, 4), (6, 3, 2)])
+def test_brute_force_unequal_lengths(causal, n_q, n_k, d):
+    q, k, v, _ = rand_head(n_q, d, 40 + n_q + n_k, n_k=n_k)
+    sc = float(np.float32(1 / math.sqrt(d)))
+    if causal and n_q > n_k:
+        with pytest.raises(ValueError):
+            orc.attn_fwd_head(q, k, v, causal, sc)
+        return
+    want_o, want_lse = brute_force_fwd_offset(q.tolist(), k.tolist(), v.tolist(), causal, sc)
+    o, lse = orc.attn_fwd_head(q, k, v, causal, sc)
+    np.testing.assert_allclose(o, np.array(want_o), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(lse, np.array(want_lse), rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("n_q,n_k", [(1, 9), (5, 12), (130, 300)])
+def test_zero_query_closed_form_offset(n_q, n_k):
+    # Q = 0, causal, queries at the end: query i sees keys 0..i + n_k - n_q,
+    # so O_i is the mean of those V rows and lse_i the log of their count.
+    d = 6
+    _, k, v, _ = rand_head(n_q, d, 50, n_k=n_k)
+    o, lse = orc.attn_fwd_head(np.zeros((n_q, d)), k, v, True, 0.3)
+    counts = np.arange(n_q) + (n_k - n_q) + 1
+    np.testing.assert_allclose(o, (np.cumsum(v, axis=0) / np.arange(1, n_k + 1)[:, None])[counts - 1],
+                               rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, np.log(counts), rtol=0, atol=1e-13)
+
+
+def test_decode_row_sees_whole_context():
+    # One query at the end of the sequence: causal and non-causal agree.
+    q, k, v, do = rand_head(1, 16, 51, n_k=37)
+    for a, b in zip(orc.attn_fwd_head(q, k, v, True, 0.25), orc.attn_fwd_head(q, k, v, False, 0.25)):
+        np.testing.assert_array_equal(a, b)
+    for a, b in zip(orc.attn_bwd_head(q, k, v, do, True, 0.25), orc.attn_bwd_head(q, k, v, do, False, 0.25)):
+        np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n_q,n_k", [(4, 6), (5, 5)])
+def test_finite_differences_grouped(causal, n_q, n_k):
+    # Two K/V heads each shared by two query heads: the gradient of a shared
+    # K or V is the derivative of the total loss over all four query heads.
+    q, k, v, do = rand_gqa(1, 4, 2, n_q, n_k, 3, 52 + n_q)
+    sc = float(np.float32(0.6))
+    got = orc.attn_bwd_ref(q, k, v, do, causal, sc)
+    want = fd_grads(lambda a, b, c, cz, s: orc.attn_fwd_ref(a, b, c, cz, s), q, k, v, do, causal, sc)
+    for g, w in zip(got, want):
+        rel = np.linalg.norm(g - w) / np.linalg.norm(w)
+        assert rel <= 1e-6, rel
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("h,h_kv,n_q,n_k", [(4, 2, 16, 24), (8, 1, 9, 9), (6, 3, 130, 257)])
+def test_against_torch_sdpa_grouped(causal, h, h_kv, n_q, n_k):
+    # torch's enable_gqa shares K/V head h // g among query heads h, and its
+    # causal_lower_right bias aligns the causal diagonal to the last query
+    # with the last key; both are the library's own definitions.
+    from torch.nn.attention.bias import causal_lower_right
+    q, k, v, do = rand_gqa(2, h, h_kv, n_q, n_k, 8, 53 + h)
+    sc = float(np.float32(0.35))
+    o, lse = orc.attn_fwd_ref(q, k, v, causal, sc)
+    dq, dk, dv = orc.attn_bwd_ref(q, k, v, do, causal, sc)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    mask = causal_lower_right(n_q, n_k) if causal else None
+    t_o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=sc, enable_gqa=True)
+    t_o.backward(torch.tensor(do))
+    np.testing.assert_allclose(o, t_o.detach().numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-10, atol=1e-11)
+    # lse: the log-sum-exp of torch's own masked scores
+    s = torch.einsum("zhqd,zhkd->zhqk", torch.tensor(q), torch.tensor(k).repeat_interleave(h // h_kv, dim=1)) * sc
+    if causal:
+        s = s.masked_fill(~causal_lower_right(n_q, n_k)._materialize(), float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_grouped_heads_subset_matches_full():
+    q, k, v, do = rand_gqa(2, 6, 2, 12, 20, 4, 54)
+    o, lse = orc.attn_fwd_ref(q, k, v, True, 0.4)
+    o_s, _ = orc.attn_fwd_ref(q, k, v, True, 0.4, heads=[7, 2])
+    np.testing.assert_array_equal(o_s[0], o.reshape(12, 12, 4)[7])
+    dq, dk, dv = orc.attn_bwd_ref(q, k, v, do, True, 0.4)
+    heads = [7, 2, 8]
+    assert orc.sampled_kv_heads(heads, 3) == [2, 0]
+    dq_s, dk_s, dv_s = orc.attn_bwd_ref(q, k, v, do, True, 0.4, heads=heads)
+    np.testing.assert_array_equal(dq_s[2], dq.reshape(12, 12, 4)[8])
+    np.testing.assert_array_equal(dk_s[0], dk.reshape(4, 20, 4)[2])
+    np.testing.assert_array_equal(dv_s[1], dv.reshape(4, 20, 4)[0])
+
+
+def test_pins_catch_planted_grouping_and_alignment_mistakes():
+    from torch.nn.attention.bias import causal_lower_right
+    q, k, v, do = rand_gqa(1, 4, 2, 3, 5, 4, 55)
+    sc = 0.5
+    # (a) query head h reading K/V head h % H_kv instead of h // g
+    o_good, _ = orc.attn_fwd_ref(q, k, v, False, sc)
+    o_bad = np.stack([orc.attn_fwd_head(q[0, hh], k[0, hh % 2], v[0, hh % 2], False, sc)[0] for hh in range(4)])
+    t_o = torch.nn.functional.scaled_dot_product_attention(
+        torch.tensor(q), torch.tensor(k), torch.tensor(v), scale=sc, enable_gqa=True).numpy()
+    assert np.allclose(o_good[0], t_o[0]) and not np.allclose(o_bad, t_o[0])
+    # (b) causal diagonal aligned to the first query instead of the last
+    s = (q[0, 0] @ k[0, 0].T) * sc
+    top_left = np.where(np.arange(5)[None, :] > np.arange(3)[:, None], -np.inf, s)
+    p_bad, _ = orc.softmax_probs(top_left)
+    t_o = torch.nn.functional.scaled_dot_product_attention(
+        torch.tensor(q[:, :1]), torch.tensor(k[:, :1]), torch.tensor(v[:, :1]), scale=sc,
+        attn_mask=causal_lower_right(3, 5)).numpy()[0, 0]
+    assert not np.allclose(p_bad @ v[0, 0], t_o)
+    np.testing.assert_allclose(orc.attn_fwd_head(q[0, 0], k[0, 0], v[0, 0], True, sc)[0], t_o, rtol=1e-12)
+    # (c) dK of a shared head taken from one query head only
+    dk_one = orc.attn_bwd_head(q[0, 0], k[0, 0], v[0, 0], do[0, 0], False, sc)[1]
+    assert not np.allclose(dk_one, orc.attn_bwd_ref(q, k, v, do, False, sc)[1][0, 0])
