@@ -23,6 +23,9 @@ FA_ERR_DEVICE = -5
 FA_ERR_TIMEOUT = -6
 FA_ERR_SCRATCH_LIMIT = -7
 
+FA_DTYPE_F16 = 0
+FA_DTYPE_BF16 = 1
+
 # Every symbol include/fa.h declares, with its ctypes signature.
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
@@ -31,6 +34,9 @@ SIGNATURES = {
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_bwd_bf16": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _f, _vp]),
+    "fa_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa_bwd_ex_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
+    "fa_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_device_status": (_i, [_vp]),
     "fa_device_status_raw": (_i, [_vp, ctypes.POINTER(ctypes.c_int)]),
@@ -39,6 +45,8 @@ SIGNATURES = {
     "fa_fwd_tile_count": (ctypes.c_longlong, [_i, _i, _i]),
     "fa_fwd_flops": (ctypes.c_double, [_i, _i, _i, _i, _i]),
     "fa_bwd_flops": (ctypes.c_double, [_i, _i, _i, _i, _i]),
+    "fa_fwd_ex_flops": (ctypes.c_double, [_i, _i, _i, _i, _i, _i]),
+    "fa_bwd_ex_flops": (ctypes.c_double, [_i, _i, _i, _i, _i, _i]),
 }
 
 _lib = None

@@ -23,7 +23,7 @@ def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
 _DTYPES = (torch.float16, torch.bfloat16)
 
 
-def _check_input(name: str, t: torch.Tensor, shape=None, dtype=None) -> None:
+def _check_input(name: str, t: torch.Tensor, dtype=None) -> None:
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
@@ -34,65 +34,88 @@ def _check_input(name: str, t: torch.Tensor, shape=None, dtype=None) -> None:
         raise ValueError(f"{name} is {t.dtype}, expected {dtype} like q")
     if t.dim() != 4 or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous [Z, H, N, D] tensor")
-    if shape is not None and tuple(t.shape) != tuple(shape):
-        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _shape(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    """(Z, H, Hkv, Nq, Nk, D) of q [Z,H,Nq,D] and k, v [Z,Hkv,Nk,D]."""
+    _check_input("q", q)
+    _check_input("k", k, q.dtype)
+    _check_input("v", v, q.dtype)
+    Z, H, Nq, D = q.shape
+    Zk, Hkv, Nk, Dk = k.shape
+    if Zk != Z or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"k {tuple(k.shape)} and v {tuple(v.shape)} must be [Z, Hkv, Nk, D] with q's Z and D")
+    if H % Hkv != 0:
+        raise ValueError(f"q's {H} heads are not a multiple of k's {Hkv} heads")
+    return Z, H, Hkv, Nq, Nk, D
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    return _native.FA_DTYPE_BF16 if t.dtype == torch.bfloat16 else _native.FA_DTYPE_F16
 
 
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         scale: Optional[float] = None, out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
         stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Exact attention forward.  Returns ``(o, lse)``: o [Z,H,N,D] in q's dtype
-    (float16 or bfloat16), lse fp32 [Z,H,N] (natural-log log-sum-exp of each
-    row of scale*Q K^T)."""
-    _check_input("q", q)
-    Z, H, N, D = q.shape
-    _check_input("k", k, q.shape, q.dtype)
-    _check_input("v", v, q.shape, q.dtype)
+    """Exact attention forward.  q [Z,H,Nq,D], k and v [Z,Hkv,Nk,D] (H a
+    multiple of Hkv; query head h reads K/V head h // (H // Hkv)), all
+    float16 or all bfloat16.  Returns ``(o, lse)``: o like q, lse fp32
+    [Z,H,Nq] (natural-log log-sum-exp of each row of scale*Q K^T).  Causal:
+    query i sees key j iff j <= i + Nk - Nq (needs Nq <= Nk)."""
+    Z, H, Hkv, Nq, Nk, D = _shape(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         o = torch.empty_like(q)
-        lse = torch.empty((Z, H, N), dtype=torch.float32, device=q.device)
+        lse = torch.empty((Z, H, Nq), dtype=torch.float32, device=q.device)
     else:
         o, lse = out
-    fn = "fa_fwd_bf16" if q.dtype == torch.bfloat16 else "fa_fwd"
-    rc = getattr(_native.lib(), fn)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                    Z, H, N, D, int(bool(causal)), float(scale), _stream_handle(stream))
-    _native.check(rc, fn)
+        _check_input("o", o, q.dtype)
+        if tuple(o.shape) != tuple(q.shape) or lse.dtype != torch.float32 or tuple(lse.shape) != (Z, H, Nq):
+            raise ValueError("out must be (o like q, float32 lse [Z, H, Nq])")
+    rc = _native.lib().fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                 Z, H, Hkv, Nq, Nk, D, int(bool(causal)), float(scale), _dtype_code(q),
+                                 _stream_handle(stream))
+    _native.check(rc, "fa_fwd_ex")
     return o, lse
 
 
-def bwd_workspace_size(Z: int, H: int, N: int, D: int, causal: bool) -> int:
-    return int(_native.lib().fa_bwd_workspace_size(Z, H, N, D, int(bool(causal))))
+def bwd_workspace_size(Z: int, H: int, N: int, D: int, causal: bool, Hkv: Optional[int] = None,
+                       Nk: Optional[int] = None) -> int:
+    """Workspace bytes of a backward call; N is the query length."""
+    Hkv = H if Hkv is None else Hkv
+    Nk = N if Nk is None else Nk
+    return int(_native.lib().fa_bwd_ex_workspace_size(Z, H, Hkv, N, Nk, D, int(bool(causal))))
 
 
 def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, do: torch.Tensor,
         lse: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
         workspace: Optional[torch.Tensor] = None, out=None,
         stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """Exact attention backward.  Returns ``(dq, dk, dv)`` [Z,H,N,D] in q's
-    dtype (float16 or bfloat16)."""
-    _check_input("q", q)
-    Z, H, N, D = q.shape
-    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
-        _check_input(name, t, q.shape, q.dtype)
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (Z, H, N) or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous float32 [Z, H, N] tensor")
+    """Exact attention backward.  Shapes as for :func:`fwd`; o and do like q.
+    Returns ``(dq, dk, dv)`` shaped like q, k, v; dk and dv of a shared K/V
+    head sum over the query heads that read it."""
+    Z, H, Hkv, Nq, Nk, D = _shape(q, k, v)
+    for name, t in (("o", o), ("do", do)):
+        _check_input(name, t, q.dtype)
+        if tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(q.shape)}")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (Z, H, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [Z, H, Nq] tensor")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    need = bwd_workspace_size(Z, H, N, D, causal)
+    need = bwd_workspace_size(Z, H, Nq, D, causal, Hkv, Nk)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     if out is None:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     else:
         dq, dk, dv = out
-    fn = "fa_bwd_bf16" if q.dtype == torch.bfloat16 else "fa_bwd"
-    rc = getattr(_native.lib(), fn)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                                    workspace.data_ptr(), workspace.numel(), Z, H, N, D, int(bool(causal)),
-                                    float(scale), _stream_handle(stream))
-    _native.check(rc, fn)
+    rc = _native.lib().fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                                 lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                 workspace.data_ptr(), workspace.numel(), Z, H, Hkv, Nq, Nk, D,
+                                 int(bool(causal)), float(scale), _dtype_code(q), _stream_handle(stream))
+    _native.check(rc, "fa_bwd_ex")
     return dq, dk, dv
 
 
@@ -104,9 +127,11 @@ def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
     return rc if rc != _native.FA_OK else 0
 
 
-def fwd_flops(Z, H, N, D, causal) -> float:
-    return float(_native.lib().fa_fwd_flops(Z, H, N, D, int(bool(causal))))
+def fwd_flops(Z, H, N, D, causal, Nk=None) -> float:
+    Nk = N if Nk is None else Nk
+    return float(_native.lib().fa_fwd_ex_flops(Z, H, N, Nk, D, int(bool(causal))))
 
 
-def bwd_flops(Z, H, N, D, causal) -> float:
-    return float(_native.lib().fa_bwd_flops(Z, H, N, D, int(bool(causal))))
+def bwd_flops(Z, H, N, D, causal, Nk=None) -> float:
+    Nk = N if Nk is None else Nk
+    return float(_native.lib().fa_bwd_ex_flops(Z, H, N, Nk, D, int(bool(causal))))

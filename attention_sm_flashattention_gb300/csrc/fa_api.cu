@@ -68,25 +68,39 @@ int current_device_info(DevInfo** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Problem shape of one call: queries [Z, H, Nq, D], keys/values [Z, Hkv, Nk, D].
+struct Shape {
+  int Z, H, Hkv, Nq, Nk, D;
+  int causal;
+  long long q_heads() const { return static_cast<long long>(Z) * H; }
+  long long kv_heads() const { return static_cast<long long>(Z) * Hkv; }
+  int group() const { return H / Hkv; }
+  int nq_pad() const { return (Nq + 127) / 128 * 128; }
+};
+
 // Shared checks of the shape arguments.
-int check_shape(int Z, int H, int N, int D, int causal, float scale) {
-  if (Z <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+int check_shape(const Shape& sh, float scale) {
+  if (sh.Z <= 0 || sh.H <= 0 || sh.Hkv <= 0 || sh.Nq <= 0 || sh.Nk <= 0) return FA_ERR_INVALID_ARG;
+  if (sh.H % sh.Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (sh.causal != 0 && sh.causal != 1) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
-  if (N % 128 != 0) return FA_ERR_UNSUPPORTED;
-  const long long rows = static_cast<long long>(Z) * H * N;
-  if (rows >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
+  if (sh.D != 64 && sh.D != 128 && sh.D != 256) return FA_ERR_UNSUPPORTED;
+  // causal with more queries than keys leaves rows with no visible key
+  if (sh.causal && sh.Nq > sh.Nk) return FA_ERR_UNSUPPORTED;
+  // 32-bit row and element-offset arithmetic inside the kernels
+  if (sh.q_heads() * sh.nq_pad() >= (1LL << 31) || sh.kv_heads() * sh.Nk >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
-// A [rows x D] tensor of 16-bit elements (fp16, or bf16 when `bf16`).
-bool map16(CUtensorMap* m, const void* base, long long rows, int D, int box_rows, bool bf16) {
+Shape square(int Z, int H, int N, int D, int causal) { return Shape{Z, H, H, N, N, D, causal}; }
+
+// `mats` matrices [rows x D] of 16-bit elements (fp16, or bf16 when
+// `bf16`), one after the other; boxes of 64 columns x box_rows rows.
+bool map16(CUtensorMap* m, const void* base, long long mats, int rows, int D, int box_rows, bool bf16) {
   std::memset(m, 0, sizeof(*m));
-  return fa::make_tmap_2d(m, base, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                          static_cast<uint64_t>(rows),
-                          static_cast<uint64_t>(D), static_cast<uint64_t>(D), 64, static_cast<uint32_t>(box_rows),
-                          true);
+  return fa::make_tmap_3d(m, base, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                          static_cast<uint64_t>(mats), static_cast<uint64_t>(rows), static_cast<uint64_t>(D), 64,
+                          static_cast<uint32_t>(box_rows), true);
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -99,24 +113,29 @@ struct BwdWorkspace {
   int grid;
 };
 
-// D <= 128 needs only Delta and lse2 (the dQ kernel owns its tiles); D = 256
-// also needs one fp32 N x D dQ accumulator per persistent CTA.
-BwdWorkspace bwd_workspace_layout(int Z, int H, int N, int D, int sms) {
+// Delta and lse2 are [Z*H, Nq_pad] (query rows padded to whole 128-row
+// tiles).  D <= 128 needs nothing else (the dQ kernel owns its tiles); D =
+// 256 also needs one fp32 N x D dQ accumulator per persistent CTA.
+BwdWorkspace bwd_workspace_layout(const Shape& sh, int sms) {
   BwdWorkspace w{};
-  const long long heads = static_cast<long long>(Z) * H;
-  const size_t vec = round_up(static_cast<size_t>(heads) * N * sizeof(float), 256);
+  const long long heads = sh.q_heads();
+  const size_t vec = round_up(static_cast<size_t>(heads) * sh.nq_pad() * sizeof(float), 256);
   w.delta_off = 0;
   w.lse2_off = vec;
   w.dq_off = 2 * vec;
-  if (D == 256) {
+  if (sh.D == 256) {
     w.grid = static_cast<int>(heads < sms ? heads : sms);
-    w.total = 2 * vec + round_up(static_cast<size_t>(w.grid) * N * D * sizeof(float), 256);
+    w.total = 2 * vec + round_up(static_cast<size_t>(w.grid) * sh.Nq * sh.D * sizeof(float), 256);
   } else {
     w.grid = sms;
     w.total = 2 * vec;
   }
   return w;
 }
+
+// The D = 256 backward kernel covers equal lengths that are a multiple of
+// 128 and one K/V head per query head.
+bool d256_bwd_supported(const Shape& sh) { return sh.group() == 1 && sh.Nq == sh.Nk && sh.Nq % 128 == 0; }
 
 }  // namespace
 
@@ -126,7 +145,8 @@ const char* fa_error_string(int code) {
   switch (code) {
     case FA_OK: return "ok";
     case FA_ERR_INVALID_ARG: return "invalid argument (null/misaligned pointer, non-positive size, bad scale or causal flag)";
-    case FA_ERR_UNSUPPORTED: return "unsupported shape (D must be 64, 128 or 256; N a multiple of 128; Z*H*N < 2^31)";
+    case FA_ERR_UNSUPPORTED: return "unsupported shape (D must be 64, 128 or 256; causal needs Nq <= Nk; Z*H*N < 2^31; "
+                                   "the D = 256 backward needs Nq == Nk, a multiple of 128, and Hkv == H)";
     case FA_ERR_WORKSPACE: return "workspace missing or smaller than fa_bwd_workspace_size()";
     case FA_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
     case FA_ERR_DEVICE: return "current device is not a compute capability 10.3 (sm_103a) GPU";
@@ -137,50 +157,64 @@ const char* fa_error_string(int code) {
 }
 
 long long fa_fwd_tile_count(int N, int D, int causal) {
-  if (N <= 0 || N % 128 != 0 || (D != 64 && D != 128 && D != 256) || (causal != 0 && causal != 1)) return -1;
-  const int bm = 128, bn = fa::fwd_block_n(D);
-  const long long nqt = N / bm, nkv = N / bn;
+  if (N <= 0 || (D != 64 && D != 128 && D != 256) || (causal != 0 && causal != 1)) return -1;
+  const long long bm = 128, bn = fa::fwd_block_n(D);
+  const long long nqt = (N + bm - 1) / bm, nkv = (N + bn - 1) / bn;
   if (!causal) return nqt * nkv;
   long long n = 0;
-  for (long long qt = 0; qt < nqt; ++qt) n += ((qt + 1) * bm) / bn;
+  for (long long qt = 0; qt < nqt; ++qt) {
+    const long long end = (qt + 1) * bm < N ? (qt + 1) * bm : N;  // one past the tile's last visible key
+    n += (end + bn - 1) / bn;
+  }
   return n;
 }
 
-double fa_fwd_flops(int Z, int H, int N, int D, int causal) {
-  const double heads = static_cast<double>(Z) * H, n = N, d = D;
-  return heads * (causal ? 2.0 * n * (n + 1.0) * d : 4.0 * n * n * d);
+double fa_fwd_ex_flops(int Z, int H, int Nq, int Nk, int D, int causal) {
+  const double heads = static_cast<double>(Z) * H, nq = Nq, d = D;
+  // (query, key) pairs that take part: all, or query i sees i + Nk - Nq + 1 keys
+  const double pairs = causal ? nq * (nq + 1.0) / 2.0 + nq * (static_cast<double>(Nk) - Nq) : nq * Nk;
+  return heads * 4.0 * pairs * d;
 }
 
+double fa_fwd_flops(int Z, int H, int N, int D, int causal) { return fa_fwd_ex_flops(Z, H, N, N, D, causal); }
+
 double fa_bwd_flops(int Z, int H, int N, int D, int causal) { return 2.5 * fa_fwd_flops(Z, H, N, D, causal); }
+
+double fa_bwd_ex_flops(int Z, int H, int Nq, int Nk, int D, int causal) {
+  return 2.5 * fa_fwd_ex_flops(Z, H, Nq, Nk, D, causal);
+}
 
 }  // extern "C"
 
 namespace {
 
-int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int N, int D,
-             int causal, float scale, cudaStream_t stream, bool bf16) {
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const Shape& sh, float scale,
+             cudaStream_t stream, bool bf16) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return FA_ERR_INVALID_ARG;
-  int rc = check_shape(Z, H, N, D, causal, scale);
+  int rc = check_shape(sh, scale);
   if (rc != FA_OK) return rc;
   DevInfo* dev = nullptr;
   if ((rc = current_device_info(&dev)) != FA_OK) return rc;
 
-  const long long rows = static_cast<long long>(Z) * H * N;
+  const int D = sh.D;
   const int bn = fa::fwd_block_n(D);
   CUtensorMap maps[4];  // q, k, v, o
-  if (!map16(&maps[0], q, rows, D, 128, bf16) || !map16(&maps[1], k, rows, D, bn, bf16) ||
-      !map16(&maps[2], v, rows, D, bn, bf16) || !map16(&maps[3], o, rows, D, 128, bf16))
+  if (!map16(&maps[0], q, sh.q_heads(), sh.Nq, D, 128, bf16) || !map16(&maps[1], k, sh.kv_heads(), sh.Nk, D, bn, bf16) ||
+      !map16(&maps[2], v, sh.kv_heads(), sh.Nk, D, bn, bf16) || !map16(&maps[3], o, sh.q_heads(), sh.Nq, D, 128, bf16))
     return FA_ERR_CUDA;
   fa::FwdParams prm{};
   prm.o = static_cast<__half*>(o);
   prm.lse = lse;
-  prm.heads = Z * H;
-  prm.N = N;
+  prm.heads = static_cast<int>(sh.q_heads());
+  prm.group = sh.group();
+  prm.Nq = sh.Nq;
+  prm.Nk = sh.Nk;
+  prm.causal_off = sh.Nk - sh.Nq;
   prm.scale_log2 = scale * kLog2e;
   prm.status = dev->status;
-  const bool c = causal != 0;
+  const bool c = sh.causal != 0;
   switch (D) {
     case 64: rc = fa::launch_fwd_d64(c, bf16, maps, prm, dev->sms, stream); break;
     case 128: rc = fa::launch_fwd_d128(c, bf16, maps, prm, dev->sms, stream); break;
@@ -195,49 +229,86 @@ extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int N, int D,
            int causal, float scale, cudaStream_t stream) {
-  return fwd_impl(q, k, v, o, lse, Z, H, N, D, causal, scale, stream, false);
+  return fwd_impl(q, k, v, o, lse, square(Z, H, N, D, causal), scale, stream, false);
 }
 
 int fa_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int N, int D,
                 int causal, float scale, cudaStream_t stream) {
-  return fwd_impl(q, k, v, o, lse, Z, H, N, D, causal, scale, stream, true);
+  return fwd_impl(q, k, v, o, lse, square(Z, H, N, D, causal), scale, stream, true);
+}
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int Hkv, int Nq,
+              int Nk, int D, int causal, float scale, int dtype, cudaStream_t stream) {
+  if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, Shape{Z, H, Hkv, Nq, Nk, D, causal}, scale, stream, dtype == FA_DTYPE_BF16);
+}
+
+size_t fa_bwd_ex_workspace_size(int Z, int H, int Hkv, int Nq, int Nk, int D, int causal) {
+  const Shape sh{Z, H, Hkv, Nq, Nk, D, causal};
+  if (check_shape(sh, 1.f) != FA_OK) return 0;
+  if (D == 256 && !d256_bwd_supported(sh)) return 0;
+  DevInfo* dev = nullptr;
+  if (current_device_info(&dev) != FA_OK) return 0;
+  return bwd_workspace_layout(sh, dev->sms).total;
 }
 
 size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal) {
-  if (check_shape(Z, H, N, D, causal, 1.f) != FA_OK) return 0;
-  DevInfo* dev = nullptr;
-  if (current_device_info(&dev) != FA_OK) return 0;
-  return bwd_workspace_layout(Z, H, N, D, dev->sms).total;
+  return fa_bwd_ex_workspace_size(Z, H, H, N, N, D, causal);
 }
 
 }  // extern "C"
 
 namespace {
 
-int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int Z, int H, int N, int D,
-             int causal, float scale, cudaStream_t stream, bool bf16) {
+// Argument checks shared by every backward entry point.
+int bwd_checks(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+               const void* dq, const void* dk, const void* dv, const Shape& sh, float scale) {
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
     return FA_ERR_INVALID_ARG;
-  int rc = check_shape(Z, H, N, D, causal, scale);
+  const int rc = check_shape(sh, scale);
+  if (rc != FA_OK) return rc;
+  if (sh.D == 256 && !d256_bwd_supported(sh)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+// Tensor maps of a backward call: q, k, v, dout (box rows chosen by the
+// kernels' tiling), then the outputs dq, dk, dv (TMA stores of the D <= 128
+// kernels).
+bool bwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
+              void* dv, const Shape& sh, bool bf16) {
+  const int D = sh.D, bq = (D == 256) ? 64 : 128;
+  const long long hq = sh.q_heads(), hk = sh.kv_heads();
+  return map16(&maps[0], q, hq, sh.Nq, D, bq, bf16) && map16(&maps[1], k, hk, sh.Nk, D, 128, bf16) &&
+         map16(&maps[2], v, hk, sh.Nk, D, 128, bf16) && map16(&maps[3], dout, hq, sh.Nq, D, bq, bf16) &&
+         map16(&maps[4], dq, hq, sh.Nq, D, 128, bf16) && map16(&maps[5], dk, hk, sh.Nk, D, 128, bf16) &&
+         map16(&maps[6], dv, hk, sh.Nk, D, 128, bf16);
+}
+
+void bwd_shape_params(fa::BwdParams& prm, const Shape& sh) {
+  prm.heads = static_cast<int>(sh.q_heads());
+  prm.group = sh.group();
+  prm.Nq = sh.Nq;
+  prm.Nk = sh.Nk;
+  prm.Nq_pad = sh.nq_pad();
+  prm.causal_off = sh.Nk - sh.Nq;
+  prm.N = sh.Nq;
+}
+
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, const Shape& sh, float scale,
+             cudaStream_t stream, bool bf16) {
+  int rc = bwd_checks(q, k, v, o, dout, lse, dq, dk, dv, sh, scale);
   if (rc != FA_OK) return rc;
   DevInfo* dev = nullptr;
   if ((rc = current_device_info(&dev)) != FA_OK) return rc;
-  const BwdWorkspace ws = bwd_workspace_layout(Z, H, N, D, dev->sms);
+  const BwdWorkspace ws = bwd_workspace_layout(sh, dev->sms);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < ws.total) return FA_ERR_WORKSPACE;
 
-  const long long rows = static_cast<long long>(Z) * H * N;
-  // maps: q, k, v, dout (fp16, box rows chosen by the kernel's tiling), then
-  // the outputs dq, dk, dv (written with TMA stores by the D <= 128 kernels)
+  const int D = sh.D;
   CUtensorMap maps[7];
-  const int bq = (D == 256) ? 64 : 128;
-  if (!map16(&maps[0], q, rows, D, bq, bf16) || !map16(&maps[1], k, rows, D, 128, bf16) ||
-      !map16(&maps[2], v, rows, D, 128, bf16) || !map16(&maps[3], dout, rows, D, bq, bf16) ||
-      !map16(&maps[4], dq, rows, D, 128, bf16) || !map16(&maps[5], dk, rows, D, 128, bf16) ||
-      !map16(&maps[6], dv, rows, D, 128, bf16))
-    return FA_ERR_CUDA;
+  if (!bwd_maps(maps, q, k, v, dout, dq, dk, dv, sh, bf16)) return FA_ERR_CUDA;
   char* wsb = static_cast<char*>(workspace);
   fa::BwdParams prm{};
   prm.o = static_cast<const __half*>(o);
@@ -249,12 +320,11 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   prm.delta = reinterpret_cast<float*>(wsb + ws.delta_off);
   prm.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
   prm.dq_acc = reinterpret_cast<float*>(wsb + ws.dq_off);
-  prm.heads = Z * H;
-  prm.N = N;
+  bwd_shape_params(prm, sh);
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
   prm.status = dev->status;
-  const bool c = causal != 0;
+  const bool c = sh.causal != 0;
   switch (D) {
     case 64: rc = fa::launch_bwd_d64(c, bf16, maps, prm, ws.grid, stream); break;
     case 128: rc = fa::launch_bwd_d128(c, bf16, maps, prm, ws.grid, stream); break;
@@ -270,15 +340,23 @@ extern "C" {
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
            void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int Z, int H, int N, int D,
            int causal, float scale, cudaStream_t stream) {
-  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, Z, H, N, D, causal, scale, stream,
-                  false);
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, square(Z, H, N, D, causal), scale,
+                  stream, false);
 }
 
 int fa_bwd_bf16(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int Z, int H, int N, int D,
                 int causal, float scale, cudaStream_t stream) {
-  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, Z, H, N, D, causal, scale, stream,
-                  true);
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, square(Z, H, N, D, causal), scale,
+                  stream, true);
+}
+
+int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+              void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int Z, int H, int Hkv, int Nq,
+              int Nk, int D, int causal, float scale, int dtype, cudaStream_t stream) {
+  if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, Shape{Z, H, Hkv, Nq, Nk, D, causal},
+                  scale, stream, dtype == FA_DTYPE_BF16);
 }
 
 int fa_device_status_raw(cudaStream_t stream, int* raw) {
@@ -329,19 +407,16 @@ void* noalloc_scratch_on_current_device() {
 extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                               const float* lse, void* dq, void* dk, void* dv, int Z, int H, int N, int D,
                               int causal, float scale, cudaStream_t stream) {
-  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
-      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
-    return FA_ERR_INVALID_ARG;
-  int rc = check_shape(Z, H, N, D, causal, scale);
+  const Shape sh = square(Z, H, N, D, causal);
+  int rc = bwd_checks(q, k, v, o, dout, lse, dq, dk, dv, sh, scale);
   if (rc != FA_OK) return rc;
   DevInfo* dev = nullptr;
   if ((rc = current_device_info(&dev)) != FA_OK) return rc;
 
   // Scratch layout [delta | lse2 | dQ accumulators], as fa_bwd's workspace;
   // for D = 256 the grid is cut to the accumulators that fit.
-  const long long heads = static_cast<long long>(Z) * H;
-  const size_t vec = round_up(static_cast<size_t>(heads) * N * sizeof(float), 256);
+  const long long heads = sh.q_heads();
+  const size_t vec = round_up(static_cast<size_t>(heads) * sh.nq_pad() * sizeof(float), 256);
   long long grid = dev->sms;
   if (D == 256) {
     const size_t acc_one = round_up(static_cast<size_t>(N) * D * sizeof(float), 256);
@@ -356,14 +431,8 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   char* scratch = static_cast<char*>(noalloc_scratch_on_current_device());
   if (scratch == nullptr) return FA_ERR_CUDA;
 
-  const long long rows = heads * N;
   CUtensorMap maps[7];
-  const int bq = (D == 256) ? 64 : 128;
-  if (!map16(&maps[0], q, rows, D, bq, false) || !map16(&maps[1], k, rows, D, 128, false) ||
-      !map16(&maps[2], v, rows, D, 128, false) || !map16(&maps[3], dout, rows, D, bq, false) ||
-      !map16(&maps[4], dq, rows, D, 128, false) || !map16(&maps[5], dk, rows, D, 128, false) ||
-      !map16(&maps[6], dv, rows, D, 128, false))
-    return FA_ERR_CUDA;
+  if (!bwd_maps(maps, q, k, v, dout, dq, dk, dv, sh, false)) return FA_ERR_CUDA;
   fa::BwdParams prm{};
   prm.o = static_cast<const __half*>(o);
   prm.dout = static_cast<const __half*>(dout);
@@ -374,8 +443,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   prm.delta = reinterpret_cast<float*>(scratch);
   prm.lse2 = reinterpret_cast<float*>(scratch + vec);
   prm.dq_acc = reinterpret_cast<float*>(scratch + 2 * vec);
-  prm.heads = Z * H;
-  prm.N = N;
+  bwd_shape_params(prm, sh);
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
   prm.status = dev->status;

@@ -45,25 +45,32 @@ namespace fa {
 
 // -------------------------------------------------------------- preprocess
 
+// Rows are those of the padded [heads, Nq_pad] workspace vectors: a query
+// row past Nq (the rest of a ragged last tile) gets Delta = 0 and lse2 =
+// +inf, so its recomputed P is exactly 0 and it adds nothing to dK or dV.
 template <int D, bool BF>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __half* __restrict__ o,
                                                           const __half* __restrict__ dout,
                                                           const float* __restrict__ lse, float* __restrict__ delta,
-                                                          float* __restrict__ lse2, int rows) {
+                                                          float* __restrict__ lse2, int heads, int Nq, int Nq_pad) {
   constexpr int TPR = D / 8;  // threads per row, 8 fp16 (16 bytes) each
   constexpr int RPB = 256 / TPR;
-  const int r = blockIdx.x * RPB + threadIdx.x / TPR;
+  const int r = blockIdx.x * RPB + threadIdx.x / TPR;  // padded row
   const int part = threadIdx.x % TPR;
+  const int rows = heads * Nq_pad;
+  const int head = r / Nq_pad, i = r - head * Nq_pad;
+  const bool live = r < rows && i < Nq;
+  const size_t src = static_cast<size_t>(head) * Nq + i;  // row of O, dO and lse
   float acc = 0.f;
-  if (r < rows) {
-    const uint4 a = reinterpret_cast<const uint4*>(o + static_cast<size_t>(r) * D)[part];
-    const uint4 b = reinterpret_cast<const uint4*>(dout + static_cast<size_t>(r) * D)[part];
+  if (live) {
+    const uint4 a = reinterpret_cast<const uint4*>(o + src * D)[part];
+    const uint4 b = reinterpret_cast<const uint4*>(dout + src * D)[part];
     const uint32_t* ha = reinterpret_cast<const uint32_t*>(&a);
     const uint32_t* hb = reinterpret_cast<const uint32_t*>(&b);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 fa2 = unpack2<BF>(ha[i]);
-      const float2 fb2 = unpack2<BF>(hb[i]);
+    for (int e = 0; e < 4; ++e) {
+      const float2 fa2 = unpack2<BF>(ha[e]);
+      const float2 fb2 = unpack2<BF>(hb[e]);
       acc = fmaf(fa2.x, fb2.x, acc);
       acc = fmaf(fa2.y, fb2.y, acc);
     }
@@ -72,8 +79,17 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __half* __restri
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (r < rows && part == 0) {
     delta[r] = acc;
-    lse2[r] = lse[r] * 1.4426950408889634f;
+    lse2[r] = live ? lse[src] * 1.4426950408889634f : INFINITY;
   }
+}
+
+template <int D, bool BF>
+int launch_prep(const BwdParams& prm, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(prm.heads) * prm.Nq_pad;
+  constexpr int RPB = 256 / (D / 8);
+  fa_bwd_prep_kernel<D, BF><<<static_cast<unsigned>((rows + RPB - 1) / RPB), 256, 0, stream>>>(
+      prm.o, prm.dout, prm.lse, prm.delta, prm.lse2, prm.heads, prm.Nq, prm.Nq_pad);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 // -------------------------------------------------------------- main kernel
@@ -217,10 +233,9 @@ __global__ void __launch_bounds__(320, 1)
         for (int j = 0; ok && j < nkv; ++j) {
           if (!(ok = mbar_wait(&bars->kv_empty, (kc & 1) ^ 1, wc, 21))) break;
           mbar_arrive_expect_tx(&bars->kv_full, 2 * T::KV_BYTES);
-          const int krow = head * N + j * T::BN;
           for (int s = 0; s < T::DSUB; ++s) {
-            tma_load_2d_hint(smem + T::SM_K + s * T::KV_SUB, &tm_k, &bars->kv_full, s * 64, krow, pol);
-            tma_load_2d_hint(smem + T::SM_V + s * T::KV_SUB, &tm_v, &bars->kv_full, s * 64, krow, pol);
+            tma_load_3d_hint(smem + T::SM_K + s * T::KV_SUB, &tm_k, &bars->kv_full, s * 64, j * T::BN, head, pol);
+            tma_load_3d_hint(smem + T::SM_V + s * T::KV_SUB, &tm_v, &bars->kv_full, s * 64, j * T::BN, head, pol);
           }
           ++kc;
           for (int h = 0; ok && h < T::NPASS; ++h) {
@@ -228,12 +243,11 @@ __global__ void __launch_bounds__(320, 1)
               const int st = t % T::Q_STAGES;
               if (!(ok = mbar_wait(&bars->q_empty[st], ((t / T::Q_STAGES) & 1) ^ 1, wc, 22))) break;
               mbar_arrive_expect_tx(&bars->q_full[st], 2 * T::Q_BYTES);
-              const int qrow = head * N + i * T::BM;
               for (int s = 0; s < T::DSUB; ++s) {
-                tma_load_2d_hint(smem + T::SM_Q + st * T::Q_BYTES + s * T::Q_SUB, &tm_q, &bars->q_full[st], s * 64,
-                                 qrow, pol);
-                tma_load_2d_hint(smem + T::SM_DO + st * T::Q_BYTES + s * T::Q_SUB, &tm_do, &bars->q_full[st],
-                                 s * 64, qrow, pol);
+                tma_load_3d_hint(smem + T::SM_Q + st * T::Q_BYTES + s * T::Q_SUB, &tm_q, &bars->q_full[st], s * 64,
+                                 i * T::BM, head, pol);
+                tma_load_3d_hint(smem + T::SM_DO + st * T::Q_BYTES + s * T::Q_SUB, &tm_do, &bars->q_full[st],
+                                 s * 64, i * T::BM, head, pol);
               }
               ++t;
             }
@@ -544,11 +558,7 @@ int launch_bwd(const CUtensorMap* maps, const BwdParams& prm, int grid, cudaStre
       return -1;
     attr_set = true;
   }
-  const int rows = prm.heads * prm.N;
-  constexpr int RPB = 256 / (D / 8);
-  fa_bwd_prep_kernel<D, BF><<<(rows + RPB - 1) / RPB, 256, 0, stream>>>(prm.o, prm.dout, prm.lse, prm.delta, prm.lse2,
-                                                                     rows);
-  if (cudaGetLastError() != cudaSuccess) return -1;
+  if (launch_prep<D, BF>(prm, stream) != 0) return -1;
   fa_bwd_kernel<D, CAUSAL, BF><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

@@ -220,9 +220,14 @@ __global__ void __launch_bounds__(384, 1)
 
   const WaitCtx wc{prm.status, &bars->abort_flag};
   const uint32_t tmem = bars->tmem_base;
-  const int N = prm.N;
-  const int nqt = N / T::BM, nkv = N / T::BN;
-  const int units = bwd2_units<CAUSAL>(prm.heads, nkv);
+  // Unit = (K/V head, key tile j).  It sweeps the query tiles of each of the
+  // G query heads that read this K/V head (one writer for dK_j and dV_j,
+  // which sum over the group), from the first query tile that sees key
+  // j * BN (causal) to the last.
+  const int G = prm.group, coff = prm.causal_off, Nq_pad = prm.Nq_pad;
+  const int nqt = (prm.Nq + T::BM - 1) / T::BM, nkv = (prm.Nk + T::BN - 1) / T::BN;
+  const int units = bwd2_units<CAUSAL>(prm.heads / G, nkv);
+  auto first_q = [&](int j) { return CAUSAL ? max(0, j * T::BN - coff) / T::BM : 0; };
 
   if (warp == PRODUCER_WARP) {
     // --------------------------------------------------------------- producer
@@ -232,32 +237,35 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t t = 0, kc = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        int head, ja, jb;
-        bwd2_decode<CAUSAL>(u, nkv, head, ja, jb);
+        int kvh, ja, jb;
+        bwd2_decode<CAUSAL>(u, nkv, kvh, ja, jb);
         for (int half = 0; ok && half < 2; ++half) {
           const int j = half ? jb : ja;
           if (j < 0) break;
           if (!(ok = mbar_wait(&bars->kv_empty, (kc & 1) ^ 1, wc, 51))) break;
           mbar_arrive_expect_tx(&bars->kv_full, 2 * T::TILE);
           for (int s = 0; s < T::DSUB; ++s) {
-            tma_load_2d_hint(smem + T::A_SM_K + s * T::SUB, &tm_k, &bars->kv_full, s * 64, head * N + j * T::BN, pol_kv);
-            tma_load_2d_hint(smem + T::A_SM_V + s * T::SUB, &tm_v, &bars->kv_full, s * 64, head * N + j * T::BN, pol_kv);
+            tma_load_3d_hint(smem + T::A_SM_K + s * T::SUB, &tm_k, &bars->kv_full, s * 64, j * T::BN, kvh, pol_kv);
+            tma_load_3d_hint(smem + T::A_SM_V + s * T::SUB, &tm_v, &bars->kv_full, s * 64, j * T::BN, kvh, pol_kv);
           }
           ++kc;
-          for (int i = CAUSAL ? j : 0; i < nqt; ++i) {
-            const int row = head * N + i * T::BM;
+          const int i0 = first_q(j), nqi = nqt - i0;
+          for (int x = 0; x < G * nqi; ++x) {
+            const int qh = kvh * G + x / nqi, i = i0 + x % nqi;
+            const size_t vrow = static_cast<size_t>(qh) * Nq_pad + i * T::BM;  // lse2 / Delta row
             const int qs = t % QS, os = t % OS;
             if (!(ok = mbar_wait(&bars->q_empty[qs], ((t / QS) & 1) ^ 1, wc, 52))) break;
             mbar_arrive_expect_tx(&bars->q_full[qs], T::TILE + 512);
             for (int s = 0; s < T::DSUB; ++s)
-              tma_load_2d_hint(smem + T::A_SM_Q + qs * T::TILE + s * T::SUB, &tm_q, &bars->q_full[qs], s * 64, row, pol_q);
-            bulk_load(smem + T::A_SM_L2 + qs * 512, prm.lse2 + row, 512, &bars->q_full[qs]);
+              tma_load_3d_hint(smem + T::A_SM_Q + qs * T::TILE + s * T::SUB, &tm_q, &bars->q_full[qs], s * 64,
+                               i * T::BM, qh, pol_q);
+            bulk_load(smem + T::A_SM_L2 + qs * 512, prm.lse2 + vrow, 512, &bars->q_full[qs]);
             if (!(ok = mbar_wait(&bars->o_empty[os], ((t / OS) & 1) ^ 1, wc, 53))) break;
             mbar_arrive_expect_tx(&bars->o_full[os], T::TILE + 512);
             for (int s = 0; s < T::DSUB; ++s)
-              tma_load_2d_hint(smem + T::A_SM_DO + os * T::TILE + s * T::SUB, &tm_do, &bars->o_full[os], s * 64, row,
-                               pol_q);
-            bulk_load(smem + T::A_SM_DL + os * 512, prm.delta + row, 512, &bars->o_full[os]);
+              tma_load_3d_hint(smem + T::A_SM_DO + os * T::TILE + s * T::SUB, &tm_do, &bars->o_full[os], s * 64,
+                               i * T::BM, qh, pol_q);
+            bulk_load(smem + T::A_SM_DL + os * 512, prm.delta + vrow, 512, &bars->o_full[os]);
             // warm L2 with the tiles that will refill these slots, so their
             // loads are short once the slots free up
             ++t;
@@ -293,16 +301,17 @@ __global__ void __launch_bounds__(384, 1)
       return true;
     };
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      int head, ja, jb;
-      bwd2_decode<CAUSAL>(u, nkv, head, ja, jb);
+      int kvh, ja, jb;
+      bwd2_decode<CAUSAL>(u, nkv, kvh, ja, jb);
       for (int half = 0; ok && half < 2; ++half) {
         const int j = half ? jb : ja;
         if (j < 0) break;
         if (!(ok = warp_wait(&bars->kv_full, kc & 1, wc, 61))) break;
         tc_fence_after();
         if (!(ok = issue_s(t))) break;
-        for (int i = CAUSAL ? j : 0; i < nqt; ++i) {
-          const bool last = (i == nqt - 1);
+        const int nx = G * (nqt - first_q(j));
+        for (int x = 0; x < nx; ++x) {
+          const bool last = (x == nx - 1);
           const int os = t % OS;
           // dP^T = V dO^T over S^T in the tile's region, once the compute
           // warps have read S^T
@@ -336,14 +345,14 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t t = 0, kc = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      int head, ja, jb;
-      bwd2_decode<CAUSAL>(u, nkv, head, ja, jb);
+      int kvh, ja, jb;
+      bwd2_decode<CAUSAL>(u, nkv, kvh, ja, jb);
       for (int half = 0; ok && half < 2; ++half) {
         const int j = half ? jb : ja;
         if (j < 0) break;
-        const int i0 = CAUSAL ? j : 0;
-        for (int i = i0; i < nqt; ++i) {
-          const bool first = (i == i0), last = (i == nqt - 1);
+        const int nx = G * (nqt - first_q(j));
+        for (int x = 0; x < nx; ++x) {
+          const bool first = (x == 0), last = (x == nx - 1);
           const int qs = t % QS, os = t % OS;
           const uint64_t qdesc_mn = sdesc_sw128(sb + T::A_SM_Q + qs * T::TILE, T::SUB, 1024);
           const uint64_t odesc_mn = sdesc_sw128(sb + T::A_SM_DO + os * T::TILE, T::SUB, 1024);
@@ -394,18 +403,18 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t t = 0, kc = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      int head, ja, jb;
-      bwd2_decode<CAUSAL>(u, nkv, head, ja, jb);
+      int kvh, ja, jb;
+      bwd2_decode<CAUSAL>(u, nkv, kvh, ja, jb);
       for (int half = 0; ok && half < 2; ++half) {
         const int j = half ? jb : ja;
         if (j < 0) break;
-        t += nqt - (CAUSAL ? j : 0);
+        t += G * (nqt - first_q(j));
         const int qs = (t - 1) % QS, os = (t - 1) % OS;
         if (!(ok = warp_wait(&bars->epi_full, kc & 1, wc, 58))) break;
         if (lane == 0) {
           for (int s = 0; s < T::DSUB; ++s) {
-            tma_store_2d(&tm_dk, smem + T::A_SM_Q + qs * T::TILE + s * T::SUB, s * 64, head * N + j * T::BN);
-            tma_store_2d(&tm_dv, smem + T::A_SM_DO + os * T::TILE + s * T::SUB, s * 64, head * N + j * T::BN);
+            tma_store_3d(&tm_dk, smem + T::A_SM_Q + qs * T::TILE + s * T::SUB, s * 64, j * T::BN, kvh);
+            tma_store_3d(&tm_dv, smem + T::A_SM_DO + os * T::TILE + s * T::SUB, s * 64, j * T::BN, kvh);
           }
           bulk_commit();
           bulk_wait_read<0>();
@@ -427,15 +436,20 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t t = 0, kc = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      int head, ja, jb;
-      bwd2_decode<CAUSAL>(u, nkv, head, ja, jb);
+      int kvh, ja, jb;
+      bwd2_decode<CAUSAL>(u, nkv, kvh, ja, jb);
       for (int half = 0; ok && half < 2; ++half) {
         const int j = half ? jb : ja;
         if (j < 0) break;
         const int key = j * T::BN + row;
-        for (int i = CAUSAL ? j : 0; i < nqt; ++i) {
+        const int i0 = first_q(j), nqi = nqt - i0;
+        for (int x = 0; x < G * nqi; ++x) {
+          const int i = i0 + x % nqi;
           const int qs = t % QS, os = t % OS;
-          const int q0 = i * T::BM + wg * T::QC;
+          // key k is hidden from query q iff k > q + coff: only tiles whose
+          // last key passes their first query's limit need the mask
+          const bool diag = CAUSAL && (j + 1) * T::BN - 1 > i * T::BM + coff;
+          const int q0 = i * T::BM + wg * T::QC + coff;  // limit of this warpgroup's first query column
           // ---- P^T = exp2(S^T * c - lse2); the region takes dP^T once S^T
           // has been read
           ok = mbar_wait(&bars->q_full[qs], (t / QS) & 1, wc, 71) && mbar_wait(&bars->s_full, t & 1, wc, 72);
@@ -465,7 +479,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               pv[e] = ex2_approx(-y[e]);
-              if (CAUSAL && i == j && key > q0 + c + e) pv[e] = 0.f;
+              if (diag && key > q0 + c + e) pv[e] = 0.f;
             }
             p2[c / 2] = f2_pack(pv[0], pv[1]);
             p2[c / 2 + 1] = f2_pack(pv[2], pv[3]);
@@ -624,10 +638,12 @@ __global__ void __launch_bounds__(384, 1)
 
   const WaitCtx wc{prm.status, &bars->abort_flag};
   const uint32_t tmem = bars->tmem_base;
-  const int N = prm.N;
-  const int nqt = N / T::BM, nkv = N / T::BN;
+  // Unit = (query head, query tile i); K/V come from head / G.  Causal: key
+  // tiles up to the last key the tile's last query sees.
+  const int G = prm.group, Nk = prm.Nk, coff = prm.causal_off, Nq_pad = prm.Nq_pad;
+  const int nqt = (prm.Nq + T::BM - 1) / T::BM, nkv = (Nk + T::BN - 1) / T::BN;
   const int units = bwd2_units<CAUSAL>(prm.heads, nqt);
-  auto num_kv = [&](int i) { return CAUSAL ? i + 1 : nkv; };
+  auto num_kv = [&](int i) { return CAUSAL ? (min((i + 1) * T::BM + coff, Nk) + T::BN - 1) / T::BN : nkv; };
 
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------ producer: Q, dO and K
@@ -652,16 +668,16 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = mbar_wait(&bars->k_empty[ks], ((k_it / KS) & 1) ^ 1, wc, 82))) break;
             mbar_arrive_expect_tx(&bars->k_full[ks], T::TILE);
             for (int s = 0; s < T::DSUB; ++s)
-              tma_load_2d_hint(smem + T::B_SM_K + ks * T::TILE + s * T::SUB, &tm_k, &bars->k_full[ks], s * 64,
-                               head * N + j * T::BN, pol_kv);
+              tma_load_3d_hint(smem + T::B_SM_K + ks * T::TILE + s * T::SUB, &tm_k, &bars->k_full[ks], s * 64,
+                               j * T::BN, head / G, pol_kv);
             ++k_it;
           }
           if (!ok) break;
           if (!(ok = mbar_wait(&bars->q_empty, (qc & 1) ^ 1, wc, 81))) break;
           mbar_arrive_expect_tx(&bars->q_full, 2 * T::TILE);
           for (int s = 0; s < T::DSUB; ++s) {
-            tma_load_2d_hint(smem + T::B_SM_Q + s * T::SUB, &tm_q, &bars->q_full, s * 64, head * N + i * T::BM, pol_q);
-            tma_load_2d_hint(smem + T::B_SM_DO + s * T::SUB, &tm_do, &bars->q_full, s * 64, head * N + i * T::BM, pol_q);
+            tma_load_3d_hint(smem + T::B_SM_Q + s * T::SUB, &tm_q, &bars->q_full, s * 64, i * T::BM, head, pol_q);
+            tma_load_3d_hint(smem + T::B_SM_DO + s * T::SUB, &tm_do, &bars->q_full, s * 64, i * T::BM, head, pol_q);
           }
           ++qc;
           for (int j = 1; j < num_kv(i); ++j) {
@@ -669,8 +685,8 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = mbar_wait(&bars->k_empty[ks], ((k_it / KS) & 1) ^ 1, wc, 82))) break;
             mbar_arrive_expect_tx(&bars->k_full[ks], T::TILE);
             for (int s = 0; s < T::DSUB; ++s)
-              tma_load_2d_hint(smem + T::B_SM_K + ks * T::TILE + s * T::SUB, &tm_k, &bars->k_full[ks], s * 64,
-                               head * N + j * T::BN, pol_kv);
+              tma_load_3d_hint(smem + T::B_SM_K + ks * T::TILE + s * T::SUB, &tm_k, &bars->k_full[ks], s * 64,
+                               j * T::BN, head / G, pol_kv);
             ++k_it;
           }
         }
@@ -695,8 +711,8 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = mbar_wait(&bars->v_empty[vs], ((v_it / VS) & 1) ^ 1, wc, 83))) break;
             mbar_arrive_expect_tx(&bars->v_full[vs], T::TILE);
             for (int s = 0; s < T::DSUB; ++s)
-              tma_load_2d_hint(smem + T::B_SM_V + vs * T::TILE + s * T::SUB, &tm_v, &bars->v_full[vs], s * 64,
-                               head * N + j * T::BN, pol_kv);
+              tma_load_3d_hint(smem + T::B_SM_V + vs * T::TILE + s * T::SUB, &tm_v, &bars->v_full[vs], s * 64,
+                               j * T::BN, head / G, pol_kv);
             ++v_it;
           }
         }
@@ -813,7 +829,7 @@ __global__ void __launch_bounds__(384, 1)
         if (lane == 0) {
           const int kl = (k_it - 1) % KS;
           for (int s = 0; s < T::DSUB; ++s)
-            tma_store_2d(&tm_dq, smem + T::B_SM_K + kl * T::TILE + s * T::SUB, s * 64, head * N + i * T::BM);
+            tma_store_3d(&tm_dq, smem + T::B_SM_K + kl * T::TILE + s * T::SUB, s * 64, i * T::BM, head);
           bulk_commit();
           bulk_wait_read<0>();
           mbar_arrive(&bars->k_empty[kl]);
@@ -841,7 +857,11 @@ __global__ void __launch_bounds__(384, 1)
         const int i = half ? ib : ia;
         if (i < 0) break;
         const int query = i * T::BM + row;
-        const size_t grow = static_cast<size_t>(head) * N + query;
+        const size_t grow = static_cast<size_t>(head) * Nq_pad + query;  // padded: lse2 = +inf past Nq
+        // last key this row sees; key tiles past the tile's smallest limit
+        // (the causal diagonal, or the ragged end of the keys) are masked
+        const int lim = CAUSAL ? min(query + coff, Nk - 1) : Nk - 1;
+        const int lim_lo = CAUSAL ? min(i * T::BM + coff, Nk - 1) : Nk - 1;
         const float lse2 = __ldg(prm.lse2 + grow);
         const float delta = __ldg(prm.delta + grow);
         const uint64_t c2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2), nd2 = f2_pack(-delta, -delta);
@@ -866,9 +886,9 @@ __global__ void __launch_bounds__(384, 1)
             float x0, x1;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nl2), x0, x1);
             float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            if (CAUSAL && j == i) {
-              if (k0 + c > query) p0 = 0.f;
-              if (k0 + c + 1 > query) p1 = 0.f;
+            if ((j + 1) * T::BN - 1 > lim_lo) {
+              if (k0 + c > lim) p0 = 0.f;
+              if (k0 + c + 1 > lim) p1 = 0.f;
             }
             p2[c / 2] = f2_pack(p0, p1);
           }
@@ -941,18 +961,17 @@ int launch_bwd2(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, cud
       return -1;
     attr_set = true;
   }
-  const int rows = prm.heads * prm.N;
-  constexpr int RPB = 256 / (D / 8);
-  fa_bwd_prep_kernel<D, BF><<<(rows + RPB - 1) / RPB, 256, 0, stream>>>(prm.o, prm.dout, prm.lse, prm.delta, prm.lse2,
-                                                                     rows);
+  if (launch_prep<D, BF>(prm, stream) != 0) return -1;
+  auto grid_for = [&](int heads, int tiles) {
+    const long long units = CAUSAL ? static_cast<long long>(heads) * ((tiles + 1) / 2) : static_cast<long long>(heads) * tiles;
+    return static_cast<int>(units < max_ctas ? units : max_ctas);
+  };
+  const int nqt = (prm.Nq + T::BM - 1) / T::BM, nkv = (prm.Nk + T::BN - 1) / T::BN;
+  fa_bwd_dkdv_kernel<D, CAUSAL, BF><<<grid_for(prm.heads / prm.group, nkv), 384, T::A_SMEM, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], maps[5], maps[6], prm);
   if (cudaGetLastError() != cudaSuccess) return -1;
-  const int nt = prm.N / 128;
-  const int units = CAUSAL ? prm.heads * ((nt + 1) / 2) : prm.heads * nt;
-  const int grid = units < max_ctas ? units : max_ctas;
-  fa_bwd_dkdv_kernel<D, CAUSAL, BF><<<grid, 384, T::A_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[5],
-                                                                   maps[6], prm);
-  if (cudaGetLastError() != cudaSuccess) return -1;
-  fa_bwd_dq_kernel<D, CAUSAL, BF><<<grid, 384, T::B_SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], prm);
+  fa_bwd_dq_kernel<D, CAUSAL, BF><<<grid_for(prm.heads, nqt), 384, T::B_SMEM, stream>>>(maps[0], maps[1], maps[2],
+                                                                                       maps[3], maps[4], prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

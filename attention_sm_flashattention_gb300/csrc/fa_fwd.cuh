@@ -133,10 +133,21 @@ __device__ __forceinline__ void fwd_decode(int u, int nqt, int& head, int& qa, i
   }
 }
 
+// Key tiles query tile qt visits: all of them, or (causal) those up to the
+// last key its last row sees, key (qt + 1) * BM - 1 + off.
 template <int D, bool CAUSAL>
-__device__ __forceinline__ int fwd_num_kv(int qt, int nkv_full) {
+__device__ __forceinline__ int fwd_num_kv(int qt, int nkv_full, int Nk, int off) {
   using T = FwdTraits<D, CAUSAL>;
-  return CAUSAL ? ((qt + 1) * T::BM) / T::BN : nkv_full;
+  if (!CAUSAL) return nkv_full;
+  const int end = min((qt + 1) * T::BM + off, Nk);  // one past the last visible key
+  return (end + T::BN - 1) / T::BN;
+}
+
+// Last key row `qi` sees (Nk - 1, or qi + off when causal).  A tile whose
+// last key is past the smallest such limit over its rows needs the mask.
+template <bool CAUSAL>
+__device__ __forceinline__ int fwd_key_limit(int qi, int Nk, int off) {
+  return CAUSAL ? min(qi + off, Nk - 1) : Nk - 1;
 }
 
 // Bounded wait that ignores the abort flag: used only while draining at exit.
@@ -156,12 +167,14 @@ struct FwdCursor {
   int u, half, head, qt, qb, j, nkv;
   uint32_t item, tile;
   bool valid;
-  int units, nqt, nkv_full;
+  int units, nqt, nkv_full, Nk, off;
 
-  __device__ void start(int first_unit, int units_, int nqt_, int nkv_full_) {
+  __device__ void start(int first_unit, int units_, int nqt_, int nkv_full_, int Nk_, int off_) {
     units = units_;
     nqt = nqt_;
     nkv_full = nkv_full_;
+    Nk = Nk_;
+    off = off_;
     item = 0;
     tile = 0;
     j = 0;
@@ -176,7 +189,7 @@ struct FwdCursor {
     fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
     qt = qa;
     half = 0;
-    nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+    nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
   }
   __device__ void advance() {
     ++tile;
@@ -186,7 +199,7 @@ struct FwdCursor {
     if (half == 0 && qb >= 0) {
       half = 1;
       qt = qb;
-      nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+      nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
     } else {
       u += gridDim.x;
       load_unit();
@@ -253,9 +266,9 @@ __global__ void __launch_bounds__(512, 1)
   tc_fence_after();
   const WaitCtx wc{prm.status, &bars->abort_flag};
   const uint32_t tmem = bars->tmem_base;
-  const int N = prm.N;
-  const int nqt = N / T::BM;
-  const int nkv_full = N / T::BN;
+  const int Nq = prm.Nq, Nk = prm.Nk, off = prm.causal_off;
+  const int nqt = (Nq + T::BM - 1) / T::BM;
+  const int nkv_full = (Nk + T::BN - 1) / T::BN;
   const int units = fwd_num_units<CAUSAL>(prm.heads, nqt);
 
   if (warp < 8) {
@@ -277,8 +290,10 @@ __global__ void __launch_bounds__(512, 1)
         for (int half = 0; ok && half < 2; ++half) {
           const int qt = half ? qb : qa;
           if (qt < 0) break;
-          const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+          const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
           const int qi = qt * T::BM + r;  // query index within the head
+          const int lim = fwd_key_limit<CAUSAL>(qi, Nk, off);             // this row's last key
+          const int lim_lo = fwd_key_limit<CAUSAL>(qt * T::BM, Nk, off);  // the tile's smallest limit
           float m = -INFINITY, l = 0.f;   // l: this half's partial row sum
           for (int j = 0; j < nkv; ++j) {
             const int b = t & 1;
@@ -292,11 +307,11 @@ __global__ void __launch_bounds__(512, 1)
             for (int c = 0; c < HC; c += 32) tmem_ld32(lane_base + T::S_COL + b * T::BN + (wg ^ 1) * HC + c, sr + c);
             tmem_wait_ld();
             reg_fence<HC>(sr);
-            if (CAUSAL && (j + 1) * T::BN - 1 > qt * T::BM) {
+            if ((j + 1) * T::BN - 1 > lim_lo) {
               const int k0 = j * T::BN + (wg ^ 1) * HC;
   #pragma unroll
               for (int c = 0; c < HC; ++c)
-                if (k0 + c > qi) sr[c] = __float_as_uint(-INFINITY);
+                if (k0 + c > lim) sr[c] = __float_as_uint(-INFINITY);
             }
   #pragma unroll
             for (int i = 0; i < 8; ++i) pm[i] = fmaxf(__uint_as_float(sr[i]), __uint_as_float(sr[i + 8]));
@@ -314,11 +329,11 @@ __global__ void __launch_bounds__(512, 1)
             float s[HC];
   #pragma unroll
             for (int c = 0; c < HC; ++c) s[c] = __uint_as_float(sr[c]);
-            if (CAUSAL && (j + 1) * T::BN - 1 > qt * T::BM) {
+            if ((j + 1) * T::BN - 1 > lim_lo) {
               const int k0 = j * T::BN + wg * HC;
   #pragma unroll
               for (int c = 0; c < HC; ++c)
-                if (k0 + c > qi) s[c] = -INFINITY;
+                if (k0 + c > lim) s[c] = -INFINITY;
             }
   #pragma unroll
             for (int c = 0; c < HC; c += 16)
@@ -432,16 +447,17 @@ __global__ void __launch_bounds__(512, 1)
             mbar_arrive_expect_tx(&bars->q_full[qs], T::Q_BYTES);
             uint8_t* sq = smem + T::SM_Q + qs * T::Q_BYTES;
             for (int s = 0; s < T::DSUB; ++s)
-              tma_load_2d_hint(sq + s * T::Q_SUB, &tm_q, &bars->q_full[qs], s * 64, head * N + qt * T::BM, pol_q);
+              tma_load_3d_hint(sq + s * T::Q_SUB, &tm_q, &bars->q_full[qs], s * 64, qt * T::BM, head, pol_q);
             ++q_it;
-            const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+            const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
             for (int j = 0; j < nkv; ++j) {
               const int st = k_it % T::K_STAGES;
               if (!(ok = mbar_wait(&bars->k_empty[st], ((k_it / T::K_STAGES) & 1) ^ 1, wc, 2))) break;
               uint8_t* sk = smem + T::SM_K + st * T::KV_BYTES;
               mbar_arrive_expect_tx(&bars->k_full[st], T::KV_BYTES);
               for (int s = 0; s < T::DSUB; ++s)
-                tma_load_2d_hint(sk + s * T::KV_SUB, &tm_k, &bars->k_full[st], s * 64, head * N + j * T::BN, pol_kv);
+                tma_load_3d_hint(sk + s * T::KV_SUB, &tm_k, &bars->k_full[st], s * 64, j * T::BN, head / prm.group,
+                                 pol_kv);
               ++k_it;
             }
           }
@@ -464,14 +480,15 @@ __global__ void __launch_bounds__(512, 1)
           for (int half = 0; ok && half < 2; ++half) {
             const int qt = half ? qb : qa;
             if (qt < 0) break;
-            const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+            const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
             for (int j = 0; j < nkv; ++j) {
               const int st = v_it % T::V_STAGES;
               if (!(ok = mbar_wait(&bars->v_empty[st], ((v_it / T::V_STAGES) & 1) ^ 1, wc, 8))) break;
               uint8_t* sv = smem + T::SM_V + st * T::KV_BYTES;
               mbar_arrive_expect_tx(&bars->v_full[st], T::KV_BYTES);
               for (int s = 0; s < T::DSUB; ++s)
-                tma_load_2d_hint(sv + s * T::KV_SUB, &tm_v, &bars->v_full[st], s * 64, head * N + j * T::BN, pol_kv);
+                tma_load_3d_hint(sv + s * T::KV_SUB, &tm_v, &bars->v_full[st], s * 64, j * T::BN, head / prm.group,
+                                 pol_kv);
               ++v_it;
             }
           }
@@ -541,7 +558,7 @@ __global__ void __launch_bounds__(512, 1)
       // P V as each tile's P becomes ready.  Neither waits behind the
       // other's dependencies.
       FwdCursor<D, CAUSAL> c;
-      c.start(blockIdx.x, units, nqt, nkv_full);
+      c.start(blockIdx.x, units, nqt, nkv_full, Nk, off);
       const bool s_side = (warp == T::MMA_WARP);
       while (ok && c.valid) {
         ok = s_side ? issue_s(c) : issue_pv(c);
@@ -568,7 +585,7 @@ __global__ void __launch_bounds__(512, 1)
         for (int half = 0; ok && half < 2; ++half) {
           const int qt = half ? qb : qa;
           if (qt < 0) break;
-          t += fwd_num_kv<D, CAUSAL>(qt, nkv_full);
+          t += fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
           ok = mbar_wait(&bars->lm_full, q_item & 1, wc, 17);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           const float l_row = lm[r] + lm[T::BM + r];
@@ -599,7 +616,8 @@ __global__ void __launch_bounds__(512, 1)
           }
           fence_proxy_async_smem();
           mbar_arrive(&bars->epi_full[q_item % T::Q_STAGES]);
-          prm.lse[static_cast<size_t>(head) * N + qt * T::BM + r] = (m + log2f(l_row)) * 0.69314718055994530942f;
+          if (qt * T::BM + r < Nq)
+            prm.lse[static_cast<size_t>(head) * Nq + qt * T::BM + r] = (m + log2f(l_row)) * 0.69314718055994530942f;
           tc_fence_before();
           mbar_arrive(&bars->o_free);
           if (warp == 8) {
@@ -610,7 +628,7 @@ __global__ void __launch_bounds__(512, 1)
             if (lane == 0) {
               const uint8_t* so_tile = smem + T::SM_Q + qs * T::Q_BYTES;
               for (int sub = 0; sub < T::DSUB; ++sub)
-                tma_store_2d(&tm_o, so_tile + sub * T::Q_SUB, sub * 64, head * N + qt * T::BM);
+                tma_store_3d(&tm_o, so_tile + sub * T::Q_SUB, sub * 64, qt * T::BM, head);
               bulk_commit();
               bulk_wait_read<0>();
               mbar_arrive(&bars->q_empty[qs]);
@@ -650,7 +668,7 @@ int launch_fwd(const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaS
       return -1;
     attr_set = true;
   }
-  const int nqt = prm.N / T::BM;
+  const int nqt = (prm.Nq + T::BM - 1) / T::BM;
   const int units = CAUSAL ? prm.heads * ((nqt + 1) / 2) : prm.heads * nqt;
   const int grid = units < num_sms ? units : num_sms;
   fa_fwd_kernel<D, CAUSAL, BF><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);

@@ -10,27 +10,37 @@
 
 namespace fa {
 
+// Shapes: queries (and O, dO, dQ) are [heads, Nq, D]; keys and values (and
+// dK, dV) are [heads / group, Nk, D]; query head h reads K/V head h / group.
+// Causal: query i sees key j iff j <= i + causal_off, causal_off = Nk - Nq
+// (the queries are the last Nq positions of the sequence; Nq <= Nk).
 struct FwdParams {
-  __half* o;         // [heads, N, D] (written through the O tensor map)
-  float* lse;        // [heads, N]
-  int heads;         // Z * H
-  int N;             // sequence length (multiple of 128)
+  __half* o;         // [heads, Nq, D] (written through the O tensor map)
+  float* lse;        // [heads, Nq]
+  int heads;         // query heads, Z * H
+  int group;         // query heads per K/V head
+  int Nq, Nk;        // query and key lengths (any >= 1)
+  int causal_off;    // Nk - Nq
   float scale_log2;  // scale * log2(e)
   int* status;       // device status word
 };
 
 struct BwdParams {
-  const __half* o;     // [heads, N, D] forward output
-  const __half* dout;  // [heads, N, D]
-  const float* lse;    // [heads, N] natural-log lse from the forward
-  __half* dq;          // [heads, N, D]
-  __half* dk;
+  const __half* o;     // [heads, Nq, D] forward output
+  const __half* dout;  // [heads, Nq, D]
+  const float* lse;    // [heads, Nq] natural-log lse from the forward
+  __half* dq;          // [heads, Nq, D]
+  __half* dk;          // [heads / group, Nk, D]
   __half* dv;
-  float* delta;        // workspace [heads, N]: rowsum(O * dO)
-  float* lse2;         // workspace [heads, N]: lse * log2(e)
+  float* delta;        // workspace [heads, Nq_pad]: rowsum(O * dO), 0 in the padding
+  float* lse2;         // workspace [heads, Nq_pad]: lse * log2(e), +inf in the padding
   float* dq_acc;       // workspace [grid, N, D]: per-CTA fp32 dQ accumulator (D = 256 only)
-  int heads;
-  int N;
+  int heads;           // query heads
+  int group;           // query heads per K/V head
+  int Nq, Nk;
+  int Nq_pad;          // Nq rounded up to the 128-row query tile
+  int causal_off;      // Nk - Nq
+  int N;               // D = 256 kernel: the common length (Nq == Nk, a multiple of 128)
   float scale;         // softmax scale
   float scale_log2;    // scale * log2(e)
   int* status;

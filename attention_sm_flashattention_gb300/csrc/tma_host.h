@@ -41,4 +41,24 @@ inline bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType
   return r == CUDA_SUCCESS;
 }
 
+// `mats` row-major matrices [rows x cols] of `elem_bytes`-byte elements,
+// stored back to back (contiguous [mats, rows, cols]), tiled in boxes of
+// box_cols x box_rows x 1.  A box that runs past `rows` is zero-filled on
+// load and clipped on store inside its own matrix.
+inline bool make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
+                         uint64_t mats, uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
+                         bool swizzle128) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {cols, rows, mats};
+  cuuint64_t strides[2] = {cols * static_cast<uint64_t>(elem_bytes), rows * cols * static_cast<uint64_t>(elem_bytes)};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace fa

@@ -4,7 +4,8 @@ and the benchmark.
 This module holds no attention arithmetic: it only names the workloads and
 draws their tensors.  Recipe: a CPU ``torch.Generator`` seeded with the
 workload's seed draws ``q``, ``k``, ``v``, ``do`` in that order, each as
-standard-normal float32 of shape ``[Z, H, N, D]``, then rounds them to fp16
+standard-normal float32 of shape ``[Z, H, N, D]`` (k and v ``[Z, Hkv, Nk, D]``
+for grouped heads or unequal lengths), then rounds them to fp16
 (round-to-nearest-even), or to bf16 for the bf16 path.  ``scale = 1/sqrt(D)`` passed as a float32.
 """
 
@@ -51,17 +52,22 @@ WORKLOADS = {
 }
 
 
-def make_inputs(Z: int, H: int, N: int, D: int, seed: int, device="cpu", dtype=torch.float16):
-    """Draw ``(q, k, v, do)`` of shape ``[Z, H, N, D]`` from ``seed``, rounded
-    to ``dtype`` (fp16 by default, or bf16; the same draw either way).
+def make_inputs(Z: int, H: int, N: int, D: int, seed: int, device="cpu", dtype=torch.float16,
+                Hkv: int | None = None, Nk: int | None = None):
+    """Draw ``(q, k, v, do)`` from ``seed``, rounded to ``dtype`` (fp16 by
+    default, or bf16; the same draw either way).  q and do are
+    ``[Z, H, N, D]``; k and v are ``[Z, Hkv, Nk, D]`` (``Hkv = H``, ``Nk = N``
+    unless given: grouped K/V heads and unequal query / key lengths).
 
     The draw always happens on the CPU generator so that every device sees
     bit-identical tensors; ``device`` only says where the result is moved.
     """
+    Hkv = H if Hkv is None else Hkv
+    Nk = N if Nk is None else Nk
     g = torch.Generator(device="cpu").manual_seed(int(seed))
-    shape = (Z, H, N, D)
+    shapes = ((Z, H, N, D), (Z, Hkv, Nk, D), (Z, Hkv, Nk, D), (Z, H, N, D))
     out = []
-    for _ in range(4):
+    for shape in shapes:
         t = torch.randn(shape, generator=g, dtype=torch.float32).to(dtype)
         out.append(t if device == "cpu" else t.to(device))
     return tuple(out)

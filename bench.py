@@ -30,6 +30,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 Z, H, N, D, CAUSAL = 128, 8, 1024, 128, False
+HKV, NK = H, N  # K/V heads and key length (grouped heads / unequal lengths; the benchmark has HKV = H, NK = N)
 DTYPE = "f16"  # element type of the inputs and outputs: "f16" (benchmark) or "bf16"
 WORKLOAD = "attention fwd+bwd, Z128 H8 N1024 D128 non-causal, fp16 inputs ~N(0,1), scale 1/sqrt(D)"
 METRIC = "attention fwd / fwd+bwd TFLOP/s at Z128 H8 N1024 D128 on 1 GB300; % of FP16 peak"
@@ -37,20 +38,31 @@ UNIT = "TFLOP/s"
 SEED = 1002
 
 
-def set_workload(z, h, n, d, causal):
-    global Z, H, N, D, CAUSAL, WORKLOAD
+def set_workload(z, h, n, d, causal, hkv=None, nk=None):
+    global Z, H, N, D, CAUSAL, HKV, NK, WORKLOAD
     Z, H, N, D, CAUSAL = z, h, n, d, bool(causal)
-    WORKLOAD = (f"attention fwd+bwd, Z{Z} H{H} N{N} D{D} {'causal' if CAUSAL else 'non-causal'}, "
+    HKV = h if hkv is None else hkv
+    NK = n if nk is None else nk
+    extra = ""
+    if HKV != H:
+        extra += f" Hkv{HKV}"
+    if NK != N:
+        extra += f" Nk{NK}"
+    WORKLOAD = (f"attention fwd+bwd, Z{Z} H{H} N{N}{extra} D{D} {'causal' if CAUSAL else 'non-causal'}, "
                 "fp16 inputs ~N(0,1), scale 1/sqrt(D)")
 
 
-def flops_fwd(z, h, n, d, causal):
-    return z * h * (2.0 * n * (n + 1) * d if causal else 4.0 * n * n * d)
+def flops_fwd(z, h, n, d, causal, nk=None):
+    """4 D FLOPs (two GEMMs) per visible (query, key) pair per query head."""
+    nk = n if nk is None else nk
+    pairs = n * (n + 1) / 2.0 + n * (nk - n) if causal else float(n) * nk
+    return z * h * 4.0 * pairs * d
 
 
 def flops_step(z=None, h=None, n=None, d=None, causal=None):
-    return 3.5 * flops_fwd(Z if z is None else z, H if h is None else h, N if n is None else n,
-                           D if d is None else d, CAUSAL if causal is None else causal)
+    n = N if n is None else n
+    return 3.5 * flops_fwd(Z if z is None else z, H if h is None else h, n, D if d is None else d,
+                           CAUSAL if causal is None else causal, NK if n == N else n)
 
 
 def measured_peaks():
@@ -159,12 +171,13 @@ def gpu_bench(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     gen = torch.Generator(device=dev).manual_seed(SEED + rank)
     elem = torch.bfloat16 if DTYPE == "bf16" else torch.float16
-    q, k, v, do = (torch.randn((Z, H, N, D), device=dev, dtype=elem, generator=gen) for _ in range(4))
+    q, k, v, do = (torch.randn(shape, device=dev, dtype=elem, generator=gen)
+                   for shape in ((Z, H, N, D), (Z, HKV, NK, D), (Z, HKV, NK, D), (Z, H, N, D)))
     scale = 1.0 / math.sqrt(D)
     o = torch.empty_like(q)
     lse = torch.empty((Z, H, N), device=dev, dtype=torch.float32)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    ws = torch.empty(fa.bwd_workspace_size(Z, H, N, D, CAUSAL), device=dev, dtype=torch.uint8)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.bwd_workspace_size(Z, H, N, D, CAUSAL, HKV, NK), device=dev, dtype=torch.uint8)
 
     def step():
         fa.fwd(q, k, v, causal=CAUSAL, scale=scale, out=(o, lse))
@@ -210,7 +223,7 @@ def gpu_bench(args, rank, world, local_rank):
 
     # ---- end to end through the public API: pinned host in, host out
     hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
-    ho, hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(4))
+    ho, hdq, hdk, hdv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, dq, dk, dv))
     e2e_steps = max(3, min(args.steps, 20))
 
     def e2e_step():
@@ -237,9 +250,10 @@ def gpu_bench(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if fa.device_status() != 0:
         raise RuntimeError("device status reports a kernel wait timeout in the end-to-end leg")
-    nbytes = q.numel() * q.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv))
     return {"total_ms": total_ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "e2e_ms": e2e_ms,
-            "h2d": 4 * nbytes, "d2h": 4 * nbytes, "clocks": clocks}
+            "h2d": h2d, "d2h": d2h, "clocks": clocks}
 
 
 def reduce_max(vals, world):
@@ -286,13 +300,15 @@ def main():
     ap.add_argument("--n", type=int, default=N)
     ap.add_argument("--d", type=int, default=D)
     ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--hkv", type=int, default=None, help="K/V heads (grouped heads; default H)")
+    ap.add_argument("--nk", type=int, default=None, help="key length (default N, the query length)")
     ap.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
                     help="element type of the inputs and outputs (the benchmark is f16)")
     args = ap.parse_args()
     global DTYPE
     DTYPE = args.dtype
     args.warmup = max(args.warmup, 3)
-    set_workload(args.z, args.h, args.n, args.d, args.causal)
+    set_workload(args.z, args.h, args.n, args.d, args.causal, args.hkv, args.nk)
     global WORKLOAD
     if DTYPE == "bf16":
         WORKLOAD = WORKLOAD.replace("fp16 inputs", "bf16 inputs")
@@ -300,9 +316,13 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    in_mb = (2 * Z * H * N + 2 * Z * HKV * NK) * D * 2 / 1e6
     config = {"workload": WORKLOAD, "Z": Z, "H": H, "N": N, "D": D, "causal": CAUSAL,
               "global_batch": Z * world, "seq_len": N, "parallelism": f"replicas{world}",
-              "l2": f"inputs larger than L2 ({4 * Z * H * N * D * 2 / 1e6:.0f} MB {DTYPE} per step), no flush needed"}
+              "l2": (f"inputs larger than L2 ({in_mb:.0f} MB {DTYPE} per step), no flush needed" if in_mb > 130
+                     else f"inputs {in_mb:.0f} MB {DTYPE} per step, smaller than L2: not flushed (profiling case)")}
+    if HKV != H or NK != N:
+        config.update({"Hkv": HKV, "Nk": NK})
 
     if args.impl == "reference":
         # The oracle as it stands, on the host cores: each step is one head of
@@ -350,8 +370,8 @@ def main():
     value = world * flops_step() / (ms_per_step * 1e-3) / 1e12
     e2e_value = world * flops_step() / (e2e_ms * 1e-3) / 1e12
     peaks = measured_peaks()
-    fwd_tf = flops_fwd(Z, H, N, D, CAUSAL) / (r["fwd_ms"] * 1e-3) / 1e12
-    bwd_tf = 2.5 * flops_fwd(Z, H, N, D, CAUSAL) / (r["bwd_ms"] * 1e-3) / 1e12
+    fwd_tf = flops_fwd(Z, H, N, D, CAUSAL, NK) / (r["fwd_ms"] * 1e-3) / 1e12
+    bwd_tf = 2.5 * flops_fwd(Z, H, N, D, CAUSAL, NK) / (r["bwd_ms"] * 1e-3) / 1e12
     traffic = load_traffic()
     bwd_traffic = traffic.get(f"fa_bwd_d{D}{'c' if CAUSAL else ''}") if traffic else None
     line = {

@@ -24,7 +24,9 @@
  *                                  log of sum_j exp(S_ij) over the visible
  *                                  keys j (j <= i when causal).
  *   Every (z, h) pair is an independent head; queries and keys have the same
- *   length N.  Causal means key j is visible to query i iff j <= i.
+ *   length N (any N >= 1; a last partial 128-row tile is masked).  Causal
+ *   means key j is visible to query i iff j <= i.  fa_fwd_ex / fa_bwd_ex
+ *   below add grouped K/V heads and different query and key lengths.
  *
  * Ownership: every pointer is device memory owned by the caller; the library
  * keeps no pointer after a call returns and allocates no device memory on
@@ -57,8 +59,10 @@ extern "C" {
 #endif
 
 #define FA_OK 0
-#define FA_ERR_INVALID_ARG (-1) /* null pointer, Z/H/N <= 0, non-finite or <= 0 scale, misaligned pointer */
-#define FA_ERR_UNSUPPORTED (-2) /* D not in {64, 128, 256}, N % 128 != 0, or sizes past 32-bit indexing */
+#define FA_ERR_INVALID_ARG (-1) /* null pointer, a size <= 0, H not a multiple of Hkv, bad causal flag or
+                                   dtype, non-finite or <= 0 scale, misaligned pointer */
+#define FA_ERR_UNSUPPORTED (-2) /* D not in {64, 128, 256}, causal with Nq > Nk, sizes past 32-bit indexing,
+                                   or a D = 256 backward with Nq != Nk, N % 128 != 0 or Hkv != H */
 #define FA_ERR_WORKSPACE (-3)   /* workspace null or smaller than fa_bwd_workspace_size() */
 #define FA_ERR_CUDA (-4)        /* a CUDA runtime call or kernel launch failed */
 #define FA_ERR_DEVICE (-5)      /* current device is not a compute capability 10.3 GPU */
@@ -73,7 +77,7 @@ extern "C" {
  *   o       : output [Z,H,N,D] fp16, O = softmax(Q K^T scale) V, rounded to
  *             nearest from the fp32 accumulator divided by l.
  *   lse     : output [Z,H,N] fp32 (natural-log log-sum-exp of each row of S).
- *   Z, H, N : batch, heads, sequence length (N % 128 == 0).
+ *   Z, H, N : batch, heads, sequence length (N >= 1).
  *   D       : head dimension, 64, 128 or 256.
  *   causal  : 0 or 1.
  *   scale   : softmax scale applied to Q K^T (usually 1/sqrt(D)); finite, > 0.
@@ -85,7 +89,8 @@ FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* l
 
 /*
  * Bytes of device workspace fa_bwd (or fa_bwd_bf16) needs on the current
- * device: Delta and the log2-scaled lse (2 x Z*H*N fp32); for D = 256 also
+ * device: Delta and the log2-scaled lse (2 x Z*H*N' fp32, N' = N rounded up to
+ * a multiple of 128); for D = 256 also
  * one fp32 N x D dQ accumulator per resident CTA.  It grows with Z*H*N (and
  * #SMs*N*D for D = 256), never with N^2 over all heads (§二, third rule).
  * Returns 0 for unsupported arguments.
@@ -126,6 +131,42 @@ FA_API int fa_fwd_bf16(const void* q, const void* k, const void* v, void* o, flo
 FA_API int fa_bwd_bf16(const void* q, const void* k, const void* v, const void* o, const void* dout,
                        const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                        int Z, int H, int N, int D, int causal, float scale, cudaStream_t stream);
+
+/*
+ * Grouped K/V heads and different query / key lengths.  Source: «把
+ * FlashAttention 搬上昇腾», the GQA Paged Attention part of the contest
+ * section: the number of query heads is an integer multiple of the number
+ * of K/V heads, several query heads share one K/V head, each sequence has
+ * its own context length and the last incomplete block is masked.
+ *
+ *   q, o, dout, dq : [Z, H, Nq, D]        lse : fp32 [Z, H, Nq]
+ *   k, v, dk, dv   : [Z, Hkv, Nk, D]      (H a multiple of Hkv; g = H / Hkv)
+ *   Query head h of batch z reads K/V head h / g of batch z (consecutive
+ *   query heads share a K/V head).  dk, dv of a shared head are the sums of
+ *   the gradients of its g query heads, each written once by one CTA.
+ *   Nq, Nk : any lengths >= 1.
+ *   causal : the queries are the last Nq positions of an Nk-long sequence:
+ *            query i sees key j iff j <= i + (Nk - Nq).  Needs Nq <= Nk
+ *            (otherwise some row would see no key): FA_ERR_UNSUPPORTED.
+ *   dtype  : FA_DTYPE_F16 or FA_DTYPE_BF16, the element type of every
+ *            [.., D] tensor (lse, Delta and accumulation stay fp32).
+ *   The D = 256 backward currently needs Nq == Nk, a multiple of 128, and
+ *   Hkv == H (FA_ERR_UNSUPPORTED otherwise); the forward has no such limit.
+ * Layout, alignment, ownership, asynchrony and errors as for fa_fwd /
+ * fa_bwd; workspace from fa_bwd_ex_workspace_size (0 = unsupported shape).
+ * fa_fwd(q, k, v, o, lse, Z, H, N, D, c, s, st) is
+ * fa_fwd_ex(q, k, v, o, lse, Z, H, H, N, N, D, c, s, FA_DTYPE_F16, st).
+ */
+#define FA_DTYPE_F16 0
+#define FA_DTYPE_BF16 1
+FA_API int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int Hkv, int Nq,
+                     int Nk, int D, int causal, float scale, int dtype, cudaStream_t stream);
+
+FA_API size_t fa_bwd_ex_workspace_size(int Z, int H, int Hkv, int Nq, int Nk, int D, int causal);
+
+FA_API int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int Z,
+                     int H, int Hkv, int Nq, int Nk, int D, int causal, float scale, int dtype, cudaStream_t stream);
 
 /*
  * Backward pass that allocates nothing and takes no workspace.
@@ -192,9 +233,10 @@ FA_API const char* fa_error_string(int code);
 
 /*
  * Number of (query tile, key tile) pairs one head's pass visits with the
- * library's forward tiling (128-row query tiles, 128- or 64-key tiles): the
- * causal loop bound of §八 (T*T tiles non-causal, 1+2+...+T causal for square
- * tiles).  Host-only helper used for the FLOP model; -1 on bad arguments.
+ * library's forward tiling (128-row query tiles, 128- or 64-key tiles, the
+ * last of each possibly partial): the causal loop bound of §八 (T*T tiles
+ * non-causal, 1+2+...+T causal for square tiles).  Host-only helper used
+ * for the FLOP model; -1 on bad arguments.
  */
 FA_API long long fa_fwd_tile_count(int N, int D, int causal);
 
@@ -205,6 +247,14 @@ FA_API long long fa_fwd_tile_count(int N, int D, int causal);
  */
 FA_API double fa_fwd_flops(int Z, int H, int N, int D, int causal);
 FA_API double fa_bwd_flops(int Z, int H, int N, int D, int causal);
+
+/*
+ * The same for the fa_fwd_ex / fa_bwd_ex shapes: 4*D per visible (query,
+ * key) pair per query head, Nq*Nk pairs non-causal, Nq*(Nq+1)/2 +
+ * Nq*(Nk-Nq) causal; backward 2.5x.
+ */
+FA_API double fa_fwd_ex_flops(int Z, int H, int Nq, int Nk, int D, int causal);
+FA_API double fa_bwd_ex_flops(int Z, int H, int Nq, int Nk, int D, int causal);
 
 #ifdef __cplusplus
 }

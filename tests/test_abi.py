@@ -71,7 +71,6 @@ def call_fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, Z=1, H=1, N=128, D=6
     (dict(scale=0.0), _native.FA_ERR_INVALID_ARG),
     (dict(D=96), _native.FA_ERR_UNSUPPORTED),
     (dict(D=32), _native.FA_ERR_UNSUPPORTED),
-    (dict(N=100), _native.FA_ERR_UNSUPPORTED),
     (dict(Z=1 << 14, H=1 << 10, N=256), _native.FA_ERR_UNSUPPORTED),  # rows >= 2^31
 ])
 def test_fwd_rejects_bad_arguments(lib, kw, code):
@@ -86,12 +85,15 @@ def call_bwd(lib, ws=FAKE, ws_bytes=1 << 40, dq=FAKE, D=64, N=128, scale=0.125):
 def test_bwd_rejects_bad_arguments(lib):
     assert call_bwd(lib, dq=None) == _native.FA_ERR_INVALID_ARG
     assert call_bwd(lib, D=80) == _native.FA_ERR_UNSUPPORTED
-    assert call_bwd(lib, N=130) == _native.FA_ERR_UNSUPPORTED
+    assert call_bwd(lib, D=256, N=130) == _native.FA_ERR_UNSUPPORTED  # D = 256 backward: N % 128 == 0
     assert call_bwd(lib, scale=-1.0) == _native.FA_ERR_INVALID_ARG
 
 
 def test_workspace_size_rejects_bad_shapes(lib):
-    assert lib.fa_bwd_workspace_size(1, 1, 100, 64, 0) == 0
+    assert lib.fa_bwd_workspace_size(1, 1, 100, 256, 0) == 0
+    assert lib.fa_bwd_ex_workspace_size(1, 4, 3, 128, 128, 64, 0) == 0    # H not a multiple of Hkv
+    assert lib.fa_bwd_ex_workspace_size(1, 4, 2, 256, 128, 64, 1) == 0    # causal with Nq > Nk
+    assert lib.fa_bwd_ex_workspace_size(1, 4, 2, 128, 128, 256, 0) == 0   # D = 256 backward, grouped heads
     assert lib.fa_bwd_workspace_size(1, 1, 128, 48, 0) == 0
 
 
@@ -107,7 +109,53 @@ def test_tile_count_matches_pages_and_oracle(lib):
         # 64-key tiles for D = 256: twice as many key tiles, causal bound 2(qt+1)
         assert lib.fa_fwd_tile_count(N, 256, 0) == 2 * t * t
         assert lib.fa_fwd_tile_count(N, 256, 1) == t * (t + 1)
-    assert lib.fa_fwd_tile_count(100, 64, 0) == -1
+    # ragged N: count the (query tile, key tile) pairs that hold at least one
+    # visible (query, key) pair, by brute force over the tile grid
+    for N, D in ((100, 64), (300, 128), (130, 256), (1, 64)):
+        bn = 64 if D == 256 else 128
+        for causal in (0, 1):
+            want = 0
+            for qt in range((N + 127) // 128):
+                for kt in range((N + bn - 1) // bn):
+                    q_last = min(N, (qt + 1) * 128) - 1
+                    if kt * bn < N and (not causal or kt * bn <= q_last):
+                        want += 1
+            assert lib.fa_fwd_tile_count(N, D, causal) == want, (N, D, causal)
+    assert lib.fa_fwd_tile_count(0, 64, 0) == -1
+
+
+def call_fwd_ex(lib, Z=1, H=4, Hkv=2, Nq=100, Nk=200, D=64, causal=0, scale=0.125, dtype=0):
+    return lib.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, Z, H, Hkv, Nq, Nk, D, causal, scale, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hkv=3), _native.FA_ERR_INVALID_ARG),       # 4 query heads over 3 K/V heads
+    (dict(Hkv=0), _native.FA_ERR_INVALID_ARG),
+    (dict(Nk=0), _native.FA_ERR_INVALID_ARG),
+    (dict(dtype=2), _native.FA_ERR_INVALID_ARG),
+    (dict(causal=1, Nq=201), _native.FA_ERR_UNSUPPORTED),  # a query row would see no key
+    (dict(D=80), _native.FA_ERR_UNSUPPORTED),
+])
+def test_fwd_ex_rejects_bad_arguments(lib, kw, code):
+    assert call_fwd_ex(lib, **kw) == code
+
+
+def test_bwd_ex_rejects_d256_shapes_it_does_not_cover(lib):
+    def call(H, Hkv, Nq, Nk):
+        return lib.fa_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40,
+                             1, H, Hkv, Nq, Nk, 256, 0, 0.0625, 0, None)
+    assert call(4, 2, 128, 128) == _native.FA_ERR_UNSUPPORTED
+    assert call(4, 4, 128, 256) == _native.FA_ERR_UNSUPPORTED
+    assert call(4, 4, 200, 200) == _native.FA_ERR_UNSUPPORTED
+
+
+def test_flop_model_general_shapes(lib):
+    # 4 D FLOPs per visible (query, key) pair per query head: count the pairs
+    for Nq, Nk in ((1, 1), (3, 7), (100, 300), (128, 128)):
+        for causal in (0, 1):
+            pairs = sum(1 for i in range(Nq) for j in range(Nk) if not causal or j <= i + Nk - Nq)
+            assert lib.fa_fwd_ex_flops(2, 3, Nq, Nk, 64, causal) == pytest.approx(6 * 4 * 64 * pairs)
+            assert lib.fa_bwd_ex_flops(2, 3, Nq, Nk, 64, causal) == pytest.approx(2.5 * 6 * 4 * 64 * pairs)
 
 
 def test_flop_model(lib):
