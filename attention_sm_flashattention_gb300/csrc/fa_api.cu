@@ -107,35 +107,21 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace layout of fa_bwd: [delta | lse2 | dq_acc], each 256-byte aligned.
+// Workspace layout of fa_bwd: [delta | lse2], each [Z*H, Nq_pad] fp32 (query
+// rows padded to whole 128-row tiles) and 256-byte aligned.  Nothing else:
+// every dQ, dK and dV tile is accumulated on chip by the CTA that owns it.
 struct BwdWorkspace {
-  size_t delta_off, lse2_off, dq_off, total;
-  int grid;
+  size_t delta_off, lse2_off, total;
 };
 
-// Delta and lse2 are [Z*H, Nq_pad] (query rows padded to whole 128-row
-// tiles).  D <= 128 needs nothing else (the dQ kernel owns its tiles); D =
-// 256 also needs one fp32 N x D dQ accumulator per persistent CTA.
-BwdWorkspace bwd_workspace_layout(const Shape& sh, int sms) {
+BwdWorkspace bwd_workspace_layout(const Shape& sh) {
   BwdWorkspace w{};
-  const long long heads = sh.q_heads();
-  const size_t vec = round_up(static_cast<size_t>(heads) * sh.nq_pad() * sizeof(float), 256);
+  const size_t vec = round_up(static_cast<size_t>(sh.q_heads()) * sh.nq_pad() * sizeof(float), 256);
   w.delta_off = 0;
   w.lse2_off = vec;
-  w.dq_off = 2 * vec;
-  if (sh.D == 256) {
-    w.grid = static_cast<int>(heads < sms ? heads : sms);
-    w.total = 2 * vec + round_up(static_cast<size_t>(w.grid) * sh.Nq * sh.D * sizeof(float), 256);
-  } else {
-    w.grid = sms;
-    w.total = 2 * vec;
-  }
+  w.total = 2 * vec;
   return w;
 }
-
-// The D = 256 backward kernel covers equal lengths that are a multiple of
-// 128 and one K/V head per query head.
-bool d256_bwd_supported(const Shape& sh) { return sh.group() == 1 && sh.Nq == sh.Nk && sh.Nq % 128 == 0; }
 
 }  // namespace
 
@@ -145,8 +131,7 @@ const char* fa_error_string(int code) {
   switch (code) {
     case FA_OK: return "ok";
     case FA_ERR_INVALID_ARG: return "invalid argument (null/misaligned pointer, non-positive size, bad scale or causal flag)";
-    case FA_ERR_UNSUPPORTED: return "unsupported shape (D must be 64, 128 or 256; causal needs Nq <= Nk; Z*H*N < 2^31; "
-                                   "the D = 256 backward needs Nq == Nk, a multiple of 128, and Hkv == H)";
+    case FA_ERR_UNSUPPORTED: return "unsupported shape (D must be 64, 128 or 256; causal needs Nq <= Nk; Z*H*N < 2^31)";
     case FA_ERR_WORKSPACE: return "workspace missing or smaller than fa_bwd_workspace_size()";
     case FA_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
     case FA_ERR_DEVICE: return "current device is not a compute capability 10.3 (sm_103a) GPU";
@@ -246,10 +231,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
 size_t fa_bwd_ex_workspace_size(int Z, int H, int Hkv, int Nq, int Nk, int D, int causal) {
   const Shape sh{Z, H, Hkv, Nq, Nk, D, causal};
   if (check_shape(sh, 1.f) != FA_OK) return 0;
-  if (D == 256 && !d256_bwd_supported(sh)) return 0;
-  DevInfo* dev = nullptr;
-  if (current_device_info(&dev) != FA_OK) return 0;
-  return bwd_workspace_layout(sh, dev->sms).total;
+  return bwd_workspace_layout(sh).total;
 }
 
 size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal) {
@@ -267,23 +249,25 @@ int bwd_checks(const void* q, const void* k, const void* v, const void* o, const
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
     return FA_ERR_INVALID_ARG;
-  const int rc = check_shape(sh, scale);
-  if (rc != FA_OK) return rc;
-  if (sh.D == 256 && !d256_bwd_supported(sh)) return FA_ERR_UNSUPPORTED;
-  return FA_OK;
+  return check_shape(sh, scale);
 }
 
-// Tensor maps of a backward call: q, k, v, dout (box rows chosen by the
-// kernels' tiling), then the outputs dq, dk, dv (TMA stores of the D <= 128
-// kernels).
+// Tensor maps of a backward call (box rows chosen by the kernels' tiling):
+// [0] q, [1] k, [2] v, [3] dout, then the outputs [4] dq, [5] dk, [6] dv
+// (TMA stores of the D <= 128 kernels); for D = 256, [0] and [3] have the
+// dK/dV kernel's 64-row query tiles and [7] q, [8] k, [2] v the dQ kernel's
+// 128-row query tiles and 64-row key tiles.
+constexpr int kBwdMaps = 9;
 bool bwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
               void* dv, const Shape& sh, bool bf16) {
-  const int D = sh.D, bq = (D == 256) ? 64 : 128;
+  const int D = sh.D;
+  const int bq = (D == 256) ? 64 : 128, bv = (D == 256) ? 64 : 128;
   const long long hq = sh.q_heads(), hk = sh.kv_heads();
   return map16(&maps[0], q, hq, sh.Nq, D, bq, bf16) && map16(&maps[1], k, hk, sh.Nk, D, 128, bf16) &&
-         map16(&maps[2], v, hk, sh.Nk, D, 128, bf16) && map16(&maps[3], dout, hq, sh.Nq, D, bq, bf16) &&
+         map16(&maps[2], v, hk, sh.Nk, D, bv, bf16) && map16(&maps[3], dout, hq, sh.Nq, D, bq, bf16) &&
          map16(&maps[4], dq, hq, sh.Nq, D, 128, bf16) && map16(&maps[5], dk, hk, sh.Nk, D, 128, bf16) &&
-         map16(&maps[6], dv, hk, sh.Nk, D, 128, bf16);
+         map16(&maps[6], dv, hk, sh.Nk, D, 128, bf16) && map16(&maps[7], q, hq, sh.Nq, D, 128, bf16) &&
+         map16(&maps[8], k, hk, sh.Nk, D, 64, bf16);
 }
 
 void bwd_shape_params(fa::BwdParams& prm, const Shape& sh) {
@@ -293,7 +277,6 @@ void bwd_shape_params(fa::BwdParams& prm, const Shape& sh) {
   prm.Nk = sh.Nk;
   prm.Nq_pad = sh.nq_pad();
   prm.causal_off = sh.Nk - sh.Nq;
-  prm.N = sh.Nq;
 }
 
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -303,14 +286,15 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   if (rc != FA_OK) return rc;
   DevInfo* dev = nullptr;
   if ((rc = current_device_info(&dev)) != FA_OK) return rc;
-  const BwdWorkspace ws = bwd_workspace_layout(sh, dev->sms);
+  const BwdWorkspace ws = bwd_workspace_layout(sh);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < ws.total) return FA_ERR_WORKSPACE;
 
   const int D = sh.D;
-  CUtensorMap maps[7];
+  CUtensorMap maps[kBwdMaps];
   if (!bwd_maps(maps, q, k, v, dout, dq, dk, dv, sh, bf16)) return FA_ERR_CUDA;
   char* wsb = static_cast<char*>(workspace);
   fa::BwdParams prm{};
+  prm.v = static_cast<const __half*>(v);
   prm.o = static_cast<const __half*>(o);
   prm.dout = static_cast<const __half*>(dout);
   prm.lse = lse;
@@ -319,16 +303,15 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   prm.dv = static_cast<__half*>(dv);
   prm.delta = reinterpret_cast<float*>(wsb + ws.delta_off);
   prm.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
-  prm.dq_acc = reinterpret_cast<float*>(wsb + ws.dq_off);
   bwd_shape_params(prm, sh);
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
   prm.status = dev->status;
   const bool c = sh.causal != 0;
   switch (D) {
-    case 64: rc = fa::launch_bwd_d64(c, bf16, maps, prm, ws.grid, stream); break;
-    case 128: rc = fa::launch_bwd_d128(c, bf16, maps, prm, ws.grid, stream); break;
-    default: rc = fa::launch_bwd_d256(c, bf16, maps, prm, ws.grid, stream); break;
+    case 64: rc = fa::launch_bwd_d64(c, bf16, maps, prm, dev->sms, stream); break;
+    case 128: rc = fa::launch_bwd_d128(c, bf16, maps, prm, dev->sms, stream); break;
+    default: rc = fa::launch_bwd_d256(c, bf16, maps, prm, dev->sms, stream); break;
   }
   return rc == 0 ? FA_OK : (rc == -2 ? FA_ERR_UNSUPPORTED : FA_ERR_CUDA);
 }
@@ -413,46 +396,34 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   DevInfo* dev = nullptr;
   if ((rc = current_device_info(&dev)) != FA_OK) return rc;
 
-  // Scratch layout [delta | lse2 | dQ accumulators], as fa_bwd's workspace;
-  // for D = 256 the grid is cut to the accumulators that fit.
-  const long long heads = sh.q_heads();
-  const size_t vec = round_up(static_cast<size_t>(heads) * sh.nq_pad() * sizeof(float), 256);
-  long long grid = dev->sms;
-  if (D == 256) {
-    const size_t acc_one = round_up(static_cast<size_t>(N) * D * sizeof(float), 256);
-    if (2 * vec + acc_one > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
-    grid = static_cast<long long>((FA_NOALLOC_SCRATCH_BYTES - 2 * vec) / (static_cast<size_t>(N) * D * sizeof(float)));
-    if (grid > dev->sms) grid = dev->sms;
-    if (grid > heads) grid = heads;
-  } else if (2 * vec > FA_NOALLOC_SCRATCH_BYTES) {
-    return FA_ERR_SCRATCH_LIMIT;
-  }
+  // Scratch layout [delta | lse2], as fa_bwd's workspace.
+  const BwdWorkspace ws = bwd_workspace_layout(sh);
+  if (ws.total > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
 
   char* scratch = static_cast<char*>(noalloc_scratch_on_current_device());
   if (scratch == nullptr) return FA_ERR_CUDA;
 
-  CUtensorMap maps[7];
+  CUtensorMap maps[kBwdMaps];
   if (!bwd_maps(maps, q, k, v, dout, dq, dk, dv, sh, false)) return FA_ERR_CUDA;
   fa::BwdParams prm{};
+  prm.v = static_cast<const __half*>(v);
   prm.o = static_cast<const __half*>(o);
   prm.dout = static_cast<const __half*>(dout);
   prm.lse = lse;
   prm.dq = static_cast<__half*>(dq);
   prm.dk = static_cast<__half*>(dk);
   prm.dv = static_cast<__half*>(dv);
-  prm.delta = reinterpret_cast<float*>(scratch);
-  prm.lse2 = reinterpret_cast<float*>(scratch + vec);
-  prm.dq_acc = reinterpret_cast<float*>(scratch + 2 * vec);
+  prm.delta = reinterpret_cast<float*>(scratch + ws.delta_off);
+  prm.lse2 = reinterpret_cast<float*>(scratch + ws.lse2_off);
   bwd_shape_params(prm, sh);
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
   prm.status = dev->status;
   const bool c = causal != 0;
-  const int g = static_cast<int>(grid);
   switch (D) {
-    case 64: rc = fa::launch_bwd_d64(c, false, maps, prm, g, stream); break;
-    case 128: rc = fa::launch_bwd_d128(c, false, maps, prm, g, stream); break;
-    default: rc = fa::launch_bwd_d256(c, false, maps, prm, g, stream); break;
+    case 64: rc = fa::launch_bwd_d64(c, false, maps, prm, dev->sms, stream); break;
+    case 128: rc = fa::launch_bwd_d128(c, false, maps, prm, dev->sms, stream); break;
+    default: rc = fa::launch_bwd_d256(c, false, maps, prm, dev->sms, stream); break;
   }
   return rc == 0 ? FA_OK : FA_ERR_CUDA;
 }

@@ -26,6 +26,7 @@ struct FwdParams {
 };
 
 struct BwdParams {
+  const __half* v;     // [heads / group, Nk, D] (read directly by the D = 256 dK/dV kernel)
   const __half* o;     // [heads, Nq, D] forward output
   const __half* dout;  // [heads, Nq, D]
   const float* lse;    // [heads, Nq] natural-log lse from the forward
@@ -34,13 +35,11 @@ struct BwdParams {
   __half* dv;
   float* delta;        // workspace [heads, Nq_pad]: rowsum(O * dO), 0 in the padding
   float* lse2;         // workspace [heads, Nq_pad]: lse * log2(e), +inf in the padding
-  float* dq_acc;       // workspace [grid, N, D]: per-CTA fp32 dQ accumulator (D = 256 only)
   int heads;           // query heads
   int group;           // query heads per K/V head
   int Nq, Nk;
   int Nq_pad;          // Nq rounded up to the 128-row query tile
   int causal_off;      // Nk - Nq
-  int N;               // D = 256 kernel: the common length (Nq == Nk, a multiple of 128)
   float scale;         // softmax scale
   float scale_log2;    // scale * log2(e)
   int* status;
@@ -48,13 +47,12 @@ struct BwdParams {
 
 // One launcher per head dimension; `causal` and `bf16` (bf16 instead of
 // fp16 inputs and outputs) select the instantiation.  Return 0 on success.
-// For the backward, `grid` caps the persistent grid: for D = 256 it is the
-// number of per-CTA dQ accumulators in the workspace, for D <= 128 (no
-// accumulators) the SM count.  The tensor maps carry the element type.
+// For the backward, `grid` caps each persistent grid (the SM count).  The
+// tensor maps carry the element type.
 #define FA_DECLARE_LAUNCHERS(D)                                                                      \
   int launch_fwd_d##D(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm,       \
                       int num_sms, cudaStream_t stream);                                              \
-  /* bwd maps: q, k, v, dout, dq, dk, dv */                                                         \
+  /* bwd maps: q, k, v, dout, dq, dk, dv, q and k with the D = 256 dQ kernel's boxes */                                                         \
   int launch_bwd_d##D(bool causal, bool bf16, const CUtensorMap* maps, const BwdParams& prm,       \
                       int grid, cudaStream_t stream);
 

@@ -61,8 +61,7 @@ extern "C" {
 #define FA_OK 0
 #define FA_ERR_INVALID_ARG (-1) /* null pointer, a size <= 0, H not a multiple of Hkv, bad causal flag or
                                    dtype, non-finite or <= 0 scale, misaligned pointer */
-#define FA_ERR_UNSUPPORTED (-2) /* D not in {64, 128, 256}, causal with Nq > Nk, sizes past 32-bit indexing,
-                                   or a D = 256 backward with Nq != Nk, N % 128 != 0 or Hkv != H */
+#define FA_ERR_UNSUPPORTED (-2) /* D not in {64, 128, 256}, causal with Nq > Nk, or sizes past 32-bit indexing */
 #define FA_ERR_WORKSPACE (-3)   /* workspace null or smaller than fa_bwd_workspace_size() */
 #define FA_ERR_CUDA (-4)        /* a CUDA runtime call or kernel launch failed */
 #define FA_ERR_DEVICE (-5)      /* current device is not a compute capability 10.3 GPU */
@@ -88,12 +87,12 @@ FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* l
            int causal, float scale, cudaStream_t stream);
 
 /*
- * Bytes of device workspace fa_bwd (or fa_bwd_bf16) needs on the current
- * device: Delta and the log2-scaled lse (2 x Z*H*N' fp32, N' = N rounded up to
- * a multiple of 128); for D = 256 also
- * one fp32 N x D dQ accumulator per resident CTA.  It grows with Z*H*N (and
- * #SMs*N*D for D = 256), never with N^2 over all heads (§二, third rule).
- * Returns 0 for unsupported arguments.
+ * Bytes of device workspace fa_bwd (or fa_bwd_bf16) needs: Delta and the
+ * log2-scaled lse (2 x Z*H*N' fp32, N' = N rounded up to a multiple of 128,
+ * each vector rounded up to 256 bytes).  It grows with Z*H*N, never with N^2
+ * over all heads (§二, third rule): every dQ, dK and dV tile is accumulated
+ * on chip by the one CTA that writes it.  Returns 0 for unsupported
+ * arguments.
  */
 FA_API size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal);
 
@@ -150,8 +149,6 @@ FA_API int fa_bwd_bf16(const void* q, const void* k, const void* v, const void* 
  *            (otherwise some row would see no key): FA_ERR_UNSUPPORTED.
  *   dtype  : FA_DTYPE_F16 or FA_DTYPE_BF16, the element type of every
  *            [.., D] tensor (lse, Delta and accumulation stay fp32).
- *   The D = 256 backward currently needs Nq == Nk, a multiple of 128, and
- *   Hkv == H (FA_ERR_UNSUPPORTED otherwise); the forward has no such limit.
  * Layout, alignment, ownership, asynchrony and errors as for fa_fwd /
  * fa_bwd; workspace from fa_bwd_ex_workspace_size (0 = unsupported shape).
  * fa_fwd(q, k, v, o, lse, Z, H, N, D, c, s, st) is
@@ -179,16 +176,14 @@ FA_API int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o,
  *
  * It computes exactly what fa_bwd computes (same kernels, same arguments
  * without workspace/workspace_bytes, same outputs bit for bit), but the
- * scratch that fa_bwd takes from the caller (Delta, the log2-scaled lse and
- * the per-CTA fp32 dQ accumulators) lives in one static device buffer of
- * FA_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into libfa.so.  Every GPU on
- * which the library is used holds that buffer until the process exits.
+ * scratch that fa_bwd takes from the caller (Delta and the log2-scaled
+ * lse) lives in one static device buffer of FA_NOALLOC_SCRATCH_BYTES (64 MiB)
+ * compiled into libfa.so.  Every GPU on which the library is used holds that
+ * buffer until the process exits.
  *
- *   Limit  : 2*Z*H*N*4 bytes plus at least one N*D*4-byte dQ accumulator must
+ *   Limit  : fa_bwd_workspace_size(Z,H,N,D,causal) (about 8*Z*H*N bytes) must
  *            fit in the buffer; otherwise FA_ERR_SCRATCH_LIMIT is returned
- *            before anything is enqueued.  When the buffer holds fewer
- *            accumulators than the GPU has SMs, fewer persistent CTAs run
- *            (slower, same result).
+ *            before anything is enqueued.
  *   Set-up : the first call on a device (with that device current) looks up
  *            the buffer's device address; make that first call before any
  *            stream capture.

@@ -49,7 +49,15 @@ D256_FWD = [
     (1, 4, 2, 256, 256, 256),
     (1, 2, 2, 70, 333, 256),
 ]
-D256_BWD = [(1, 2, 2, 256, 256, 256), (2, 1, 1, 384, 384, 256)]
+D256_BWD = [
+    (1, 2, 2, 256, 256, 256),
+    (2, 1, 1, 384, 384, 256),
+    (1, 2, 2, 1, 1, 256),
+    (1, 2, 2, 100, 100, 256),
+    (1, 4, 2, 200, 333, 256),
+    (1, 4, 1, 130, 130, 256),
+    (1, 2, 2, 300, 70, 256),
+]
 
 
 def ident(s):
@@ -121,16 +129,13 @@ def test_d256_forward_general(shape, causal):
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", D256_BWD, ids=ident)
-def test_d256_backward_plain_shapes(shape, causal):
+def test_d256_backward_general(shape, causal):
     run_and_check(shape, causal)
 
 
-def test_d256_backward_general_shape_is_refused():
-    q, k, v, do = (t.cuda() for t in make_inputs(1, 4, 256, 256, 1, Hkv=2))
-    o, lse = api.fwd(q, k, v)
-    with pytest.raises(_native.FaError) as e:
-        api.bwd(q, k, v, o, do, lse)
-    assert e.value.code == _native.FA_ERR_UNSUPPORTED
+@pytest.mark.parametrize("causal", [False, True])
+def test_d256_backward_general_bf16(causal):
+    run_and_check((1, 4, 2, 200, 333, 256), causal, dtype=torch.bfloat16)
 
 
 def test_output_rows_past_the_end_are_untouched():
@@ -165,6 +170,7 @@ LARGE = [
     ("gqa_z16h32kv4n1024d128c", (16, 32, 4, 1024, 1024, 128), True),
     ("ragged_z32h8n1000d128", (32, 8, 8, 1000, 1000, 128), False),
     ("prefill_z8h16kv2q512k2048d64c", (8, 16, 2, 512, 2048, 64), True),
+    ("gqa_z8h16kv4n1000d256c", (8, 16, 4, 1000, 1000, 256), True),
 ]
 
 
