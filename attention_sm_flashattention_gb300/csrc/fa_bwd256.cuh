@@ -32,8 +32,9 @@
 //    i); 64-key tiles of K and V stream through rings:
 //      S = Q_i K_j^T, P = exp2(S * c - lse2), dP = dO_i V_j^T (dO_i in TMEM),
 //      dS = P * (dP - Delta) -> fp16 into TMEM over dP, dQ_i += dS K_j.
-//    TMEM: dO_i (128 columns), dQ_i (256), S (64), dP/dS (64).  Shared
-//    memory: Q_i (64 KB), three K stages and two V stages of 32 KB.
+//    TMEM: dO_i (128 columns), dQ_i (256), two 64-column regions that the
+//    key tiles use in turn (S, then dP over it, then dS).  Shared memory:
+//    Q_i (64 KB), three K stages and two V stages of 32 KB.
 // The compute warps write the TMEM-resident operand from global memory at the
 // start of a unit and write dK, dV and dQ (times the scale where §二 puts it)
 // straight from TMEM to global memory at the end.
@@ -61,7 +62,7 @@ struct B256 {
   static constexpr int A_SM_DL = A_SM_L2 + A_QS * 256;      // Delta[64] per dO stage
   static constexpr int A_SM_BAR = A_SM_DL + A_OS * 256;
   static constexpr int A_SMEM = A_SM_BAR + 256;
-  static constexpr int A_THREADS = 352;  // 8 compute warps, producer, two MMA warps
+  static constexpr int A_THREADS = 384;  // 8 compute warps, producer, three MMA warps
   static_assert(A_SMEM <= 232448, "dK/dV kernel shared memory budget");
   static_assert(A_R + 2 * A_BM <= 512, "dK/dV kernel TMEM budget");
   // ---- dQ kernel
@@ -72,13 +73,13 @@ struct B256 {
   static constexpr int B_QTILE = 4 * B_QSUB;    // 64 KB
   static constexpr int B_KTILE = 4 * B_KSUB;    // 32 KB
   static constexpr int B_KS = 3, B_VS = 2;
-  static constexpr int B_DO = 0, B_DQ = 128, B_S = 384, B_DP = 448;  // TMEM columns
+  static constexpr int B_DO = 0, B_DQ = 128, B_R = 384;  // TMEM columns; region r (S, then dP, then dS) at B_R + 64 r
   static constexpr int B_SM_Q = 0, B_SM_K = B_QTILE, B_SM_V = B_SM_K + B_KS * B_KTILE;
   static constexpr int B_SM_BAR = B_SM_V + B_VS * B_KTILE;
   static constexpr int B_SMEM = B_SM_BAR + 256;
-  static constexpr int B_THREADS = 384;  // 8 compute warps, two producers, two MMA warps
+  static constexpr int B_THREADS = 416;  // 8 compute warps, two producers, three MMA warps
   static_assert(B_SMEM <= 232448, "dQ kernel shared memory budget");
-  static_assert(B_DP + B_BN <= 512, "dQ kernel TMEM budget");
+  static_assert(B_R + 2 * B_BN <= 512, "dQ kernel TMEM budget");
 };
 
 // 128 16-bit values (256 bytes) of one row from global memory, as 64 packed
@@ -118,15 +119,15 @@ __device__ __forceinline__ void store_row32(uint32_t taddr, float mul, __half* d
 struct Bwd256ABars {
   uint64_t k_full, k_empty, v_full, v_free;
   uint64_t q_full[3], q_empty[3], o_full[2], o_empty[2];
-  uint64_t s_full, s_free, dp_full, p_full, ds_full, dk_done[2];
-  uint64_t dkv_full, dkv_free, mma_done[2];
+  uint64_t s_full[2], s_free, dp_full[2], p_full, ds_full, dk_done[2];  // [2]: per TMEM region
+  uint64_t dkv_full, dkv_free, mma_done[3];
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(Bwd256ABars) <= 256, "barrier area");
 
 template <bool CAUSAL, bool BF>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     fa_bwd256_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_do, const BwdParams prm) {
   using T = B256;
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(352, 1)
   }
   Bwd256ABars* bars = reinterpret_cast<Bwd256ABars*>(smem + T::A_SM_BAR);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, GRAD_MMA_WARP = 10;
+  constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, GRAD_MMA_WARP = 10, DP_MMA_WARP = 11;
   constexpr int QS = T::A_QS, OS = T::A_OS;
 
   if (threadIdx.x == 0) {
@@ -153,11 +154,11 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(&bars->o_full[i], 1);
       mbar_init(&bars->o_empty[i], 1);
       mbar_init(&bars->dk_done[i], 1);
-      mbar_init(&bars->mma_done[i], 1);
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->dp_full[i], 1);
     }
-    mbar_init(&bars->s_full, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&bars->mma_done[i], 1);
     mbar_init(&bars->s_free, T::NCOMPUTE);
-    mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_full, T::NCOMPUTE);
     mbar_init(&bars->ds_full, T::NCOMPUTE);
     mbar_init(&bars->dkv_full, 1);
@@ -233,26 +234,15 @@ __global__ void __launch_bounds__(352, 1)
       for (uint32_t i = (t > OS ? t - OS : 0); i < t; ++i) bwd2_drain(&bars->o_full[i % OS], (i / OS) & 1);
     }
   } else if (warp == MMA_WARP) {
-    // ----------------------------------- MMA warp: S^T = K Q^T, dP^T = V dO^T
+    // ------------------------------------------ MMA warp: S^T = K Q^T
+    // S^T(t) goes into region t % 2 as soon as that region is free (the dK
+    // MMA of tile t - 2 completed) and Q_t has landed: it runs ahead of the
+    // compute warps, independent of the dP^T issuer.
     constexpr uint32_t id_s = idesc_16<BF>(128, T::A_BM, false, false);  // M keys, N queries
     const uint32_t sb = smem_u32(smem);
     const uint64_t kdesc = sdesc_sw128(sb + T::A_SM_K, 16, 1024);
     uint32_t t = 0, kc = 0;
     bool ok = true;
-    // S^T(tile) into region tile % 2, free once the dK MMA of tile - 2 completed
-    auto issue_s = [&](uint32_t tile) -> bool {
-      const int qs = tile % QS, r = tile & 1;
-      if (!warp_wait(&bars->q_full[qs], (tile / QS) & 1, wc, 162)) return false;
-      if (tile >= 2 && !warp_wait(&bars->dk_done[r], ((tile - 2) >> 1) & 1, wc, 163)) return false;
-      tc_fence_after();
-      const uint64_t qdesc = sdesc_sw128(sb + T::A_SM_Q + qs * T::A_QTILE, 16, 1024);
-#pragma unroll
-      for (int kk = 0; kk < 16; ++kk)
-        mma_f16_ss_warp(tmem + T::A_R + r * T::A_BM, sdesc_add(kdesc, (kk / 4) * T::A_KSUB + (kk % 4) * 32),
-                        sdesc_add(qdesc, (kk / 4) * T::A_QSUB + (kk % 4) * 32), id_s, kk > 0 ? 1u : 0u);
-      mma_commit_warp(&bars->s_full);
-      return true;
-    };
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
       int kvh, ja, jb;
       bwd2_decode<CAUSAL>(u, nkv, kvh, ja, jb);
@@ -260,15 +250,46 @@ __global__ void __launch_bounds__(352, 1)
         const int j = half ? jb : ja;
         if (j < 0) break;
         if (!(ok = warp_wait(&bars->k_full, kc & 1, wc, 161))) break;
-        tc_fence_after();
-        if (!(ok = issue_s(t))) break;
         const int nx = G * (nqt - first_q(j));
         for (int h = 0; ok && h < 2; ++h) {
           for (int x = 0; x < nx; ++x) {
-            const bool last = (h == 1 && x == nx - 1);
+            const int qs = t % QS, r = t & 1;
+            if (!(ok = warp_wait(&bars->q_full[qs], (t / QS) & 1, wc, 162))) break;
+            if (t >= 2 && !(ok = warp_wait(&bars->dk_done[r], ((t - 2) >> 1) & 1, wc, 163))) break;
+            tc_fence_after();
+            const uint64_t qdesc = sdesc_sw128(sb + T::A_SM_Q + qs * T::A_QTILE, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+              mma_f16_ss_warp(tmem + T::A_R + r * T::A_BM, sdesc_add(kdesc, (kk / 4) * T::A_KSUB + (kk % 4) * 32),
+                              sdesc_add(qdesc, (kk / 4) * T::A_QSUB + (kk % 4) * 32), id_s, kk > 0 ? 1u : 0u);
+            mma_commit_warp(&bars->s_full[r]);
+            if (h == 1 && x == nx - 1) mma_commit_warp(&bars->k_empty);  // K_j is not read again
+            ++t;
+          }
+        }
+        ++kc;
+      }
+    }
+    mma_commit_warp(&bars->mma_done[0]);
+    bwd2_drain(&bars->mma_done[0], 0);
+  } else if (warp == DP_MMA_WARP) {
+    // ----------------------------------------- MMA warp: dP^T = V dO^T
+    // over S^T in the tile's region once the compute warps have read S^T;
+    // V_j must be in TMEM (first tile of the unit)
+    constexpr uint32_t id_s = idesc_16<BF>(128, T::A_BM, false, false);
+    const uint32_t sb = smem_u32(smem);
+    uint32_t t = 0, kc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      int kvh, ja, jb;
+      bwd2_decode<CAUSAL>(u, nkv, kvh, ja, jb);
+      for (int half = 0; ok && half < 2; ++half) {
+        const int j = half ? jb : ja;
+        if (j < 0) break;
+        const int nx = G * (nqt - first_q(j));
+        for (int h = 0; ok && h < 2; ++h) {
+          for (int x = 0; x < nx; ++x) {
             const int os = t % OS;
-            // dP^T over S^T in the tile's region once the compute warps have
-            // read S^T; V_j must be in TMEM (first tile of the unit)
             if (!(ok = warp_wait(&bars->o_full[os], (t / OS) & 1, wc, 164))) break;
             if (!(ok = warp_wait(&bars->s_free, t & 1, wc, 165))) break;
             if (h == 0 && x == 0 && !(ok = warp_wait(&bars->v_full, kc & 1, wc, 166))) break;
@@ -278,21 +299,16 @@ __global__ void __launch_bounds__(352, 1)
             for (int kk = 0; kk < 16; ++kk)
               mma_f16_ts_warp(tmem + T::A_R + (t & 1) * T::A_BM, tmem + T::A_V + kk * 8,
                               sdesc_add(odesc, (kk / 4) * T::A_QSUB + (kk % 4) * 32), id_s, kk > 0 ? 1u : 0u);
-            mma_commit_warp(&bars->dp_full);
-            if (last) {
-              mma_commit_warp(&bars->k_empty);  // K_j and V_j are not read again
-              mma_commit_warp(&bars->v_free);
-            } else if (!(ok = issue_s(t + 1))) {
-              break;
-            }
+            mma_commit_warp(&bars->dp_full[t & 1]);
+            if (h == 1 && x == nx - 1) mma_commit_warp(&bars->v_free);  // V_j is not read again
             ++t;
           }
         }
         ++kc;
       }
     }
-    mma_commit_warp(&bars->mma_done[0]);
-    bwd2_drain(&bars->mma_done[0], 0);
+    mma_commit_warp(&bars->mma_done[2]);
+    bwd2_drain(&bars->mma_done[2], 0);
   } else if (warp == GRAD_MMA_WARP) {
     // ------------------------- MMA warp: dV[:, h] += P^T dO, dK[:, h] += dS^T Q
     constexpr uint32_t id_g = idesc_16<BF>(128, 128, false, true);  // N = 128 columns of D, B MN-major
@@ -385,7 +401,8 @@ __global__ void __launch_bounds__(352, 1)
             // key k is hidden from query q iff k > q + coff
             const bool diag = CAUSAL && (j + 1) * T::A_BN - 1 > i * T::A_BM + coff;
             const int q0 = i * T::A_BM + wg * T::A_QC + coff;  // limit of this warpgroup's first query column
-            ok = mbar_wait(&bars->q_full[qs], (t / QS) & 1, wc, 171) && mbar_wait(&bars->s_full, t & 1, wc, 172);
+            ok = mbar_wait(&bars->q_full[qs], (t / QS) & 1, wc, 171) &&
+                 mbar_wait(&bars->s_full[t & 1], (t >> 1) & 1, wc, 172);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             uint32_t sr[T::A_QC];
@@ -421,7 +438,8 @@ __global__ void __launch_bounds__(352, 1)
             for (int c = 0; c < T::A_QC / 2; ++c) pk[c] = f2_to_pack2<BF>(p2[c]);
             // ---- P^T (16-bit) over the first half of this warpgroup's dP^T
             // columns, dS^T = P^T * (dP^T - Delta) over the second half
-            ok = mbar_wait(&bars->o_full[os], (t / OS) & 1, wc, 173) && mbar_wait(&bars->dp_full, t & 1, wc, 174);
+            ok = mbar_wait(&bars->o_full[os], (t / OS) & 1, wc, 173) &&
+                 mbar_wait(&bars->dp_full[t & 1], (t >> 1) & 1, wc, 174);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             tmem_ld32(rb, sr);
@@ -481,15 +499,15 @@ struct Bwd256BBars {
   uint64_t q_full, q_empty;
   uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
   uint64_t do_full, do_free;
-  uint64_t s_full, s_free, dp_full, ds_full, dq_done;
-  uint64_t dq_full, dq_free, mma_done[2];
+  uint64_t s_full[2], s_free, dp_full[2], ds_full[2], dq_done[2];  // [2]: per TMEM region
+  uint64_t dq_full, dq_free, mma_done[3];
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(Bwd256BBars) <= 256, "barrier area");
 
 template <bool CAUSAL, bool BF>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(416, 1)
     fa_bwd256_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const BwdParams prm) {
   using T = B256;
@@ -500,7 +518,7 @@ __global__ void __launch_bounds__(384, 1)
   }
   Bwd256BBars* bars = reinterpret_cast<Bwd256BBars*>(smem + T::B_SM_BAR);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, V_PRODUCER_WARP = 10, DQ_MMA_WARP = 11;
+  constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, V_PRODUCER_WARP = 10, DQ_MMA_WARP = 11, DP_MMA_WARP = 12;
   constexpr int KS = T::B_KS, VS = T::B_VS;
 
   if (threadIdx.x == 0) {
@@ -513,15 +531,15 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
-      mbar_init(&bars->mma_done[i], 1);
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->dp_full[i], 1);
+      mbar_init(&bars->ds_full[i], T::NCOMPUTE);
+      mbar_init(&bars->dq_done[i], 1);
     }
+    for (int i = 0; i < 3; ++i) mbar_init(&bars->mma_done[i], 1);
     mbar_init(&bars->do_full, T::NCOMPUTE);
     mbar_init(&bars->do_free, 1);
-    mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, T::NCOMPUTE);
-    mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->ds_full, T::NCOMPUTE);
-    mbar_init(&bars->dq_done, 1);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, T::NCOMPUTE);
     bars->abort_flag = 0;
@@ -614,27 +632,14 @@ __global__ void __launch_bounds__(384, 1)
       for (uint32_t i = (v_it > VS ? v_it - VS : 0); i < v_it; ++i) bwd2_drain(&bars->v_full[i % VS], (i / VS) & 1);
     }
   } else if (warp == MMA_WARP) {
-    // ------------------------------------------- MMA warp: S = Q K^T, dP = dO V^T
+    // --------------------------------------------- MMA warp: S = Q K^T
+    // S(t) goes into region t % 2 once that region is free (the dQ MMA of
+    // tile t - 2 read its dS) and K_t has landed.
     constexpr uint32_t id_s = idesc_16<BF>(128, T::B_BN, false, false);  // M queries, N keys
     const uint32_t sb = smem_u32(smem);
     const uint64_t qdesc = sdesc_sw128(sb + T::B_SM_Q, 16, 1024);
-    uint32_t t = 0, k_it = 0, v_it = 0, qc = 0;
+    uint32_t t = 0, k_it = 0, qc = 0;
     bool ok = true;
-    // S(tile) from K stage `kidx`; the S buffer is free once the compute
-    // warps have read the previous tile's S
-    auto issue_s = [&](uint32_t tile, uint32_t kidx) -> bool {
-      const int ks = kidx % KS;
-      if (!warp_wait(&bars->k_full[ks], (kidx / KS) & 1, wc, 191)) return false;
-      if (tile >= 1 && !warp_wait(&bars->s_free, (tile - 1) & 1, wc, 192)) return false;
-      tc_fence_after();
-      const uint64_t kdesc = sdesc_sw128(sb + T::B_SM_K + ks * T::B_KTILE, 16, 1024);
-#pragma unroll
-      for (int kk = 0; kk < 16; ++kk)
-        mma_f16_ss_warp(tmem + T::B_S, sdesc_add(qdesc, (kk / 4) * T::B_QSUB + (kk % 4) * 32),
-                        sdesc_add(kdesc, (kk / 4) * T::B_KSUB + (kk % 4) * 32), id_s, kk > 0 ? 1u : 0u);
-      mma_commit_warp(&bars->s_full);
-      return true;
-    };
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
       int head, ia, ib;
       bwd2_decode<CAUSAL>(u, nqt, head, ia, ib);
@@ -643,39 +648,63 @@ __global__ void __launch_bounds__(384, 1)
         if (i < 0) break;
         const int nj = num_kv(i);
         if (!(ok = warp_wait(&bars->q_full, qc & 1, wc, 193))) break;
-        tc_fence_after();
-        if (!(ok = issue_s(t, k_it))) break;
         for (int j = 0; j < nj; ++j) {
-          const bool last = (j == nj - 1);
-          const int vs = v_it % VS;
-          // dP = dO V^T into the dP region, which holds dS of tile t - 1 until
-          // that tile's dQ MMA has read it; dO_i must be in TMEM
-          if (!(ok = warp_wait(&bars->v_full[vs], (v_it / VS) & 1, wc, 194))) break;
-          if (t >= 1 && !(ok = warp_wait(&bars->dq_done, (t - 1) & 1, wc, 195))) break;
-          if (j == 0 && !(ok = warp_wait(&bars->do_full, qc & 1, wc, 196))) break;
+          const int ks = k_it % KS, r = t & 1;
+          if (!(ok = warp_wait(&bars->k_full[ks], (k_it / KS) & 1, wc, 191))) break;
+          if (t >= 2 && !(ok = warp_wait(&bars->dq_done[r], ((t - 2) >> 1) & 1, wc, 192))) break;
           tc_fence_after();
-          const uint64_t vdesc = sdesc_sw128(sb + T::B_SM_V + vs * T::B_KTILE, 16, 1024);
+          const uint64_t kdesc = sdesc_sw128(sb + T::B_SM_K + ks * T::B_KTILE, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < 16; ++kk)
-            mma_f16_ts_warp(tmem + T::B_DP, tmem + T::B_DO + kk * 8,
-                            sdesc_add(vdesc, (kk / 4) * T::B_KSUB + (kk % 4) * 32), id_s, kk > 0 ? 1u : 0u);
-          mma_commit_warp(&bars->dp_full);
-          mma_commit_warp(&bars->v_empty[vs]);
-          if (last) {
-            mma_commit_warp(&bars->q_empty);  // Q_i and dO_i are not read again
-            mma_commit_warp(&bars->do_free);
-          } else if (!(ok = issue_s(t + 1, k_it + 1))) {
-            break;
-          }
+            mma_f16_ss_warp(tmem + T::B_R + r * T::B_BN, sdesc_add(qdesc, (kk / 4) * T::B_QSUB + (kk % 4) * 32),
+                            sdesc_add(kdesc, (kk / 4) * T::B_KSUB + (kk % 4) * 32), id_s, kk > 0 ? 1u : 0u);
+          mma_commit_warp(&bars->s_full[r]);
+          if (j == nj - 1) mma_commit_warp(&bars->q_empty);  // Q_i is not read again
           ++t;
           ++k_it;
-          ++v_it;
         }
         ++qc;
       }
     }
     mma_commit_warp(&bars->mma_done[0]);
     bwd2_drain(&bars->mma_done[0], 0);
+  } else if (warp == DP_MMA_WARP) {
+    // -------------------------------------------- MMA warp: dP = dO V^T
+    // over S in the tile's region once the compute warps have read S; dO_i
+    // must be in TMEM (first tile of the item)
+    constexpr uint32_t id_s = idesc_16<BF>(128, T::B_BN, false, false);
+    const uint32_t sb = smem_u32(smem);
+    uint32_t t = 0, v_it = 0, qc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      int head, ia, ib;
+      bwd2_decode<CAUSAL>(u, nqt, head, ia, ib);
+      for (int half = 0; ok && half < 2; ++half) {
+        const int i = half ? ib : ia;
+        if (i < 0) break;
+        const int nj = num_kv(i);
+        for (int j = 0; j < nj; ++j) {
+          const int vs = v_it % VS;
+          if (!(ok = warp_wait(&bars->v_full[vs], (v_it / VS) & 1, wc, 194))) break;
+          if (!(ok = warp_wait(&bars->s_free, t & 1, wc, 195))) break;
+          if (j == 0 && !(ok = warp_wait(&bars->do_full, qc & 1, wc, 196))) break;
+          tc_fence_after();
+          const uint64_t vdesc = sdesc_sw128(sb + T::B_SM_V + vs * T::B_KTILE, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk)
+            mma_f16_ts_warp(tmem + T::B_R + (t & 1) * T::B_BN, tmem + T::B_DO + kk * 8,
+                            sdesc_add(vdesc, (kk / 4) * T::B_KSUB + (kk % 4) * 32), id_s, kk > 0 ? 1u : 0u);
+          mma_commit_warp(&bars->dp_full[t & 1]);
+          mma_commit_warp(&bars->v_empty[vs]);
+          if (j == nj - 1) mma_commit_warp(&bars->do_free);  // dO_i is not read again
+          ++t;
+          ++v_it;
+        }
+        ++qc;
+      }
+    }
+    mma_commit_warp(&bars->mma_done[2]);
+    bwd2_drain(&bars->mma_done[2], 0);
   } else if (warp == DQ_MMA_WARP) {
     // ------------------------------------------------- MMA warp: dQ += dS K
     constexpr uint32_t id_q = idesc_16<BF>(128, T::D, false, true);  // N = 256, B = K MN-major
@@ -695,15 +724,15 @@ __global__ void __launch_bounds__(384, 1)
           // the first tile overwrites dQ, which the previous item's write-out
           // must have read
           if (first && qc > 0 && !(ok = warp_wait(&bars->dq_free, (qc - 1) & 1, wc, 197))) break;
-          if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 198))) break;
+          if (!(ok = warp_wait(&bars->ds_full[t & 1], (t >> 1) & 1, wc, 198))) break;
           tc_fence_after();
           const uint64_t kdesc_mn = sdesc_sw128(sb + T::B_SM_K + ks * T::B_KTILE, T::B_KSUB, 1024);
 #pragma unroll
           for (int kk = 0; kk < T::B_BN / 16; ++kk) {
-            const uint32_t a_t = tmem + T::B_DP + (kk / 2) * T::B_KC + (kk % 2) * 8;
+            const uint32_t a_t = tmem + T::B_R + (t & 1) * T::B_BN + (kk / 2) * T::B_KC + (kk % 2) * 8;
             mma_f16_ts_warp(tmem + T::B_DQ, a_t, sdesc_add(kdesc_mn, kk * 2048), id_q, (first && kk == 0) ? 0u : 1u);
           }
-          mma_commit_warp(&bars->dq_done);
+          mma_commit_warp(&bars->dq_done[t & 1]);
           if (last) mma_commit_warp(&bars->dq_full);
           // K_j is free: S of the tile completed before ds_full
           mma_commit_warp(&bars->k_empty[ks]);
@@ -755,11 +784,12 @@ __global__ void __launch_bounds__(384, 1)
         }
         for (int j = 0; j < num_kv(i); ++j) {
           const int k0 = j * T::B_BN + wg * T::B_KC;  // first key column of this warpgroup
-          ok = mbar_wait(&bars->s_full, t & 1, wc, 201);
+          const uint32_t rb = lb + T::B_R + (t & 1) * T::B_BN + wg * T::B_KC;  // this warpgroup's columns
+          ok = mbar_wait(&bars->s_full[t & 1], (t >> 1) & 1, wc, 201);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
           uint32_t sr[T::B_KC];
-          tmem_ld32(lb + T::B_S + wg * T::B_KC, sr);
+          tmem_ld32(rb, sr);
           tmem_wait_ld();
           reg_fence<T::B_KC>(sr);
           tc_fence_before();
@@ -779,21 +809,20 @@ __global__ void __launch_bounds__(384, 1)
             p2[c / 2] = f2_pack(p0, p1);
           }
           // ---- dS = P * (dP - Delta), 16-bit into TMEM over dP
-          ok = mbar_wait(&bars->dp_full, t & 1, wc, 202);
+          ok = mbar_wait(&bars->dp_full[t & 1], (t >> 1) & 1, wc, 202);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t dpc = lb + T::B_DP + wg * T::B_KC;
-          tmem_ld32(dpc, sr);
+          tmem_ld32(rb, sr);
           tmem_wait_ld();
           reg_fence<T::B_KC>(sr);
           uint32_t pk[T::B_KC / 2];
 #pragma unroll
           for (int c = 0; c < T::B_KC; c += 2)
             pk[c / 2] = f2_to_pack2<BF>(f2_mul(p2[c / 2], f2_add(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), nd2)));
-          tmem_st16(dpc, pk);
+          tmem_st16(rb, pk);
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(&bars->ds_full);
+          mbar_arrive(&bars->ds_full[t & 1]);
           ++t;
         }
         if (!ok) break;
