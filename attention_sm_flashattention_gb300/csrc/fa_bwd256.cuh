@@ -36,8 +36,9 @@
 //    key tiles use in turn (S, then dP over it, then dS).  Shared memory:
 //    Q_i (64 KB), three K stages and two V stages of 32 KB.
 // The compute warps write the TMEM-resident operand from global memory at the
-// start of a unit and write dK, dV and dQ (times the scale where §二 puts it)
-// straight from TMEM to global memory at the end.
+// start of a unit, and at its end stage dK, dV and dQ (times the scale where
+// §二 puts it) as 16-bit tiles in ring slots that the last tile no longer
+// needs, which a TMA store writes out.
 #pragma once
 
 #include "fa_bwd.cuh"
@@ -96,10 +97,12 @@ __device__ __forceinline__ void load_row128(const __half* src, bool live, uint32
   }
 }
 
-// 32 fp32 TMEM columns of this thread's row, times `mul`, to 32 16-bit values
-// in global memory (64 bytes, 16-byte aligned).
+// 32 fp32 TMEM columns of this thread's row, times `mul`, as 16-bit values
+// into row `row`, columns col0..col0+31, of a [128 x 128] staging tile in
+// shared memory laid out as two 128-byte-swizzled [128 x 64] boxes (what a
+// TMA store of 64 x 128 boxes reads).  A 32-KB ring slot holds one tile.
 template <bool BF>
-__device__ __forceinline__ void store_row32(uint32_t taddr, float mul, __half* dst, bool live) {
+__device__ __forceinline__ void stage_tmem32(uint32_t taddr, float mul, uint32_t tile, int row, int col0) {
   uint32_t v[32];
   tmem_ld32(taddr, v);
   tmem_wait_ld();
@@ -107,11 +110,7 @@ __device__ __forceinline__ void store_row32(uint32_t taddr, float mul, __half* d
   uint32_t h[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) h[e] = pack2<BF>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-  if (live) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) d4[e] = make_uint4(h[4 * e], h[4 * e + 1], h[4 * e + 2], h[4 * e + 3]);
-  }
+  stage_row32(tile, row, col0, h);
 }
 
 // ===================================================================== dK, dV
@@ -121,6 +120,7 @@ struct Bwd256ABars {
   uint64_t q_full[3], q_empty[3], o_full[2], o_empty[2];
   uint64_t s_full[2], s_free, dp_full[2], p_full, ds_full, dk_done[2];  // [2]: per TMEM region
   uint64_t dkv_full, dkv_free, mma_done[3];
+  uint64_t epi_full;  // dK and dV halves staged in the last tile's Q and dO slots
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -129,7 +129,8 @@ static_assert(sizeof(Bwd256ABars) <= 256, "barrier area");
 template <bool CAUSAL, bool BF>
 __global__ void __launch_bounds__(384, 1)
     fa_bwd256_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_do, const BwdParams prm) {
+                          const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dk,
+                          const __grid_constant__ CUtensorMap tm_dv, const BwdParams prm) {
   using T = B256;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bars->p_full, T::NCOMPUTE);
     mbar_init(&bars->ds_full, T::NCOMPUTE);
     mbar_init(&bars->dkv_full, 1);
+    mbar_init(&bars->epi_full, T::NCOMPUTE);
     mbar_init(&bars->dkv_free, T::NCOMPUTE);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -174,6 +176,9 @@ __global__ void __launch_bounds__(384, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_do);
+  } else if (warp == GRAD_MMA_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_dk);
+    tma_prefetch_desc(&tm_dv);
   }
   tc_fence_before();
   __syncthreads();
@@ -311,10 +316,34 @@ __global__ void __launch_bounds__(384, 1)
     bwd2_drain(&bars->mma_done[2], 0);
   } else if (warp == GRAD_MMA_WARP) {
     // ------------------------- MMA warp: dV[:, h] += P^T dO, dK[:, h] += dS^T Q
+    // It also writes out each half's dK and dV, which the compute warps stage
+    // in the Q and dO slots of the half's last tile: before the first MMA of
+    // the next half (which needs the compute warps' next P^T anyway) and at
+    // the end.
     constexpr uint32_t id_g = idesc_16<BF>(128, 128, false, true);  // N = 128 columns of D, B MN-major
     const uint32_t sb = smem_u32(smem);
     uint32_t t = 0, sc = 0;
+    int p_kvh = 0, p_j = 0, p_h = 0;  // the previous half (kvh, key tile, D half)
     bool ok = true;
+    // store the staged tiles of half `sc - 1` (last tile t - 1), then release its slots
+    auto store_prev = [&]() -> bool {
+      if (!warp_wait(&bars->epi_full, (sc - 1) & 1, wc, 158)) return false;
+      if (lane == 0) {
+        const int qs = (t - 1) % QS, os = (t - 1) % OS;
+        for (int s2 = 0; s2 < 2; ++s2) {
+          tma_store_3d(&tm_dk, smem + T::A_SM_Q + qs * T::A_QTILE + s2 * 16384, p_h * 128 + s2 * 64, p_j * T::A_BN,
+                       p_kvh);
+          tma_store_3d(&tm_dv, smem + T::A_SM_DO + os * T::A_QTILE + s2 * 16384, p_h * 128 + s2 * 64, p_j * T::A_BN,
+                       p_kvh);
+        }
+        bulk_commit();
+        bulk_wait_read<0>();
+        mbar_arrive(&bars->q_empty[qs]);
+        mbar_arrive(&bars->o_empty[os]);
+      }
+      __syncwarp();
+      return true;
+    };
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
       int kvh, ja, jb;
       bwd2_decode<CAUSAL>(u, nkv, kvh, ja, jb);
@@ -325,13 +354,16 @@ __global__ void __launch_bounds__(384, 1)
         for (int h = 0; ok && h < 2; ++h) {
           for (int x = 0; x < nx; ++x) {
             const bool first = (x == 0), last = (x == nx - 1);
+            // the first tile of a half overwrites the accumulators, which the
+            // previous half's write-out must have read
+            if (first && sc > 0) {
+              if (!(ok = warp_wait(&bars->dkv_free, (sc - 1) & 1, wc, 167))) break;
+              if (!(ok = store_prev())) break;
+            }
             const int qs = t % QS, os = t % OS;
             // columns [128 h, 128 h + 128) of the Q / dO tile: sub-tiles 2h, 2h + 1
             const uint64_t qdesc_mn = sdesc_sw128(sb + T::A_SM_Q + qs * T::A_QTILE + 2 * h * T::A_QSUB, T::A_QSUB, 1024);
             const uint64_t odesc_mn = sdesc_sw128(sb + T::A_SM_DO + os * T::A_QTILE + 2 * h * T::A_QSUB, T::A_QSUB, 1024);
-            // the first tile of a half overwrites the accumulators, which the
-            // previous half's write-out must have read
-            if (first && sc > 0 && !(ok = warp_wait(&bars->dkv_free, (sc - 1) & 1, wc, 167))) break;
             if (!(ok = warp_wait(&bars->o_full[os], (t / OS) & 1, wc, 160))) break;
             if (!(ok = warp_wait(&bars->p_full, t & 1, wc, 168))) break;
             tc_fence_after();
@@ -340,8 +372,9 @@ __global__ void __launch_bounds__(384, 1)
               const uint32_t a_t = tmem + T::A_R + (t & 1) * T::A_BM + (kk / 2) * T::A_QC + (kk % 2) * 8;
               mma_f16_ts_warp(tmem + T::A_DV, a_t, sdesc_add(odesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
             }
-            // dO_i is free: dP^T of the tile completed before p_full
-            mma_commit_warp(&bars->o_empty[os]);
+            // dO_i is free: dP^T of the tile completed before p_full (the
+            // half's last slot receives dV and is released after its store)
+            if (!last) mma_commit_warp(&bars->o_empty[os]);
             if (!(ok = warp_wait(&bars->q_full[qs], (t / QS) & 1, wc, 159))) break;
             if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 169))) break;
             tc_fence_after();
@@ -351,15 +384,23 @@ __global__ void __launch_bounds__(384, 1)
               mma_f16_ts_warp(tmem + T::A_DK, a_t, sdesc_add(qdesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
             }
             mma_commit_warp(&bars->dk_done[t & 1]);
-            if (last) mma_commit_warp(&bars->dkv_full);
-            // Q_i is free: S^T of the tile completed before p_full
-            mma_commit_warp(&bars->q_empty[qs]);
+            if (last) {
+              mma_commit_warp(&bars->dkv_full);  // the Q slot receives dK; released after its store
+            } else {
+              mma_commit_warp(&bars->q_empty[qs]);  // S^T of the tile completed before p_full
+            }
             ++t;
           }
+          p_kvh = kvh;
+          p_j = j;
+          p_h = h;
           ++sc;
         }
       }
     }
+    if (ok && sc > 0) store_prev();
+    if (lane == 0) bulk_wait<0>();  // all stores complete before the CTA exits
+    __syncwarp();
     mma_commit_warp(&bars->mma_done[1]);
     bwd2_drain(&bars->mma_done[1], 0);
   } else if (warp < 8) {
@@ -466,18 +507,23 @@ __global__ void __launch_bounds__(384, 1)
             ++t;
           }
           if (!ok) break;
-          // ---- dV_j[:, h] and dK_j[:, h] (times scale) straight to global
+          // ---- dV_j[:, h] and dK_j[:, h] (times scale) -> 16-bit, staged in
+          // the dO and Q slots of the half's last tile; the store warp writes
+          // them out (rows past Nk are dropped by the TMA store)
           ok = mbar_wait(&bars->dkv_full, sc & 1, wc, 175);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
-          const int col0 = h * 128 + wg * 64;  // this thread's 64 columns of D
+          const uint32_t st_dv = smem_u32(smem + T::A_SM_DO + ((t - 1) % OS) * T::A_QTILE);
+          const uint32_t st_dk = smem_u32(smem + T::A_SM_Q + ((t - 1) % QS) * T::A_QTILE);
 #pragma unroll 1
           for (int c = 0; c < 64; c += 32) {
-            store_row32<BF>(lb + T::A_DV + wg * 64 + c, 1.f, prm.dv + kv_row * T::D + col0 + c, key_live);
-            store_row32<BF>(lb + T::A_DK + wg * 64 + c, prm.scale, prm.dk + kv_row * T::D + col0 + c, key_live);
+            stage_tmem32<BF>(lb + T::A_DV + wg * 64 + c, 1.f, st_dv, row, wg * 64 + c);
+            stage_tmem32<BF>(lb + T::A_DK + wg * 64 + c, prm.scale, st_dk, row, wg * 64 + c);
           }
+          fence_proxy_async_smem();
           tc_fence_before();
           mbar_arrive(&bars->dkv_free);
+          mbar_arrive(&bars->epi_full);
           ++sc;
         }
         ++kc;
@@ -501,6 +547,7 @@ struct Bwd256BBars {
   uint64_t do_full, do_free;
   uint64_t s_full[2], s_free, dp_full[2], ds_full[2], dq_done[2];  // [2]: per TMEM region
   uint64_t dq_full, dq_free, mma_done[3];
+  uint64_t epi_full;  // dQ_i staged in the last tile's K and V slots
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -509,7 +556,8 @@ static_assert(sizeof(Bwd256BBars) <= 256, "barrier area");
 template <bool CAUSAL, bool BF>
 __global__ void __launch_bounds__(416, 1)
     fa_bwd256_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const BwdParams prm) {
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dq,
+                        const BwdParams prm) {
   using T = B256;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
@@ -541,6 +589,7 @@ __global__ void __launch_bounds__(416, 1)
     mbar_init(&bars->do_free, 1);
     mbar_init(&bars->s_free, T::NCOMPUTE);
     mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->epi_full, T::NCOMPUTE);
     mbar_init(&bars->dq_free, T::NCOMPUTE);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -553,6 +602,8 @@ __global__ void __launch_bounds__(416, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+  } else if (warp == DQ_MMA_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -695,8 +746,11 @@ __global__ void __launch_bounds__(416, 1)
             mma_f16_ts_warp(tmem + T::B_R + (t & 1) * T::B_BN, tmem + T::B_DO + kk * 8,
                             sdesc_add(vdesc, (kk / 4) * T::B_KSUB + (kk % 4) * 32), id_s, kk > 0 ? 1u : 0u);
           mma_commit_warp(&bars->dp_full[t & 1]);
-          mma_commit_warp(&bars->v_empty[vs]);
-          if (j == nj - 1) mma_commit_warp(&bars->do_free);  // dO_i is not read again
+          if (j == nj - 1) {
+            mma_commit_warp(&bars->do_free);  // dO_i is not read again
+          } else {
+            mma_commit_warp(&bars->v_empty[vs]);  // the item's last V slot receives half of dQ_i
+          }
           ++t;
           ++v_it;
         }
@@ -733,15 +787,36 @@ __global__ void __launch_bounds__(416, 1)
             mma_f16_ts_warp(tmem + T::B_DQ, a_t, sdesc_add(kdesc_mn, kk * 2048), id_q, (first && kk == 0) ? 0u : 1u);
           }
           mma_commit_warp(&bars->dq_done[t & 1]);
-          if (last) mma_commit_warp(&bars->dq_full);
-          // K_j is free: S of the tile completed before ds_full
-          mma_commit_warp(&bars->k_empty[ks]);
+          if (last) {
+            mma_commit_warp(&bars->dq_full);  // the K slot receives half of dQ_i
+          } else {
+            mma_commit_warp(&bars->k_empty[ks]);  // S of the tile completed before ds_full
+          }
           ++t;
           ++k_it;
         }
+        if (!ok) break;
+        // the compute warps stage dQ_i in the K and V slots of the item's
+        // last tile (columns 0-127 and 128-255); store it with TMA, then
+        // release both slots
+        if (!(ok = warp_wait(&bars->epi_full, qc & 1, wc, 199))) break;
+        if (lane == 0) {
+          const int kl = (t - 1) % KS, vl = (t - 1) % VS;  // one K and one V stage per tile
+          for (int s = 0; s < 2; ++s) {
+            tma_store_3d(&tm_dq, smem + T::B_SM_K + kl * T::B_KTILE + s * 16384, s * 64, i * T::B_BM, head);
+            tma_store_3d(&tm_dq, smem + T::B_SM_V + vl * T::B_KTILE + s * 16384, 128 + s * 64, i * T::B_BM, head);
+          }
+          bulk_commit();
+          bulk_wait_read<0>();
+          mbar_arrive(&bars->k_empty[kl]);
+          mbar_arrive(&bars->v_empty[vl]);
+        }
+        __syncwarp();
         ++qc;
       }
     }
+    if (lane == 0) bulk_wait<0>();  // all stores complete before the CTA exits
+    __syncwarp();
     mma_commit_warp(&bars->mma_done[1]);
     bwd2_drain(&bars->mma_done[1], 0);
   } else {
@@ -826,15 +901,21 @@ __global__ void __launch_bounds__(416, 1)
           ++t;
         }
         if (!ok) break;
-        // ---- dQ_i (times scale) straight to global
+        // ---- dQ_i (times scale) -> 16-bit, staged in the K slot (columns
+        // 0-127, warpgroup 0) and the V slot (128-255, warpgroup 1) of the
+        // item's last tile; the dQ MMA warp writes it out (rows past Nq are
+        // dropped by the TMA store)
         ok = mbar_wait(&bars->dq_full, qc & 1, wc, 203);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t st_q = smem_u32(smem + (wg == 0 ? T::B_SM_K + ((t - 1) % KS) * T::B_KTILE
+                                                       : T::B_SM_V + ((t - 1) % VS) * T::B_KTILE));
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 32)
-          store_row32<BF>(lb + T::B_DQ + wg * 128 + c, prm.scale, prm.dq + q_row * T::D + wg * 128 + c, q_live);
+        for (int c = 0; c < 128; c += 32) stage_tmem32<BF>(lb + T::B_DQ + wg * 128 + c, prm.scale, st_q, row, c);
+        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bars->dq_free);
+        mbar_arrive(&bars->epi_full);
         ++qc;
       }
     }
@@ -871,10 +952,10 @@ int launch_bwd256(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, c
   };
   const int nkv = (prm.Nk + T::A_BN - 1) / T::A_BN, nqt = (prm.Nq + T::B_BM - 1) / T::B_BM;
   fa_bwd256_dkdv_kernel<CAUSAL, BF><<<grid_for(prm.heads / prm.group, nkv), T::A_THREADS, T::A_SMEM, stream>>>(
-      maps[0], maps[1], maps[3], prm);
+      maps[0], maps[1], maps[3], maps[5], maps[6], prm);
   if (cudaGetLastError() != cudaSuccess) return -1;
-  fa_bwd256_dq_kernel<CAUSAL, BF><<<grid_for(prm.heads, nqt), T::B_THREADS, T::B_SMEM, stream>>>(maps[7], maps[8],
-                                                                                                 maps[2], prm);
+  fa_bwd256_dq_kernel<CAUSAL, BF><<<grid_for(prm.heads, nqt), T::B_THREADS, T::B_SMEM, stream>>>(
+      maps[7], maps[8], maps[2], maps[4], prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
