@@ -84,17 +84,39 @@ struct B256 {
 };
 
 // 128 16-bit values (256 bytes) of one row from global memory, as 64 packed
-// words in column order; zeros past the end of the matrix.
+// words in column order; zeros past the end of the matrix.  32-byte loads
+// (one whole sector each) when the row is 32-byte aligned -- rows are 512
+// bytes apart, so that is a property of the tensor's base address and the
+// same for every thread -- else 16-byte loads.
 __device__ __forceinline__ void load_row128(const __half* src, bool live, uint32_t* w) {
-  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  if (!live) {
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    const uint4 x = live ? __ldg(s4 + e) : make_uint4(0u, 0u, 0u, 0u);
-    w[4 * e] = x.x;
-    w[4 * e + 1] = x.y;
-    w[4 * e + 2] = x.z;
-    w[4 * e + 3] = x.w;
+    for (int k = 0; k < 64; ++k) w[k] = 0u;
+  } else if ((reinterpret_cast<uintptr_t>(src) & 31u) == 0) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                   : "=r"(w[8 * e]), "=r"(w[8 * e + 1]), "=r"(w[8 * e + 2]), "=r"(w[8 * e + 3]), "=r"(w[8 * e + 4]),
+                     "=r"(w[8 * e + 5]), "=r"(w[8 * e + 6]), "=r"(w[8 * e + 7])
+                   : "l"(src + 16 * e));
+  } else {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const uint4 x = __ldg(s4 + e);
+      w[4 * e] = x.x;
+      w[4 * e + 1] = x.y;
+      w[4 * e + 2] = x.z;
+      w[4 * e + 3] = x.w;
+    }
   }
+}
+
+// Ask L2 to fetch the 256 bytes at `p` (two 128-byte lines) ahead of a
+// load_row128 of them.
+__device__ __forceinline__ void prefetch_row128(const __half* p) {
+  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p + 64));
 }
 
 // 32 fp32 TMEM columns of this thread's row, times `mul`, as 16-bit values
@@ -435,6 +457,18 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive(&bars->v_full);
         }
         const int i0 = first_q(j), nqi = nqt - i0;
+        {
+          // the CTA's next key tile: its V rows into L2 while this one runs
+          int nkvh = kvh, nj = -1;
+          if (half == 0 && jb >= 0) {
+            nj = jb;
+          } else if (u + static_cast<int>(gridDim.x) < units) {
+            int nb;
+            bwd2_decode<CAUSAL>(u + gridDim.x, nkv, nkvh, nj, nb);
+          }
+          if (nj >= 0 && nj * T::A_BN + row < Nk)
+            prefetch_row128(prm.v + (static_cast<size_t>(nkvh) * Nk + nj * T::A_BN + row) * T::D + wg * 128);
+        }
         for (int h = 0; ok && h < 2; ++h) {
           for (int x = 0; x < G * nqi; ++x) {
             const int i = i0 + x % nqi;
@@ -856,6 +890,24 @@ __global__ void __launch_bounds__(416, 1)
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->do_full);
+        }
+        {
+          // the CTA's next item: its dO rows into L2 while this one runs
+          int nhead = head, ni = -1;
+          if (half == 0 && ib >= 0) {
+            ni = ib;
+          } else if (u + static_cast<int>(gridDim.x) < units) {
+            int nb;
+            bwd2_decode<CAUSAL>(u + gridDim.x, nqt, nhead, ni, nb);
+          }
+          if (ni >= 0 && ni * T::B_BM + row < Nq) {
+            prefetch_row128(prm.dout + (static_cast<size_t>(nhead) * Nq + ni * T::B_BM + row) * T::D + wg * 128);
+            if (wg == 0 && lane == 0) {  // one line of lse2 and of Delta covers this warp's 32 rows
+              const size_t nrow = static_cast<size_t>(nhead) * Nq_pad + ni * T::B_BM + row;
+              asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(prm.lse2 + nrow));
+              asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(prm.delta + nrow));
+            }
+          }
         }
         for (int j = 0; j < num_kv(i); ++j) {
           const int k0 = j * T::B_BN + wg * T::B_KC;  // first key column of this warpgroup

@@ -197,3 +197,27 @@ def test_large_general_shapes_sampled_heads(name, shape, causal):
     for i, kvh in enumerate(kv_heads):
         assert rel_fro(dkf[kvh], dk_ref[i]) <= GRAD_RTOL, (name, "dk", kvh)
         assert rel_fro(dvf[kvh], dv_ref[i]) <= GRAD_RTOL, (name, "dv", kvh)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_d256_backward_inputs_only_16_byte_aligned(causal):
+    # V and dO are read row by row by the D = 256 backward; views that start
+    # 16 bytes into an allocation are 16- but not 32-byte aligned.
+    Z, H, Hkv, Nq, Nk, D = 1, 4, 2, 200, 333, 256
+    q, k, v, do = make_inputs(Z, H, Nq, D, 9700 + int(causal), Hkv=Hkv, Nk=Nk)
+    scale = 1 / math.sqrt(D)
+
+    def shifted(t):
+        buf = torch.empty(t.numel() + 8, dtype=t.dtype, device="cuda")
+        view = buf[8:].view(t.shape)
+        view.copy_(t.cuda())
+        assert view.data_ptr() % 32 == 16
+        return view
+
+    qd, kd = q.cuda(), k.cuda()
+    vd, dod = shifted(v), shifted(do)
+    o, lse = api.fwd(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = api.bwd(qd, kd, vd, o, dod, lse, causal=causal, scale=scale)
+    assert api.device_status() == 0
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), orc.attn_bwd_ref(q, k, v, do, causal, scale)):
+        assert rel_fro(g, r) <= GRAD_RTOL, name
