@@ -269,13 +269,13 @@ def reduce_max(vals, world):
 def bwd_kernel_names(d, causal):
     c = str(bool(causal)).lower()
     if d == 256:
-        return f"fa_bwd call: fa_bwd_prep_kernel<{d}> + fa_bwd_kernel<{d},{c}>"
+        return f"fa_bwd call: fa_bwd_prep_kernel<{d}> + fa_bwd256_dkdv_kernel<{c}> + fa_bwd256_dq_kernel<{c}>"
     return f"fa_bwd call: fa_bwd_prep_kernel<{d}> + fa_bwd_dkdv_kernel<{d},{c}> + fa_bwd_dq_kernel<{d},{c}>"
 
 
 def bwd_launches(d):
-    """Kernels one fa_bwd call launches (Delta preprocess + main kernel(s))."""
-    return 2 if d == 256 else 3
+    """Kernels one fa_bwd call launches (Delta preprocess, dK/dV kernel, dQ kernel)."""
+    return 3
 
 
 def load_traffic():
