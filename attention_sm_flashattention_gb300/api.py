@@ -80,6 +80,44 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
     return o, lse
 
 
+def fwd_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+              context_lens: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
+              out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
+              stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Attention forward over a paged K/V cache.  q [B,H,Nq,D]; k_cache,
+    v_cache [num_pages, page_size, Hkv, D] (q's dtype); block_table int32
+    [B, max_pages] (sequence b's key p is in page block_table[b, p //
+    page_size]); context_lens int32 [B].  Causal: the queries are the last
+    Nq of each sequence's context.  Returns ``(o, lse)`` like :func:`fwd`."""
+    _check_input("q", q)
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _check_input(name, t, q.dtype)
+    B, H, Nq, D = q.shape
+    num_pages, page_size, Hkv, Dk = k_cache.shape
+    if Dk != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache must be [num_pages, page_size, Hkv, D] with q's D")
+    if H % Hkv != 0:
+        raise ValueError(f"q's {H} heads are not a multiple of the cache's {Hkv} heads")
+    for name, t in (("block_table", block_table), ("context_lens", context_lens)):
+        if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    if block_table.dim() != 2 or block_table.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_table must be [B, max_pages] and context_lens [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+    rc = _native.lib().fa_fwd_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+                                    context_lens.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, Nq, D,
+                                    num_pages, page_size, block_table.shape[1], int(bool(causal)), float(scale),
+                                    _dtype_code(q), _stream_handle(stream))
+    _native.check(rc, "fa_fwd_paged")
+    return o, lse
+
+
 def bwd_workspace_size(Z: int, H: int, N: int, D: int, causal: bool, Hkv: Optional[int] = None,
                        Nk: Optional[int] = None) -> int:
     """Workspace bytes of a backward call; N is the query length."""

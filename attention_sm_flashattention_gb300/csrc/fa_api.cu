@@ -222,6 +222,64 @@ int fa_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse
   return fwd_impl(q, k, v, o, lse, square(Z, H, N, D, causal), scale, stream, true);
 }
 
+int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                 const int* context_lens, void* o, float* lse, int B, int H, int Hkv, int Nq, int D, int num_pages,
+                 int page_size, int max_pages, int causal, float scale, int dtype, cudaStream_t stream) {
+  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(block_table, 4) || !aligned(context_lens, 4))
+    return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || Hkv <= 0 || Nq <= 0 || num_pages <= 0 || page_size <= 0 || max_pages <= 0)
+    return FA_ERR_INVALID_ARG;
+  if (H % Hkv != 0 || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  // a key tile is a whole number of pages, each a whole number of 8-row swizzle atoms
+  if ((page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) || page_size > fa::fwd_block_n(D))
+    return FA_ERR_UNSUPPORTED;
+  const long long nq_pad = (Nq + 127LL) / 128 * 128;
+  if (static_cast<long long>(B) * H * nq_pad >= (1LL << 31) || static_cast<long long>(max_pages) * page_size >= (1LL << 31) ||
+      static_cast<long long>(B) * max_pages >= (1LL << 31))
+    return FA_ERR_UNSUPPORTED;
+  DevInfo* dev = nullptr;
+  int rc = current_device_info(&dev);
+  if (rc != FA_OK) return rc;
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  const auto et = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap maps[4];  // q, k cache, v cache, o
+  std::memset(&maps[1], 0, sizeof(CUtensorMap));
+  std::memset(&maps[2], 0, sizeof(CUtensorMap));
+  if (!map16(&maps[0], q, static_cast<long long>(B) * H, Nq, D, 128, bf16) ||
+      !fa::make_tmap_paged(&maps[1], k_cache, et, 2, num_pages, page_size, Hkv, D, 64, true) ||
+      !fa::make_tmap_paged(&maps[2], v_cache, et, 2, num_pages, page_size, Hkv, D, 64, true) ||
+      !map16(&maps[3], o, static_cast<long long>(B) * H, Nq, D, 128, bf16))
+    return FA_ERR_CUDA;
+  fa::FwdParams prm{};
+  prm.o = static_cast<__half*>(o);
+  prm.lse = lse;
+  prm.heads = B * H;
+  prm.group = H / Hkv;
+  prm.Nq = Nq;
+  prm.Nk = max_pages * page_size;  // per sequence: context_lens[b], clamped
+  prm.causal_off = 0;
+  prm.scale_log2 = scale * kLog2e;
+  prm.status = dev->status;
+  prm.block_table = block_table;
+  prm.context_lens = context_lens;
+  prm.H = H;
+  prm.num_pages = num_pages;
+  prm.page_size = page_size;
+  prm.max_pages = max_pages;
+  const bool c = causal != 0;
+  switch (D) {
+    case 64: rc = fa::launch_fwd_paged_d64(c, bf16, maps, prm, dev->sms, stream); break;
+    case 128: rc = fa::launch_fwd_paged_d128(c, bf16, maps, prm, dev->sms, stream); break;
+    default: rc = fa::launch_fwd_paged_d256(c, bf16, maps, prm, dev->sms, stream); break;
+  }
+  return rc == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int Hkv, int Nq,
               int Nk, int D, int causal, float scale, int dtype, cudaStream_t stream) {
   if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;

@@ -150,6 +150,24 @@ __device__ __forceinline__ int fwd_key_limit(int qi, int Nk, int off) {
   return CAUSAL ? min(qi + off, Nk - 1) : Nk - 1;
 }
 
+// Key count, causal offset and key-tile count of the work items of query
+// head `head`: the call's Nk, or (paged cache) its sequence's context length
+// clamped to [causal ? Nq : 1, max_pages * page_size].
+template <int D, bool CAUSAL, bool PAGED>
+struct FwdItemShape {
+  int nk, off, nkv_full;
+  __device__ __forceinline__ FwdItemShape(const FwdParams& prm, int head) {
+    int n = prm.Nk;
+    if (PAGED) {
+      n = __ldg(prm.context_lens + head / prm.H);
+      n = min(max(n, CAUSAL ? prm.Nq : 1), prm.max_pages * prm.page_size);
+    }
+    nk = n;
+    off = n - prm.Nq;
+    nkv_full = (n + FwdTraits<D, CAUSAL>::BN - 1) / FwdTraits<D, CAUSAL>::BN;
+  }
+};
+
 // Bounded wait that ignores the abort flag: used only while draining at exit.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
@@ -162,19 +180,18 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // The CTA's tiles in the order it processes them: work items (query tiles)
 // in schedule order, the key tiles of each item in order.  Global tile index
 // `tile` also indexes the K and V rings, which hold one tile per key tile.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool PAGED>
 struct FwdCursor {
   int u, half, head, qt, qb, j, nkv;
   uint32_t item, tile;
   bool valid;
   int units, nqt, nkv_full, Nk, off;
+  const FwdParams* prm;
 
-  __device__ void start(int first_unit, int units_, int nqt_, int nkv_full_, int Nk_, int off_) {
+  __device__ void start(int first_unit, int units_, int nqt_, const FwdParams* prm_) {
     units = units_;
     nqt = nqt_;
-    nkv_full = nkv_full_;
-    Nk = Nk_;
-    off = off_;
+    prm = prm_;
     item = 0;
     tile = 0;
     j = 0;
@@ -187,6 +204,10 @@ struct FwdCursor {
     if (!valid) return;
     int qa;
     fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+    const FwdItemShape<D, CAUSAL, PAGED> sh(*prm, head);
+    Nk = sh.nk;
+    off = sh.off;
+    nkv_full = sh.nkv_full;
     qt = qa;
     half = 0;
     nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
@@ -207,7 +228,31 @@ struct FwdCursor {
   }
 };
 
-template <int D, bool CAUSAL, bool BF>
+// One K or V tile (BN keys, tile j of query head `head`) from the paged
+// cache: BN / page_size boxes per 64-column sub-tile, box p going to rows
+// [p * page_size, (p + 1) * page_size) of the sub-tile (page_size is a
+// multiple of 8, so every box starts on a 1024-byte swizzle atom).  Pages
+// wholly past the sequence's key count get an out-of-range page coordinate,
+// which TMA fills with zeros; so does a block-table entry outside [0,
+// num_pages).  Every box counts its full size towards the barrier.
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void fwd_load_paged_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
+                                                    const FwdParams& prm, int head, int j, int nk, uint64_t pol) {
+  using T = FwdTraits<D, CAUSAL>;
+  const int ps = prm.page_size;
+  const int ppt = T::BN / ps;                  // pages per tile
+  const int b = head / prm.H, kvh = (head % prm.H) / prm.group;
+  const int lp0 = j * (T::BN / ps);            // first logical page of the tile
+  const int* row = prm.block_table + static_cast<size_t>(b) * prm.max_pages;
+  for (int pg = 0; pg < ppt; ++pg) {
+    const int lp = lp0 + pg;
+    const int page = (lp * ps < nk) ? __ldg(row + lp) : prm.num_pages;
+    for (int s = 0; s < T::DSUB; ++s)
+      tma_load_4d_hint(dst + s * T::KV_SUB + pg * ps * 128, map, bar, s * 64, kvh, 0, page, pol);
+  }
+}
+
+template <int D, bool CAUSAL, bool BF, bool PAGED>
 __global__ void __launch_bounds__(512, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -266,9 +311,8 @@ __global__ void __launch_bounds__(512, 1)
   tc_fence_after();
   const WaitCtx wc{prm.status, &bars->abort_flag};
   const uint32_t tmem = bars->tmem_base;
-  const int Nq = prm.Nq, Nk = prm.Nk, off = prm.causal_off;
+  const int Nq = prm.Nq;
   const int nqt = (Nq + T::BM - 1) / T::BM;
-  const int nkv_full = (Nk + T::BN - 1) / T::BN;
   const int units = fwd_num_units<CAUSAL>(prm.heads, nqt);
 
   if (warp < 8) {
@@ -287,10 +331,12 @@ __global__ void __launch_bounds__(512, 1)
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         int head, qa, qb;
         fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+        const FwdItemShape<D, CAUSAL, PAGED> sh(prm, head);
+        const int Nk = sh.nk, off = sh.off;
         for (int half = 0; ok && half < 2; ++half) {
           const int qt = half ? qb : qa;
           if (qt < 0) break;
-          const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
+          const int nkv = fwd_num_kv<D, CAUSAL>(qt, sh.nkv_full, Nk, off);
           const int qi = qt * T::BM + r;  // query index within the head
           const int lim = fwd_key_limit<CAUSAL>(qi, Nk, off);             // this row's last key
           const int lim_lo = fwd_key_limit<CAUSAL>(qt * T::BM, Nk, off);  // the tile's smallest limit
@@ -439,6 +485,7 @@ __global__ void __launch_bounds__(512, 1)
         for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
           int head, qa, qb;
           fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+          const FwdItemShape<D, CAUSAL, PAGED> sh(prm, head);
           for (int half = 0; ok && half < 2; ++half) {
             const int qt = half ? qb : qa;
             if (qt < 0) break;
@@ -449,15 +496,19 @@ __global__ void __launch_bounds__(512, 1)
             for (int s = 0; s < T::DSUB; ++s)
               tma_load_3d_hint(sq + s * T::Q_SUB, &tm_q, &bars->q_full[qs], s * 64, qt * T::BM, head, pol_q);
             ++q_it;
-            const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
+            const int nkv = fwd_num_kv<D, CAUSAL>(qt, sh.nkv_full, sh.nk, sh.off);
             for (int j = 0; j < nkv; ++j) {
               const int st = k_it % T::K_STAGES;
               if (!(ok = mbar_wait(&bars->k_empty[st], ((k_it / T::K_STAGES) & 1) ^ 1, wc, 2))) break;
               uint8_t* sk = smem + T::SM_K + st * T::KV_BYTES;
               mbar_arrive_expect_tx(&bars->k_full[st], T::KV_BYTES);
-              for (int s = 0; s < T::DSUB; ++s)
-                tma_load_3d_hint(sk + s * T::KV_SUB, &tm_k, &bars->k_full[st], s * 64, j * T::BN, head / prm.group,
-                                 pol_kv);
+              if (PAGED) {
+                fwd_load_paged_tile<D, CAUSAL>(sk, &tm_k, &bars->k_full[st], prm, head, j, sh.nk, pol_kv);
+              } else {
+                for (int s = 0; s < T::DSUB; ++s)
+                  tma_load_3d_hint(sk + s * T::KV_SUB, &tm_k, &bars->k_full[st], s * 64, j * T::BN, head / prm.group,
+                                   pol_kv);
+              }
               ++k_it;
             }
           }
@@ -477,18 +528,23 @@ __global__ void __launch_bounds__(512, 1)
         for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
           int head, qa, qb;
           fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+          const FwdItemShape<D, CAUSAL, PAGED> sh(prm, head);
           for (int half = 0; ok && half < 2; ++half) {
             const int qt = half ? qb : qa;
             if (qt < 0) break;
-            const int nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
+            const int nkv = fwd_num_kv<D, CAUSAL>(qt, sh.nkv_full, sh.nk, sh.off);
             for (int j = 0; j < nkv; ++j) {
               const int st = v_it % T::V_STAGES;
               if (!(ok = mbar_wait(&bars->v_empty[st], ((v_it / T::V_STAGES) & 1) ^ 1, wc, 8))) break;
               uint8_t* sv = smem + T::SM_V + st * T::KV_BYTES;
               mbar_arrive_expect_tx(&bars->v_full[st], T::KV_BYTES);
-              for (int s = 0; s < T::DSUB; ++s)
-                tma_load_3d_hint(sv + s * T::KV_SUB, &tm_v, &bars->v_full[st], s * 64, j * T::BN, head / prm.group,
-                                 pol_kv);
+              if (PAGED) {
+                fwd_load_paged_tile<D, CAUSAL>(sv, &tm_v, &bars->v_full[st], prm, head, j, sh.nk, pol_kv);
+              } else {
+                for (int s = 0; s < T::DSUB; ++s)
+                  tma_load_3d_hint(sv + s * T::KV_SUB, &tm_v, &bars->v_full[st], s * 64, j * T::BN, head / prm.group,
+                                   pol_kv);
+              }
               ++v_it;
             }
           }
@@ -506,7 +562,7 @@ __global__ void __launch_bounds__(512, 1)
 
       // S = Q K^T of the cursor's tile into S buffer tile % 2, which the
       // softmax of tile - 2 has read by then.
-      auto issue_s = [&](const FwdCursor<D, CAUSAL>& c) -> bool {
+      auto issue_s = [&](const FwdCursor<D, CAUSAL, PAGED>& c) -> bool {
         const int qs = c.item % T::Q_STAGES;
         const int st = c.tile % T::K_STAGES;
         const int b = c.tile & 1;
@@ -529,7 +585,7 @@ __global__ void __launch_bounds__(512, 1)
 
       // O += P V of the cursor's tile; the first tile of an item overwrites O,
       // which the previous item's epilogue must have read.
-      auto issue_pv = [&](const FwdCursor<D, CAUSAL>& c) -> bool {
+      auto issue_pv = [&](const FwdCursor<D, CAUSAL, PAGED>& c) -> bool {
         const int b = c.tile & 1;
         const int st = c.tile % T::V_STAGES;
         const bool first = (c.j == 0);
@@ -537,6 +593,20 @@ __global__ void __launch_bounds__(512, 1)
         if (!warp_wait(&bars->p_full[b], (c.tile >> 1) & 1, wc, 11)) return false;
         if (!warp_wait(&bars->v_full[st], (c.tile / T::V_STAGES) & 1, wc, 12)) return false;
         tc_fence_after();
+        if (PAGED && (c.j + 1) * T::BN > c.Nk) {
+          // Rows of the sequence's last page past its key count hold whatever
+          // the cache holds there; P is 0 for them, but 0 * NaN is NaN, so
+          // zero those V rows before P V reads them.  (Each row is the same
+          // 128 bytes of its sub-tile under the 128-byte swizzle.)
+          const int valid = c.Nk - c.j * T::BN;
+          const uint32_t sv = smem_u32(smem + T::SM_V + st * T::KV_BYTES);
+          for (int idx = lane; idx < (T::BN - valid) * 8 * T::DSUB; idx += 32) {
+            const int row = valid + idx / (8 * T::DSUB), rem = idx % (8 * T::DSUB);
+            st_shared_v4(sv + (rem / 8) * T::KV_SUB + row * 128 + (rem % 8) * 16, 0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
         const uint64_t vdesc = sdesc_sw128(sbase + T::SM_V + st * T::KV_BYTES, T::KV_SUB, 1024);
   #pragma unroll
         for (int kk = 0; kk < T::BN / 16; ++kk) {
@@ -557,8 +627,8 @@ __global__ void __launch_bounds__(512, 1)
       // two tiles ahead of the softmax, across work items; warp 15 issues
       // P V as each tile's P becomes ready.  Neither waits behind the
       // other's dependencies.
-      FwdCursor<D, CAUSAL> c;
-      c.start(blockIdx.x, units, nqt, nkv_full, Nk, off);
+      FwdCursor<D, CAUSAL, PAGED> c;
+      c.start(blockIdx.x, units, nqt, &prm);
       const bool s_side = (warp == T::MMA_WARP);
       while (ok && c.valid) {
         ok = s_side ? issue_s(c) : issue_pv(c);
@@ -582,10 +652,11 @@ __global__ void __launch_bounds__(512, 1)
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         int head, qa, qb;
         fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+        const FwdItemShape<D, CAUSAL, PAGED> sh(prm, head);
         for (int half = 0; ok && half < 2; ++half) {
           const int qt = half ? qb : qa;
           if (qt < 0) break;
-          t += fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
+          t += fwd_num_kv<D, CAUSAL>(qt, sh.nkv_full, sh.nk, sh.off);
           ok = mbar_wait(&bars->lm_full, q_item & 1, wc, 17);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           const float l_row = lm[r] + lm[T::BM + r];
@@ -651,19 +722,19 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BF>
+template <int D, bool CAUSAL, bool BF, bool PAGED = false>
 int launch_fwd(const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaStream_t stream) {
   using T = FwdTraits<D, CAUSAL>;
   static bool attr_set = false;  // per process; the attribute is per function, not per device
   if (!attr_set) {
-    if (cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL, BF, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              T::SMEM_ALLOC) != cudaSuccess)
       return -1;
     // the kernel splits its launch registers between warpgroups
     // (setmaxnreg); refuse to launch if the build gave it fewer than the
     // split needs, rather than let the raising warpgroups wait forever
     cudaFuncAttributes fa_attr;
-    if (cudaFuncGetAttributes(&fa_attr, fa_fwd_kernel<D, CAUSAL, BF>) != cudaSuccess ||
+    if (cudaFuncGetAttributes(&fa_attr, fa_fwd_kernel<D, CAUSAL, BF, PAGED>) != cudaSuccess ||
         fa_attr.numRegs * T::THREADS < T::SOFTMAX_THREADS * T::SOFTMAX_REGS + (T::THREADS - T::SOFTMAX_THREADS) * T::OTHER_REGS)
       return -1;
     attr_set = true;
@@ -671,7 +742,8 @@ int launch_fwd(const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaS
   const int nqt = (prm.Nq + T::BM - 1) / T::BM;
   const int units = CAUSAL ? prm.heads * ((nqt + 1) / 2) : prm.heads * nqt;
   const int grid = units < num_sms ? units : num_sms;
-  fa_fwd_kernel<D, CAUSAL, BF><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  fa_fwd_kernel<D, CAUSAL, BF, PAGED><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3],
+                                                                                  prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

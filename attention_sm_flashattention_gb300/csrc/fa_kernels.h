@@ -23,6 +23,16 @@ struct FwdParams {
   int causal_off;    // Nk - Nq
   float scale_log2;  // scale * log2(e)
   int* status;       // device status word
+  // Paged K/V cache (paged launchers only).  K and V are [num_pages,
+  // page_size, Hkv, D]; query head h of sequence b = head / H reads K/V head
+  // (head % H) / group of its cache pages; sequence b's key p lives in page
+  // block_table[b * max_pages + p / page_size] at row p % page_size, and its
+  // key count is context_lens[b], clamped to [causal ? Nq : 1, max_pages *
+  // page_size].
+  const int* block_table;
+  const int* context_lens;
+  int H;             // query heads per sequence
+  int num_pages, page_size, max_pages;
 };
 
 struct BwdParams {
@@ -60,6 +70,15 @@ FA_DECLARE_LAUNCHERS(64)
 FA_DECLARE_LAUNCHERS(128)
 FA_DECLARE_LAUNCHERS(256)
 #undef FA_DECLARE_LAUNCHERS
+
+// Forward over a paged K/V cache; maps: q, k cache, v cache (4-D, one page
+// row block per box), o.
+int launch_fwd_paged_d64(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,
+                         cudaStream_t stream);
+int launch_fwd_paged_d128(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,
+                          cudaStream_t stream);
+int launch_fwd_paged_d256(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,
+                          cudaStream_t stream);
 
 // Tile sizes the host needs to build tensor maps and size grids.
 inline int fwd_block_n(int D) { return D == 256 ? 64 : 128; }

@@ -61,4 +61,25 @@ inline bool make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType
   return r == CUDA_SUCCESS;
 }
 
+// Paged cache [pages, page_rows, heads, cols] of `elem_bytes`-byte elements,
+// as a 4-D tensor (cols, heads, page_rows, pages); boxes of box_cols x 1
+// head x page_rows rows x 1 page, so one box is one head's rows of one page
+// and lands in shared memory as a [page_rows x box_cols] tile.
+inline bool make_tmap_paged(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
+                            uint64_t pages, uint64_t page_rows, uint64_t heads, uint64_t cols, uint32_t box_cols,
+                            bool swizzle128) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const uint64_t eb = static_cast<uint64_t>(elem_bytes);
+  cuuint64_t dims[4] = {cols, heads, page_rows, pages};
+  cuuint64_t strides[3] = {cols * eb, heads * cols * eb, page_rows * heads * cols * eb};
+  cuuint32_t box[4] = {box_cols, 1, static_cast<cuuint32_t>(page_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, dtype, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace fa

@@ -75,3 +75,34 @@ def make_inputs(Z: int, H: int, N: int, D: int, seed: int, device="cpu", dtype=t
 
 def workload_inputs(w: Workload, device="cpu"):
     return make_inputs(w.Z, w.H, w.N, w.D, w.seed, device=device)
+
+
+def make_paged_inputs(B: int, H: int, Hkv: int, Nq: int, context_lens, D: int, page_size: int, seed: int,
+                      spare_pages: int = 3, device="cpu", dtype=torch.float16):
+    """Draw a paged-cache problem from ``seed``: ``(q, k_cache, v_cache,
+    block_table, context_lens)``.
+
+    q is ``[B, H, Nq, D]``; the caches are ``[num_pages, page_size, Hkv, D]``
+    with every slot drawn (slots past a context length hold values too);
+    sequence b owns ceil(context_lens[b] / page_size) pages, taken from a
+    random permutation of all pages (``spare_pages`` more than needed), and
+    its block-table row is padded with -1 to the longest sequence.  Draw
+    order: q, k_cache, v_cache, page permutation.
+    """
+    lens = [int(x) for x in context_lens]
+    need = [(n + page_size - 1) // page_size for n in lens]
+    num_pages = sum(need) + spare_pages
+    max_pages = max(need)
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    q = torch.randn((B, H, Nq, D), generator=g, dtype=torch.float32).to(dtype)
+    kc = torch.randn((num_pages, page_size, Hkv, D), generator=g, dtype=torch.float32).to(dtype)
+    vc = torch.randn((num_pages, page_size, Hkv, D), generator=g, dtype=torch.float32).to(dtype)
+    perm = torch.randperm(num_pages, generator=g)
+    table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    pos = 0
+    for b in range(B):
+        table[b, :need[b]] = perm[pos:pos + need[b]].to(torch.int32)
+        pos += need[b]
+    cl = torch.tensor(lens, dtype=torch.int32)
+    out = (q, kc, vc, table, cl)
+    return out if device == "cpu" else tuple(t.to(device) for t in out)

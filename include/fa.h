@@ -159,6 +159,40 @@ FA_API int fa_bwd_bf16(const void* q, const void* k, const void* v, const void* 
 FA_API int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int Hkv, int Nq,
                      int Nk, int D, int causal, float scale, int dtype, cudaStream_t stream);
 
+/*
+ * Forward over a paged K/V cache.  Source: «把 FlashAttention 搬上昇腾», the
+ * contest section's ReshapeAndCache and GQA Paged Attention parts: the cache
+ * is kept in physical blocks ("pages") of page_size tokens (token slot s in
+ * page s / page_size, row s % page_size); block_tables maps each sequence's
+ * logical blocks to physical ones; context_lens gives each sequence's real
+ * length and the invalid tokens of its last block are masked; query heads
+ * share K/V heads as in fa_fwd_ex.
+ *
+ *   q, o         : [B, H, Nq, D] (dtype), contiguous, 16-byte aligned.
+ *   lse          : fp32 [B, H, Nq].
+ *   k_cache,
+ *   v_cache      : [num_pages, page_size, Hkv, D] (dtype), 16-byte aligned.
+ *   block_table  : int32 [B, max_pages], device memory: sequence b's key p
+ *                  is in page block_table[b * max_pages + p / page_size].
+ *                  Entries outside [0, num_pages) read as zero keys/values
+ *                  (never out of bounds).
+ *   context_lens : int32 [B], device memory: sequence b attends to its first
+ *                  context_lens[b] keys, clamped to [causal ? Nq : 1,
+ *                  max_pages * page_size].
+ *   causal       : the Nq queries are the last Nq of the sequence's
+ *                  context_lens[b] tokens (query i sees key p iff p <= i +
+ *                  context_lens[b] - Nq).
+ *   page_size    : 16, 32, 64 or 128, and at most 64 when D = 256.
+ * Returns FA_OK (enqueued), FA_ERR_INVALID_ARG (null / misaligned pointer,
+ * a size <= 0, H % Hkv != 0, bad dtype / causal / scale),
+ * FA_ERR_UNSUPPORTED (D or page_size not supported, sizes past 32-bit
+ * indexing), FA_ERR_DEVICE or FA_ERR_CUDA.
+ */
+FA_API int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                        const int* context_lens, void* o, float* lse, int B, int H, int Hkv, int Nq, int D,
+                        int num_pages, int page_size, int max_pages, int causal, float scale, int dtype,
+                        cudaStream_t stream);
+
 FA_API size_t fa_bwd_ex_workspace_size(int Z, int H, int Hkv, int Nq, int Nk, int D, int causal);
 
 FA_API int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,

@@ -162,3 +162,25 @@ def test_flop_model(lib):
     assert lib.fa_fwd_flops(128, 8, 1024, 128, 0) == pytest.approx(4 * 1024 * 1024 * 128 * 1024)
     assert lib.fa_fwd_flops(1, 1, 1024, 128, 1) == pytest.approx(2 * 1024 * 1025 * 128)
     assert lib.fa_bwd_flops(2, 3, 256, 64, 1) == pytest.approx(2.5 * lib.fa_fwd_flops(2, 3, 256, 64, 1))
+
+
+def call_fwd_paged(lib, B=2, H=4, Hkv=2, Nq=1, D=128, num_pages=8, page_size=64, max_pages=4, causal=0,
+                   scale=0.125, dtype=0, table=FAKE):
+    return lib.fa_fwd_paged(FAKE, FAKE, FAKE, table, FAKE, FAKE, FAKE, B, H, Hkv, Nq, D, num_pages, page_size,
+                            max_pages, causal, scale, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(table=None), _native.FA_ERR_INVALID_ARG),
+    (dict(table=FAKE + 2), _native.FA_ERR_INVALID_ARG),   # int32 table not 4-byte aligned
+    (dict(Hkv=3), _native.FA_ERR_INVALID_ARG),
+    (dict(num_pages=0), _native.FA_ERR_INVALID_ARG),
+    (dict(max_pages=0), _native.FA_ERR_INVALID_ARG),
+    (dict(dtype=5), _native.FA_ERR_INVALID_ARG),
+    (dict(page_size=48), _native.FA_ERR_UNSUPPORTED),     # not a power-of-two page of 16-128 rows
+    (dict(page_size=8), _native.FA_ERR_UNSUPPORTED),
+    (dict(D=256, page_size=128), _native.FA_ERR_UNSUPPORTED),  # D = 256 key tiles hold 64 keys
+    (dict(D=96), _native.FA_ERR_UNSUPPORTED),
+])
+def test_fwd_paged_rejects_bad_arguments(lib, kw, code):
+    assert call_fwd_paged(lib, **kw) == code
