@@ -286,6 +286,74 @@ def load_traffic():
         return json.load(f)
 
 
+def paged_bench(args):
+    """Forward over a paged K/V cache (fa_fwd_paged): Z sequences of N queries
+    at the end of an NK-token context, HKV K/V heads, pages of args.paged
+    tokens assigned from a random permutation.  Times the paged call and, for
+    comparison, the dense call on the same shape; prints one JSON line."""
+    import torch
+
+    import attention_sm_flashattention_gb300 as fa
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device=dev).manual_seed(SEED)
+    elem = torch.bfloat16 if DTYPE == "bf16" else torch.float16
+    ps = args.paged
+    pages_per_seq = (NK + ps - 1) // ps
+    num_pages = Z * pages_per_seq
+    q = torch.randn((Z, H, N, D), device=dev, dtype=elem, generator=gen)
+    kc = torch.randn((num_pages, ps, HKV, D), device=dev, dtype=elem, generator=gen)
+    vc = torch.randn((num_pages, ps, HKV, D), device=dev, dtype=elem, generator=gen)
+    table = torch.randperm(num_pages, device=dev, generator=gen).to(torch.int32).view(Z, pages_per_seq)
+    lens = torch.full((Z,), NK, dtype=torch.int32, device=dev)
+    k = torch.randn((Z, HKV, NK, D), device=dev, dtype=elem, generator=gen)
+    v = torch.randn_like(k)
+    o = torch.empty_like(q)
+    lse = torch.empty((Z, H, N), device=dev, dtype=torch.float32)
+    scale = 1.0 / math.sqrt(D)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    sampler = ClockSampler(0 if "CUDA_VISIBLE_DEVICES" not in os.environ else os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0])
+    sampler.start()
+    time.sleep(0.3)
+    ms = timed(lambda: fa.fwd_paged(q, kc, vc, table, lens, causal=CAUSAL, scale=scale, out=(o, lse)))
+    clocks = sampler.stop()
+    ms_dense = timed(lambda: fa.fwd(q, k, v, causal=CAUSAL, scale=scale, out=(o, lse)))
+    if fa.device_status() != 0:
+        raise RuntimeError("device status reports a kernel wait timeout")
+    fl = flops_fwd(Z, H, N, D, CAUSAL, NK)
+    tf = fl / (ms * 1e-3) / 1e12
+    kv_bytes = 2 * Z * HKV * NK * D * q.element_size()
+    peaks = measured_peaks()
+    line = {
+        "metric": "attention fwd over a paged K/V cache, TFLOP/s", "value": tf, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
+        "config": {"workload": f"paged attention fwd, {Z} sequences, H{H} Hkv{HKV}, {N} queries at the end of "
+                               f"{NK}-token contexts, D{D}, pages of {ps} tokens, {'causal' if CAUSAL else 'non-causal'}",
+                   "B": Z, "H": H, "Hkv": HKV, "Nq": N, "context": NK, "D": D, "page_size": ps, "causal": CAUSAL},
+        "dense_fwd_tflops": fl / (ms_dense * 1e-3) / 1e12, "dense_fwd_ms": ms_dense,
+        "kv_cache_gbs": kv_bytes / (ms * 1e-3) / 1e9,
+        "roofline": {"bound": "tensor", "kernel": f"fa_fwd_kernel<{D},{str(CAUSAL).lower()},paged>", "achieved": tf,
+                     "peak": peaks["tflops"], "unit": "TFLOP/s", "frac": tf / peaks["tflops"], "traffic": None},
+        "clocks": clocks, "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -302,6 +370,8 @@ def main():
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--hkv", type=int, default=None, help="K/V heads (grouped heads; default H)")
     ap.add_argument("--nk", type=int, default=None, help="key length (default N, the query length)")
+    ap.add_argument("--paged", type=int, default=0, metavar="PAGE_SIZE",
+                    help="time the forward over a paged K/V cache with pages of this many tokens instead")
     ap.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
                     help="element type of the inputs and outputs (the benchmark is f16)")
     args = ap.parse_args()
@@ -323,6 +393,10 @@ def main():
                      else f"inputs {in_mb:.0f} MB {DTYPE} per step, smaller than L2: not flushed (profiling case)")}
     if HKV != H or NK != N:
         config.update({"Hkv": HKV, "Nk": NK})
+
+    if args.paged:
+        paged_bench(args)
+        return
 
     if args.impl == "reference":
         # The oracle as it stands, on the host cores: each step is one head of
