@@ -80,6 +80,28 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
     return o, lse
 
 
+def reshape_and_cache(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Write new tokens' K and V ([T, Hkv, D]) into the paged caches
+    ([num_pages, page_size, Hkv, D]) at the slots of ``slot_mapping`` (int64
+    [T]); negative slots are skipped."""
+    for name, t in (("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
+        if not t.is_cuda or t.dtype not in _DTYPES or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float16/bfloat16 CUDA tensor")
+        if t.dtype != k_cache.dtype:
+            raise ValueError(f"{name} is {t.dtype}, expected {k_cache.dtype} like k_cache")
+    T, Hkv, D = k_new.shape
+    num_pages, page_size, Hkv_c, Dc = k_cache.shape
+    if tuple(v_new.shape) != (T, Hkv, D) or (Hkv_c, Dc) != (Hkv, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_new, v_new must be [T, Hkv, D] and the caches [num_pages, page_size, Hkv, D]")
+    if not slot_mapping.is_cuda or slot_mapping.dtype != torch.int64 or tuple(slot_mapping.shape) != (T,):
+        raise ValueError("slot_mapping must be an int64 CUDA tensor [T]")
+    rc = _native.lib().fa_reshape_and_cache(k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(),
+                                            k_cache.data_ptr(), v_cache.data_ptr(), T, Hkv, D, num_pages,
+                                            page_size, _stream_handle(stream))
+    _native.check(rc, "fa_reshape_and_cache")
+
+
 def fwd_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
               context_lens: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
               out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,

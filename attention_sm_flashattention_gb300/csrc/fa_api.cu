@@ -222,6 +222,26 @@ int fa_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse
   return fwd_impl(q, k, v, o, lse, square(Z, H, N, D, causal), scale, stream, true);
 }
 
+int fa_reshape_and_cache(const void* k_new, const void* v_new, const long long* slot_mapping, void* k_cache,
+                         void* v_cache, int tokens, int Hkv, int D, int num_pages, int page_size,
+                         cudaStream_t stream) {
+  if (tokens < 0 || Hkv <= 0 || D <= 0 || num_pages <= 0 || page_size <= 0) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  if (tokens == 0) return FA_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return FA_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return FA_ERR_INVALID_ARG;
+  DevInfo* dev = nullptr;
+  const int rc = current_device_info(&dev);
+  if (rc != FA_OK) return rc;
+  const long long rows = static_cast<long long>(num_pages) * page_size;
+  return fa::launch_cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, tokens, Hkv, D, rows, dev->sms,
+                                stream) == 0
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
 int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
                  const int* context_lens, void* o, float* lse, int B, int H, int Hkv, int Nq, int D, int num_pages,
                  int page_size, int max_pages, int causal, float scale, int dtype, cudaStream_t stream) {

@@ -71,6 +71,12 @@ FA_DECLARE_LAUNCHERS(128)
 FA_DECLARE_LAUNCHERS(256)
 #undef FA_DECLARE_LAUNCHERS
 
+// Paged cache write: token t's K and V rows ([Hkv, D] 16-bit values each) to
+// cache row slots[t] of [cache_rows, Hkv, D] caches; negative slots and slots
+// >= cache_rows are skipped.
+int launch_cache_write(const void* k_new, const void* v_new, const long long* slots, void* k_cache, void* v_cache,
+                       int tokens, int Hkv, int D, long long cache_rows, int num_sms, cudaStream_t stream);
+
 // Forward over a paged K/V cache; maps: q, k cache, v cache (4-D, one page
 // row block per box), o.
 int launch_fwd_paged_d64(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,

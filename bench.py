@@ -332,6 +332,12 @@ def paged_bench(args):
     ms = timed(lambda: fa.fwd_paged(q, kc, vc, table, lens, causal=CAUSAL, scale=scale, out=(o, lse)))
     clocks = sampler.stop()
     ms_dense = timed(lambda: fa.fwd(q, k, v, causal=CAUSAL, scale=scale, out=(o, lse)))
+    # cache write of the Z * N new tokens (ReshapeAndCache) to distinct slots
+    toks = Z * N
+    k_new = torch.randn((toks, HKV, D), device=dev, dtype=elem, generator=gen)
+    v_new = torch.randn_like(k_new)
+    slots = torch.randperm(num_pages * ps, device=dev, generator=gen)[:toks].to(torch.int64)
+    ms_write = timed(lambda: fa.reshape_and_cache(k_new, v_new, slots, kc, vc))
     if fa.device_status() != 0:
         raise RuntimeError("device status reports a kernel wait timeout")
     fl = flops_fwd(Z, H, N, D, CAUSAL, NK)
@@ -347,6 +353,9 @@ def paged_bench(args):
                    "B": Z, "H": H, "Hkv": HKV, "Nq": N, "context": NK, "D": D, "page_size": ps, "causal": CAUSAL},
         "dense_fwd_tflops": fl / (ms_dense * 1e-3) / 1e12, "dense_fwd_ms": ms_dense,
         "kv_cache_gbs": kv_bytes / (ms * 1e-3) / 1e9,
+        "cache_write": {"tokens": toks, "ms": ms_write,
+                        "gbs": 4 * toks * HKV * D * q.element_size() / (ms_write * 1e-3) / 1e9,
+                        "peak_hbm_gbs": peaks["hbm_gbs"]},
         "roofline": {"bound": "tensor", "kernel": f"fa_fwd_kernel<{D},{str(CAUSAL).lower()},paged>", "achieved": tf,
                      "peak": peaks["tflops"], "unit": "TFLOP/s", "frac": tf / peaks["tflops"], "traffic": None},
         "clocks": clocks, "gpu_launches": args.steps,

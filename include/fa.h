@@ -188,6 +188,27 @@ FA_API int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float
  * FA_ERR_UNSUPPORTED (D or page_size not supported, sizes past 32-bit
  * indexing), FA_ERR_DEVICE or FA_ERR_CUDA.
  */
+/*
+ * Paged cache write (ReshapeAndCache).  Source: «把 FlashAttention 搬上昇腾»,
+ * the contest section's ReshapeAndCache part: token t's K and V go to block
+ * slot_mapping[t] / page_size at offset slot_mapping[t] % page_size of the
+ * caches; a negative slot skips the token.
+ *   k_new, v_new : [tokens, Hkv, D] 16-bit (fp16 or bf16; copied bit for
+ *                  bit), contiguous, 16-byte aligned.
+ *   slot_mapping : int64 [tokens], device memory.  Slots >= num_pages *
+ *                  page_size are skipped as well (never written out of
+ *                  bounds).
+ *   k_cache,
+ *   v_cache      : [num_pages, page_size, Hkv, D], same element type,
+ *                  written in place.
+ * tokens == 0 enqueues nothing.  Two tokens with the same slot: one of them
+ * wins (unspecified which).  Returns FA_OK, FA_ERR_INVALID_ARG,
+ * FA_ERR_UNSUPPORTED (D not 64/128/256), FA_ERR_DEVICE or FA_ERR_CUDA.
+ */
+FA_API int fa_reshape_and_cache(const void* k_new, const void* v_new, const long long* slot_mapping, void* k_cache,
+                                void* v_cache, int tokens, int Hkv, int D, int num_pages, int page_size,
+                                cudaStream_t stream);
+
 FA_API int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
                         const int* context_lens, void* o, float* lse, int B, int H, int Hkv, int Nq, int D,
                         int num_pages, int page_size, int max_pages, int causal, float scale, int dtype,

@@ -184,3 +184,12 @@ def call_fwd_paged(lib, B=2, H=4, Hkv=2, Nq=1, D=128, num_pages=8, page_size=64,
 ])
 def test_fwd_paged_rejects_bad_arguments(lib, kw, code):
     assert call_fwd_paged(lib, **kw) == code
+
+
+def test_reshape_and_cache_argument_checks(lib):
+    f = lib.fa_reshape_and_cache
+    assert f(None, None, None, None, None, 0, 2, 64, 4, 16, None) == _native.FA_OK   # nothing to write
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 3, 2, 96, 4, 16, None) == _native.FA_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, None, FAKE, FAKE, 3, 2, 64, 4, 16, None) == _native.FA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE + 4, FAKE, FAKE, 3, 2, 64, 4, 16, None) == _native.FA_ERR_INVALID_ARG  # int64 slots
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 2, 64, 4, 16, None) == _native.FA_ERR_INVALID_ARG

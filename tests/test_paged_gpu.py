@@ -16,6 +16,7 @@ import torch
 
 from attention_sm_flashattention_gb300 import _native, api
 from attention_sm_flashattention_gb300.inputs import make_paged_inputs
+from oracle import attention as orc
 from oracle import paged as porc
 
 from helpers import LSE_ATOL, O_ATOL, O_ATOL_BF16, max_abs
@@ -128,3 +129,54 @@ def test_paged_decode_batch_sampled():
                                                  True, 1 / math.sqrt(D))
         assert max_abs(o[b:b + 1], o_ref) <= O_ATOL, b
         assert max_abs(lse[b:b + 1], lse_ref) <= LSE_ATOL, b
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("T,Hkv,D,num_pages,ps", [(37, 2, 64, 8, 16), (300, 8, 128, 12, 64), (5, 4, 256, 3, 32)])
+def test_reshape_and_cache_matches_oracle(T, Hkv, D, num_pages, ps, dtype):
+    g = torch.Generator().manual_seed(T + D)
+    k_new = torch.randn((T, Hkv, D), generator=g).to(dtype)
+    v_new = torch.randn((T, Hkv, D), generator=g).to(dtype)
+    rows = num_pages * ps
+    slots = torch.randperm(rows, generator=g)[:T].to(torch.int64)
+    slots[::7] = -1                     # skipped tokens
+    if T > 3:
+        slots[3] = rows + 5             # outside the cache: skipped, never written
+    kc = torch.randn((num_pages, ps, Hkv, D), generator=g).to(dtype)
+    vc = torch.randn((num_pages, ps, Hkv, D), generator=g).to(dtype)
+    kc_d, vc_d = kc.cuda(), vc.cuda()
+    api.reshape_and_cache(k_new.cuda(), v_new.cuda(), slots.cuda(), kc_d, vc_d)
+    torch.cuda.synchronize()
+    kc_ref, vc_ref = kc.float().numpy().copy(), vc.float().numpy().copy()
+    keep = slots < rows
+    porc.reshape_and_cache(k_new.float().numpy()[keep.numpy()], v_new.float().numpy()[keep.numpy()],
+                           slots.numpy()[keep.numpy()], kc_ref, vc_ref)
+    # a pure copy: bit-exact
+    assert np.array_equal(kc_d.float().cpu().numpy(), kc_ref)
+    assert np.array_equal(vc_d.float().cpu().numpy(), vc_ref)
+
+
+def test_cache_written_then_attended_equals_dense():
+    # Decode-style round trip: write each sequence's tokens into scattered
+    # pages with the cache write, then attend through the block table.
+    B, H, Hkv, N, D, ps = 3, 8, 2, 200, 128, 32
+    g = torch.Generator().manual_seed(21)
+    k = torch.randn((B, Hkv, N, D), generator=g).half()
+    v = torch.randn((B, Hkv, N, D), generator=g).half()
+    q = torch.randn((B, H, 1, D), generator=g).half()
+    npg = (N + ps - 1) // ps
+    num_pages = B * npg + 2
+    perm = torch.randperm(num_pages, generator=g)
+    table = perm[:B * npg].view(B, npg).to(torch.int32)
+    pos = torch.arange(N)
+    slots = (table[:, pos // ps].to(torch.int64) * ps + (pos % ps)).reshape(-1)      # [B * N]
+    kc = torch.zeros((num_pages, ps, Hkv, D), dtype=torch.float16, device="cuda")
+    vc = torch.zeros_like(kc)
+    api.reshape_and_cache(k.permute(0, 2, 1, 3).reshape(B * N, Hkv, D).contiguous().cuda(),
+                          v.permute(0, 2, 1, 3).reshape(B * N, Hkv, D).contiguous().cuda(), slots.cuda(), kc, vc)
+    cl = torch.full((B,), N, dtype=torch.int32, device="cuda")
+    o, lse = api.fwd_paged(q.cuda(), kc, vc, table.cuda(), cl, causal=True)
+    assert api.device_status() == 0
+    o_ref, lse_ref = orc.attn_fwd_ref(q, k, v, True, 1 / math.sqrt(D))
+    assert max_abs(o, o_ref) <= O_ATOL
+    assert max_abs(lse, lse_ref) <= LSE_ATOL
