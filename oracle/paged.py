@@ -14,7 +14,10 @@ contest section's ReshapeAndCache and GQA Paged Attention parts:
   sequence -> physical block), uses ``context_lens`` for the real length of
   each sequence and masks the invalid tokens of the last block;
 * query heads are an integer multiple of the K/V heads (grouped heads, as
-  in ``oracle/attention.py``).
+  in ``oracle/attention.py``);
+* the Quest Sparse Attention part: only a chosen subset of a sequence's
+  blocks gets exact attention (``sparse_attn_fwd_ref``; how the blocks are
+  chosen -- the scoring and Top-K -- is an input here).
 
 Readings (listed in the design doc): the cache layout is
 ``[num_blocks, block_size, H_kv, D]`` (one token's K for all K/V heads is
@@ -33,7 +36,7 @@ import numpy as np
 
 from . import attention as dense
 
-__all__ = ["reshape_and_cache", "gather_sequence", "paged_attn_fwd_ref"]
+__all__ = ["reshape_and_cache", "gather_sequence", "paged_attn_fwd_ref", "sparse_attn_fwd_ref"]
 
 
 def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache):
@@ -83,4 +86,53 @@ def paged_attn_fwd_ref(q, k_cache, v_cache, block_table, context_lens, causal: b
         k_b = gather_sequence(k_cache, table[b], n_k)[None]
         v_b = gather_sequence(v_cache, table[b], n_k)[None]
         o[b:b + 1], lse[b:b + 1] = dense.attn_fwd_ref(q[b:b + 1], k_b, v_b, causal, scale)
+    return o, lse
+
+
+def sparse_attn_fwd_ref(q, k_cache, v_cache, sel_pages, sel_blocks, sel_count, context_lens, causal: bool,
+                        scale: float):
+    """Exact attention over selected cache blocks (the contest section's
+    Quest Sparse Attention: only the chosen blocks get full attention).
+
+    For sequence b and K/V head kvh, the first ``sel_count[b, kvh]`` entries
+    of ``sel_pages[b, kvh]`` / ``sel_blocks[b, kvh]`` name physical pages and
+    the logical blocks they hold.  Row r of logical block L is the token at
+    position ``L * block_size + r``; it takes part iff that position is below
+    ``context_lens[b]`` and, when causal, at most the query's own position
+    (queries are the last n_q tokens of the context).  A query row with no
+    such token gets O = 0 and lse = -inf (an empty softmax).
+    Returns fp64 ``(O [B, H, n_q, D], lse [B, H, n_q])``.
+    """
+    q = dense._f64(q)
+    kc, vc = dense._f64(k_cache), dense._f64(v_cache)
+    B, H, n_q, D = q.shape
+    bs, h_kv = kc.shape[1], kc.shape[2]
+    g = H // h_kv
+    sc = dense._scale64(scale)
+    pages, blocks, counts = np.asarray(sel_pages), np.asarray(sel_blocks), np.asarray(sel_count)
+    lens = np.asarray(context_lens)
+    o = np.zeros((B, H, n_q, D))
+    lse = np.full((B, H, n_q), -np.inf)
+    for b in range(B):
+        n_k = int(lens[b])
+        for h in range(H):
+            kvh = h // g
+            keys, vals, pos = [], [], []
+            for e in range(int(counts[b, kvh])):
+                for r in range(bs):
+                    keys.append(kc[int(pages[b, kvh, e]), r, kvh])
+                    vals.append(vc[int(pages[b, kvh, e]), r, kvh])
+                    pos.append(int(blocks[b, kvh, e]) * bs + r)
+            if not keys:
+                continue
+            keys, vals, pos = np.array(keys), np.array(vals), np.array(pos)
+            for i in range(n_q):
+                limit = (i + n_k - n_q) if causal else (n_k - 1)
+                visible = (pos < n_k) & (pos <= limit)
+                if not visible.any():
+                    continue
+                s = (keys[visible] @ q[b, h, i]) * sc
+                p, l = dense.softmax_probs(s[None, :])
+                o[b, h, i] = p[0] @ vals[visible]
+                lse[b, h, i] = l[0]
     return o, lse

@@ -145,3 +145,118 @@ def test_pins_catch_planted_paging_mistakes():
     # (c) the whole last block attended to (no invalid-token mask)
     o_bad3, _ = paged.paged_attn_fwd_ref(q, kc, vc, table, np.array([12]), True, 0.6)
     assert not np.allclose(o_bad3, want)
+
+
+# ---------------------------------------------------------- selected blocks
+
+
+def full_selection(table, lens, h_kv, bs):
+    """Every block of every sequence, in order, for every K/V head."""
+    B = table.shape[0]
+    nb = [(int(n) + bs - 1) // bs for n in lens]
+    m = max(nb)
+    pages = np.zeros((B, h_kv, m), dtype=np.int64)
+    blocks = np.zeros((B, h_kv, m), dtype=np.int64)
+    count = np.zeros((B, h_kv), dtype=np.int64)
+    for b in range(B):
+        for kvh in range(h_kv):
+            pages[b, kvh, :nb[b]] = table[b, :nb[b]]
+            blocks[b, kvh, :nb[b]] = np.arange(nb[b])
+            count[b, kvh] = nb[b]
+    return pages, blocks, count
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sparse_with_every_block_equals_paged(causal):
+    rng = np.random.default_rng(20)
+    kc, vc = rand_cache(10, 8, 2, 4, 21)
+    table = np.array([[3, 7, 1, 9], [0, 2, 4, 6]])
+    lens = np.array([29, 20])
+    q = rng.standard_normal((2, 4, 3, 4))
+    o, lse = paged.paged_attn_fwd_ref(q, kc, vc, table, lens, causal, 0.5)
+    o2, lse2 = paged.sparse_attn_fwd_ref(q, kc, vc, *full_selection(table, lens, 2, 8), lens, causal, 0.5)
+    np.testing.assert_allclose(o2, o, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(lse2, lse, rtol=1e-13, atol=1e-14)
+
+
+def brute_sparse(q, kc, vc, pages, blocks, count, lens, causal, scale):
+    B, H, n_q, D = q.shape
+    bs, h_kv = kc.shape[1], kc.shape[2]
+    o = np.zeros(q.shape)
+    lse = np.full((B, H, n_q), -np.inf)
+    for b in range(B):
+        for h in range(H):
+            kvh = h // (H // h_kv)
+            for i in range(n_q):
+                s = []
+                for e in range(int(count[b, kvh])):
+                    for r in range(bs):
+                        p = int(blocks[b, kvh, e]) * bs + r
+                        if p >= lens[b] or (causal and p > i + int(lens[b]) - n_q):
+                            continue
+                        pg = int(pages[b, kvh, e])
+                        s.append((pg, r, scale * sum(q[b, h, i, t] * kc[pg, r, kvh, t] for t in range(D))))
+                if not s:
+                    continue
+                mx = max(x for _, _, x in s)
+                w = [(pg, r, math.exp(x - mx)) for pg, r, x in s]
+                tot = sum(x for _, _, x in w)
+                lse[b, h, i] = mx + math.log(tot)
+                for t in range(D):
+                    o[b, h, i, t] = sum(x * vc[pg, r, kvh, t] for pg, r, x in w) / tot
+    return o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sparse_brute_force(causal):
+    rng = np.random.default_rng(22)
+    kc, vc = rand_cache(9, 4, 2, 3, 23)
+    # per (sequence, K/V head): a few blocks of the context, out of order,
+    # one of them wholly past the context (sequence 1: 9 tokens = blocks 0-2)
+    pages = np.array([[[5, 1, 8], [2, 0, 0]], [[7, 3, 4], [6, 2, 0]]])
+    blocks = np.array([[[2, 0, 4], [1, 0, 0]], [[1, 3, 0], [2, 0, 0]]])
+    count = np.array([[3, 1], [3, 2]])
+    lens = np.array([19, 9])
+    q = rng.standard_normal((2, 4, 2, 3))
+    sc = float(np.float32(0.8))
+    o, lse = paged.sparse_attn_fwd_ref(q, kc, vc, pages, blocks, count, lens, causal, sc)
+    bo, blse = brute_sparse(q, kc, vc, pages, blocks, count, lens, causal, sc)
+    np.testing.assert_allclose(o, bo, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, blse, rtol=1e-12, atol=1e-13)
+
+
+def test_sparse_selection_order_and_empty_rows():
+    rng = np.random.default_rng(24)
+    kc, vc = rand_cache(6, 8, 1, 4, 25)
+    q = rng.standard_normal((1, 2, 1, 4))
+    pages = np.array([[[4, 0, 5, 2]]])
+    blocks = np.array([[[3, 0, 1, 2]]])
+    lens = np.array([30])
+    o, lse = paged.sparse_attn_fwd_ref(q, kc, vc, pages, blocks, np.array([[4]]), lens, False, 0.5)
+    perm = [2, 0, 3, 1]
+    o2, lse2 = paged.sparse_attn_fwd_ref(q, kc, vc, pages[:, :, perm], blocks[:, :, perm], np.array([[4]]), lens,
+                                         False, 0.5)
+    np.testing.assert_allclose(o2, o, rtol=1e-13, atol=1e-14)   # softmax over a set: order is irrelevant
+    np.testing.assert_allclose(lse2, lse, rtol=1e-13, atol=1e-14)
+    # only a block wholly past the context, or nothing selected: empty rows
+    for cnt, blk in ((1, np.array([[[4, 0, 0, 0]]])), (0, blocks)):
+        o3, lse3 = paged.sparse_attn_fwd_ref(q, kc, vc, pages, blk, np.array([[cnt]]), lens, False, 0.5)
+        assert np.all(o3 == 0) and np.all(np.isneginf(lse3))
+
+
+def test_pins_catch_planted_sparse_mistakes():
+    rng = np.random.default_rng(26)
+    kc, vc = rand_cache(8, 4, 1, 3, 27)
+    q = rng.standard_normal((1, 1, 2, 3))
+    pages = np.array([[[6, 1, 3]]])
+    blocks = np.array([[[2, 0, 1]]])
+    count = np.array([[3]])
+    lens = np.array([10])                 # block 2 holds 2 valid tokens
+    sc = float(np.float32(0.6))
+    want, _ = brute_sparse(q, kc, vc, pages, blocks, count, lens, True, sc)
+    # (a) positions from the entry index instead of the logical block
+    bad, _ = paged.sparse_attn_fwd_ref(q, kc, vc, pages, np.array([[[0, 1, 2]]]), count, lens, True, sc)
+    assert not np.allclose(bad, want)
+    # (b) physical page taken as the logical block
+    bad2, _ = paged.sparse_attn_fwd_ref(q, kc, vc, pages, pages, count, lens, True, sc)
+    assert not np.allclose(bad2, want)
