@@ -36,6 +36,7 @@ SIGNATURES = {
     "fa_bwd_bf16": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fa_reshape_and_cache": (_i, [_vp] * 5 + [_i] * 5 + [_vp]),
+    "fa_fwd_sparse": (_i, [_vp] * 9 + [_i] * 9 + [_f, _i, _vp]),
     "fa_fwd_paged": (_i, [_vp] * 7 + [_i] * 9 + [_f, _i, _vp]),
     "fa_bwd_ex_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
     "fa_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),

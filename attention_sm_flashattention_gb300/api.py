@@ -140,6 +140,43 @@ def fwd_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, blo
     return o, lse
 
 
+def fwd_sparse(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, sel_pages: torch.Tensor,
+               sel_blocks: torch.Tensor, sel_count: torch.Tensor, context_lens: torch.Tensor, causal: bool = False,
+               scale: Optional[float] = None, stream: Optional[torch.cuda.Stream] = None
+               ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Attention forward over selected blocks of a paged cache.  q
+    [B,H,Nq,D]; caches as for :func:`fwd_paged`; sel_pages, sel_blocks int32
+    [B, Hkv, max_sel] (physical page and logical block of each selected
+    entry), sel_count int32 [B, Hkv], context_lens int32 [B].  Returns
+    ``(o, lse)``; rows with no visible selected token get o = 0, lse = -inf."""
+    _check_input("q", q)
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _check_input(name, t, q.dtype)
+    B, H, Nq, D = q.shape
+    num_pages, page_size, Hkv, Dk = k_cache.shape
+    if Dk != D or tuple(v_cache.shape) != tuple(k_cache.shape) or H % Hkv != 0:
+        raise ValueError("caches must be [num_pages, page_size, Hkv, D] with q's D and Hkv dividing H")
+    for name, t in (("sel_pages", sel_pages), ("sel_blocks", sel_blocks), ("sel_count", sel_count),
+                    ("context_lens", context_lens)):
+        if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    if sel_pages.dim() != 3 or tuple(sel_pages.shape[:2]) != (B, Hkv) or tuple(sel_blocks.shape) != tuple(sel_pages.shape):
+        raise ValueError("sel_pages and sel_blocks must be [B, Hkv, max_sel]")
+    if tuple(sel_count.shape) != (B, Hkv) or tuple(context_lens.shape) != (B,):
+        raise ValueError("sel_count must be [B, Hkv] and context_lens [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    rc = _native.lib().fa_fwd_sparse(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), sel_pages.data_ptr(),
+                                     sel_blocks.data_ptr(), sel_count.data_ptr(), context_lens.data_ptr(),
+                                     o.data_ptr(), lse.data_ptr(), B, H, Hkv, Nq, D, num_pages, page_size,
+                                     sel_pages.shape[2], int(bool(causal)), float(scale), _dtype_code(q),
+                                     _stream_handle(stream))
+    _native.check(rc, "fa_fwd_sparse")
+    return o, lse
+
+
 def bwd_workspace_size(Z: int, H: int, N: int, D: int, causal: bool, Hkv: Optional[int] = None,
                        Nk: Optional[int] = None) -> int:
     """Workspace bytes of a backward call; N is the query length."""

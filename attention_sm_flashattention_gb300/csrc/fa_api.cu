@@ -242,15 +242,26 @@ int fa_reshape_and_cache(const void* k_new, const void* v_new, const long long* 
              : FA_ERR_CUDA;
 }
 
-int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
-                 const int* context_lens, void* o, float* lse, int B, int H, int Hkv, int Nq, int D, int num_pages,
-                 int page_size, int max_pages, int causal, float scale, int dtype, cudaStream_t stream) {
-  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !o || !lse) return FA_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// Shared by the paged and the selected-block forward: argument checks, the
+// 4-D cache maps and the launch.  `lists` is the block table (paged) or the
+// selected-page list (sparse); `blocks` and `counts` are the sparse-only
+// logical blocks and selection counts.
+int paged_impl(int mode, const void* q, const void* k_cache, const void* v_cache, const int* lists,
+               const int* blocks, const int* counts, const int* context_lens, void* o, float* lse, int B, int H,
+               int Hkv, int Nq, int D, int num_pages, int page_size, int max_entries, int causal, float scale,
+               int dtype, cudaStream_t stream) {
+  const bool sparse = mode == 2;
+  if (!q || !k_cache || !v_cache || !lists || !context_lens || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (sparse && (!blocks || !counts)) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
-      !aligned(block_table, 4) || !aligned(context_lens, 4))
+      !aligned(lists, 4) || !aligned(context_lens, 4) || (sparse && (!aligned(blocks, 4) || !aligned(counts, 4))))
     return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
-  if (B <= 0 || H <= 0 || Hkv <= 0 || Nq <= 0 || num_pages <= 0 || page_size <= 0 || max_pages <= 0)
+  if (B <= 0 || H <= 0 || Hkv <= 0 || Nq <= 0 || num_pages <= 0 || page_size <= 0 || max_entries <= 0)
     return FA_ERR_INVALID_ARG;
   if (H % Hkv != 0 || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
@@ -259,8 +270,9 @@ int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const 
   if ((page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) || page_size > fa::fwd_block_n(D))
     return FA_ERR_UNSUPPORTED;
   const long long nq_pad = (Nq + 127LL) / 128 * 128;
-  if (static_cast<long long>(B) * H * nq_pad >= (1LL << 31) || static_cast<long long>(max_pages) * page_size >= (1LL << 31) ||
-      static_cast<long long>(B) * max_pages >= (1LL << 31))
+  if (static_cast<long long>(B) * H * nq_pad >= (1LL << 31) ||
+      static_cast<long long>(max_entries) * page_size >= (1LL << 31) ||
+      static_cast<long long>(B) * (sparse ? Hkv : 1) * max_entries >= (1LL << 31))
     return FA_ERR_UNSUPPORTED;
   DevInfo* dev = nullptr;
   int rc = current_device_info(&dev);
@@ -281,23 +293,54 @@ int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const 
   prm.heads = B * H;
   prm.group = H / Hkv;
   prm.Nq = Nq;
-  prm.Nk = max_pages * page_size;  // per sequence: context_lens[b], clamped
+  prm.Nk = max_entries * page_size;  // per sequence: context_lens[b] (paged), the selection (sparse)
   prm.causal_off = 0;
   prm.scale_log2 = scale * kLog2e;
   prm.status = dev->status;
-  prm.block_table = block_table;
+  prm.block_table = sparse ? nullptr : lists;
+  prm.sel_pages = sparse ? lists : nullptr;
+  prm.sel_blocks = blocks;
+  prm.sel_count = counts;
   prm.context_lens = context_lens;
   prm.H = H;
+  prm.Hkv = Hkv;
   prm.num_pages = num_pages;
   prm.page_size = page_size;
-  prm.max_pages = max_pages;
+  prm.max_pages = max_entries;
   const bool c = causal != 0;
-  switch (D) {
-    case 64: rc = fa::launch_fwd_paged_d64(c, bf16, maps, prm, dev->sms, stream); break;
-    case 128: rc = fa::launch_fwd_paged_d128(c, bf16, maps, prm, dev->sms, stream); break;
-    default: rc = fa::launch_fwd_paged_d256(c, bf16, maps, prm, dev->sms, stream); break;
+  if (sparse) {
+    switch (D) {
+      case 64: rc = fa::launch_fwd_sparse_d64(c, bf16, maps, prm, dev->sms, stream); break;
+      case 128: rc = fa::launch_fwd_sparse_d128(c, bf16, maps, prm, dev->sms, stream); break;
+      default: rc = fa::launch_fwd_sparse_d256(c, bf16, maps, prm, dev->sms, stream); break;
+    }
+  } else {
+    switch (D) {
+      case 64: rc = fa::launch_fwd_paged_d64(c, bf16, maps, prm, dev->sms, stream); break;
+      case 128: rc = fa::launch_fwd_paged_d128(c, bf16, maps, prm, dev->sms, stream); break;
+      default: rc = fa::launch_fwd_paged_d256(c, bf16, maps, prm, dev->sms, stream); break;
+    }
   }
   return rc == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                 const int* context_lens, void* o, float* lse, int B, int H, int Hkv, int Nq, int D, int num_pages,
+                 int page_size, int max_pages, int causal, float scale, int dtype, cudaStream_t stream) {
+  return paged_impl(1, q, k_cache, v_cache, block_table, nullptr, nullptr, context_lens, o, lse, B, H, Hkv, Nq, D,
+                    num_pages, page_size, max_pages, causal, scale, dtype, stream);
+}
+
+int fa_fwd_sparse(const void* q, const void* k_cache, const void* v_cache, const int* sel_pages,
+                  const int* sel_blocks, const int* sel_count, const int* context_lens, void* o, float* lse, int B,
+                  int H, int Hkv, int Nq, int D, int num_pages, int page_size, int max_sel, int causal, float scale,
+                  int dtype, cudaStream_t stream) {
+  return paged_impl(2, q, k_cache, v_cache, sel_pages, sel_blocks, sel_count, context_lens, o, lse, B, H, Hkv, Nq,
+                    D, num_pages, page_size, max_sel, causal, scale, dtype, stream);
 }
 
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int Hkv, int Nq,

@@ -150,23 +150,75 @@ __device__ __forceinline__ int fwd_key_limit(int qi, int Nk, int off) {
   return CAUSAL ? min(qi + off, Nk - 1) : Nk - 1;
 }
 
-// Key count, causal offset and key-tile count of the work items of query
-// head `head`: the call's Nk, or (paged cache) its sequence's context length
-// clamped to [causal ? Nq : 1, max_pages * page_size].
-template <int D, bool CAUSAL, bool PAGED>
+// Work modes of the forward kernel: K/V dense [heads / group, Nk, D]; a
+// paged cache read in key order through a block table; a paged cache read
+// through a per-(sequence, K/V head) list of selected blocks.
+enum FwdMode : int { kDense = 0, kPaged = 1, kSparse = 2 };
+
+// Key count, causal offset and key tiles of the work items of query head
+// `head`.  Dense: the call's Nk.  Paged: the sequence's context length,
+// clamped to [causal ? Nq : 1, max_pages * page_size].  Sparse: key slots of
+// the selected blocks (at least one block, so that every item has a tile);
+// `ctx` is the context length that the keys' logical positions are masked
+// against, `sel` the number of selected blocks.
+template <int D, bool CAUSAL, int MODE>
 struct FwdItemShape {
-  int nk, off, nkv_full;
+  int nk, off, nkv_full, ctx, sel;
   __device__ __forceinline__ FwdItemShape(const FwdParams& prm, int head) {
     int n = prm.Nk;
-    if (PAGED) {
+    ctx = 0;
+    sel = 0;
+    if (MODE == kPaged) {
       n = __ldg(prm.context_lens + head / prm.H);
       n = min(max(n, CAUSAL ? prm.Nq : 1), prm.max_pages * prm.page_size);
+    } else if (MODE == kSparse) {
+      const int b = head / prm.H, kvh = (head % prm.H) / prm.group;
+      ctx = max(__ldg(prm.context_lens + b), 0);
+      sel = min(max(__ldg(prm.sel_count + b * prm.Hkv + kvh), 0), prm.max_pages);
+      n = max(sel, 1) * prm.page_size;
     }
     nk = n;
-    off = n - prm.Nq;
+    off = (MODE == kSparse ? ctx : n) - prm.Nq;
     nkv_full = (n + FwdTraits<D, CAUSAL>::BN - 1) / FwdTraits<D, CAUSAL>::BN;
   }
+  // key tiles of query tile qt (selected blocks carry arbitrary positions,
+  // so the causal bound does not shorten a sparse item)
+  __device__ __forceinline__ int tiles(int qt) const {
+    return MODE == kSparse ? nkv_full : fwd_num_kv<D, CAUSAL>(qt, nkv_full, nk, off);
+  }
 };
+
+// Sparse mode: which of key tile j's BN columns query row qi may see, as a
+// bit mask over BN / 32 words (bit c of word w = column 32 w + c).  Column c
+// is row c % page_size of list entry j * BN / page_size + c / page_size,
+// logical position block * page_size + c % page_size; it is visible iff the
+// entry is selected and the position is at most the row's limit (the last
+// context position, or the query's own position when causal).  Within an
+// entry the visible rows are a prefix, so each entry adds one bit range.
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void fwd_sparse_mask(const FwdParams& prm, int head, int j, int sel, int limit,
+                                                uint32_t* mask) {
+  using T = FwdTraits<D, CAUSAL>;
+  constexpr int W = T::BN / 32;
+  const int ps = prm.page_size, epb = T::BN / ps;
+  const int b = head / prm.H, kvh = (head % prm.H) / prm.group;
+  const int* blk = prm.sel_blocks + (static_cast<size_t>(b) * prm.Hkv + kvh) * prm.max_pages;
+#pragma unroll
+  for (int w = 0; w < W; ++w) mask[w] = 0u;
+#pragma unroll
+  for (int e = 0; e < T::BN / 16; ++e) {
+    if (e >= epb) break;
+    const int eg = j * epb + e;
+    if (eg >= sel) break;
+    const int n = min(max(limit - __ldg(blk + eg) * ps + 1, 0), ps);  // visible rows of the entry
+    const int lo = e * ps, hi = lo + n;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const int a = max(lo - 32 * w, 0), z = min(hi - 32 * w, 32);
+      if (z > a) mask[w] |= (z - a == 32 ? 0xffffffffu : ((1u << (z - a)) - 1u)) << a;
+    }
+  }
+}
 
 // Bounded wait that ignores the abort flag: used only while draining at exit.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
@@ -180,12 +232,13 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // The CTA's tiles in the order it processes them: work items (query tiles)
 // in schedule order, the key tiles of each item in order.  Global tile index
 // `tile` also indexes the K and V rings, which hold one tile per key tile.
-template <int D, bool CAUSAL, bool PAGED>
+template <int D, bool CAUSAL, int MODE>
 struct FwdCursor {
   int u, half, head, qt, qb, j, nkv;
   uint32_t item, tile;
   bool valid;
-  int units, nqt, nkv_full, Nk, off;
+  int units, nqt, nkv_full, Nk, off, ctx, sel;
+  bool sparse;
   const FwdParams* prm;
 
   __device__ void start(int first_unit, int units_, int nqt_, const FwdParams* prm_) {
@@ -204,13 +257,16 @@ struct FwdCursor {
     if (!valid) return;
     int qa;
     fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
-    const FwdItemShape<D, CAUSAL, PAGED> sh(*prm, head);
+    const FwdItemShape<D, CAUSAL, MODE> sh(*prm, head);
     Nk = sh.nk;
     off = sh.off;
     nkv_full = sh.nkv_full;
+    ctx = sh.ctx;
+    sel = sh.sel;
     qt = qa;
     half = 0;
-    nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
+    sparse = MODE == kSparse;
+    nkv = sparse ? nkv_full : fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
   }
   __device__ void advance() {
     ++tile;
@@ -220,7 +276,7 @@ struct FwdCursor {
     if (half == 0 && qb >= 0) {
       half = 1;
       qt = qb;
-      nkv = fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
+      nkv = sparse ? nkv_full : fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
     } else {
       u += gridDim.x;
       load_unit();
@@ -235,29 +291,35 @@ struct FwdCursor {
 // wholly past the sequence's key count get an out-of-range page coordinate,
 // which TMA fills with zeros; so does a block-table entry outside [0,
 // num_pages).  Every box counts its full size towards the barrier.
-template <int D, bool CAUSAL>
+// Sparse mode: the tile's pages are entries j * BN / page_size ... of the
+// item's selected-block list; entries past the selection count load zeros.
+template <int D, bool CAUSAL, int MODE>
 __device__ __forceinline__ void fwd_load_paged_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
-                                                    const FwdParams& prm, int head, int j, int nk, uint64_t pol) {
+                                                    const FwdParams& prm, int head, int j, int nk, int sel,
+                                                    uint64_t pol) {
   using T = FwdTraits<D, CAUSAL>;
   const int ps = prm.page_size;
   const int ppt = T::BN / ps;                  // pages per tile
   const int b = head / prm.H, kvh = (head % prm.H) / prm.group;
-  const int lp0 = j * (T::BN / ps);            // first logical page of the tile
-  const int* row = prm.block_table + static_cast<size_t>(b) * prm.max_pages;
+  const int lp0 = j * (T::BN / ps);            // first logical page (list entry) of the tile
+  const int* row = MODE == kSparse ? prm.sel_pages + (static_cast<size_t>(b) * prm.Hkv + kvh) * prm.max_pages
+                                   : prm.block_table + static_cast<size_t>(b) * prm.max_pages;
   for (int pg = 0; pg < ppt; ++pg) {
     const int lp = lp0 + pg;
-    const int page = (lp * ps < nk) ? __ldg(row + lp) : prm.num_pages;
+    const bool live = MODE == kSparse ? lp < sel : lp * ps < nk;
+    const int page = live ? __ldg(row + lp) : prm.num_pages;
     for (int s = 0; s < T::DSUB; ++s)
       tma_load_4d_hint(dst + s * T::KV_SUB + pg * ps * 128, map, bar, s * 64, kvh, 0, page, pol);
   }
 }
 
-template <int D, bool CAUSAL, bool BF, bool PAGED>
+template <int D, bool CAUSAL, bool BF, int MODE>
 __global__ void __launch_bounds__(512, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams prm) {
   using T = FwdTraits<D, CAUSAL>;
+  constexpr bool PAGED = MODE != kDense;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // the 128-byte-swizzled tiles need a 1024-byte aligned base
     if (threadIdx.x == 0) record_timeout(prm.status, 99);
@@ -331,17 +393,21 @@ __global__ void __launch_bounds__(512, 1)
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         int head, qa, qb;
         fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
-        const FwdItemShape<D, CAUSAL, PAGED> sh(prm, head);
+        const FwdItemShape<D, CAUSAL, MODE> sh(prm, head);
         const int Nk = sh.nk, off = sh.off;
         for (int half = 0; ok && half < 2; ++half) {
           const int qt = half ? qb : qa;
           if (qt < 0) break;
-          const int nkv = fwd_num_kv<D, CAUSAL>(qt, sh.nkv_full, Nk, off);
+          const int nkv = sh.tiles(qt);
           const int qi = qt * T::BM + r;  // query index within the head
           const int lim = fwd_key_limit<CAUSAL>(qi, Nk, off);             // this row's last key
           const int lim_lo = fwd_key_limit<CAUSAL>(qt * T::BM, Nk, off);  // the tile's smallest limit
+          // sparse: the row's last visible logical position
+          const int slim = CAUSAL ? min(qi + sh.off, sh.ctx - 1) : sh.ctx - 1;
           float m = -INFINITY, l = 0.f;   // l: this half's partial row sum
           for (int j = 0; j < nkv; ++j) {
+            uint32_t vis[T::BN / 32];  // sparse: visible columns of this tile
+            if (MODE == kSparse) fwd_sparse_mask<D, CAUSAL>(prm, head, j, sh.sel, slim, vis);
             const int b = t & 1;
             ok = mbar_wait(&bars->s_full[b], (t >> 1) & 1, wc, 5);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -353,7 +419,13 @@ __global__ void __launch_bounds__(512, 1)
             for (int c = 0; c < HC; c += 32) tmem_ld32(lane_base + T::S_COL + b * T::BN + (wg ^ 1) * HC + c, sr + c);
             tmem_wait_ld();
             reg_fence<HC>(sr);
-            if ((j + 1) * T::BN - 1 > lim_lo) {
+            if (MODE == kSparse) {
+  #pragma unroll
+              for (int c = 0; c < HC; ++c) {
+                const uint32_t wv = (wg ^ 1) ? vis[(HC + c) / 32] : vis[c / 32];
+                if (!((wv >> (c % 32)) & 1u)) sr[c] = __float_as_uint(-INFINITY);
+              }
+            } else if ((j + 1) * T::BN - 1 > lim_lo) {
               const int k0 = j * T::BN + (wg ^ 1) * HC;
   #pragma unroll
               for (int c = 0; c < HC; ++c)
@@ -375,7 +447,13 @@ __global__ void __launch_bounds__(512, 1)
             float s[HC];
   #pragma unroll
             for (int c = 0; c < HC; ++c) s[c] = __uint_as_float(sr[c]);
-            if ((j + 1) * T::BN - 1 > lim_lo) {
+            if (MODE == kSparse) {
+  #pragma unroll
+              for (int c = 0; c < HC; ++c) {
+                const uint32_t wv = wg ? vis[(HC + c) / 32] : vis[c / 32];
+                if (!((wv >> (c % 32)) & 1u)) s[c] = -INFINITY;
+              }
+            } else if ((j + 1) * T::BN - 1 > lim_lo) {
               const int k0 = j * T::BN + wg * HC;
   #pragma unroll
               for (int c = 0; c < HC; ++c)
@@ -395,7 +473,9 @@ __global__ void __launch_bounds__(512, 1)
             // same decision.
             const float m_tile = mx * sl2;
             const float m_new = (m_tile > m + kRescaleLog2) ? m_tile : m;
-            const float neg = -m_new;
+            // sparse: a row that has seen no visible key yet keeps m = -inf;
+            // its P must be 0, not exp2(-inf + inf)
+            const float neg = (MODE == kSparse && m_new == -INFINITY) ? 0.f : -m_new;
             // x = s * c - m and the row sum in packed fp32 pairs (one f32x2
             // instruction per two columns)
             const uint64_t c2 = f2_pack(sl2, sl2), neg2 = f2_pack(neg, neg);
@@ -416,7 +496,9 @@ __global__ void __launch_bounds__(512, 1)
   #pragma unroll
             for (int i = 0; i < 4; ++i) f2_unpack(ps2[i], ps[2 * i], ps[2 * i + 1]);
             const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-            const float alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
+            const float alpha = (MODE == kSparse && m_new == -INFINITY)
+                                    ? 1.f
+                                    : ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
             l = l * alpha + rs;
             m = m_new;
             // With two 128-column O halves (D = 256), letting P V of this tile
@@ -485,7 +567,7 @@ __global__ void __launch_bounds__(512, 1)
         for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
           int head, qa, qb;
           fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
-          const FwdItemShape<D, CAUSAL, PAGED> sh(prm, head);
+          const FwdItemShape<D, CAUSAL, MODE> sh(prm, head);
           for (int half = 0; ok && half < 2; ++half) {
             const int qt = half ? qb : qa;
             if (qt < 0) break;
@@ -496,14 +578,14 @@ __global__ void __launch_bounds__(512, 1)
             for (int s = 0; s < T::DSUB; ++s)
               tma_load_3d_hint(sq + s * T::Q_SUB, &tm_q, &bars->q_full[qs], s * 64, qt * T::BM, head, pol_q);
             ++q_it;
-            const int nkv = fwd_num_kv<D, CAUSAL>(qt, sh.nkv_full, sh.nk, sh.off);
+            const int nkv = sh.tiles(qt);
             for (int j = 0; j < nkv; ++j) {
               const int st = k_it % T::K_STAGES;
               if (!(ok = mbar_wait(&bars->k_empty[st], ((k_it / T::K_STAGES) & 1) ^ 1, wc, 2))) break;
               uint8_t* sk = smem + T::SM_K + st * T::KV_BYTES;
               mbar_arrive_expect_tx(&bars->k_full[st], T::KV_BYTES);
               if (PAGED) {
-                fwd_load_paged_tile<D, CAUSAL>(sk, &tm_k, &bars->k_full[st], prm, head, j, sh.nk, pol_kv);
+                fwd_load_paged_tile<D, CAUSAL, MODE>(sk, &tm_k, &bars->k_full[st], prm, head, j, sh.nk, sh.sel, pol_kv);
               } else {
                 for (int s = 0; s < T::DSUB; ++s)
                   tma_load_3d_hint(sk + s * T::KV_SUB, &tm_k, &bars->k_full[st], s * 64, j * T::BN, head / prm.group,
@@ -528,18 +610,18 @@ __global__ void __launch_bounds__(512, 1)
         for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
           int head, qa, qb;
           fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
-          const FwdItemShape<D, CAUSAL, PAGED> sh(prm, head);
+          const FwdItemShape<D, CAUSAL, MODE> sh(prm, head);
           for (int half = 0; ok && half < 2; ++half) {
             const int qt = half ? qb : qa;
             if (qt < 0) break;
-            const int nkv = fwd_num_kv<D, CAUSAL>(qt, sh.nkv_full, sh.nk, sh.off);
+            const int nkv = sh.tiles(qt);
             for (int j = 0; j < nkv; ++j) {
               const int st = v_it % T::V_STAGES;
               if (!(ok = mbar_wait(&bars->v_empty[st], ((v_it / T::V_STAGES) & 1) ^ 1, wc, 8))) break;
               uint8_t* sv = smem + T::SM_V + st * T::KV_BYTES;
               mbar_arrive_expect_tx(&bars->v_full[st], T::KV_BYTES);
               if (PAGED) {
-                fwd_load_paged_tile<D, CAUSAL>(sv, &tm_v, &bars->v_full[st], prm, head, j, sh.nk, pol_kv);
+                fwd_load_paged_tile<D, CAUSAL, MODE>(sv, &tm_v, &bars->v_full[st], prm, head, j, sh.nk, sh.sel, pol_kv);
               } else {
                 for (int s = 0; s < T::DSUB; ++s)
                   tma_load_3d_hint(sv + s * T::KV_SUB, &tm_v, &bars->v_full[st], s * 64, j * T::BN, head / prm.group,
@@ -562,7 +644,7 @@ __global__ void __launch_bounds__(512, 1)
 
       // S = Q K^T of the cursor's tile into S buffer tile % 2, which the
       // softmax of tile - 2 has read by then.
-      auto issue_s = [&](const FwdCursor<D, CAUSAL, PAGED>& c) -> bool {
+      auto issue_s = [&](const FwdCursor<D, CAUSAL, MODE>& c) -> bool {
         const int qs = c.item % T::Q_STAGES;
         const int st = c.tile % T::K_STAGES;
         const int b = c.tile & 1;
@@ -585,7 +667,7 @@ __global__ void __launch_bounds__(512, 1)
 
       // O += P V of the cursor's tile; the first tile of an item overwrites O,
       // which the previous item's epilogue must have read.
-      auto issue_pv = [&](const FwdCursor<D, CAUSAL, PAGED>& c) -> bool {
+      auto issue_pv = [&](const FwdCursor<D, CAUSAL, MODE>& c) -> bool {
         const int b = c.tile & 1;
         const int st = c.tile % T::V_STAGES;
         const bool first = (c.j == 0);
@@ -593,7 +675,31 @@ __global__ void __launch_bounds__(512, 1)
         if (!warp_wait(&bars->p_full[b], (c.tile >> 1) & 1, wc, 11)) return false;
         if (!warp_wait(&bars->v_full[st], (c.tile / T::V_STAGES) & 1, wc, 12)) return false;
         tc_fence_after();
-        if (PAGED && (c.j + 1) * T::BN > c.Nk) {
+        if (MODE == kSparse) {
+          // Sparse: a selected block that holds the context's end carries
+          // stale cache rows past it; zero those V rows (blocks past the
+          // selection count were loaded as zeros).
+          const int ps = prm.page_size, epb = T::BN / ps;
+          const int sb = c.head / prm.H, kvh = (c.head % prm.H) / prm.group;
+          const int* blk = prm.sel_blocks + (static_cast<size_t>(sb) * prm.Hkv + kvh) * prm.max_pages;
+          const uint32_t sv = smem_u32(smem + T::SM_V + st * T::KV_BYTES);
+          bool wrote = false;
+          for (int e = 0; e < epb; ++e) {
+            const int eg = c.j * epb + e;
+            if (eg >= c.sel) break;
+            const int valid = min(max(c.ctx - __ldg(blk + eg) * ps, 0), ps);
+            if (valid == ps) continue;
+            for (int idx = lane; idx < (ps - valid) * 8 * T::DSUB; idx += 32) {
+              const int row = e * ps + valid + idx / (8 * T::DSUB), rem = idx % (8 * T::DSUB);
+              st_shared_v4(sv + (rem / 8) * T::KV_SUB + row * 128 + (rem % 8) * 16, 0u, 0u, 0u, 0u);
+            }
+            wrote = true;
+          }
+          if (wrote) {
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        } else if (PAGED && (c.j + 1) * T::BN > c.Nk) {
           // Rows of the sequence's last page past its key count hold whatever
           // the cache holds there; P is 0 for them, but 0 * NaN is NaN, so
           // zero those V rows before P V reads them.  (Each row is the same
@@ -627,7 +733,7 @@ __global__ void __launch_bounds__(512, 1)
       // two tiles ahead of the softmax, across work items; warp 15 issues
       // P V as each tile's P becomes ready.  Neither waits behind the
       // other's dependencies.
-      FwdCursor<D, CAUSAL, PAGED> c;
+      FwdCursor<D, CAUSAL, MODE> c;
       c.start(blockIdx.x, units, nqt, &prm);
       const bool s_side = (warp == T::MMA_WARP);
       while (ok && c.valid) {
@@ -652,11 +758,11 @@ __global__ void __launch_bounds__(512, 1)
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         int head, qa, qb;
         fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
-        const FwdItemShape<D, CAUSAL, PAGED> sh(prm, head);
+        const FwdItemShape<D, CAUSAL, MODE> sh(prm, head);
         for (int half = 0; ok && half < 2; ++half) {
           const int qt = half ? qb : qa;
           if (qt < 0) break;
-          t += fwd_num_kv<D, CAUSAL>(qt, sh.nkv_full, sh.nk, sh.off);
+          t += sh.tiles(qt);
           ok = mbar_wait(&bars->lm_full, q_item & 1, wc, 17);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           const float l_row = lm[r] + lm[T::BM + r];
@@ -666,7 +772,8 @@ __global__ void __launch_bounds__(512, 1)
           ok = mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, wc, 7);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
-          const float inv_l = 1.f / l_row;
+          // sparse: a row with no visible key at all has an empty softmax
+          const float inv_l = (MODE == kSparse && !(l_row > 0.f)) ? 0.f : 1.f / l_row;
           const uint32_t so = smem_u32(smem + T::SM_Q + (q_item % T::Q_STAGES) * T::Q_BYTES) + r * 128;
   #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
@@ -688,7 +795,8 @@ __global__ void __launch_bounds__(512, 1)
           fence_proxy_async_smem();
           mbar_arrive(&bars->epi_full[q_item % T::Q_STAGES]);
           if (qt * T::BM + r < Nq)
-            prm.lse[static_cast<size_t>(head) * Nq + qt * T::BM + r] = (m + log2f(l_row)) * 0.69314718055994530942f;
+            prm.lse[static_cast<size_t>(head) * Nq + qt * T::BM + r] =
+                (MODE == kSparse && !(l_row > 0.f)) ? -INFINITY : (m + log2f(l_row)) * 0.69314718055994530942f;
           tc_fence_before();
           mbar_arrive(&bars->o_free);
           if (warp == 8) {
@@ -722,19 +830,19 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BF, bool PAGED = false>
+template <int D, bool CAUSAL, bool BF, int MODE = kDense>
 int launch_fwd(const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaStream_t stream) {
   using T = FwdTraits<D, CAUSAL>;
   static bool attr_set = false;  // per process; the attribute is per function, not per device
   if (!attr_set) {
-    if (cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL, BF, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL, BF, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              T::SMEM_ALLOC) != cudaSuccess)
       return -1;
     // the kernel splits its launch registers between warpgroups
     // (setmaxnreg); refuse to launch if the build gave it fewer than the
     // split needs, rather than let the raising warpgroups wait forever
     cudaFuncAttributes fa_attr;
-    if (cudaFuncGetAttributes(&fa_attr, fa_fwd_kernel<D, CAUSAL, BF, PAGED>) != cudaSuccess ||
+    if (cudaFuncGetAttributes(&fa_attr, fa_fwd_kernel<D, CAUSAL, BF, MODE>) != cudaSuccess ||
         fa_attr.numRegs * T::THREADS < T::SOFTMAX_THREADS * T::SOFTMAX_REGS + (T::THREADS - T::SOFTMAX_THREADS) * T::OTHER_REGS)
       return -1;
     attr_set = true;
@@ -742,7 +850,7 @@ int launch_fwd(const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaS
   const int nqt = (prm.Nq + T::BM - 1) / T::BM;
   const int units = CAUSAL ? prm.heads * ((nqt + 1) / 2) : prm.heads * nqt;
   const int grid = units < num_sms ? units : num_sms;
-  fa_fwd_kernel<D, CAUSAL, BF, PAGED><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3],
+  fa_fwd_kernel<D, CAUSAL, BF, MODE><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3],
                                                                                   prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

@@ -33,6 +33,16 @@ struct FwdParams {
   const int* context_lens;
   int H;             // query heads per sequence
   int num_pages, page_size, max_pages;
+  // Selected blocks (sparse launchers): for sequence b and K/V head kvh, list
+  // entries e < sel_count[b * Hkv + kvh] (at most max_pages) name physical
+  // page sel_pages[(b * Hkv + kvh) * max_pages + e] holding logical block
+  // sel_blocks[...]; row r of it is the token at logical position block *
+  // page_size + r, visible iff below context_lens[b] (and, causal, at most
+  // the query's own position, the queries being the context's last Nq).
+  const int* sel_pages;
+  const int* sel_blocks;
+  const int* sel_count;
+  int Hkv;
 };
 
 struct BwdParams {
@@ -85,6 +95,13 @@ int launch_fwd_paged_d128(bool causal, bool bf16, const CUtensorMap* maps, const
                           cudaStream_t stream);
 int launch_fwd_paged_d256(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,
                           cudaStream_t stream);
+// Forward over selected blocks of a paged cache; maps as for the paged launchers.
+int launch_fwd_sparse_d64(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,
+                          cudaStream_t stream);
+int launch_fwd_sparse_d128(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,
+                           cudaStream_t stream);
+int launch_fwd_sparse_d256(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,
+                           cudaStream_t stream);
 
 // Tile sizes the host needs to build tensor maps and size grids.
 inline int fwd_block_n(int D) { return D == 256 ? 64 : 128; }

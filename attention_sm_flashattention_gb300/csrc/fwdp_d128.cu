@@ -6,10 +6,10 @@ namespace fa {
 int launch_fwd_paged_d128(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,
                          cudaStream_t stream) {
   if (bf16)
-    return causal ? launch_fwd<128, true, true, true>(maps, prm, num_sms, stream)
-                  : launch_fwd<128, false, true, true>(maps, prm, num_sms, stream);
-  return causal ? launch_fwd<128, true, false, true>(maps, prm, num_sms, stream)
-                : launch_fwd<128, false, false, true>(maps, prm, num_sms, stream);
+    return causal ? launch_fwd<128, true, true, kPaged>(maps, prm, num_sms, stream)
+                  : launch_fwd<128, false, true, kPaged>(maps, prm, num_sms, stream);
+  return causal ? launch_fwd<128, true, false, kPaged>(maps, prm, num_sms, stream)
+                : launch_fwd<128, false, false, kPaged>(maps, prm, num_sms, stream);
 }
 
 }  // namespace fa

@@ -332,6 +332,22 @@ def paged_bench(args):
     ms = timed(lambda: fa.fwd_paged(q, kc, vc, table, lens, causal=CAUSAL, scale=scale, out=(o, lse)))
     clocks = sampler.stop()
     ms_dense = timed(lambda: fa.fwd(q, k, v, causal=CAUSAL, scale=scale, out=(o, lse)))
+    sparse = None
+    if args.sparse_keep > 0:
+        # selected blocks: the same random share of every sequence's blocks for
+        # each K/V head (in shuffled order), the last block always included
+        nsel = max(1, min(pages_per_seq, int(round(args.sparse_keep * pages_per_seq))))
+        order = torch.argsort(torch.rand((Z, HKV, pages_per_seq), device=dev, generator=gen), dim=2)[:, :, :nsel]
+        order[:, :, 0] = pages_per_seq - 1
+        sel_blocks = order.to(torch.int32).contiguous()
+        sel_pages = torch.gather(table.unsqueeze(1).expand(Z, HKV, pages_per_seq), 2, order).to(torch.int32).contiguous()
+        sel_count = torch.full((Z, HKV), nsel, dtype=torch.int32, device=dev)
+        ms_sparse = timed(lambda: fa.fwd_sparse(q, kc, vc, sel_pages, sel_blocks, sel_count, lens, causal=CAUSAL,
+                                                scale=scale))
+        sel_keys = Z * HKV * nsel * ps
+        sparse = {"blocks_selected": nsel, "of": pages_per_seq, "ms": ms_sparse,
+                  "speedup_vs_paged": ms / ms_sparse,
+                  "kv_gbs": 2 * sel_keys * D * q.element_size() / (ms_sparse * 1e-3) / 1e9}
     # cache write of the Z * N new tokens (ReshapeAndCache) to distinct slots
     toks = Z * N
     k_new = torch.randn((toks, HKV, D), device=dev, dtype=elem, generator=gen)
@@ -353,6 +369,7 @@ def paged_bench(args):
                    "B": Z, "H": H, "Hkv": HKV, "Nq": N, "context": NK, "D": D, "page_size": ps, "causal": CAUSAL},
         "dense_fwd_tflops": fl / (ms_dense * 1e-3) / 1e12, "dense_fwd_ms": ms_dense,
         "kv_cache_gbs": kv_bytes / (ms * 1e-3) / 1e9,
+        "sparse": sparse,
         "cache_write": {"tokens": toks, "ms": ms_write,
                         "gbs": 4 * toks * HKV * D * q.element_size() / (ms_write * 1e-3) / 1e9,
                         "peak_hbm_gbs": peaks["hbm_gbs"]},
@@ -381,6 +398,8 @@ def main():
     ap.add_argument("--nk", type=int, default=None, help="key length (default N, the query length)")
     ap.add_argument("--paged", type=int, default=0, metavar="PAGE_SIZE",
                     help="time the forward over a paged K/V cache with pages of this many tokens instead")
+    ap.add_argument("--sparse-keep", type=float, default=0.0, metavar="FRACTION",
+                    help="with --paged: also time the forward over this share of each sequence's blocks")
     ap.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
                     help="element type of the inputs and outputs (the benchmark is f16)")
     args = ap.parse_args()

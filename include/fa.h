@@ -214,6 +214,33 @@ FA_API int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache,
                         int num_pages, int page_size, int max_pages, int causal, float scale, int dtype,
                         cudaStream_t stream);
 
+/*
+ * Forward over selected blocks of a paged cache.  Source: «把 FlashAttention
+ * 搬上昇腾», the contest section's Quest Sparse Attention part: only the
+ * chosen (Top-K) blocks of a sequence get exact attention, read through the
+ * paged mapping, with per-sequence context lengths and grouped heads.  The
+ * choice itself (block scoring, Top-K) is an input of this call.
+ *
+ *   q, o, lse, k_cache, v_cache, page_size, causal, dtype : as fa_fwd_paged.
+ *   sel_pages    : int32 [B, Hkv, max_sel], device: physical pages of the
+ *                  selected blocks of sequence b for K/V head kvh.
+ *   sel_blocks   : int32 [B, Hkv, max_sel], device: the logical block each
+ *                  of them holds (row r is the token at position block *
+ *                  page_size + r).
+ *   sel_count    : int32 [B, Hkv], device: entries in use (clamped to
+ *                  [0, max_sel]).
+ *   context_lens : int32 [B], device: tokens at positions >= context_lens[b]
+ *                  never take part (the last block's invalid tokens); with
+ *                  causal, the queries are the last Nq tokens of the context
+ *                  and see positions up to their own.
+ * Selected blocks may come in any order.  A query row that sees no selected
+ * token gets O = 0 and lse = -inf.  Errors as for fa_fwd_paged.
+ */
+FA_API int fa_fwd_sparse(const void* q, const void* k_cache, const void* v_cache, const int* sel_pages,
+                         const int* sel_blocks, const int* sel_count, const int* context_lens, void* o, float* lse,
+                         int B, int H, int Hkv, int Nq, int D, int num_pages, int page_size, int max_sel, int causal,
+                         float scale, int dtype, cudaStream_t stream);
+
 FA_API size_t fa_bwd_ex_workspace_size(int Z, int H, int Hkv, int Nq, int Nk, int D, int causal);
 
 FA_API int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,

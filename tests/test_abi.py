@@ -193,3 +193,14 @@ def test_reshape_and_cache_argument_checks(lib):
     assert f(FAKE, FAKE, None, FAKE, FAKE, 3, 2, 64, 4, 16, None) == _native.FA_ERR_INVALID_ARG
     assert f(FAKE, FAKE, FAKE + 4, FAKE, FAKE, 3, 2, 64, 4, 16, None) == _native.FA_ERR_INVALID_ARG  # int64 slots
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 2, 64, 4, 16, None) == _native.FA_ERR_INVALID_ARG
+
+
+def test_fwd_sparse_argument_checks(lib):
+    def call(pages=FAKE, blocks=FAKE, count=FAKE, page_size=64, D=128, max_sel=4):
+        return lib.fa_fwd_sparse(FAKE, FAKE, FAKE, pages, blocks, count, FAKE, FAKE, FAKE, 2, 4, 2, 1, D, 8,
+                                 page_size, max_sel, 0, 0.125, 0, None)
+    assert call(blocks=None) == _native.FA_ERR_INVALID_ARG
+    assert call(count=FAKE + 2) == _native.FA_ERR_INVALID_ARG
+    assert call(max_sel=0) == _native.FA_ERR_INVALID_ARG
+    assert call(page_size=24) == _native.FA_ERR_UNSUPPORTED
+    assert call(D=256, page_size=128) == _native.FA_ERR_UNSUPPORTED
