@@ -185,16 +185,23 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, c
 
   const int D = sh.D;
   const int bn = fa::fwd_block_n(D);
+  // Few queries per head (decode): the G query heads of a K/V head run as one
+  // head of G * Nq rows (consecutive in q, o and lse), so K/V tiles are read
+  // once per K/V head and the 128-row query tiles are filled.
+  const bool pack = sh.group() > 1 && sh.group() * sh.Nq <= 128;
+  const long long qh = pack ? sh.kv_heads() : sh.q_heads();
+  const int rows = pack ? sh.group() * sh.Nq : sh.Nq;
   CUtensorMap maps[4];  // q, k, v, o
-  if (!map16(&maps[0], q, sh.q_heads(), sh.Nq, D, 128, bf16) || !map16(&maps[1], k, sh.kv_heads(), sh.Nk, D, bn, bf16) ||
-      !map16(&maps[2], v, sh.kv_heads(), sh.Nk, D, bn, bf16) || !map16(&maps[3], o, sh.q_heads(), sh.Nq, D, 128, bf16))
+  if (!map16(&maps[0], q, qh, rows, D, 128, bf16) || !map16(&maps[1], k, sh.kv_heads(), sh.Nk, D, bn, bf16) ||
+      !map16(&maps[2], v, sh.kv_heads(), sh.Nk, D, bn, bf16) || !map16(&maps[3], o, qh, rows, D, 128, bf16))
     return FA_ERR_CUDA;
   fa::FwdParams prm{};
   prm.o = static_cast<__half*>(o);
   prm.lse = lse;
-  prm.heads = static_cast<int>(sh.q_heads());
-  prm.group = sh.group();
-  prm.Nq = sh.Nq;
+  prm.heads = static_cast<int>(qh);
+  prm.group = pack ? 1 : sh.group();
+  prm.q_period = pack ? sh.Nq : 0;
+  prm.Nq = rows;
   prm.Nk = sh.Nk;
   prm.causal_off = sh.Nk - sh.Nq;
   prm.scale_log2 = scale * kLog2e;
@@ -279,20 +286,26 @@ int paged_impl(int mode, const void* q, const void* k_cache, const void* v_cache
   if (rc != FA_OK) return rc;
   const bool bf16 = dtype == FA_DTYPE_BF16;
   const auto et = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  // decode-sized calls pack the query heads of a K/V head (see fwd_impl)
+  const int g = H / Hkv;
+  const bool pack = g > 1 && g * Nq <= 128;
+  const int hps = pack ? Hkv : H;         // (packed) query heads per sequence
+  const int rows = pack ? g * Nq : Nq;
   CUtensorMap maps[4];  // q, k cache, v cache, o
   std::memset(&maps[1], 0, sizeof(CUtensorMap));
   std::memset(&maps[2], 0, sizeof(CUtensorMap));
-  if (!map16(&maps[0], q, static_cast<long long>(B) * H, Nq, D, 128, bf16) ||
+  if (!map16(&maps[0], q, static_cast<long long>(B) * hps, rows, D, 128, bf16) ||
       !fa::make_tmap_paged(&maps[1], k_cache, et, 2, num_pages, page_size, Hkv, D, 64, true) ||
       !fa::make_tmap_paged(&maps[2], v_cache, et, 2, num_pages, page_size, Hkv, D, 64, true) ||
-      !map16(&maps[3], o, static_cast<long long>(B) * H, Nq, D, 128, bf16))
+      !map16(&maps[3], o, static_cast<long long>(B) * hps, rows, D, 128, bf16))
     return FA_ERR_CUDA;
   fa::FwdParams prm{};
   prm.o = static_cast<__half*>(o);
   prm.lse = lse;
-  prm.heads = B * H;
-  prm.group = H / Hkv;
-  prm.Nq = Nq;
+  prm.heads = B * hps;
+  prm.group = pack ? 1 : g;
+  prm.q_period = pack ? Nq : 0;
+  prm.Nq = rows;
   prm.Nk = max_entries * page_size;  // per sequence: context_lens[b] (paged), the selection (sparse)
   prm.causal_off = 0;
   prm.scale_log2 = scale * kLog2e;
@@ -302,7 +315,7 @@ int paged_impl(int mode, const void* q, const void* k_cache, const void* v_cache
   prm.sel_blocks = blocks;
   prm.sel_count = counts;
   prm.context_lens = context_lens;
-  prm.H = H;
+  prm.H = hps;
   prm.Hkv = Hkv;
   prm.num_pages = num_pages;
   prm.page_size = page_size;

@@ -161,16 +161,28 @@ enum FwdMode : int { kDense = 0, kPaged = 1, kSparse = 2 };
 // the selected blocks (at least one block, so that every item has a tile);
 // `ctx` is the context length that the keys' logical positions are masked
 // against, `sel` the number of selected blocks.
+// Key tiles of query tile qt: all of them when sparse, or when packed
+// grouped heads put every query position in every tile (then up to the last
+// key the last position sees); otherwise fwd_num_kv.
+template <int D, bool CAUSAL, int MODE>
+__device__ __forceinline__ int fwd_item_tiles(int qt, int nkv_full, int nk, int off, int qp) {
+  if (MODE == kSparse) return nkv_full;
+  if (CAUSAL && qp > 0) return (min(qp + off, nk) + FwdTraits<D, CAUSAL>::BN - 1) / FwdTraits<D, CAUSAL>::BN;
+  return fwd_num_kv<D, CAUSAL>(qt, nkv_full, nk, off);
+}
+
 template <int D, bool CAUSAL, int MODE>
 struct FwdItemShape {
-  int nk, off, nkv_full, ctx, sel;
+  int nk, off, nkv_full, ctx, sel, qp;
   __device__ __forceinline__ FwdItemShape(const FwdParams& prm, int head) {
     int n = prm.Nk;
     ctx = 0;
     sel = 0;
+    qp = prm.q_period;
+    const int nq_pos = qp > 0 ? qp : prm.Nq;  // query positions per head
     if (MODE == kPaged) {
       n = __ldg(prm.context_lens + head / prm.H);
-      n = min(max(n, CAUSAL ? prm.Nq : 1), prm.max_pages * prm.page_size);
+      n = min(max(n, CAUSAL ? nq_pos : 1), prm.max_pages * prm.page_size);
     } else if (MODE == kSparse) {
       const int b = head / prm.H, kvh = (head % prm.H) / prm.group;
       ctx = max(__ldg(prm.context_lens + b), 0);
@@ -178,14 +190,12 @@ struct FwdItemShape {
       n = max(sel, 1) * prm.page_size;
     }
     nk = n;
-    off = (MODE == kSparse ? ctx : n) - prm.Nq;
+    off = (MODE == kSparse ? ctx : n) - nq_pos;
     nkv_full = (n + FwdTraits<D, CAUSAL>::BN - 1) / FwdTraits<D, CAUSAL>::BN;
   }
   // key tiles of query tile qt (selected blocks carry arbitrary positions,
   // so the causal bound does not shorten a sparse item)
-  __device__ __forceinline__ int tiles(int qt) const {
-    return MODE == kSparse ? nkv_full : fwd_num_kv<D, CAUSAL>(qt, nkv_full, nk, off);
-  }
+  __device__ __forceinline__ int tiles(int qt) const { return fwd_item_tiles<D, CAUSAL, MODE>(qt, nkv_full, nk, off, qp); }
 };
 
 // Sparse mode: which of key tile j's BN columns query row qi may see, as a
@@ -237,8 +247,7 @@ struct FwdCursor {
   int u, half, head, qt, qb, j, nkv;
   uint32_t item, tile;
   bool valid;
-  int units, nqt, nkv_full, Nk, off, ctx, sel;
-  bool sparse;
+  int units, nqt, nkv_full, Nk, off, ctx, sel, qp;
   const FwdParams* prm;
 
   __device__ void start(int first_unit, int units_, int nqt_, const FwdParams* prm_) {
@@ -263,10 +272,10 @@ struct FwdCursor {
     nkv_full = sh.nkv_full;
     ctx = sh.ctx;
     sel = sh.sel;
+    qp = sh.qp;
     qt = qa;
     half = 0;
-    sparse = MODE == kSparse;
-    nkv = sparse ? nkv_full : fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
+    nkv = fwd_item_tiles<D, CAUSAL, MODE>(qt, nkv_full, Nk, off, qp);
   }
   __device__ void advance() {
     ++tile;
@@ -276,7 +285,7 @@ struct FwdCursor {
     if (half == 0 && qb >= 0) {
       half = 1;
       qt = qb;
-      nkv = sparse ? nkv_full : fwd_num_kv<D, CAUSAL>(qt, nkv_full, Nk, off);
+      nkv = fwd_item_tiles<D, CAUSAL, MODE>(qt, nkv_full, Nk, off, qp);
     } else {
       u += gridDim.x;
       load_unit();
@@ -399,11 +408,13 @@ __global__ void __launch_bounds__(512, 1)
           const int qt = half ? qb : qa;
           if (qt < 0) break;
           const int nkv = sh.tiles(qt);
-          const int qi = qt * T::BM + r;  // query index within the head
-          const int lim = fwd_key_limit<CAUSAL>(qi, Nk, off);             // this row's last key
-          const int lim_lo = fwd_key_limit<CAUSAL>(qt * T::BM, Nk, off);  // the tile's smallest limit
+          const int qi = qt * T::BM + r;  // query row within the head
+          const int qpos = sh.qp > 0 ? qi % sh.qp : qi;  // its query position
+          const int lim = fwd_key_limit<CAUSAL>(qpos, Nk, off);  // this row's last key
+          // the tile's smallest limit (packed heads: every tile holds position 0)
+          const int lim_lo = fwd_key_limit<CAUSAL>(sh.qp > 0 ? 0 : qt * T::BM, Nk, off);
           // sparse: the row's last visible logical position
-          const int slim = CAUSAL ? min(qi + sh.off, sh.ctx - 1) : sh.ctx - 1;
+          const int slim = CAUSAL ? min(qpos + sh.off, sh.ctx - 1) : sh.ctx - 1;
           float m = -INFINITY, l = 0.f;   // l: this half's partial row sum
           for (int j = 0; j < nkv; ++j) {
             uint32_t vis[T::BN / 32];  // sparse: visible columns of this tile

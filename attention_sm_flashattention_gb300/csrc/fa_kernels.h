@@ -43,6 +43,11 @@ struct FwdParams {
   const int* sel_blocks;
   const int* sel_count;
   int Hkv;
+  // Packed grouped heads (0 = off): the G query heads that share a K/V head
+  // run as one head of G * q_period rows (they are consecutive in memory);
+  // row r is query position r % q_period, and `heads`, `group`, `Nq` and `H`
+  // describe the packed problem (group 1).
+  int q_period;
 };
 
 struct BwdParams {

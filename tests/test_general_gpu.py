@@ -38,6 +38,12 @@ UNEQUAL = [
     (1, 2, 2, 300, 100, 128),   # more queries than keys: non-causal only
 ]
 GROUPED = [
+    # few queries per head: the query heads of a K/V head are packed into
+    # one tile (rows cycle through the query positions)
+    (2, 8, 2, 8, 300, 128),
+    (1, 16, 2, 16, 16, 64),
+    (2, 4, 1, 1, 500, 256),
+    (3, 6, 2, 40, 77, 128),
     (2, 8, 2, 256, 256, 128),
     (1, 4, 1, 384, 384, 64),
     (1, 6, 3, 200, 333, 128),

@@ -34,6 +34,8 @@ CASES = [
     (2, 6, 3, 200, (300, 713), 128, 32),
     (1, 4, 2, 128, (128,), 64, 16),
     (2, 4, 4, 130, (500, 131), 256, 32),
+    (2, 8, 2, 16, (300, 500), 128, 32),     # packed query heads, causal positions cycle every 16 rows
+    (2, 12, 3, 5, (37, 260), 64, 16),
 ]
 
 

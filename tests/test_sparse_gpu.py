@@ -64,6 +64,7 @@ CASES = [
     (2, 4, 2, 1, (200, 333), 256, 32, 0.5),
     (2, 6, 3, 64, (300, 713), 128, 32, 0.7),
     (1, 4, 2, 130, (500,), 256, 64, 0.5),
+    (2, 8, 2, 4, (300, 700), 128, 64, 0.5),   # packed query heads
 ]
 
 
