@@ -7,8 +7,10 @@
 //
 // fa_bwd_prep_kernel: Delta in fp32 and lse2 = lse * log2(e) for every query
 // row (HBM-bound, one pass over O and dO), into the padded [heads, Nq_pad]
-// workspace vectors that the dK/dV and dQ kernels (fa_bwd2.cuh for D <= 128,
-// fa_bwd256.cuh for D = 256) read per query tile.
+// workspace vectors that the dK/dV and dQ kernels read per query tile (D =
+// 64 in fa_bwd2.cuh, D = 256 in fa_bwd256.cuh).  For D = 128 the dQ kernel
+// (fa_bwd2.cuh) forms the same two vectors itself, from the dO tile it holds
+// anyway.
 #pragma once
 
 #include "fa_kernels.h"

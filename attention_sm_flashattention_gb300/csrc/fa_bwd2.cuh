@@ -20,9 +20,13 @@
 //      dV_j += P^T dO_i                 (A from TMEM)
 //      dK_j += dS^T Q_i                 (A from TMEM)
 //    and dK_j (times scale), dV_j are written once at the end of the unit.
-//  fa_bwd_dq_kernel: one work unit per (head, query tile i).  Q_i and dO_i
-//    stay in shared memory; K_j and V_j stream through separate rings.  Per
-//    tile, with M = queries: S = Q_i K_j^T, P = exp2(S * c - lse2_i),
+//  fa_bwd_dq_kernel (runs first): one work unit per (head, query tile i).
+//    Q_i and dO_i stay in shared memory; K_j and V_j stream through separate
+//    rings.  For D = 128, in its first key tile the compute warps form Delta_i =
+//    rowsum(O_i * dO_i) from dO_i in shared memory and O_i read from global
+//    memory (prefetched into L2 during the previous unit), and write Delta_i
+//    and lse2_i to the workspace that the dK/dV kernel reads.  Per tile,
+//    with M = queries: S = Q_i K_j^T, P = exp2(S * c - lse2_i),
 //    dP = dO_i V_j^T (double-buffered in TMEM), dS = P * (dP - Delta_i)
 //    (fp16 into TMEM over its dP), dQ_i += dS K_j (A from TMEM); dQ_i (times
 //    scale) is written once at the end of the unit.  S is released as soon
@@ -72,7 +76,12 @@ struct Bwd2Traits {
   static constexpr int B_SM_Q = 0, B_SM_DO = TILE, B_SM_K = 2 * TILE;
   static constexpr int B_SM_V = B_SM_K + B_K_STAGES * TILE;
   static constexpr int B_SM_BAR = B_SM_V + B_V_STAGES * TILE;
-  static constexpr int B_SM_BYTES = B_SM_BAR + 256;
+  // D = 128: the dQ kernel forms Delta and lse2 itself (from the dO tile it
+  // holds); D = 64 (half the MMA work per tile, so the fixed per-item cost
+  // weighs twice as much) measured faster with the separate preprocess.
+  static constexpr bool kFuseDelta = (D == 128);
+  static constexpr int B_SM_DX = B_SM_BAR + 512;        // Delta halves: [unit parity][warpgroup][BM] fp32
+  static constexpr int B_SM_BYTES = B_SM_DX + 2 * 2 * BM * 4;
   static constexpr int B_SMEM = B_SM_BYTES > MIN_SMEM ? B_SM_BYTES : MIN_SMEM;
   static_assert(B_SMEM <= 232448, "dQ kernel shared memory budget");
   static_assert(B_DP + 2 * BN <= 512, "dQ kernel TMEM budget");
@@ -575,10 +584,11 @@ struct DqBars {
   uint64_t dp_full[2], ds_full[2], dq_done[2];
   uint64_t dq_full, dq_free, mma_done[2];
   uint64_t epi_full;  // dQ_i staged in the Q buffer
+  uint64_t dx_full[2];  // both Delta halves of a unit's rows are in shared memory
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(DqBars) <= 256, "barrier area");
+static_assert(sizeof(DqBars) <= 512, "barrier area");
 
 template <int D, bool CAUSAL, bool BF>
 __global__ void __launch_bounds__(384, 1)
@@ -600,8 +610,12 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
+    // Q_i, dO_i are free once the unit's last dP completed (MMA commit) and
+    // the compute warps have read dO_i for Delta
+    mbar_init(&bars->q_empty, T::kFuseDelta ? 1 + NCOMPUTE : 1);
     mbar_init(&bars->epi_full, NCOMPUTE);
+    mbar_init(&bars->dx_full[0], NCOMPUTE);
+    mbar_init(&bars->dx_full[1], NCOMPUTE);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
@@ -862,9 +876,42 @@ __global__ void __launch_bounds__(384, 1)
         // (the causal diagonal, or the ragged end of the keys) are masked
         const int lim = CAUSAL ? min(query + coff, Nk - 1) : Nk - 1;
         const int lim_lo = CAUSAL ? min(i * T::BM + coff, Nk - 1) : Nk - 1;
-        const float lse2 = __ldg(prm.lse2 + grow);
-        const float delta = __ldg(prm.delta + grow);
-        const uint64_t c2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2), nd2 = f2_pack(-delta, -delta);
+        // ---- Delta_i = rowsum(O_i * dO_i) and lse2 = lse * log2(e) of this
+        // row.  O_i is read here (its line was prefetched into L2 during the
+        // previous item); the sum is formed after P of the item's first key
+        // tile, so the load hides behind S of that tile.
+        const bool live = query < prm.Nq;
+        const size_t src = static_cast<size_t>(head) * prm.Nq + query;  // row of O, dO and lse
+        constexpr int NV = D / 16;  // 16-byte vectors in half a row
+        uint4 ov[NV];
+        if (T::kFuseDelta && live) {
+          const __half* orow = prm.o + src * D + wg * (D / 2);
+#pragma unroll
+          for (int e = 0; e < NV; ++e) ov[e] = ldg_nc_v4(orow + e * 8);
+        } else {
+#pragma unroll
+          for (int e = 0; e < NV; ++e) ov[e] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        const float lse2 = !T::kFuseDelta ? __ldg(prm.lse2 + grow)
+                           : live ? __ldg(prm.lse + src) * 1.4426950408889634f : INFINITY;
+        if (T::kFuseDelta) {
+          // the next item's O rows into L2
+          int nh = head, ni = -1;
+          if (half == 0 && ib >= 0) {
+            ni = ib;
+          } else if (u + static_cast<int>(gridDim.x) < units) {
+            int nb;
+            bwd2_decode<CAUSAL>(u + gridDim.x, nqt, nh, ni, nb);
+          }
+          const int nq = ni * T::BM + row;
+          if (ni >= 0 && nq < prm.Nq) prefetch_l2(prm.o + (static_cast<size_t>(nh) * prm.Nq + nq) * D + wg * (D / 2));
+        }
+        uint64_t nd2 = 0ull;
+        if (!T::kFuseDelta) {
+          const float delta = __ldg(prm.delta + grow);
+          nd2 = f2_pack(-delta, -delta);
+        }
+        const uint64_t c2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2);
         for (int j = 0; j < num_kv(i); ++j) {
           const int pb = t & 1;
           const int k0 = j * T::BN + wg * T::QC;  // first key column of this warpgroup
@@ -891,6 +938,40 @@ __global__ void __launch_bounds__(384, 1)
               if (k0 + c + 1 > lim) p1 = 0.f;
             }
             p2[c / 2] = f2_pack(p0, p1);
+          }
+          if (T::kFuseDelta && j == 0) {
+            // Delta: this warpgroup's half of the columns (dO_i from the tile
+            // in shared memory), the two halves summed through shared memory
+            ok = mbar_wait(&bars->q_full, qc & 1, wc, 104);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            float dacc[2] = {0.f, 0.f};
+#pragma unroll
+            for (int e = 0; e < NV; ++e) {
+              const int col = wg * (D / 2) + e * 8;
+              const uint32_t a = smem_u32(smem + T::B_SM_DO) + (col / 64) * T::SUB + row * 128 +
+                                 ((((col % 64) / 8) ^ (row & 7)) << 4);
+              const uint4 dv4 = ld_shared_v4(a);
+              const uint32_t dw[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+              const uint32_t ow[4] = {ov[e].x, ov[e].y, ov[e].z, ov[e].w};
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                const float2 x = unpack2<BF>(ow[w]), y = unpack2<BF>(dw[w]);
+                dacc[w & 1] = fmaf(x.x, y.x, dacc[w & 1]);
+                dacc[w & 1] = fmaf(x.y, y.y, dacc[w & 1]);
+              }
+            }
+            mbar_arrive(&bars->q_empty);  // dO_i read
+            float* dx = reinterpret_cast<float*>(smem + T::B_SM_DX) + (qc & 1) * 2 * T::BM;
+            dx[wg * T::BM + row] = dacc[0] + dacc[1];
+            mbar_arrive(&bars->dx_full[qc & 1]);
+            ok = mbar_wait(&bars->dx_full[qc & 1], (qc >> 1) & 1, wc, 105);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            const float delta = dx[row] + dx[T::BM + row];  // the same sum in both warpgroups
+            nd2 = f2_pack(-delta, -delta);
+            if (wg == 0) {
+              prm.delta[grow] = delta;
+              prm.lse2[grow] = lse2;
+            }
           }
           // ---- dS = P * (dP - Delta), fp16 into TMEM over dP
           ok = mbar_wait(&bars->dp_full[pb], (t >> 1) & 1, wc, 102);
@@ -947,8 +1028,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-// Delta/lse2 preprocess, then the dK/dV and dQ kernels on the same stream.
-// `max_ctas` caps each persistent grid (normally the SM count).
+// The dQ kernel (for D = 128 it also writes Delta and lse2 of every query
+// row; for D = 64 the preprocess kernel runs first), then the dK/dV kernel,
+// on the same stream.  `max_ctas` caps each persistent
+// grid (normally the SM count).
 template <int D, bool CAUSAL, bool BF>
 int launch_bwd2(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, cudaStream_t stream) {
   using T = Bwd2Traits<D>;
@@ -961,17 +1044,19 @@ int launch_bwd2(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, cud
       return -1;
     attr_set = true;
   }
-  if (launch_prep<D, BF>(prm, stream) != 0) return -1;
+  if constexpr (!T::kFuseDelta) {
+    if (launch_prep<D, BF>(prm, stream) != 0) return -1;
+  }
   auto grid_for = [&](int heads, int tiles) {
     const long long units = CAUSAL ? static_cast<long long>(heads) * ((tiles + 1) / 2) : static_cast<long long>(heads) * tiles;
     return static_cast<int>(units < max_ctas ? units : max_ctas);
   };
   const int nqt = (prm.Nq + T::BM - 1) / T::BM, nkv = (prm.Nk + T::BN - 1) / T::BN;
-  fa_bwd_dkdv_kernel<D, CAUSAL, BF><<<grid_for(prm.heads / prm.group, nkv), 384, T::A_SMEM, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], maps[5], maps[6], prm);
-  if (cudaGetLastError() != cudaSuccess) return -1;
   fa_bwd_dq_kernel<D, CAUSAL, BF><<<grid_for(prm.heads, nqt), 384, T::B_SMEM, stream>>>(maps[0], maps[1], maps[2],
                                                                                        maps[3], maps[4], prm);
+  if (cudaGetLastError() != cudaSuccess) return -1;
+  fa_bwd_dkdv_kernel<D, CAUSAL, BF><<<grid_for(prm.heads / prm.group, nkv), 384, T::A_SMEM, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], maps[5], maps[6], prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

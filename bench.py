@@ -1,7 +1,8 @@
 """Benchmark: attention fwd + bwd TFLOP/s on one GB300 (Z128 H8 N1024 D128).
 
 One step = one pass of the whole hot path over one batch: fa_fwd (O, lse)
-then fa_bwd (Delta preprocess + main kernel -> dQ, dK, dV), fp16 in, fp32
+then fa_bwd (D128: dQ kernel with Delta, dK/dV kernel; D64 and D256 add a
+Delta preprocess kernel), fp16 in, fp32
 accumulate.  FLOPs are the algorithmic count (forward 4 N^2 D per head, the
 backward 2.5x that); the work the method avoids is not counted.
 
@@ -270,12 +271,16 @@ def bwd_kernel_names(d, causal):
     c = str(bool(causal)).lower()
     if d == 256:
         return f"fa_bwd call: fa_bwd_prep_kernel<{d}> + fa_bwd256_dkdv_kernel<{c}> + fa_bwd256_dq_kernel<{c}>"
-    return f"fa_bwd call: fa_bwd_prep_kernel<{d}> + fa_bwd_dkdv_kernel<{d},{c}> + fa_bwd_dq_kernel<{d},{c}>"
+    if d == 64:
+        return f"fa_bwd call: fa_bwd_prep_kernel<{d}> + fa_bwd_dq_kernel<{d},{c}> + fa_bwd_dkdv_kernel<{d},{c}>"
+    return f"fa_bwd call: fa_bwd_dq_kernel<{d},{c}> (with Delta) + fa_bwd_dkdv_kernel<{d},{c}>"
 
 
 def bwd_launches(d):
-    """Kernels one fa_bwd call launches (Delta preprocess, dK/dV kernel, dQ kernel)."""
-    return 3
+    """Kernels one fa_bwd call launches: D = 64 and 256 run a Delta
+    preprocess, a dK/dV and a dQ kernel; D = 128 a dQ kernel that also forms
+    Delta, then a dK/dV kernel."""
+    return 2 if d == 128 else 3
 
 
 def load_traffic():
