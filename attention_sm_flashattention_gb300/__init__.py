@@ -5,4 +5,4 @@
 first call; if it is missing the call raises -- there is no other path.
 """
 
-from .api import bwd, bwd_flops, bwd_workspace_size, device_status, fwd, fwd_flops, fwd_paged, fwd_sparse, reshape_and_cache  # noqa: F401
+from .api import bwd, bwd_flops, bwd_workspace_size, device_status, fwd, fwd_flops, fwd_paged, fwd_sparse, paged_split_count, reshape_and_cache  # noqa: F401

@@ -38,6 +38,9 @@ SIGNATURES = {
     "fa_reshape_and_cache": (_i, [_vp] * 5 + [_i] * 5 + [_vp]),
     "fa_fwd_sparse": (_i, [_vp] * 9 + [_i] * 9 + [_f, _i, _vp]),
     "fa_fwd_paged": (_i, [_vp] * 7 + [_i] * 9 + [_f, _i, _vp]),
+    "fa_fwd_paged_split": (_i, [_vp] * 8 + [_sz] + [_i] * 10 + [_f, _i, _vp]),
+    "fa_fwd_paged_split_workspace_size": (_sz, [_i] * 5),
+    "fa_fwd_paged_split_count": (_i, [_i] * 8),
     "fa_bwd_ex_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
     "fa_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),

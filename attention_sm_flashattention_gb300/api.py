@@ -105,12 +105,19 @@ def reshape_and_cache(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: to
 def fwd_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
               context_lens: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
               out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
-              stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+              stream: Optional[torch.cuda.Stream] = None, splits: int = 1,
+              workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Attention forward over a paged K/V cache.  q [B,H,Nq,D]; k_cache,
     v_cache [num_pages, page_size, Hkv, D] (q's dtype); block_table int32
     [B, max_pages] (sequence b's key p is in page block_table[b, p //
     page_size]); context_lens int32 [B].  Causal: the queries are the last
-    Nq of each sequence's context.  Returns ``(o, lse)`` like :func:`fwd`."""
+    Nq of each sequence's context.  Returns ``(o, lse)`` like :func:`fwd`.
+
+    ``splits`` > 1 cuts each sequence's key range into that many slices
+    (``fa_fwd_paged_split``, for batches too small to fill the GPU); 0 lets
+    the library choose (``fa_fwd_paged_split_count``).  ``workspace`` is an
+    optional uint8 CUDA tensor of at least
+    ``fa_fwd_paged_split_workspace_size`` bytes; one is allocated if None."""
     _check_input("q", q)
     for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
         _check_input(name, t, q.dtype)
@@ -132,12 +139,33 @@ def fwd_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, blo
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     else:
         o, lse = out
-    rc = _native.lib().fa_fwd_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
-                                    context_lens.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, Nq, D,
-                                    num_pages, page_size, block_table.shape[1], int(bool(causal)), float(scale),
-                                    _dtype_code(q), _stream_handle(stream))
-    _native.check(rc, "fa_fwd_paged")
+    lib = _native.lib()
+    max_pages = block_table.shape[1]
+    if splits == 0:
+        splits = lib.fa_fwd_paged_split_count(B, H, Hkv, Nq, D, page_size, max_pages, int(bool(causal)))
+    if splits == 1:
+        rc = lib.fa_fwd_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+                              context_lens.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, Nq, D, num_pages,
+                              page_size, max_pages, int(bool(causal)), float(scale), _dtype_code(q),
+                              _stream_handle(stream))
+        _native.check(rc, "fa_fwd_paged")
+        return o, lse
+    need = lib.fa_fwd_paged_split_workspace_size(B, H, Nq, D, int(splits))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    rc = lib.fa_fwd_paged_split(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+                                context_lens.data_ptr(), o.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), B, H, Hkv, Nq, D, num_pages, page_size,
+                                max_pages, int(splits), int(bool(causal)), float(scale), _dtype_code(q),
+                                _stream_handle(stream))
+    _native.check(rc, "fa_fwd_paged_split")
     return o, lse
+
+
+def paged_split_count(B: int, H: int, Hkv: int, Nq: int, D: int, page_size: int, max_pages: int,
+                      causal: bool = False) -> int:
+    """The slice count ``fwd_paged(splits=0)`` would use on the current device."""
+    return _native.lib().fa_fwd_paged_split_count(B, H, Hkv, Nq, D, page_size, max_pages, int(bool(causal)))
 
 
 def fwd_sparse(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, sel_pages: torch.Tensor,

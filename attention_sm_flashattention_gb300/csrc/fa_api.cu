@@ -132,7 +132,7 @@ const char* fa_error_string(int code) {
     case FA_OK: return "ok";
     case FA_ERR_INVALID_ARG: return "invalid argument (null/misaligned pointer, non-positive size, bad scale or causal flag)";
     case FA_ERR_UNSUPPORTED: return "unsupported shape (D must be 64, 128 or 256; causal needs Nq <= Nk; Z*H*N < 2^31)";
-    case FA_ERR_WORKSPACE: return "workspace missing or smaller than fa_bwd_workspace_size()";
+    case FA_ERR_WORKSPACE: return "workspace missing, misaligned or smaller than its size query returns";
     case FA_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
     case FA_ERR_DEVICE: return "current device is not a compute capability 10.3 (sm_103a) GPU";
     case FA_ERR_TIMEOUT: return "a device-side wait gave up; outputs since the last status check are invalid";
@@ -253,15 +253,26 @@ int fa_reshape_and_cache(const void* k_new, const void* v_new, const long long* 
 
 namespace {
 
-// Shared by the paged and the selected-block forward: argument checks, the
-// 4-D cache maps and the launch.  `lists` is the block table (paged) or the
-// selected-page list (sparse); `blocks` and `counts` are the sparse-only
-// logical blocks and selection counts.
+// Split paged forward workspace: per-slice lse [splits, rows] then per-slice
+// O [splits, rows, D], fp32, rows = B * H * Nq (query rows of the call).
+constexpr int kMaxSplits = 256;
+long long split_lse_bytes(long long rows, int splits) { return (rows * splits * 4 + 255) / 256 * 256; }
+long long split_workspace_bytes(long long rows, int D, int splits) {
+  return split_lse_bytes(rows, splits) + rows * splits * D * 4;
+}
+
+// Shared by the paged, the split paged and the selected-block forward:
+// argument checks, the 4-D cache maps and the launch.  `lists` is the block
+// table (paged) or the selected-page list (sparse); `blocks` and `counts` are
+// the sparse-only logical blocks and selection counts; `splits` and the
+// workspace are the split mode's (mode 3).
 int paged_impl(int mode, const void* q, const void* k_cache, const void* v_cache, const int* lists,
                const int* blocks, const int* counts, const int* context_lens, void* o, float* lse, int B, int H,
                int Hkv, int Nq, int D, int num_pages, int page_size, int max_entries, int causal, float scale,
-               int dtype, cudaStream_t stream) {
-  const bool sparse = mode == 2;
+               int dtype, int splits, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const bool sparse = mode == 2, split = mode == 3;
+  if (split && (splits < 1 || splits > kMaxSplits)) return FA_ERR_INVALID_ARG;
+  if (split && (!workspace || !aligned(workspace, 16))) return FA_ERR_WORKSPACE;
   if (!q || !k_cache || !v_cache || !lists || !context_lens || !o || !lse) return FA_ERR_INVALID_ARG;
   if (sparse && (!blocks || !counts)) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
@@ -320,8 +331,23 @@ int paged_impl(int mode, const void* q, const void* k_cache, const void* v_cache
   prm.num_pages = num_pages;
   prm.page_size = page_size;
   prm.max_pages = max_entries;
+  prm.splits = 1;
+  if (split) {
+    const long long rows_total = static_cast<long long>(B) * H * Nq;
+    if (static_cast<unsigned long long>(split_workspace_bytes(rows_total, D, splits)) > workspace_bytes)
+      return FA_ERR_WORKSPACE;
+    prm.splits = splits;
+    prm.part_lse = static_cast<float*>(workspace);
+    prm.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + split_lse_bytes(rows_total, splits));
+  }
   const bool c = causal != 0;
-  if (sparse) {
+  if (split) {
+    switch (D) {
+      case 64: rc = fa::launch_fwd_paged_split_d64(c, bf16, maps, prm, dev->sms, stream); break;
+      case 128: rc = fa::launch_fwd_paged_split_d128(c, bf16, maps, prm, dev->sms, stream); break;
+      default: rc = fa::launch_fwd_paged_split_d256(c, bf16, maps, prm, dev->sms, stream); break;
+    }
+  } else if (sparse) {
     switch (D) {
       case 64: rc = fa::launch_fwd_sparse_d64(c, bf16, maps, prm, dev->sms, stream); break;
       case 128: rc = fa::launch_fwd_sparse_d128(c, bf16, maps, prm, dev->sms, stream); break;
@@ -345,7 +371,45 @@ int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const 
                  const int* context_lens, void* o, float* lse, int B, int H, int Hkv, int Nq, int D, int num_pages,
                  int page_size, int max_pages, int causal, float scale, int dtype, cudaStream_t stream) {
   return paged_impl(1, q, k_cache, v_cache, block_table, nullptr, nullptr, context_lens, o, lse, B, H, Hkv, Nq, D,
-                    num_pages, page_size, max_pages, causal, scale, dtype, stream);
+                    num_pages, page_size, max_pages, causal, scale, dtype, 1, nullptr, 0, stream);
+}
+
+size_t fa_fwd_paged_split_workspace_size(int B, int H, int Nq, int D, int num_splits) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  if (D != 64 && D != 128 && D != 256) return 0;
+  return split_workspace_bytes(static_cast<long long>(B) * H * Nq, D, num_splits);
+}
+
+int fa_fwd_paged_split_count(int B, int H, int Hkv, int Nq, int D, int page_size, int max_pages, int causal) {
+  if (B <= 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || Nq <= 0 || page_size <= 0 || max_pages <= 0) return 1;
+  if (D != 64 && D != 128 && D != 256) return 1;
+  DevInfo* dev = nullptr;
+  if (current_device_info(&dev) != FA_OK) return 1;
+  const int g = H / Hkv;
+  const bool pack = g > 1 && g * Nq <= 128;
+  const long long rows = pack ? static_cast<long long>(g) * Nq : Nq;
+  const long long nqt = (rows + 127) / 128;
+  const long long per_head = causal ? (nqt + 1) / 2 : nqt;
+  const long long units = static_cast<long long>(B) * (pack ? Hkv : H) * per_head;
+  const long long tiles = (static_cast<long long>(max_pages) * page_size + fa::fwd_block_n(D) - 1) / fa::fwd_block_n(D);
+  // one wave: as many slices as keep every unit on its own SM, never more
+  // slices than key tiles
+  long long s = units >= dev->sms ? 1 : dev->sms / units;
+  if (s > tiles) s = tiles;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return static_cast<int>(s < 1 ? 1 : s);
+}
+
+int fa_fwd_paged_split(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                       const int* context_lens, void* o, float* lse, void* workspace, size_t workspace_bytes, int B,
+                       int H, int Hkv, int Nq, int D, int num_pages, int page_size, int max_pages, int num_splits,
+                       int causal, float scale, int dtype, cudaStream_t stream) {
+  if (num_splits == 1)
+    return paged_impl(1, q, k_cache, v_cache, block_table, nullptr, nullptr, context_lens, o, lse, B, H, Hkv, Nq,
+                      D, num_pages, page_size, max_pages, causal, scale, dtype, 1, nullptr, 0, stream);
+  return paged_impl(3, q, k_cache, v_cache, block_table, nullptr, nullptr, context_lens, o, lse, B, H, Hkv, Nq, D,
+                    num_pages, page_size, max_pages, causal, scale, dtype, num_splits, workspace, workspace_bytes,
+                    stream);
 }
 
 int fa_fwd_sparse(const void* q, const void* k_cache, const void* v_cache, const int* sel_pages,
@@ -353,7 +417,7 @@ int fa_fwd_sparse(const void* q, const void* k_cache, const void* v_cache, const
                   int H, int Hkv, int Nq, int D, int num_pages, int page_size, int max_sel, int causal, float scale,
                   int dtype, cudaStream_t stream) {
   return paged_impl(2, q, k_cache, v_cache, sel_pages, sel_blocks, sel_count, context_lens, o, lse, B, H, Hkv, Nq,
-                    D, num_pages, page_size, max_sel, causal, scale, dtype, stream);
+                    D, num_pages, page_size, max_sel, causal, scale, dtype, 1, nullptr, 0, stream);
 }
 
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int H, int Hkv, int Nq,

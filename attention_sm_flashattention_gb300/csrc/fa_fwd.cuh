@@ -152,8 +152,28 @@ __device__ __forceinline__ int fwd_key_limit(int qi, int Nk, int off) {
 
 // Work modes of the forward kernel: K/V dense [heads / group, Nk, D]; a
 // paged cache read in key order through a block table; a paged cache read
-// through a per-(sequence, K/V head) list of selected blocks.
-enum FwdMode : int { kDense = 0, kPaged = 1, kSparse = 2 };
+// through a per-(sequence, K/V head) list of selected blocks; the paged
+// cache with every work item's key tiles split into slices that are
+// separate work units writing partial results (FwdParams::splits).
+enum FwdMode : int { kDense = 0, kPaged = 1, kSparse = 2, kPagedSplit = 3 };
+
+// Work units of a launch: the schedule's units, times the key-range slices
+// in split mode; unit u is then slice u % splits of schedule unit u / splits.
+template <bool CAUSAL, int MODE>
+__device__ __forceinline__ int fwd_units(const FwdParams& prm, int nqt) {
+  return fwd_num_units<CAUSAL>(prm.heads, nqt) * (MODE == kPagedSplit ? prm.splits : 1);
+}
+
+template <bool CAUSAL, int MODE>
+__device__ __forceinline__ void fwd_unit(const FwdParams& prm, int u, int nqt, int& head, int& qa, int& qb,
+                                         int& split) {
+  split = 0;
+  if (MODE == kPagedSplit) {
+    split = u % prm.splits;
+    u /= prm.splits;
+  }
+  fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+}
 
 // Key count, causal offset and key tiles of the work items of query head
 // `head`.  Dense: the call's Nk.  Paged: the sequence's context length,
@@ -171,16 +191,34 @@ __device__ __forceinline__ int fwd_item_tiles(int qt, int nkv_full, int nk, int 
   return fwd_num_kv<D, CAUSAL>(qt, nkv_full, nk, off);
 }
 
+// The key tiles a work unit visits for query tile qt: [j0, j0 + return).
+// Without splitting, all of the item's tiles from 0.  Split: slice `split`
+// of min(splits, tiles) balanced slices of them (each slice non-empty), and
+// none for a slice index past that.
+template <int D, bool CAUSAL, int MODE>
+__device__ __forceinline__ int fwd_range(int qt, int nkv_full, int nk, int off, int qp, int split, int nsplit,
+                                         int& j0) {
+  const int total = fwd_item_tiles<D, CAUSAL, MODE>(qt, nkv_full, nk, off, qp);
+  j0 = 0;
+  if (MODE != kPagedSplit) return total;
+  const int ns = min(nsplit, total);
+  if (split >= ns) return 0;
+  j0 = split * total / ns;
+  return (split + 1) * total / ns - j0;
+}
+
 template <int D, bool CAUSAL, int MODE>
 struct FwdItemShape {
-  int nk, off, nkv_full, ctx, sel, qp;
-  __device__ __forceinline__ FwdItemShape(const FwdParams& prm, int head) {
+  int nk, off, nkv_full, ctx, sel, qp, split, nsplit;
+  __device__ __forceinline__ FwdItemShape(const FwdParams& prm, int head, int split_ = 0) {
     int n = prm.Nk;
     ctx = 0;
     sel = 0;
     qp = prm.q_period;
+    split = split_;
+    nsplit = MODE == kPagedSplit ? prm.splits : 1;
     const int nq_pos = qp > 0 ? qp : prm.Nq;  // query positions per head
-    if (MODE == kPaged) {
+    if (MODE == kPaged || MODE == kPagedSplit) {
       n = __ldg(prm.context_lens + head / prm.H);
       n = min(max(n, CAUSAL ? nq_pos : 1), prm.max_pages * prm.page_size);
     } else if (MODE == kSparse) {
@@ -196,6 +234,10 @@ struct FwdItemShape {
   // key tiles of query tile qt (selected blocks carry arbitrary positions,
   // so the causal bound does not shorten a sparse item)
   __device__ __forceinline__ int tiles(int qt) const { return fwd_item_tiles<D, CAUSAL, MODE>(qt, nkv_full, nk, off, qp); }
+  // this unit's tiles of query tile qt: [j0, j0 + return)
+  __device__ __forceinline__ int range(int qt, int& j0) const {
+    return fwd_range<D, CAUSAL, MODE>(qt, nkv_full, nk, off, qp, split, nsplit, j0);
+  }
 };
 
 // Sparse mode: which of key tile j's BN columns query row qi may see, as a
@@ -244,7 +286,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // `tile` also indexes the K and V rings, which hold one tile per key tile.
 template <int D, bool CAUSAL, int MODE>
 struct FwdCursor {
-  int u, half, head, qt, qb, j, nkv;
+  int u, half, head, qt, qb, j, nkv, j0, split;  // j: index within the unit's tiles; key tile j0 + j
   uint32_t item, tile;
   bool valid;
   int units, nqt, nkv_full, Nk, off, ctx, sel, qp;
@@ -257,36 +299,84 @@ struct FwdCursor {
     item = 0;
     tile = 0;
     j = 0;
+    j0 = 0;
     u = first_unit;
     half = 0;
     load_unit();
   }
+  __device__ int range(int q) {
+    if (MODE != kPagedSplit) return fwd_item_tiles<D, CAUSAL, MODE>(q, nkv_full, Nk, off, qp);
+    return fwd_range<D, CAUSAL, MODE>(q, nkv_full, Nk, off, qp, split, prm->splits, j0);
+  }
   __device__ void load_unit() {
-    valid = u < units;
-    if (!valid) return;
-    int qa;
-    fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
-    const FwdItemShape<D, CAUSAL, MODE> sh(*prm, head);
-    Nk = sh.nk;
-    off = sh.off;
-    nkv_full = sh.nkv_full;
-    ctx = sh.ctx;
-    sel = sh.sel;
-    qp = sh.qp;
-    qt = qa;
-    half = 0;
-    nkv = fwd_item_tiles<D, CAUSAL, MODE>(qt, nkv_full, Nk, off, qp);
+    if constexpr (MODE != kPagedSplit) {
+      valid = u < units;
+      if (!valid) return;
+      int qa;
+      fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
+      const FwdItemShape<D, CAUSAL, MODE> sh(*prm, head);
+      Nk = sh.nk;
+      off = sh.off;
+      nkv_full = sh.nkv_full;
+      ctx = sh.ctx;
+      sel = sh.sel;
+      qp = sh.qp;
+      qt = qa;
+      half = 0;
+      nkv = fwd_item_tiles<D, CAUSAL, MODE>(qt, nkv_full, Nk, off, qp);
+    } else {
+      load_split_unit();
+    }
+  }
+  // split mode: the next unit (from u on) with at least one tile; only split
+  // units can have none, and every role skips them the same way
+  __device__ void load_split_unit() {
+    for (;;) {
+      valid = u < units;
+      if (!valid) return;
+      int qa;
+      fwd_unit<CAUSAL, MODE>(*prm, u, nqt, head, qa, qb, split);
+      const FwdItemShape<D, CAUSAL, MODE> sh(*prm, head, split);
+      Nk = sh.nk;
+      off = sh.off;
+      nkv_full = sh.nkv_full;
+      ctx = sh.ctx;
+      sel = sh.sel;
+      qp = sh.qp;
+      qt = qa;
+      half = 0;
+      nkv = range(qt);
+      if (nkv > 0) return;
+      if (qb >= 0) {
+        half = 1;
+        qt = qb;
+        nkv = range(qt);
+        if (nkv > 0) return;
+      }
+      u += gridDim.x;
+    }
   }
   __device__ void advance() {
     ++tile;
     if (++j < nkv) return;
     j = 0;
     ++item;
-    if (half == 0 && qb >= 0) {
-      half = 1;
-      qt = qb;
-      nkv = fwd_item_tiles<D, CAUSAL, MODE>(qt, nkv_full, Nk, off, qp);
+    if constexpr (MODE != kPagedSplit) {
+      if (half == 0 && qb >= 0) {
+        half = 1;
+        qt = qb;
+        nkv = fwd_item_tiles<D, CAUSAL, MODE>(qt, nkv_full, Nk, off, qp);
+      } else {
+        u += gridDim.x;
+        load_unit();
+      }
     } else {
+      if (half == 0 && qb >= 0) {
+        half = 1;
+        qt = qb;
+        nkv = range(qt);
+        if (nkv > 0) return;
+      }
       u += gridDim.x;
       load_unit();
     }
@@ -384,7 +474,10 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t tmem = bars->tmem_base;
   const int Nq = prm.Nq;
   const int nqt = (Nq + T::BM - 1) / T::BM;
-  const int units = fwd_num_units<CAUSAL>(prm.heads, nqt);
+  const int units = fwd_units<CAUSAL, MODE>(prm, nqt);
+  // split mode: a row can see no key of its slice; it then keeps m = -inf
+  // and l = 0 (an empty partial softmax), as a sparse row can
+  constexpr bool kEmptyRows = MODE == kSparse || MODE == kPagedSplit;
 
   if (warp < 8) {
     reg_alloc<T::SOFTMAX_REGS>();
@@ -400,14 +493,17 @@ __global__ void __launch_bounds__(512, 1)
       uint32_t t = 0, q_item = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        int head, qa, qb;
-        fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
-        const FwdItemShape<D, CAUSAL, MODE> sh(prm, head);
+        int head, qa, qb, sp;
+        fwd_unit<CAUSAL, MODE>(prm, u, nqt, head, qa, qb, sp);
+        const FwdItemShape<D, CAUSAL, MODE> sh(prm, head, sp);
         const int Nk = sh.nk, off = sh.off;
         for (int half = 0; ok && half < 2; ++half) {
           const int qt = half ? qb : qa;
           if (qt < 0) break;
-          const int nkv = sh.tiles(qt);
+          int j0 = 0;
+          const int nkv = MODE == kPagedSplit ? sh.range(qt, j0) : sh.tiles(qt);
+          if (MODE == kPagedSplit && nkv == 0) continue;
+          const int jb = MODE == kPagedSplit ? j0 : 0;  // the unit's first key tile
           const int qi = qt * T::BM + r;  // query row within the head
           const int qpos = sh.qp > 0 ? qi % sh.qp : qi;  // its query position
           const int lim = fwd_key_limit<CAUSAL>(qpos, Nk, off);  // this row's last key
@@ -416,7 +512,7 @@ __global__ void __launch_bounds__(512, 1)
           // sparse: the row's last visible logical position
           const int slim = CAUSAL ? min(qpos + sh.off, sh.ctx - 1) : sh.ctx - 1;
           float m = -INFINITY, l = 0.f;   // l: this half's partial row sum
-          for (int j = 0; j < nkv; ++j) {
+          for (int j = jb; j < jb + nkv; ++j) {
             uint32_t vis[T::BN / 32];  // sparse: visible columns of this tile
             if (MODE == kSparse) fwd_sparse_mask<D, CAUSAL>(prm, head, j, sh.sel, slim, vis);
             const int b = t & 1;
@@ -486,7 +582,7 @@ __global__ void __launch_bounds__(512, 1)
             const float m_new = (m_tile > m + kRescaleLog2) ? m_tile : m;
             // sparse: a row that has seen no visible key yet keeps m = -inf;
             // its P must be 0, not exp2(-inf + inf)
-            const float neg = (MODE == kSparse && m_new == -INFINITY) ? 0.f : -m_new;
+            const float neg = (kEmptyRows && m_new == -INFINITY) ? 0.f : -m_new;
             // x = s * c - m and the row sum in packed fp32 pairs (one f32x2
             // instruction per two columns)
             const uint64_t c2 = f2_pack(sl2, sl2), neg2 = f2_pack(neg, neg);
@@ -507,7 +603,7 @@ __global__ void __launch_bounds__(512, 1)
   #pragma unroll
             for (int i = 0; i < 4; ++i) f2_unpack(ps2[i], ps[2 * i], ps[2 * i + 1]);
             const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-            const float alpha = (MODE == kSparse && m_new == -INFINITY)
+            const float alpha = (kEmptyRows && m_new == -INFINITY)
                                     ? 1.f
                                     : ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
             l = l * alpha + rs;
@@ -517,7 +613,7 @@ __global__ void __launch_bounds__(512, 1)
             // (the MMAs alternate between the two accumulators); there the
             // softmax always waits for the previous P V before releasing P.
             constexpr bool kSerialPV = (T::NOH > 1);
-            if (j > 0 && (kSerialPV || __any_sync(0xffffffffu, alpha != 1.f))) {
+            if (j > jb && (kSerialPV || __any_sync(0xffffffffu, alpha != 1.f))) {
               // O holds P V of the previous tiles: wait for the last P V, then
               // rescale (this half's columns of) rows whose max moved.
               ok = mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, wc, 6);
@@ -576,12 +672,15 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t q_it = 0, k_it = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-          int head, qa, qb;
-          fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
-          const FwdItemShape<D, CAUSAL, MODE> sh(prm, head);
+          int head, qa, qb, sp;
+          fwd_unit<CAUSAL, MODE>(prm, u, nqt, head, qa, qb, sp);
+          const FwdItemShape<D, CAUSAL, MODE> sh(prm, head, sp);
           for (int half = 0; ok && half < 2; ++half) {
             const int qt = half ? qb : qa;
             if (qt < 0) break;
+            int j0 = 0;
+            const int nkv = MODE == kPagedSplit ? sh.range(qt, j0) : sh.tiles(qt);
+            if (MODE == kPagedSplit && nkv == 0) continue;
             const int qs = q_it % T::Q_STAGES;
             if (!(ok = mbar_wait(&bars->q_empty[qs], ((q_it / T::Q_STAGES) & 1) ^ 1, wc, 1))) break;
             mbar_arrive_expect_tx(&bars->q_full[qs], T::Q_BYTES);
@@ -589,8 +688,7 @@ __global__ void __launch_bounds__(512, 1)
             for (int s = 0; s < T::DSUB; ++s)
               tma_load_3d_hint(sq + s * T::Q_SUB, &tm_q, &bars->q_full[qs], s * 64, qt * T::BM, head, pol_q);
             ++q_it;
-            const int nkv = sh.tiles(qt);
-            for (int j = 0; j < nkv; ++j) {
+            for (int j = j0; j < j0 + nkv; ++j) {
               const int st = k_it % T::K_STAGES;
               if (!(ok = mbar_wait(&bars->k_empty[st], ((k_it / T::K_STAGES) & 1) ^ 1, wc, 2))) break;
               uint8_t* sk = smem + T::SM_K + st * T::KV_BYTES;
@@ -619,14 +717,16 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t v_it = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-          int head, qa, qb;
-          fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
-          const FwdItemShape<D, CAUSAL, MODE> sh(prm, head);
+          int head, qa, qb, sp;
+          fwd_unit<CAUSAL, MODE>(prm, u, nqt, head, qa, qb, sp);
+          const FwdItemShape<D, CAUSAL, MODE> sh(prm, head, sp);
           for (int half = 0; ok && half < 2; ++half) {
             const int qt = half ? qb : qa;
             if (qt < 0) break;
-            const int nkv = sh.tiles(qt);
-            for (int j = 0; j < nkv; ++j) {
+            int j0 = 0;
+            const int nkv = MODE == kPagedSplit ? sh.range(qt, j0) : sh.tiles(qt);
+            if (MODE == kPagedSplit && nkv == 0) continue;
+            for (int j = j0; j < j0 + nkv; ++j) {
               const int st = v_it % T::V_STAGES;
               if (!(ok = mbar_wait(&bars->v_empty[st], ((v_it / T::V_STAGES) & 1) ^ 1, wc, 8))) break;
               uint8_t* sv = smem + T::SM_V + st * T::KV_BYTES;
@@ -696,7 +796,7 @@ __global__ void __launch_bounds__(512, 1)
           const uint32_t sv = smem_u32(smem + T::SM_V + st * T::KV_BYTES);
           bool wrote = false;
           for (int e = 0; e < epb; ++e) {
-            const int eg = c.j * epb + e;
+            const int eg = (c.j0 + c.j) * epb + e;
             if (eg >= c.sel) break;
             const int valid = min(max(c.ctx - __ldg(blk + eg) * ps, 0), ps);
             if (valid == ps) continue;
@@ -710,12 +810,12 @@ __global__ void __launch_bounds__(512, 1)
             fence_proxy_async_smem();
             __syncwarp();
           }
-        } else if (PAGED && (c.j + 1) * T::BN > c.Nk) {
+        } else if (PAGED && (c.j0 + c.j + 1) * T::BN > c.Nk) {
           // Rows of the sequence's last page past its key count hold whatever
           // the cache holds there; P is 0 for them, but 0 * NaN is NaN, so
           // zero those V rows before P V reads them.  (Each row is the same
           // 128 bytes of its sub-tile under the 128-byte swizzle.)
-          const int valid = c.Nk - c.j * T::BN;
+          const int valid = c.Nk - (c.j0 + c.j) * T::BN;
           const uint32_t sv = smem_u32(smem + T::SM_V + st * T::KV_BYTES);
           for (int idx = lane; idx < (T::BN - valid) * 8 * T::DSUB; idx += 32) {
             const int row = valid + idx / (8 * T::DSUB), rem = idx % (8 * T::DSUB);
@@ -766,14 +866,26 @@ __global__ void __launch_bounds__(512, 1)
       const float* lm = reinterpret_cast<const float*>(smem + T::SM_LM);
       uint32_t t = 0, q_item = 0;
       bool ok = true;
+      const size_t part_rows = static_cast<size_t>(prm.heads) * Nq;  // rows of one slice's partial result
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        int head, qa, qb;
-        fwd_decode<CAUSAL>(u, nqt, head, qa, qb);
-        const FwdItemShape<D, CAUSAL, MODE> sh(prm, head);
+        int head, qa, qb, sp;
+        fwd_unit<CAUSAL, MODE>(prm, u, nqt, head, qa, qb, sp);
+        const FwdItemShape<D, CAUSAL, MODE> sh(prm, head, sp);
         for (int half = 0; ok && half < 2; ++half) {
           const int qt = half ? qb : qa;
           if (qt < 0) break;
-          t += sh.tiles(qt);
+          int j0 = 0;
+          const int nkv = MODE == kPagedSplit ? sh.range(qt, j0) : sh.tiles(qt);
+          // split mode: this row's slot in the slice's partial result
+          const size_t prow = MODE == kPagedSplit ? static_cast<size_t>(sp) * part_rows +
+                                                        static_cast<size_t>(head) * Nq + qt * T::BM + r
+                                                  : 0;
+          if (MODE == kPagedSplit && nkv == 0) {
+            // a slice past the item's tiles: nothing visible
+            if (qt * T::BM + r < Nq) prm.part_lse[prow] = -INFINITY;
+            continue;
+          }
+          t += nkv;
           ok = mbar_wait(&bars->lm_full, q_item & 1, wc, 17);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           const float l_row = lm[r] + lm[T::BM + r];
@@ -784,30 +896,53 @@ __global__ void __launch_bounds__(512, 1)
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
           // sparse: a row with no visible key at all has an empty softmax
-          const float inv_l = (MODE == kSparse && !(l_row > 0.f)) ? 0.f : 1.f / l_row;
-          const uint32_t so = smem_u32(smem + T::SM_Q + (q_item % T::Q_STAGES) * T::Q_BYTES) + r * 128;
+          const float inv_l = (kEmptyRows && !(l_row > 0.f)) ? 0.f : 1.f / l_row;
+          if constexpr (MODE == kPagedSplit) {
+            // the slice's partial O (normalised by its own row sum) in fp32
+            // and its lse, straight to global memory
+            const bool live_row = qt * T::BM + r < Nq;
   #pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tmem_ld32(lane_base + T::O_COL + c, o);
-            tmem_wait_ld();
-            reg_fence<32>(o);
-            uint32_t h[16];
+            for (int c = 0; c < D; c += 32) {
+              uint32_t o[32];
+              tmem_ld32(lane_base + T::O_COL + c, o);
+              tmem_wait_ld();
+              reg_fence<32>(o);
+              if (live_row) {
+                float4* dst = reinterpret_cast<float4*>(prm.part_o + prow * D + c);
   #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              h[i] = pack2<BF>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-            const uint32_t sub = so + (c / 64) * T::Q_SUB;
-  #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int ch = ((c % 64) / 8 + i) ^ (r & 7);
-              st_shared_v4(sub + ch * 16, h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+                for (int i = 0; i < 8; ++i)
+                  dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                       __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+              }
             }
+            mbar_arrive(&bars->epi_full[q_item % T::Q_STAGES]);
+            if (live_row)
+              prm.part_lse[prow] = !(l_row > 0.f) ? -INFINITY : (m + log2f(l_row)) * 0.69314718055994530942f;
+          } else {
+            const uint32_t so = smem_u32(smem + T::SM_Q + (q_item % T::Q_STAGES) * T::Q_BYTES) + r * 128;
+  #pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t o[32];
+              tmem_ld32(lane_base + T::O_COL + c, o);
+              tmem_wait_ld();
+              reg_fence<32>(o);
+              uint32_t h[16];
+  #pragma unroll
+              for (int i = 0; i < 16; ++i)
+                h[i] = pack2<BF>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+              const uint32_t sub = so + (c / 64) * T::Q_SUB;
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int ch = ((c % 64) / 8 + i) ^ (r & 7);
+                st_shared_v4(sub + ch * 16, h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+              }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->epi_full[q_item % T::Q_STAGES]);
+            if (qt * T::BM + r < Nq)
+              prm.lse[static_cast<size_t>(head) * Nq + qt * T::BM + r] =
+                  (MODE == kSparse && !(l_row > 0.f)) ? -INFINITY : (m + log2f(l_row)) * 0.69314718055994530942f;
           }
-          fence_proxy_async_smem();
-          mbar_arrive(&bars->epi_full[q_item % T::Q_STAGES]);
-          if (qt * T::BM + r < Nq)
-            prm.lse[static_cast<size_t>(head) * Nq + qt * T::BM + r] =
-                (MODE == kSparse && !(l_row > 0.f)) ? -INFINITY : (m + log2f(l_row)) * 0.69314718055994530942f;
           tc_fence_before();
           mbar_arrive(&bars->o_free);
           if (warp == 8) {
@@ -816,11 +951,13 @@ __global__ void __launch_bounds__(512, 1)
             const int qs = q_item % T::Q_STAGES;
             if (!(ok = warp_wait(&bars->epi_full[qs], (q_item / T::Q_STAGES) & 1, wc, 13))) break;
             if (lane == 0) {
-              const uint8_t* so_tile = smem + T::SM_Q + qs * T::Q_BYTES;
-              for (int sub = 0; sub < T::DSUB; ++sub)
-                tma_store_3d(&tm_o, so_tile + sub * T::Q_SUB, sub * 64, qt * T::BM, head);
-              bulk_commit();
-              bulk_wait_read<0>();
+              if (MODE != kPagedSplit) {  // split: the partial result went straight to global memory
+                const uint8_t* so_tile = smem + T::SM_Q + qs * T::Q_BYTES;
+                for (int sub = 0; sub < T::DSUB; ++sub)
+                  tma_store_3d(&tm_o, so_tile + sub * T::Q_SUB, sub * 64, qt * T::BM, head);
+                bulk_commit();
+                bulk_wait_read<0>();
+              }
               mbar_arrive(&bars->q_empty[qs]);
             }
             __syncwarp();
@@ -859,8 +996,10 @@ int launch_fwd(const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaS
     attr_set = true;
   }
   const int nqt = (prm.Nq + T::BM - 1) / T::BM;
-  const int units = CAUSAL ? prm.heads * ((nqt + 1) / 2) : prm.heads * nqt;
-  const int grid = units < num_sms ? units : num_sms;
+  const long long units = (CAUSAL ? static_cast<long long>(prm.heads) * ((nqt + 1) / 2)
+                                  : static_cast<long long>(prm.heads) * nqt) *
+                          (MODE == kPagedSplit ? prm.splits : 1);
+  const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   fa_fwd_kernel<D, CAUSAL, BF, MODE><<<grid, T::THREADS, T::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3],
                                                                                   prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;

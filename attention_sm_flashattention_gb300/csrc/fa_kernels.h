@@ -48,6 +48,15 @@ struct FwdParams {
   // row r is query position r % q_period, and `heads`, `group`, `Nq` and `H`
   // describe the packed problem (group 1).
   int q_period;
+  // Split key range (paged split launchers): each work item's key tiles are
+  // cut into `splits` contiguous slices, one work unit each.  A unit writes
+  // its rows' partial result to part_o ([splits, heads * Nq, D] fp32, O
+  // normalised by the slice's own row sum) and part_lse ([splits, heads *
+  // Nq] fp32, natural log; -inf for a slice with no visible key), and the
+  // combine kernel merges the slices into o and lse.
+  int splits;
+  float* part_o;
+  float* part_lse;
 };
 
 struct BwdParams {
@@ -107,6 +116,20 @@ int launch_fwd_sparse_d128(bool causal, bool bf16, const CUtensorMap* maps, cons
                            cudaStream_t stream);
 int launch_fwd_sparse_d256(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,
                            cudaStream_t stream);
+
+// Forward over a paged K/V cache with the key range of every work item split
+// into prm.splits slices (partial results into prm.part_o / part_lse), then
+// the combine kernel (o, lse); maps as for the paged launchers.
+int launch_fwd_paged_split_d64(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,
+                               cudaStream_t stream);
+int launch_fwd_paged_split_d128(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,
+                                cudaStream_t stream);
+int launch_fwd_paged_split_d256(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm, int num_sms,
+                                cudaStream_t stream);
+// Merge `splits` partial results per row: rows = heads * Nq, O and lse as
+// described for FwdParams::part_o / part_lse.
+int launch_split_combine(const float* part_o, const float* part_lse, void* o, float* lse, long long rows, int D,
+                         int splits, bool bf16, int num_sms, cudaStream_t stream);
 
 // Tile sizes the host needs to build tensor maps and size grids.
 inline int fwd_block_n(int D) { return D == 256 ? 64 : 128; }

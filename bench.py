@@ -379,6 +379,19 @@ def paged_bench(args):
         sparse = {"blocks_selected": nsel, "of": pages_per_seq, "ms": ms_sparse,
                   "speedup_vs_paged": ms / ms_sparse,
                   "kv_gbs": 2 * sel_keys * D * q.element_size() / (ms_sparse * 1e-3) / 1e9}
+    # the same call with every sequence's key range split into slices
+    # (fa_fwd_paged_split), the library's slice count for this shape
+    split = None
+    nsplit = fa.paged_split_count(Z, H, HKV, N, D, ps, pages_per_seq, CAUSAL)
+    if nsplit > 1:
+        from attention_sm_flashattention_gb300 import _native
+        ws = torch.empty(_native.lib().fa_fwd_paged_split_workspace_size(Z, H, N, D, nsplit), dtype=torch.uint8,
+                         device=dev)
+        ms_split = timed(lambda: fa.fwd_paged(q, kc, vc, table, lens, causal=CAUSAL, scale=scale, out=(o, lse),
+                                              splits=nsplit, workspace=ws))
+        split = {"splits": nsplit, "ms": ms_split, "speedup_vs_paged": ms / ms_split,
+                 "tflops": flops_fwd(Z, H, N, D, CAUSAL, NK) / (ms_split * 1e-3) / 1e12,
+                 "kv_gbs": 2 * Z * HKV * NK * D * q.element_size() / (ms_split * 1e-3) / 1e9}
     # cache write of the Z * N new tokens (ReshapeAndCache) to distinct slots
     toks = Z * N
     k_new = torch.randn((toks, HKV, D), device=dev, dtype=elem, generator=gen)
@@ -401,6 +414,7 @@ def paged_bench(args):
         "dense_fwd_tflops": fl / (ms_dense * 1e-3) / 1e12, "dense_fwd_ms": ms_dense,
         "kv_cache_gbs": kv_bytes / (ms * 1e-3) / 1e9,
         "sparse": sparse,
+        "split": split,
         "cache_write": {"tokens": toks, "ms": ms_write,
                         "gbs": 4 * toks * HKV * D * q.element_size() / (ms_write * 1e-3) / 1e9,
                         "peak_hbm_gbs": peaks["hbm_gbs"]},

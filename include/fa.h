@@ -215,6 +215,46 @@ FA_API int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache,
                         cudaStream_t stream);
 
 /*
+ * Paged forward with each sequence's key range split into slices, for calls
+ * with too few (sequence, head) work items to fill the GPU (decode with a
+ * small batch and long contexts).  Source: «把 FlashAttention 搬上昇腾», §一
+ * -- the online softmax merges blocks of keys through a running max and sum;
+ * whole slices of keys merge the same way: slice s reports lse_s and its own
+ * normalised O_s, and lse = log sum_s exp(lse_s), O = sum_s exp(lse_s - lse)
+ * O_s.  The result equals fa_fwd_paged's up to rounding.
+ *
+ *   all arguments as fa_fwd_paged, plus
+ *   num_splits      : slices per work item, 1 .. 256; a work item with T key
+ *                     tiles (128 keys, 64 at D = 256) uses min(num_splits, T)
+ *                     balanced slices.  1 runs fa_fwd_paged's path.
+ *   workspace       : device memory of at least
+ *                     fa_fwd_paged_split_workspace_size(B, H, Nq, D,
+ *                     num_splits) bytes, 16-byte aligned, caller-owned, only
+ *                     used by this call on `stream` (fp32 per-slice lse and O).
+ *
+ * Launches the paged kernel over (work item, slice) units, then a merge
+ * kernel that writes o and lse.  Errors as fa_fwd_paged, plus
+ * FA_ERR_INVALID_ARG for num_splits out of range and FA_ERR_WORKSPACE for a
+ * missing, misaligned or short workspace.
+ */
+FA_API int fa_fwd_paged_split(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                              const int* context_lens, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                              int B, int H, int Hkv, int Nq, int D, int num_pages, int page_size, int max_pages,
+                              int num_splits, int causal, float scale, int dtype, cudaStream_t stream);
+
+/* Bytes of workspace fa_fwd_paged_split needs (0 for invalid arguments). */
+FA_API size_t fa_fwd_paged_split_workspace_size(int B, int H, int Nq, int D, int num_splits);
+
+/*
+ * A slice count for fa_fwd_paged_split on the current device: the largest
+ * that keeps every (work item, slice) unit in one wave of the SM count (1
+ * when the work items alone fill the GPU), at most the key tiles of the
+ * longest context (max_pages * page_size keys) and 256.  Returns 1 for
+ * invalid arguments.
+ */
+FA_API int fa_fwd_paged_split_count(int B, int H, int Hkv, int Nq, int D, int page_size, int max_pages, int causal);
+
+/*
  * Forward over selected blocks of a paged cache.  Source: «把 FlashAttention
  * 搬上昇腾», the contest section's Quest Sparse Attention part: only the
  * chosen (Top-K) blocks of a sequence get exact attention, read through the

@@ -204,3 +204,37 @@ def test_fwd_sparse_argument_checks(lib):
     assert call(max_sel=0) == _native.FA_ERR_INVALID_ARG
     assert call(page_size=24) == _native.FA_ERR_UNSUPPORTED
     assert call(D=256, page_size=128) == _native.FA_ERR_UNSUPPORTED
+
+
+def call_fwd_paged_split(lib, ws=FAKE, ws_bytes=1 << 30, splits=4, page_size=64, D=128, B=2, H=4, Nq=1):
+    return lib.fa_fwd_paged_split(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, ws_bytes, B, H, 2, Nq, D, 8,
+                                  page_size, 4, splits, 0, 0.125, 0, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(splits=0), _native.FA_ERR_INVALID_ARG),
+    (dict(splits=257), _native.FA_ERR_INVALID_ARG),
+    (dict(ws=None), _native.FA_ERR_WORKSPACE),
+    (dict(ws=FAKE + 8), _native.FA_ERR_WORKSPACE),          # workspace not 16-byte aligned
+    (dict(page_size=48), _native.FA_ERR_UNSUPPORTED),       # the paged checks still apply
+    (dict(D=96), _native.FA_ERR_UNSUPPORTED),
+])
+def test_fwd_paged_split_rejects_bad_arguments(lib, kw, code):
+    assert call_fwd_paged_split(lib, **kw) == code
+
+
+def test_paged_split_workspace_is_per_slice_lse_then_o(lib):
+    f = lib.fa_fwd_paged_split_workspace_size
+    rows = 2 * 4 * 3                                         # B * H * Nq query rows
+    lse_bytes = (rows * 5 * 4 + 255) // 256 * 256             # padded to 256 bytes so O stays aligned
+    assert f(2, 4, 3, 128, 5) == lse_bytes + rows * 5 * 128 * 4
+    assert f(2, 4, 3, 256, 1) == (rows * 4 + 255) // 256 * 256 + rows * 256 * 4
+    for bad in [(0, 4, 3, 128, 5), (2, 4, 3, 96, 5), (2, 4, 3, 128, 0), (2, 4, 3, 128, 257)]:
+        assert f(*bad) == 0
+
+
+def test_paged_split_count_rejects_bad_arguments(lib):
+    f = lib.fa_fwd_paged_split_count
+    assert f(2, 6, 4, 1, 128, 64, 8, 0) == 1                  # H not a multiple of Hkv
+    assert f(2, 8, 2, 1, 96, 64, 8, 0) == 1                   # unsupported D
+    assert f(0, 8, 2, 1, 128, 64, 8, 0) == 1
