@@ -39,12 +39,30 @@ def ident(c):
     return f"b{B}h{H}kv{Hkv}q{Nq}d{D}p{ps}s{sp}_" + "-".join(map(str, lens))
 
 
-def run_case(case, causal, dtype=torch.float16, splits=None):
+def poison_unreadable(kc, vc, table, lens, ps):
+    """Inf / NaN in every cache slot no sequence may read: past each context
+    in its last page, and the spare pages."""
+    used = set()
+    for b, n in enumerate(lens):
+        pages = table[b, :(n + ps - 1) // ps].tolist()
+        used.update(pages)
+        if n % ps:
+            kc[pages[-1], n % ps:] = float("inf")
+            vc[pages[-1], n % ps:] = float("nan")
+    for pg in range(kc.shape[0]):
+        if pg not in used:
+            kc[pg] = float("nan")
+            vc[pg] = float("inf")
+
+
+def run_case(case, causal, dtype=torch.float16, splits=None, poison=False):
     B, H, Hkv, Nq, lens, D, ps, sp = case
     if splits is not None:
         sp = splits
     seed = 9100 + B + 3 * H + Hkv + Nq + sum(lens) + D + ps + int(causal)
     q, kc, vc, table, cl = make_paged_inputs(B, H, Hkv, Nq, lens, D, ps, seed, dtype=dtype)
+    if poison:
+        poison_unreadable(kc, vc, table, lens, ps)
     scale = 1 / math.sqrt(D)
     o, lse = api.fwd_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), cl.cuda(), causal=causal, scale=scale,
                            splits=sp)
@@ -64,6 +82,16 @@ def test_paged_split_forward(case, causal):
 
 def test_paged_split_forward_bf16():
     run_case(CASES[1], True, dtype=torch.bfloat16)
+
+
+def test_paged_split_forward_bf16_d256():
+    run_case(CASES[3], False, dtype=torch.bfloat16)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("case", [CASES[0], CASES[2], CASES[3], CASES[6]], ids=ident)
+def test_paged_split_forward_ignores_unreadable_slots(case, causal):
+    run_case(case, causal, poison=True)
 
 
 def test_paged_split_library_count():
