@@ -20,15 +20,17 @@
 //               item.
 //   warps 8-11  epilogue: O / l -> fp16 into the item's (now unused) Q
 //               buffer, lse; this overlaps the softmax of the next item.
+//               Warp 8 then writes the tile out with a TMA store and
+//               releases the Q buffer.  (Split key ranges: fp32 O / l and
+//               lse of the slice straight to global memory instead.)
 //   warp 12     TMA producer: Q tile per work item, K tiles into a ring.
-//   warp 13     MMA issuer (converged warp, one elected lane per MMA) and
+//   warp 13     QK^T issuer (converged warp, one elected lane per MMA) and
 //               TMEM owner.  It walks the CTA's tiles as one flat sequence
-//               (across work items) and issues S = Q K^T two tiles ahead of
-//               P V, into one of two S buffers, and O += P V (P read from
-//               TMEM) as soon as a tile's P is ready.
+//               (across work items) and issues S = Q K^T up to two tiles
+//               ahead of P V, into one of two S buffers.
 //   warp 14     TMA producer: V tiles into their own ring.
-//   warp 15     O store: TMA store of the epilogue's tile, then releases the
-//               Q buffer.
+//   warp 15     P V issuer: O += P V (P read from TMEM) as soon as a tile's
+//               P is ready, over the same flat tile sequence.
 // The softmax warpgroups run with more registers than the others
 // (setmaxnreg), since they hold a whole S half-row and its P.
 #pragma once
