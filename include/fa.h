@@ -62,7 +62,8 @@ extern "C" {
 #define FA_ERR_INVALID_ARG (-1) /* null pointer, a size <= 0, H not a multiple of Hkv, bad causal flag or
                                    dtype, non-finite or <= 0 scale, misaligned pointer */
 #define FA_ERR_UNSUPPORTED (-2) /* D not in {64, 128, 256}, causal with Nq > Nk, or sizes past 32-bit indexing */
-#define FA_ERR_WORKSPACE (-3)   /* workspace null or smaller than fa_bwd_workspace_size() */
+#define FA_ERR_WORKSPACE (-3)   /* workspace null, misaligned or smaller than its size query
+                                   (fa_bwd_workspace_size, fa_fwd_paged_split_workspace_size) */
 #define FA_ERR_CUDA (-4)        /* a CUDA runtime call or kernel launch failed */
 #define FA_ERR_DEVICE (-5)      /* current device is not a compute capability 10.3 GPU */
 #define FA_ERR_TIMEOUT (-6)     /* (fa_device_status) a kernel wait gave up; results invalid */
@@ -110,6 +111,10 @@ FA_API size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal);
  *                      undefined.  Must not be used by another call that runs
  *                      concurrently on the GPU.
  *   other arguments  : as for fa_fwd.
+ * Enqueues a persistent dQ kernel and a persistent dK/dV kernel: at D = 128
+ * the dQ kernel runs first and also forms Delta = rowsum(O * dO) into the
+ * workspace; at D = 64 a Delta kernel runs first, then dQ, then dK/dV; at
+ * D = 256 a Delta kernel, then dK/dV, then dQ.
  * Returns FA_OK or a negative FA_ERR_* code.
  */
 FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
