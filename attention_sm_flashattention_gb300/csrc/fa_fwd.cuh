@@ -535,10 +535,23 @@ __global__ void __launch_bounds__(512, 1)
                 if (!((wv >> (c % 32)) & 1u)) sr[c] = __float_as_uint(-INFINITY);
               }
             } else if ((j + 1) * T::BN - 1 > lim_lo) {
-              const int k0 = j * T::BN + (wg ^ 1) * HC;
+              if constexpr (CAUSAL) {
+                // visibility as one bit per column of each 32-column word
+                const int nv = lim - (j * T::BN + (wg ^ 1) * HC) + 1;  // visible columns of the half
   #pragma unroll
-              for (int c = 0; c < HC; ++c)
-                if (k0 + c > lim) sr[c] = __float_as_uint(-INFINITY);
+                for (int w = 0; w < HC / 32; ++w) {
+                  const int n = min(max(nv - 32 * w, 0), 32);
+                  const uint32_t keep = n == 32 ? 0xffffffffu : ((1u << n) - 1u);
+  #pragma unroll
+                  for (int c = 0; c < 32; ++c)
+                    sr[32 * w + c] = ((keep >> c) & 1u) ? sr[32 * w + c] : __float_as_uint(-INFINITY);
+                }
+              } else {
+                const int k0 = j * T::BN + (wg ^ 1) * HC;
+  #pragma unroll
+                for (int c = 0; c < HC; ++c)
+                  if (k0 + c > lim) sr[c] = __float_as_uint(-INFINITY);
+              }
             }
   #pragma unroll
             for (int i = 0; i < 8; ++i) pm[i] = fmaxf(__uint_as_float(sr[i]), __uint_as_float(sr[i + 8]));
@@ -563,10 +576,22 @@ __global__ void __launch_bounds__(512, 1)
                 if (!((wv >> (c % 32)) & 1u)) s[c] = -INFINITY;
               }
             } else if ((j + 1) * T::BN - 1 > lim_lo) {
-              const int k0 = j * T::BN + wg * HC;
+              if constexpr (CAUSAL) {
+                const int nv = lim - (j * T::BN + wg * HC) + 1;
   #pragma unroll
-              for (int c = 0; c < HC; ++c)
-                if (k0 + c > lim) s[c] = -INFINITY;
+                for (int w = 0; w < HC / 32; ++w) {
+                  const int n = min(max(nv - 32 * w, 0), 32);
+                  const uint32_t keep = n == 32 ? 0xffffffffu : ((1u << n) - 1u);
+  #pragma unroll
+                  for (int c = 0; c < 32; ++c)
+                    s[32 * w + c] = ((keep >> c) & 1u) ? s[32 * w + c] : -INFINITY;
+                }
+              } else {
+                const int k0 = j * T::BN + wg * HC;
+  #pragma unroll
+                for (int c = 0; c < HC; ++c)
+                  if (k0 + c > lim) s[c] = -INFINITY;
+              }
             }
   #pragma unroll
             for (int c = 0; c < HC; c += 16)
