@@ -475,6 +475,17 @@ __global__ void __launch_bounds__(384, 1)
           // y = lse2 - S^T * c in packed fp32 pairs, P^T = exp2(-y)
           const float4* l4 = reinterpret_cast<const float4*>(smem + T::A_SM_L2 + qs * 512) + wg * (T::QC / 4);
           const uint64_t nc2 = f2_pack(-sl2, -sl2);
+          // diagonal tile: the query columns this key row sees (a suffix,
+          // query >= key - coff) as one bit per column of each 32-column word
+          uint32_t keep[T::QC / 32];
+          if (diag) {
+            const int nh = key - q0;  // hidden columns
+#pragma unroll
+            for (int w = 0; w < T::QC / 32; ++w) {
+              const int h = min(max(nh - 32 * w, 0), 32);
+              keep[w] = h == 32 ? 0u : (0xffffffffu << h);
+            }
+          }
           uint64_t p2[T::QC / 2];
 #pragma unroll
           for (int c = 0; c < T::QC; c += 4) {
@@ -488,7 +499,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               pv[e] = ex2_approx(-y[e]);
-              if (diag && key > q0 + c + e) pv[e] = 0.f;
+              if (diag) pv[e] = ((keep[(c + e) / 32] >> ((c + e) % 32)) & 1u) ? pv[e] : 0.f;
             }
             p2[c / 2] = f2_pack(pv[0], pv[1]);
             p2[c / 2 + 1] = f2_pack(pv[2], pv[3]);
@@ -928,12 +939,29 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive(&bars->s_free);
           // x = S * c - lse2 in packed fp32 pairs, P = exp2(x)
           uint64_t p2[T::QC / 2];
+          const bool masked = (j + 1) * T::BN - 1 > lim_lo;
+          // causal: the row's visible columns of this warpgroup's half as one
+          // bit per column of each 32-column word
+          uint32_t keep[T::QC / 32];
+          if constexpr (CAUSAL) {
+            const int nv = lim - k0 + 1;
+#pragma unroll
+            for (int w = 0; w < T::QC / 32; ++w) {
+              const int n = min(max(nv - 32 * w, 0), 32);
+              keep[w] = n == 32 ? 0xffffffffu : ((1u << n) - 1u);
+            }
+          }
 #pragma unroll
           for (int c = 0; c < T::QC; c += 2) {
             float x0, x1;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nl2), x0, x1);
             float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            if ((j + 1) * T::BN - 1 > lim_lo) {
+            if constexpr (CAUSAL) {
+              if (masked) {
+                p0 = ((keep[c / 32] >> (c % 32)) & 1u) ? p0 : 0.f;
+                p1 = ((keep[c / 32] >> ((c + 1) % 32)) & 1u) ? p1 : 0.f;
+              }
+            } else if (masked) {
               if (k0 + c > lim) p0 = 0.f;
               if (k0 + c + 1 > lim) p1 = 0.f;
             }
