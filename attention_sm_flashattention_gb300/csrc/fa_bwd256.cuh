@@ -490,6 +490,13 @@ __global__ void __launch_bounds__(384, 1)
             // P^T = exp2(S^T * c - lse2) in packed fp32 pairs
             const float4* l4 = reinterpret_cast<const float4*>(smem + T::A_SM_L2 + qs * 256) + wg * (T::A_QC / 4);
             const uint64_t nc2 = f2_pack(-sl2, -sl2);
+            // diagonal tile: the query columns this key row sees (a suffix)
+            // as one bit per column
+            uint32_t keep = 0xffffffffu;
+            if (diag) {
+              const int h = min(max(key - q0, 0), 32);  // hidden columns
+              keep = h == 32 ? 0u : (0xffffffffu << h);
+            }
             uint64_t p2[T::A_QC / 2];
 #pragma unroll
             for (int c = 0; c < T::A_QC; c += 4) {
@@ -503,7 +510,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 pv[e] = ex2_approx(-y[e]);
-                if (diag && key > q0 + c + e) pv[e] = 0.f;
+                if (diag) pv[e] = ((keep >> (c + e)) & 1u) ? pv[e] : 0.f;
               }
               p2[c / 2] = f2_pack(pv[0], pv[1]);
               p2[c / 2 + 1] = f2_pack(pv[2], pv[3]);
@@ -924,12 +931,23 @@ __global__ void __launch_bounds__(416, 1)
           // P = exp2(S * c - lse2) in packed fp32 pairs
           uint64_t p2[T::B_KC / 2];
           const bool masked = (j + 1) * T::B_BN - 1 > lim_lo;
+          // causal: the row's visible prefix of columns as one bit per column
+          uint32_t keep = 0xffffffffu;
+          if constexpr (CAUSAL) {
+            const int n = min(max(lim - k0 + 1, 0), 32);
+            keep = n == 32 ? 0xffffffffu : ((1u << n) - 1u);
+          }
 #pragma unroll
           for (int c = 0; c < T::B_KC; c += 2) {
             float x0, x1;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nl2), x0, x1);
             float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            if (masked) {
+            if constexpr (CAUSAL) {
+              if (masked) {
+                p0 = ((keep >> c) & 1u) ? p0 : 0.f;
+                p1 = ((keep >> (c + 1)) & 1u) ? p1 : 0.f;
+              }
+            } else if (masked) {
               if (k0 + c > lim) p0 = 0.f;
               if (k0 + c + 1 > lim) p1 = 0.f;
             }
