@@ -22,6 +22,7 @@ FA_ERR_CUDA = -4
 FA_ERR_DEVICE = -5
 FA_ERR_TIMEOUT = -6
 FA_ERR_SCRATCH_LIMIT = -7
+FA_NOALLOC_SCRATCH_BYTES = 64 << 20  # fa_bwd_noalloc's static device buffer (include/fa.h)
 
 FA_DTYPE_F16 = 0
 FA_DTYPE_BF16 = 1

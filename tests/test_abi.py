@@ -238,3 +238,14 @@ def test_paged_split_count_rejects_bad_arguments(lib):
     assert f(2, 6, 4, 1, 128, 64, 8, 0) == 1                  # H not a multiple of Hkv
     assert f(2, 8, 2, 1, 96, 64, 8, 0) == 1                   # unsupported D
     assert f(0, 8, 2, 1, 128, 64, 8, 0) == 1
+
+
+def test_binding_constants_match_the_header():
+    import re
+    text = open(HEADER).read()
+    codes = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define (FA_(?:OK|ERR_\w+))\s+\(?(-?\d+)\)?", text)}
+    assert codes, "no status codes found in the header"
+    for name, value in codes.items():
+        assert getattr(_native, name) == value, name
+    m = re.search(r"#define FA_NOALLOC_SCRATCH_BYTES \((\d+)ull << (\d+)\)", text)
+    assert m and _native.FA_NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
