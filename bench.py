@@ -288,13 +288,21 @@ def gpu_bench(args, rank, world, local_rank):
 
 
 def reduce_max(vals, world):
+    """Element-wise max of `vals` over the ranks (the slowest rank's times)."""
     if world == 1:
         return vals
     import torch
     import torch.distributed as dist
-    t = torch.tensor(vals, dtype=torch.float64, device="cuda")
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return t.tolist()
+
+
+def job_throughput(flops_per_step_per_rank, world, steps, max_total_ms):
+    """Whole-job rate in TFLOP/s: the work of all ranks' steps over the
+    slowest rank's time (each rank runs its own replica: weak scaling)."""
+    return world * flops_per_step_per_rank * steps / (max_total_ms * 1e-3) / 1e12
 
 
 def bwd_kernel_names(d, causal):
@@ -518,8 +526,8 @@ def main():
     r = gpu_bench(args, rank, world, local_rank)
     total_ms, e2e_ms = reduce_max([r["total_ms"], r["e2e_ms"]], world)
     ms_per_step = total_ms / args.steps
-    value = world * flops_step() / (ms_per_step * 1e-3) / 1e12
-    e2e_value = world * flops_step() / (e2e_ms * 1e-3) / 1e12
+    value = job_throughput(flops_step(), world, args.steps, total_ms)
+    e2e_value = job_throughput(flops_step(), world, 1, e2e_ms)
     peaks = measured_peaks()
     fwd_tf = flops_fwd(Z, H, N, D, CAUSAL, NK) / (r["fwd_ms"] * 1e-3) / 1e12
     bwd_tf = 2.5 * flops_fwd(Z, H, N, D, CAUSAL, NK) / (r["bwd_ms"] * 1e-3) / 1e12
