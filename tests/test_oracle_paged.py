@@ -260,3 +260,44 @@ def test_pins_catch_planted_sparse_mistakes():
     # (b) physical page taken as the logical block
     bad2, _ = paged.sparse_attn_fwd_ref(q, kc, vc, pages, pages, count, lens, True, sc)
     assert not np.allclose(bad2, want)
+
+
+def merge_slices(parts):
+    """Merge per-slice (O_s normalised by its own row sum, lse_s) results
+    with the online-softmax rule: lse = log sum exp lse_s and O = sum
+    exp(lse_s - lse) O_s; a slice with lse_s = -inf has weight 0."""
+    lses = np.stack([l for _, l in parts])                      # [slices, rows]
+    mx = np.max(lses, axis=0)
+    lse = mx + np.log(np.sum(np.exp(lses - mx), axis=0))
+    o = sum(np.exp(l - lse)[:, None] * np.nan_to_num(o_s) for o_s, l in parts)
+    return o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_slices_merge_to_the_full_attention(causal):
+    # The identity the split paged forward relies on, checked with the
+    # oracle's one-head forward: attention over slices of the keys, merged,
+    # equals attention over all of them.  Causal rows see only keys up to
+    # their position, so some rows see nothing of the later slices
+    # (lse_s = -inf there).
+    rng = np.random.default_rng(77)
+    n_q, n_k, d = 40, 300, 32
+    q, k, v = (rng.standard_normal(s) for s in ((n_q, d), (n_k, d), (n_k, d)))
+    scale = 1 / math.sqrt(d)
+    full_o, full_lse = orc.attn_fwd_head(q, k, v, causal, scale)
+    off = n_k - n_q                                          # queries are the last n_q positions
+    parts = []
+    for lo, hi in ((0, 100), (100, 255), (255, 270), (270, 300)):
+        o_s = np.zeros((n_q, d))
+        l_s = np.full(n_q, -np.inf)
+        for i in range(n_q):
+            top = min(hi, i + off + 1) if causal else hi     # one past the last key row i sees here
+            if top > lo:
+                o_i, l_i = orc.attn_fwd_head(q[i:i + 1], k[lo:top], v[lo:top], False, scale)
+                o_s[i], l_s[i] = o_i[0], l_i[0]
+        parts.append((o_s, l_s))
+    if causal:
+        assert np.isinf(parts[3][1]).any()                   # rows at positions 260-269 see nothing of keys 270-299
+    o, lse = merge_slices(parts)
+    assert np.max(np.abs(o - full_o)) < 1e-12
+    assert np.max(np.abs(lse - full_lse)) < 1e-12
