@@ -28,7 +28,7 @@ reordered:
   its sequence (``context_lens``), and the last incomplete block is masked.
   Queries and keys may have different lengths n_q and n_k, any length >= 1.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * ``lse`` is the natural-log log-sum-exp of the *scaled* scores of each row,
   ``lse_i = log(sum_j exp(S_ij))``.  The pages only say the backward

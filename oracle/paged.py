@@ -19,7 +19,7 @@ contest section's ReshapeAndCache and GQA Paged Attention parts:
   blocks gets exact attention (``sparse_attn_fwd_ref``; how the blocks are
   chosen -- the scoring and Top-K -- is an input here).
 
-Readings (listed in the design doc): the cache layout is
+Readings where the pages are silent: the cache layout is
 ``[num_blocks, block_size, H_kv, D]`` (one token's K for all K/V heads is
 contiguous, which is what a per-token cache write produces); the queries of
 sequence b are the last ``n_q`` tokens of its ``context_lens[b]`` tokens, so
