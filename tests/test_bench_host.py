@@ -75,3 +75,23 @@ def test_launch_and_kernel_bookkeeping():
     assert "fa_bwd_prep_kernel<256>" in bench.bwd_kernel_names(256, False)
     # the benchmark's algorithmic count: 4 N^2 D per head forward, 2.5x backward
     assert bench.flops_fwd(128, 8, 1024, 128, False, 1024) == pytest.approx(4 * 1024 * 1024 ** 2 * 128)
+
+
+def test_reference_arm_prints_its_line():
+    # the reference arm is the fp64 CPU oracle on a bounded sample of the
+    # workload; it needs no GPU
+    import json
+    import subprocess
+    import sys
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [json.loads(x) for x in out.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    line = lines[0]
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["warmup"] >= 3
