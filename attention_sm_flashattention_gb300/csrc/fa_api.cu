@@ -477,6 +477,39 @@ void bwd_shape_params(fa::BwdParams& prm, const Shape& sh) {
   prm.causal_off = sh.Nk - sh.Nq;
 }
 
+// The backward launch sequence, once the arguments passed their checks:
+// `scratch` holds the [delta | lse2] layout of `ws` (a caller workspace or the
+// library's built-in buffer).  Every entry point maps launch failures the
+// same way: FA_OK or FA_ERR_CUDA.
+int bwd_run(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+            void* dq, void* dk, void* dv, char* scratch, const BwdWorkspace& ws, const Shape& sh, float scale,
+            cudaStream_t stream, bool bf16, const DevInfo* dev) {
+  CUtensorMap maps[kBwdMaps];
+  if (!bwd_maps(maps, q, k, v, dout, dq, dk, dv, sh, bf16)) return FA_ERR_CUDA;
+  fa::BwdParams prm{};
+  prm.v = static_cast<const __half*>(v);
+  prm.o = static_cast<const __half*>(o);
+  prm.dout = static_cast<const __half*>(dout);
+  prm.lse = lse;
+  prm.dq = static_cast<__half*>(dq);
+  prm.dk = static_cast<__half*>(dk);
+  prm.dv = static_cast<__half*>(dv);
+  prm.delta = reinterpret_cast<float*>(scratch + ws.delta_off);
+  prm.lse2 = reinterpret_cast<float*>(scratch + ws.lse2_off);
+  bwd_shape_params(prm, sh);
+  prm.scale = scale;
+  prm.scale_log2 = scale * kLog2e;
+  prm.status = dev->status;
+  const bool c = sh.causal != 0;
+  int rc;
+  switch (sh.D) {
+    case 64: rc = fa::launch_bwd_d64(c, bf16, maps, prm, dev->sms, stream); break;
+    case 128: rc = fa::launch_bwd_d128(c, bf16, maps, prm, dev->sms, stream); break;
+    default: rc = fa::launch_bwd_d256(c, bf16, maps, prm, dev->sms, stream); break;
+  }
+  return rc == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
              void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, const Shape& sh, float scale,
              cudaStream_t stream, bool bf16) {
@@ -486,32 +519,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   if ((rc = current_device_info(&dev)) != FA_OK) return rc;
   const BwdWorkspace ws = bwd_workspace_layout(sh);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < ws.total) return FA_ERR_WORKSPACE;
-
-  const int D = sh.D;
-  CUtensorMap maps[kBwdMaps];
-  if (!bwd_maps(maps, q, k, v, dout, dq, dk, dv, sh, bf16)) return FA_ERR_CUDA;
-  char* wsb = static_cast<char*>(workspace);
-  fa::BwdParams prm{};
-  prm.v = static_cast<const __half*>(v);
-  prm.o = static_cast<const __half*>(o);
-  prm.dout = static_cast<const __half*>(dout);
-  prm.lse = lse;
-  prm.dq = static_cast<__half*>(dq);
-  prm.dk = static_cast<__half*>(dk);
-  prm.dv = static_cast<__half*>(dv);
-  prm.delta = reinterpret_cast<float*>(wsb + ws.delta_off);
-  prm.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
-  bwd_shape_params(prm, sh);
-  prm.scale = scale;
-  prm.scale_log2 = scale * kLog2e;
-  prm.status = dev->status;
-  const bool c = sh.causal != 0;
-  switch (D) {
-    case 64: rc = fa::launch_bwd_d64(c, bf16, maps, prm, dev->sms, stream); break;
-    case 128: rc = fa::launch_bwd_d128(c, bf16, maps, prm, dev->sms, stream); break;
-    default: rc = fa::launch_bwd_d256(c, bf16, maps, prm, dev->sms, stream); break;
-  }
-  return rc == 0 ? FA_OK : (rc == -2 ? FA_ERR_UNSUPPORTED : FA_ERR_CUDA);
+  return bwd_run(q, k, v, o, dout, lse, dq, dk, dv, static_cast<char*>(workspace), ws, sh, scale, stream, bf16, dev);
 }
 
 }  // namespace
@@ -601,29 +609,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   char* scratch = static_cast<char*>(noalloc_scratch_on_current_device());
   if (scratch == nullptr) return FA_ERR_CUDA;
 
-  CUtensorMap maps[kBwdMaps];
-  if (!bwd_maps(maps, q, k, v, dout, dq, dk, dv, sh, false)) return FA_ERR_CUDA;
-  fa::BwdParams prm{};
-  prm.v = static_cast<const __half*>(v);
-  prm.o = static_cast<const __half*>(o);
-  prm.dout = static_cast<const __half*>(dout);
-  prm.lse = lse;
-  prm.dq = static_cast<__half*>(dq);
-  prm.dk = static_cast<__half*>(dk);
-  prm.dv = static_cast<__half*>(dv);
-  prm.delta = reinterpret_cast<float*>(scratch + ws.delta_off);
-  prm.lse2 = reinterpret_cast<float*>(scratch + ws.lse2_off);
-  bwd_shape_params(prm, sh);
-  prm.scale = scale;
-  prm.scale_log2 = scale * kLog2e;
-  prm.status = dev->status;
-  const bool c = causal != 0;
-  switch (D) {
-    case 64: rc = fa::launch_bwd_d64(c, false, maps, prm, dev->sms, stream); break;
-    case 128: rc = fa::launch_bwd_d128(c, false, maps, prm, dev->sms, stream); break;
-    default: rc = fa::launch_bwd_d256(c, false, maps, prm, dev->sms, stream); break;
-  }
-  return rc == 0 ? FA_OK : FA_ERR_CUDA;
+  return bwd_run(q, k, v, o, dout, lse, dq, dk, dv, scratch, ws, sh, scale, stream, false, dev);
 }
 
 extern "C" int fa_selftest_wait_timeout(cudaStream_t stream) {

@@ -1063,15 +1063,16 @@ __global__ void __launch_bounds__(384, 1)
 template <int D, bool CAUSAL, bool BF>
 int launch_bwd2(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, cudaStream_t stream) {
   using T = Bwd2Traits<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, CAUSAL, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::A_SMEM) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(fa_bwd_dq_kernel<D, CAUSAL, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::B_SMEM) !=
-            cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
+  static DeviceOnceFlags attr_done;  // the attributes are per device
+  if (once_per_device(attr_done, current_device_index(), [] {
+        return cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, CAUSAL, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    T::A_SMEM) == cudaSuccess &&
+                       cudaFuncSetAttribute(fa_bwd_dq_kernel<D, CAUSAL, BF>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, T::B_SMEM) == cudaSuccess
+                   ? 0
+                   : -1;
+      }) != 0)
+    return -1;
   if constexpr (!T::kFuseDelta) {
     if (launch_prep<D, BF>(prm, stream) != 0) return -1;
   }

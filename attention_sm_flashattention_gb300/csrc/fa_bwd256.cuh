@@ -1006,15 +1006,16 @@ __global__ void __launch_bounds__(416, 1)
 template <bool CAUSAL, bool BF>
 int launch_bwd256(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, cudaStream_t stream) {
   using T = B256;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(fa_bwd256_dkdv_kernel<CAUSAL, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             T::A_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(fa_bwd256_dq_kernel<CAUSAL, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             T::B_SMEM) != cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
+  static DeviceOnceFlags attr_done;  // the attributes are per device
+  if (once_per_device(attr_done, current_device_index(), [] {
+        return cudaFuncSetAttribute(fa_bwd256_dkdv_kernel<CAUSAL, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    T::A_SMEM) == cudaSuccess &&
+                       cudaFuncSetAttribute(fa_bwd256_dq_kernel<CAUSAL, BF>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, T::B_SMEM) == cudaSuccess
+                   ? 0
+                   : -1;
+      }) != 0)
+    return -1;
   if (launch_prep<256, BF>(prm, stream) != 0) return -1;
   auto grid_for = [&](int heads, int tiles) {
     const long long units = CAUSAL ? static_cast<long long>(heads) * ((tiles + 1) / 2) : static_cast<long long>(heads) * tiles;

@@ -635,12 +635,14 @@ __global__ void __launch_bounds__(512, 1)
                                     : ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
             l = l * alpha + rs;
             m = m_new;
-            // With two 128-column O halves (D = 256), letting P V of this tile
-            // start while the previous P V still runs gave wrong O on GB300
-            // (the MMAs alternate between the two accumulators); there the
-            // softmax always waits for the previous P V before releasing P.
-            constexpr bool kSerialPV = (T::NOH > 1);
-            if (j > jb && (kSerialPV || __any_sync(0xffffffffu, alpha != 1.f))) {
+            // P V of this tile may start while the previous P V still runs
+            // (the tensor pipe executes one issuer's MMAs in order); only a
+            // rescale has to wait for it.  Every wait names the barrier of
+            // the tile's own P buffer and the phase of that use, and the
+            // previous use of the same buffer (tile t - 3) is known to be
+            // complete (waited at tile t - 1), so no wait can pass on a
+            // phase two uses old.
+            if (j > jb && __any_sync(0xffffffffu, alpha != 1.f)) {
               // O holds P V of the previous tiles: wait for the last P V, then
               // rescale (this half's columns of) rows whose max moved.
               ok = mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, wc, 6);
@@ -1008,8 +1010,10 @@ __global__ void __launch_bounds__(512, 1)
 template <int D, bool CAUSAL, bool BF, int MODE = kDense>
 int launch_fwd(const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaStream_t stream) {
   using T = FwdTraits<D, CAUSAL>;
-  static bool attr_set = false;  // per process; the attribute is per function, not per device
-  if (!attr_set) {
+  // Function attributes belong to the device current when they are set: set
+  // them once per device.
+  static DeviceOnceFlags attr_done;
+  const int rc = once_per_device(attr_done, current_device_index(), [] {
     if (cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL, BF, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              T::SMEM_ALLOC) != cudaSuccess)
       return -1;
@@ -1020,8 +1024,9 @@ int launch_fwd(const CUtensorMap* maps, const FwdParams& prm, int num_sms, cudaS
     if (cudaFuncGetAttributes(&fa_attr, fa_fwd_kernel<D, CAUSAL, BF, MODE>) != cudaSuccess ||
         fa_attr.numRegs * T::THREADS < T::SOFTMAX_THREADS * T::SOFTMAX_REGS + (T::THREADS - T::SOFTMAX_THREADS) * T::OTHER_REGS)
       return -1;
-    attr_set = true;
-  }
+    return 0;
+  });
+  if (rc != 0) return -1;
   const int nqt = (prm.Nq + T::BM - 1) / T::BM;
   const long long units = (CAUSAL ? static_cast<long long>(prm.heads) * ((nqt + 1) / 2)
                                   : static_cast<long long>(prm.heads) * nqt) *

@@ -8,6 +8,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "device_once.h"
+
 namespace fa {
 
 // Shapes: queries (and O, dO, dQ) are [heads, Nq, D]; keys and values (and
@@ -130,6 +132,12 @@ int launch_fwd_paged_split_d256(bool causal, bool bf16, const CUtensorMap* maps,
 // described for FwdParams::part_o / part_lse.
 int launch_split_combine(const float* part_o, const float* part_lse, void* o, float* lse, long long rows, int D,
                          int splits, bool bf16, int num_sms, cudaStream_t stream);
+
+// Index of the current device, or -1 if the runtime cannot tell.
+inline int current_device_index() {
+  int dev = -1;
+  return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
+}
 
 // Tile sizes the host needs to build tensor maps and size grids.
 inline int fwd_block_n(int D) { return D == 256 ? 64 : 128; }

@@ -22,25 +22,6 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Row-major 2-D matrix [rows x cols] of `elem_bytes`-byte elements with row
-// pitch `ld` elements, tiled in boxes of box_cols x box_rows.  128-byte
-// swizzle when box_cols * elem_bytes == 128, none otherwise.
-inline bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
-                         uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_cols, uint32_t box_rows,
-                         bool swizzle128) {
-  auto enc = tensor_map_encoder();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {ld * static_cast<uint64_t>(elem_bytes)};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 // `mats` row-major matrices [rows x cols] of `elem_bytes`-byte elements,
 // stored back to back (contiguous [mats, rows, cols]), tiled in boxes of
 // box_cols x box_rows x 1.  A box that runs past `rows` is zero-filled on

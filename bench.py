@@ -109,7 +109,8 @@ def oracle_sample(budget_s=12.0, max_heads=256):
     el = time.perf_counter() - t0
     fl = flops_step(1, done, N, D, CAUSAL)
     return {"value": fl / el / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"{done} of the {Z * H} heads (N{N} D{D} non-causal), fp64 numpy forward+backward, "
+            "sample": f"{done} of the {Z * H} heads (N{N} D{D} {'causal' if CAUSAL else 'non-causal'}), "
+                      f"fp64 numpy forward+backward, "
                       f"{el:.1f} s wall"}
 
 
@@ -166,6 +167,12 @@ class ClockSampler:
 # ----------------------------------------------------------------- GPU bench
 
 
+def smi_index(local_rank):
+    """nvidia-smi's index of this rank's GPU."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    return vis.split(",")[local_rank] if vis else local_rank
+
+
 def gpu_bench(args, rank, world, local_rank):
     import torch
 
@@ -174,10 +181,11 @@ def gpu_bench(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
-    gen = torch.Generator(device=dev).manual_seed(SEED + rank)
+    from attention_sm_flashattention_gb300.inputs import make_inputs
+
     elem = torch.bfloat16 if DTYPE == "bf16" else torch.float16
-    q, k, v, do = (torch.randn(shape, device=dev, dtype=elem, generator=gen)
-                   for shape in ((Z, H, N, D), (Z, HKV, NK, D), (Z, HKV, NK, D), (Z, H, N, D)))
+    # the seeded recipe the parity tests use (drawn on the CPU, then moved)
+    q, k, v, do = make_inputs(Z, H, N, D, SEED, device=dev, dtype=elem, Hkv=HKV, Nk=NK)
     scale = 1.0 / math.sqrt(D)
     o = torch.empty_like(q)
     lse = torch.empty((Z, H, N), device=dev, dtype=torch.float32)
@@ -199,8 +207,7 @@ def gpu_bench(args, rank, world, local_rank):
             import torch.distributed as dist
             dist.barrier()
 
-    sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
-                           os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank])
+    sampler = ClockSampler(smi_index(local_rank))
     sampler.start()
     time.sleep(0.3)  # let the sampler start before the timed region
     # per-call events on the launching stream: forward kernel and backward call
@@ -223,8 +230,10 @@ def gpu_bench(args, rank, world, local_rank):
     if fa.device_status() != 0:
         raise RuntimeError("device status reports a kernel wait timeout in the timed region")
     total_ms = t_start.elapsed_time(t_end)
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    fwd_all = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_all = [e[1].elapsed_time(e[2]) for e in ev]
+    fwd_ms = statistics.mean(fwd_all)
+    bwd_ms = statistics.mean(bwd_all)
 
     # ---- end to end through the public API: pinned host in, host out.
     # Every step copies its four inputs in and its four results out.  The
@@ -283,8 +292,122 @@ def gpu_bench(args, rank, world, local_rank):
         raise RuntimeError("device status reports a kernel wait timeout in the end-to-end leg")
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv))
+    del bufs, hq, hk, hv, hdo, ho, hdq, hdk, hdv
     return {"total_ms": total_ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "e2e_ms": e2e_ms,
-            "h2d": h2d, "d2h": d2h, "clocks": clocks}
+            "fwd_stats": call_stats(fwd_all), "bwd_stats": call_stats(bwd_all),
+            "h2d": h2d, "d2h": d2h, "clocks": clocks, "step": step}
+
+
+def call_stats(ms):
+    """Median, min and 90th percentile of per-call times (ms)."""
+    xs = sorted(ms)
+    return {"median_ms": statistics.median(xs), "min_ms": xs[0],
+            "p90_ms": xs[max(0, math.ceil(0.9 * len(xs)) - 1)], "calls": len(xs)}
+
+
+# The other benchmark shapes, reported beside the headline in the same line:
+# (workload, flush L2 before every timed call).  The Z4 D64 shape's inputs
+# (17 MB) fit in L2, so a 256 MB buffer is written before each call.
+SIDE_CONFIGS = (("z4h8n1024d64", True), ("z128h8n1024d128c", False), ("z128h8n1024d256", False),
+                ("z128h8n1024d256c", False))
+
+
+def config_bench(name, flush, dev, calls=50, warmup=10):
+    """fa_fwd then fa_bwd on one benchmark shape (inputs from the seeded
+    recipe): `warmup` untimed calls, then `calls` calls of each, every call
+    timed alone with CUDA events on the launching stream."""
+    import torch
+
+    import attention_sm_flashattention_gb300 as fa
+    from attention_sm_flashattention_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS[name]
+    stream = torch.cuda.current_stream()
+    q, k, v, do = make_inputs(w.Z, w.H, w.N, w.D, w.seed, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.Z, w.H, w.N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.bwd_workspace_size(w.Z, w.H, w.N, w.D, w.causal), device=dev, dtype=torch.uint8)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
+
+    def fwd():
+        fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=(o, lse))
+
+    def bwd():
+        fa.bwd(q, k, v, o, do, lse, causal=w.causal, scale=w.scale, workspace=ws, out=(dq, dk, dv))
+
+    for _ in range(warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(calls)]
+    for e in ev:
+        if flush:
+            flush_buf.zero_()
+        e[0].record(stream)
+        fwd()
+        e[1].record(stream)
+        if flush:
+            flush_buf.zero_()
+        e[2].record(stream)
+        bwd()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    if fa.device_status() != 0:
+        raise RuntimeError(f"device status reports a kernel wait timeout ({name})")
+    f_st = call_stats([e[0].elapsed_time(e[1]) for e in ev])
+    b_st = call_stats([e[2].elapsed_time(e[3]) for e in ev])
+    peak = measured_peaks()["tflops"]
+    f_fl = flops_fwd(w.Z, w.H, w.N, w.D, w.causal)
+    f_tf = f_fl / (f_st["median_ms"] * 1e-3) / 1e12
+    b_tf = 2.5 * f_fl / (b_st["median_ms"] * 1e-3) / 1e12
+    in_mb = 4 * w.Z * w.H * w.N * w.D * 2 / 1e6
+    return {
+        "workload": f"attention fwd+bwd, {w.describe()}, fp16 inputs ~N(0,1), scale 1/sqrt(D)",
+        "fwd": dict(f_st, tflops=f_tf, frac=f_tf / peak),
+        "bwd": dict(b_st, tflops=b_tf, frac=b_tf / peak, kernels=bwd_kernel_names(w.D, w.causal)),
+        "fwd_bwd_tflops": 3.5 * f_fl / ((f_st["median_ms"] + b_st["median_ms"]) * 1e-3) / 1e12,
+        "l2": (f"inputs {in_mb:.0f} MB, smaller than L2: a 256 MB buffer written before every timed call"
+               if flush else f"inputs larger than L2 ({in_mb:.0f} MB), no flush needed"),
+    }
+
+
+def side_configs(dev, sampler_index):
+    """Every SIDE_CONFIGS shape through config_bench, clocks sampled throughout."""
+    sampler = ClockSampler(sampler_index)
+    sampler.start()
+    time.sleep(0.3)
+    out = {name: config_bench(name, flush, dev) for name, flush in SIDE_CONFIGS}
+    out["clocks"] = sampler.stop()
+    out["timing"] = ("per call: 10 warm-up calls, then 50 calls of fa_fwd and of fa_bwd, each timed alone with "
+                     "CUDA events; TFLOP/s and frac (of the measured burst bf16 peak) from the median")
+    return out
+
+
+def sustained_bench(step, ms_per_step, sampler_index, seconds=2.5):
+    """The headline step repeated back to back for about `seconds`, against
+    the sustained (power-capped) peak."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    n = max(50, int(seconds * 1e3 / ms_per_step))
+    sampler = ClockSampler(sampler_index)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / n
+    val = flops_step() / (ms * 1e-3) / 1e12
+    peaks = measured_peaks()
+    peak = peaks.get("tflops_sustained") or peaks["tflops"]
+    return {"steps": n, "seconds": ms * n / 1e3, "ms_per_step": ms, "value": val, "unit": UNIT, "peak": peak,
+            "peak_kind": "sustained bf16 cuBLAS (" + peaks["source"] + ")", "frac": val / peak, "clocks": clocks}
 
 
 def reduce_max(vals, world):
@@ -369,7 +492,7 @@ def paged_bench(args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / args.steps
 
-    sampler = ClockSampler(0 if "CUDA_VISIBLE_DEVICES" not in os.environ else os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0])
+    sampler = ClockSampler(smi_index(0))
     sampler.start()
     time.sleep(0.3)
     ms = timed(lambda: fa.fwd_paged(q, kc, vc, table, lens, causal=CAUSAL, scale=scale, out=(o, lse)))
@@ -444,6 +567,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the other benchmark shapes and the sustained leg (profiling runs)")
     # Workload overrides, for profiling the same step on a smaller case; the
     # default is the benchmark workload above.
     ap.add_argument("--z", type=int, default=Z)
@@ -505,14 +630,15 @@ def main():
         per_head = flops_step(1, 1, N, D, CAUSAL)
         el = sum(times)
         val = per_head * len(times) / el / 1e12
-        ms = flops_step() / (val * 1e12) * 1e3
+        ms = el / len(times) * 1e3  # a timed step is one head
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "step": "one head of the workload (fa_fwd + fa_bwd's arithmetic in fp64 numpy)",
+                "ms_all_heads_extrapolated": ms * Z * H,
                 "cpu_baseline": {"value": val, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                                 "sample": f"{len(times)} heads of the workload, one per step, fp64 numpy "
-                                           f"forward+backward, {el:.1f} s; ms_per_step extrapolates to all "
-                                           f"{Z * H} heads"},
+                                 "sample": f"{len(times)} heads of the workload ({'causal' if CAUSAL else 'non-causal'}), "
+                                           f"one per step, fp64 numpy forward+backward, {el:.1f} s"},
                 "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -544,6 +670,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DTYPE, "data": "synthetic", "config": config,
         "fwd_ms": r["fwd_ms"], "bwd_ms": r["bwd_ms"], "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+        "fwd_call": r["fwd_stats"], "bwd_call": r["bwd_stats"],
         "pct_of_peak": {"fwd": fwd_tf / peaks["tflops"], "fwd_bwd": value / world / peaks["tflops"],
                         "bwd": bwd_tf / peaks["tflops"], "peak_tflops": peaks["tflops"],
                         "peak_source": peaks["source"]},
@@ -558,6 +685,11 @@ def main():
                           "buffer sets, overlapped with the kernels of the neighbouring steps"},
         "gpu_launches": (1 + bwd_launches(D)) * args.steps,
     }
+    if world == 1 and not args.no_side:
+        # the other benchmark shapes, then the headline step held for seconds
+        import torch
+        line["configs"] = side_configs(torch.device("cuda", local_rank), smi_index(local_rank))
+        line["sustained"] = sustained_bench(r["step"], ms_per_step, smi_index(local_rank))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample()
     if rank == 0:

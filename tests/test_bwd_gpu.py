@@ -7,10 +7,10 @@ import pytest
 import torch
 
 from attention_sm_flashattention_gb300 import api
-from attention_sm_flashattention_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
+from attention_sm_flashattention_gb300.inputs import make_inputs
 from oracle import attention as orc
 
-from helpers import GRAD_RTOL, rel_fro, sample_heads
+from helpers import GRAD_RTOL, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -69,20 +69,6 @@ def test_bwd_gradient_sum_invariants(D):
     assert np.max(np.abs(sdv - sdo)) <= 2e-2 * max(1.0, np.max(np.abs(sdo)))
     sdk = dk.double().sum(dim=2).cpu().numpy()
     assert np.max(np.abs(sdk)) <= 2e-2 * max(1.0, float(dk.double().abs().sum(dim=2).max()))
-
-
-@pytest.mark.parametrize("name", list(WORKLOADS))
-def test_bwd_workloads_sampled_heads(name):
-    w = WORKLOADS[name]
-    q, k, v, do = workload_inputs(w)
-    dq, dk, dv = run(q, k, v, do, w.causal, w.scale)
-    heads = sample_heads(w.heads, 4)
-    ref = orc.attn_bwd_ref(q, k, v, do, w.causal, w.scale, heads=heads)
-    for g, r in zip((dq, dk, dv), ref):
-        gf = g.reshape(w.heads, w.N, w.D)
-        for i, h in enumerate(heads):
-            assert rel_fro(gf[h], r[i]) <= GRAD_RTOL, (name, h)
-        assert torch.isfinite(g).all()
 
 
 @pytest.mark.parametrize("causal", [False, True])

@@ -7,10 +7,10 @@ import pytest
 import torch
 
 from attention_sm_flashattention_gb300 import api
-from attention_sm_flashattention_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
+from attention_sm_flashattention_gb300.inputs import make_inputs
 from oracle import attention as orc
 
-from helpers import LSE_ATOL, O_ATOL, max_abs, sample_heads
+from helpers import LSE_ATOL, O_ATOL, max_abs
 
 pytestmark = pytest.mark.gpu
 
@@ -69,23 +69,6 @@ def test_fwd_causal_row0_is_v0():
     assert max_abs(o[0, 0, 0], v[0, 0, 0].double().numpy()) <= 1e-3
     want = sc * float(q[0, 0, 0].double() @ k[0, 0, 0].double())
     assert abs(float(lse[0, 0, 0]) - want) <= LSE_ATOL
-
-
-@pytest.mark.parametrize("name", list(WORKLOADS))
-def test_fwd_workloads_sampled_heads(name):
-    # The benchmark shapes, launched exactly as the benchmark launches them;
-    # compared on a sample of heads (all heads for the small shapes).
-    w = WORKLOADS[name]
-    q, k, v, _ = workload_inputs(w)
-    o, lse = run_fwd(q, k, v, w.causal, w.scale)
-    heads = sample_heads(w.heads, 6)
-    o_ref, lse_ref = orc.attn_fwd_ref(q, k, v, w.causal, w.scale, heads=heads)
-    o_f = o.reshape(w.heads, w.N, w.D)
-    lse_f = lse.reshape(w.heads, w.N)
-    for i, h in enumerate(heads):
-        assert max_abs(o_f[h], o_ref[i]) <= O_ATOL, (name, h)
-        assert max_abs(lse_f[h], lse_ref[i]) <= LSE_ATOL, (name, h)
-    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
 
 
 @pytest.mark.parametrize("causal", [False, True])
