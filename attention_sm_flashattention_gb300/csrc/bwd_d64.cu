@@ -1,6 +1,5 @@
-// Backward kernel instantiations for head dimension 64: Delta preprocess,
-// then the dK/dV kernel and the dQ kernel.
-#include "fa_bwd.cuh"
+// Backward kernel instantiations for head dimension 64: the dQ kernel (which
+// also forms Delta and lse2), then the dK/dV kernel.
 #include "fa_bwd2.cuh"
 
 namespace fa {

@@ -454,10 +454,11 @@ int bwd_checks(const void* q, const void* k, const void* v, const void* o, const
 // [0] q, [1] k, [2] v, [3] dout, then the outputs [4] dq, [5] dk, [6] dv
 // (TMA stores of the D <= 128 kernels); for D = 256, [0] and [3] have the
 // dK/dV kernel's 64-row query tiles and [7] q, [8] k, [2] v the dQ kernel's
-// 128-row query tiles and 64-row key tiles.
-constexpr int kBwdMaps = 9;
-bool bwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
-              void* dv, const Shape& sh, bool bf16) {
+// 128-row query tiles and 64-row key tiles; [9] the forward output o
+// (128-row tiles, read by the D <= 128 dQ kernel to form Delta).
+constexpr int kBwdMaps = 10;
+bool bwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v, const void* o, const void* dout,
+              void* dq, void* dk, void* dv, const Shape& sh, bool bf16) {
   const int D = sh.D;
   const int bq = (D == 256) ? 64 : 128, bv = (D == 256) ? 64 : 128;
   const long long hq = sh.q_heads(), hk = sh.kv_heads();
@@ -465,7 +466,7 @@ bool bwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v, co
          map16(&maps[2], v, hk, sh.Nk, D, bv, bf16) && map16(&maps[3], dout, hq, sh.Nq, D, bq, bf16) &&
          map16(&maps[4], dq, hq, sh.Nq, D, 128, bf16) && map16(&maps[5], dk, hk, sh.Nk, D, 128, bf16) &&
          map16(&maps[6], dv, hk, sh.Nk, D, 128, bf16) && map16(&maps[7], q, hq, sh.Nq, D, 128, bf16) &&
-         map16(&maps[8], k, hk, sh.Nk, D, 64, bf16);
+         map16(&maps[8], k, hk, sh.Nk, D, 64, bf16) && map16(&maps[9], o, hq, sh.Nq, D, 128, bf16);
 }
 
 void bwd_shape_params(fa::BwdParams& prm, const Shape& sh) {
@@ -485,7 +486,7 @@ int bwd_run(const void* q, const void* k, const void* v, const void* o, const vo
             void* dq, void* dk, void* dv, char* scratch, const BwdWorkspace& ws, const Shape& sh, float scale,
             cudaStream_t stream, bool bf16, const DevInfo* dev) {
   CUtensorMap maps[kBwdMaps];
-  if (!bwd_maps(maps, q, k, v, dout, dq, dk, dv, sh, bf16)) return FA_ERR_CUDA;
+  if (!bwd_maps(maps, q, k, v, o, dout, dq, dk, dv, sh, bf16)) return FA_ERR_CUDA;
   fa::BwdParams prm{};
   prm.v = static_cast<const __half*>(v);
   prm.o = static_cast<const __half*>(o);

@@ -69,22 +69,25 @@ struct Bwd2Traits {
   static_assert(A_SMEM <= 232448, "dK/dV kernel shared memory budget");
   static_assert(A_R + 2 * BM <= 512, "dK/dV kernel TMEM budget");
 
-  // ---- dQ kernel
+  // ---- dQ kernel.  TMEM: dQ, then Q_i and dO_i as MMA A operands (16-bit
+  // pairs: D / 2 columns each), then two 128-column regions for the key
+  // tiles.  Shared memory: staging buffers for the next item's Q and dO (the
+  // Q buffer then receives dQ for its store), a K ring and a V ring.
+  // O_i, for Delta: staged by TMA beside Q_i and dO_i where shared memory
+  // has room (D = 64); at D = 128 the compute warps read it from global
+  // memory (a single V stage to make room measured slower).
+  static constexpr bool kStageO = (D == 64);
   static constexpr int B_K_STAGES = (D == 64) ? 4 : 3;
   static constexpr int B_V_STAGES = (D == 64) ? 4 : 2;
-  static constexpr int B_DQ = 0, B_S = D, B_DP = D + BN;  // dP/dS buffer b at B_DP + b * BN
-  static constexpr int B_SM_Q = 0, B_SM_DO = TILE, B_SM_K = 2 * TILE;
+  static constexpr int B_DQ = 0, B_QT = D, B_OT = D + D / 2, B_R = 2 * D;  // region r at B_R + r * BN
+  static constexpr int B_SM_Q = 0, B_SM_DO = TILE, B_SM_O = 2 * TILE, B_SM_K = (kStageO ? 3 : 2) * TILE;
   static constexpr int B_SM_V = B_SM_K + B_K_STAGES * TILE;
   static constexpr int B_SM_BAR = B_SM_V + B_V_STAGES * TILE;
-  // D = 128: the dQ kernel forms Delta and lse2 itself (from the dO tile it
-  // holds); D = 64 (half the MMA work per tile, so the fixed per-item cost
-  // weighs twice as much) measured faster with the separate preprocess.
-  static constexpr bool kFuseDelta = (D == 128);
-  static constexpr int B_SM_DX = B_SM_BAR + 512;        // Delta halves: [unit parity][warpgroup][BM] fp32
+  static constexpr int B_SM_DX = B_SM_BAR + 512;        // Delta halves: [item parity][warpgroup][BM] fp32
   static constexpr int B_SM_BYTES = B_SM_DX + 2 * 2 * BM * 4;
   static constexpr int B_SMEM = B_SM_BYTES > MIN_SMEM ? B_SM_BYTES : MIN_SMEM;
   static_assert(B_SMEM <= 232448, "dQ kernel shared memory budget");
-  static_assert(B_DP + 2 * BN <= 512, "dQ kernel TMEM budget");
+  static_assert(B_R + 2 * BN <= 512, "dQ kernel TMEM budget");
 };
 
 // Work units of the two kernels.  Non-causal: one unit per (head, tile),
@@ -588,24 +591,65 @@ __global__ void __launch_bounds__(384, 1)
 
 // ========================================================================= dQ
 
+// The query-tile items of one CTA in processing order: units blockIdx.x,
+// blockIdx.x + gridDim.x, ...; a causal unit is two items (tiles t and
+// n-1-t of one head).
+template <bool CAUSAL>
+struct DqItems {
+  int u, units, nt, head, ta, tb, half;
+  __device__ DqItems(int units_, int nt_) : u(blockIdx.x), units(units_), nt(nt_), head(0), ta(0), tb(-1), half(0) {
+    if (u < units) bwd2_decode<CAUSAL>(u, nt, head, ta, tb);
+  }
+  __device__ bool valid() const { return u < units; }
+  __device__ int tile() const { return half ? tb : ta; }
+  __device__ void next() {
+    if (half == 0 && tb >= 0) {
+      half = 1;
+      return;
+    }
+    half = 0;
+    u += gridDim.x;
+    if (u < units) bwd2_decode<CAUSAL>(u, nt, head, ta, tb);
+  }
+};
+
 struct DqBars {
-  uint64_t q_full, q_empty;
+  // Q_n, dO_n landed in the staging buffers; the compute warps have read
+  // them (copied into TMEM, Delta formed); Q_n and dO_n are in TMEM
+  uint64_t qo_full, qo_empty, qo_tmem;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full, s_free;
-  uint64_t dp_full[2], ds_full[2], dq_done[2];
+  uint64_t s_full[2], dq_done[2];  // [2]: per TMEM region
+  uint64_t s_free, dp_full, ds_full;
   uint64_t dq_full, dq_free, mma_done[2];
-  uint64_t epi_full;  // dQ_i staged in the Q buffer
-  uint64_t dx_full[2];  // both Delta halves of a unit's rows are in shared memory
+  uint64_t epi_full[2];  // dQ of item n staged for its store (barrier n % 2)
+  uint64_t dx_full[2];   // both Delta halves of an item's rows are in shared memory
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(DqBars) <= 512, "barrier area");
 
+// TMEM of the dQ kernel: dQ_i, then Q_i and dO_i as MMA A operands (16-bit
+// pairs, one query row per lane), then two 128-column regions that the key
+// tiles use in turn.  Key tile t works in region t % 2 from start to end: S,
+// read into registers at once; then dP over it; then dS (16-bit) over the
+// first half of each warpgroup's dP columns, the A operand of dQ += dS K.
+// The region is free again once that dQ MMA completed, so S of tile t+1
+// runs while the compute warps work on tile t.  S and dP read only K and V
+// from shared memory (their A operands are in TMEM), which keeps the MMAs
+// below the shared-memory bandwidth that the K/V loads also use.
+//
+// Item boundaries: Q_n and dO_n arrive in shared-memory staging buffers
+// during item n-1.  At the boundary the compute warps copy them into TMEM
+// (and form Delta_n from dO_n and O_n), then stage dQ of item n-1 (times
+// scale, 16-bit) in the Q staging buffer they just emptied; the producer
+// writes it out with a TMA store before loading Q_{n+1} there.  The last
+// item's dQ goes to the dO staging buffer.
 template <int D, bool CAUSAL, bool BF>
 __global__ void __launch_bounds__(384, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                     const __grid_constant__ CUtensorMap tm_dq, const BwdParams prm) {
+                     const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_o,
+                     const BwdParams prm) {
   using T = Bwd2Traits<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
@@ -614,48 +658,48 @@ __global__ void __launch_bounds__(384, 1)
   }
   DqBars* bars = reinterpret_cast<DqBars*>(smem + T::B_SM_BAR);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Two MMA warps: warp 9 issues S and dP, warp 11 issues dQ, so that one
-  // can issue while the other waits on the compute warps.
-  constexpr int PRODUCER_WARP = 8, MMA_WARP = 9, V_PRODUCER_WARP = 10, DQ_MMA_WARP = 11, NCOMPUTE = 256;
+  // warp 9 issues S and dP (and owns TMEM); warp 11 issues dQ; warp 8 loads
+  // Q, dO and K and stores dQ; warp 10 loads V
+  constexpr int PRODUCER_WARP = 8, S_MMA_WARP = 9, V_PRODUCER_WARP = 10, GRAD_MMA_WARP = 11, NCOMPUTE = 256;
   constexpr int KS = T::B_K_STAGES, VS = T::B_V_STAGES;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    // Q_i, dO_i are free once the unit's last dP completed (MMA commit) and
-    // the compute warps have read dO_i for Delta
-    mbar_init(&bars->q_empty, T::kFuseDelta ? 1 + NCOMPUTE : 1);
-    mbar_init(&bars->epi_full, NCOMPUTE);
-    mbar_init(&bars->dx_full[0], NCOMPUTE);
-    mbar_init(&bars->dx_full[1], NCOMPUTE);
+    mbar_init(&bars->qo_full, 1);
+    mbar_init(&bars->qo_empty, NCOMPUTE);
+    mbar_init(&bars->qo_tmem, NCOMPUTE);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, NCOMPUTE);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->dp_full[i], 1);
-      mbar_init(&bars->ds_full[i], NCOMPUTE);
+      mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->dq_done[i], 1);
+      mbar_init(&bars->epi_full[i], NCOMPUTE);
+      mbar_init(&bars->dx_full[i], NCOMPUTE);
+      mbar_init(&bars->mma_done[i], 1);
     }
+    mbar_init(&bars->s_free, NCOMPUTE);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->ds_full, NCOMPUTE);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, NCOMPUTE);
-    mbar_init(&bars->mma_done[0], 1);
-    mbar_init(&bars->mma_done[1], 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == MMA_WARP) {
+  if (warp == S_MMA_WARP) {
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
   if (warp == PRODUCER_WARP && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dq);
+    tma_prefetch_desc(&tm_o);
+  } else if (warp == V_PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_v);
   }
   tc_fence_before();
   __syncthreads();
@@ -663,7 +707,7 @@ __global__ void __launch_bounds__(384, 1)
 
   const WaitCtx wc{prm.status, &bars->abort_flag};
   const uint32_t tmem = bars->tmem_base;
-  // Unit = (query head, query tile i); K/V come from head / G.  Causal: key
+  // Item = (query head, query tile i); K/V come from head / G.  Causal: key
   // tiles up to the last key the tile's last query sees.
   const int G = prm.group, Nk = prm.Nk, coff = prm.causal_off, Nq_pad = prm.Nq_pad;
   const int nqt = (prm.Nq + T::BM - 1) / T::BM, nkv = (Nk + T::BN - 1) / T::BN;
@@ -671,53 +715,71 @@ __global__ void __launch_bounds__(384, 1)
   auto num_kv = [&](int i) { return CAUSAL ? (min((i + 1) * T::BM + coff, Nk) + T::BN - 1) / T::BN : nkv; };
 
   if (warp == PRODUCER_WARP) {
-    // ------------------------------------------------ producer: Q, dO and K
+    // ------------------------------------- producer: Q, dO, K; dQ write-out
     if (lane == 0) {
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      uint32_t qc = 0, k_it = 0;
+      uint32_t n = 0, qc = 0, k_it = 0;  // items begun, Q/dO loads issued, K loads issued
+      int h1 = 0, i1 = 0, h2 = 0, i2 = 0;  // (head, tile) of items n-1 and n-2
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        int head, ia, ib;
-        bwd2_decode<CAUSAL>(u, nqt, head, ia, ib);
-        for (int half = 0; ok && half < 2; ++half) {
-          const int i = half ? ib : ia;
-          if (i < 0) break;
-          // The item's first K tile goes first: its ring slot frees up early
-          // (tile t-3's dQ), while the Q, dO buffer waits for the previous
-          // item's last dP, so loading K_0 first lets the two latencies
-          // overlap instead of adding up at the item boundary.
-          for (int j = 0; j < num_kv(i); ++j) {
-            if (j == 1 || num_kv(i) == 0) break;
-            const int ks = k_it % KS;
-            if (!(ok = mbar_wait(&bars->k_empty[ks], ((k_it / KS) & 1) ^ 1, wc, 82))) break;
-            mbar_arrive_expect_tx(&bars->k_full[ks], T::TILE);
-            for (int s = 0; s < T::DSUB; ++s)
-              tma_load_3d_hint(smem + T::B_SM_K + ks * T::TILE + s * T::SUB, &tm_k, &bars->k_full[ks], s * 64,
-                               j * T::BN, head / G, pol_kv);
-            ++k_it;
-          }
-          if (!ok) break;
-          if (!(ok = mbar_wait(&bars->q_empty, (qc & 1) ^ 1, wc, 81))) break;
-          mbar_arrive_expect_tx(&bars->q_full, 2 * T::TILE);
-          for (int s = 0; s < T::DSUB; ++s) {
-            tma_load_3d_hint(smem + T::B_SM_Q + s * T::SUB, &tm_q, &bars->q_full, s * 64, i * T::BM, head, pol_q);
-            tma_load_3d_hint(smem + T::B_SM_DO + s * T::SUB, &tm_do, &bars->q_full, s * 64, i * T::BM, head, pol_q);
-          }
-          ++qc;
-          for (int j = 1; j < num_kv(i); ++j) {
-            const int ks = k_it % KS;
-            if (!(ok = mbar_wait(&bars->k_empty[ks], ((k_it / KS) & 1) ^ 1, wc, 82))) break;
-            mbar_arrive_expect_tx(&bars->k_full[ks], T::TILE);
-            for (int s = 0; s < T::DSUB; ++s)
-              tma_load_3d_hint(smem + T::B_SM_K + ks * T::TILE + s * T::SUB, &tm_k, &bars->k_full[ks], s * 64,
-                               j * T::BN, head / G, pol_kv);
-            ++k_it;
+      // write dQ of item m (query head h, tile i), staged in buffer `buf`
+      auto store_dq = [&](uint32_t m, int h, int i, int buf) -> bool {
+        if (!mbar_wait(&bars->epi_full[m & 1], (m >> 1) & 1, wc, 84)) return false;
+        for (int s = 0; s < T::DSUB; ++s) tma_store_3d(&tm_dq, smem + buf + s * T::SUB, s * 64, i * T::BM, h);
+        bulk_commit();
+        bulk_wait_read<0>();
+        return true;
+      };
+      // Q_n, dO_n (and O_n where staged) into the (empty) staging buffers
+      auto load_qo = [&](int head, int i) {
+        mbar_arrive_expect_tx(&bars->qo_full, (T::kStageO ? 3 : 2) * T::TILE);
+        for (int s = 0; s < T::DSUB; ++s) {
+          tma_load_3d_hint(smem + T::B_SM_Q + s * T::SUB, &tm_q, &bars->qo_full, s * 64, i * T::BM, head, pol_q);
+          tma_load_3d_hint(smem + T::B_SM_DO + s * T::SUB, &tm_do, &bars->qo_full, s * 64, i * T::BM, head, pol_q);
+          if (T::kStageO)
+            tma_load_3d_hint(smem + T::B_SM_O + s * T::SUB, &tm_o, &bars->qo_full, s * 64, i * T::BM, head, pol_q);
+        }
+        ++qc;
+      };
+      DqItems<CAUSAL> it(units, nqt);
+      if (it.valid()) load_qo(it.head, it.tile());
+      for (; ok && it.valid(); ++n) {
+        const int head = it.head, i = it.tile(), nj = num_kv(i);
+        DqItems<CAUSAL> nx = it;
+        nx.next();
+        for (int j = 0; ok && j < nj; ++j) {
+          const int ks = k_it % KS;
+          if (!(ok = mbar_wait(&bars->k_empty[ks], ((k_it / KS) & 1) ^ 1, wc, 82))) break;
+          mbar_arrive_expect_tx(&bars->k_full[ks], T::TILE);
+          for (int s = 0; s < T::DSUB; ++s)
+            tma_load_3d_hint(smem + T::B_SM_K + ks * T::TILE + s * T::SUB, &tm_k, &bars->k_full[ks], s * 64,
+                             j * T::BN, head / G, pol_kv);
+          ++k_it;
+          // Once the item's first two K tiles are on their way (they load
+          // during the previous item), the next item's Q and dO go into the
+          // staging buffers: the compute warps empty them at this item's
+          // start, after which dQ of the previous item, staged in the Q
+          // buffer, is written out.  They then land a whole item ahead.
+          if (j == min(1, nj - 1) && nx.valid()) {
+            if (n >= 1 && !(ok = store_dq(n - 1, h1, i1, T::B_SM_Q))) break;
+            if (!(ok = mbar_wait(&bars->qo_empty, n & 1, wc, 81))) break;
+            load_qo(nx.head, nx.tile());
           }
         }
+        h2 = h1;
+        i2 = i1;
+        h1 = head;
+        i1 = i;
+        it = nx;
       }
-      if (qc > 0) bwd2_drain(&bars->q_full, (qc - 1) & 1);
-      for (uint32_t i = (k_it > KS ? k_it - KS : 0); i < k_it; ++i) bwd2_drain(&bars->k_full[i % KS], (i / KS) & 1);
+      // the last two items' dQ: item n-2 (staged in the Q buffer at the
+      // start of the last item, which loaded no successor) and item n-1, the
+      // CTA's last (in the dO buffer)
+      if (ok && n >= 2) ok = store_dq(n - 2, h2, i2, T::B_SM_Q);
+      if (ok && n >= 1) ok = store_dq(n - 1, h1, i1, T::B_SM_DO);
+      bulk_wait<0>();  // all stores complete before the CTA exits
+      if (qc > 0) bwd2_drain(&bars->qo_full, (qc - 1) & 1);
+      for (uint32_t x = (k_it > KS ? k_it - KS : 0); x < k_it; ++x) bwd2_drain(&bars->k_full[x % KS], (x / KS) & 1);
     }
   } else if (warp == V_PRODUCER_WARP) {
     // --------------------------------------------------------- producer: V
@@ -725,146 +787,108 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t pol_kv = l2_policy_evict_last();
       uint32_t v_it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        int head, ia, ib;
-        bwd2_decode<CAUSAL>(u, nqt, head, ia, ib);
-        for (int half = 0; ok && half < 2; ++half) {
-          const int i = half ? ib : ia;
-          if (i < 0) break;
-          for (int j = 0; j < num_kv(i); ++j) {
-            const int vs = v_it % VS;
-            if (!(ok = mbar_wait(&bars->v_empty[vs], ((v_it / VS) & 1) ^ 1, wc, 83))) break;
-            mbar_arrive_expect_tx(&bars->v_full[vs], T::TILE);
-            for (int s = 0; s < T::DSUB; ++s)
-              tma_load_3d_hint(smem + T::B_SM_V + vs * T::TILE + s * T::SUB, &tm_v, &bars->v_full[vs], s * 64,
-                               j * T::BN, head / G, pol_kv);
-            ++v_it;
-          }
+      for (DqItems<CAUSAL> it(units, nqt); ok && it.valid(); it.next()) {
+        for (int j = 0; j < num_kv(it.tile()); ++j) {
+          const int vs = v_it % VS;
+          if (!(ok = mbar_wait(&bars->v_empty[vs], ((v_it / VS) & 1) ^ 1, wc, 83))) break;
+          mbar_arrive_expect_tx(&bars->v_full[vs], T::TILE);
+          for (int s = 0; s < T::DSUB; ++s)
+            tma_load_3d_hint(smem + T::B_SM_V + vs * T::TILE + s * T::SUB, &tm_v, &bars->v_full[vs], s * 64,
+                             j * T::BN, it.head / G, pol_kv);
+          ++v_it;
         }
       }
-      for (uint32_t i = (v_it > VS ? v_it - VS : 0); i < v_it; ++i) bwd2_drain(&bars->v_full[i % VS], (i / VS) & 1);
+      for (uint32_t x = (v_it > VS ? v_it - VS : 0); x < v_it; ++x) bwd2_drain(&bars->v_full[x % VS], (x / VS) & 1);
     }
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------- MMA warp: S = Q K^T, dP = dO V^T
+  } else if (warp == S_MMA_WARP) {
+    // -------------------------------- MMA warp: S = Q K^T and dP = dO V^T
+    // The tensor pipe runs its queue in issue order.  This warp issues per
+    // key tile dP(t), then S(t+1): the compute warps need dP(t) first, and
+    // S(t+1) (into region (t+1) % 2, free once the dQ MMA of tile t-1
+    // completed) runs while they turn dP(t) into dS(t).
     constexpr uint32_t id_s = idesc_16<BF>(128, T::BN, false, false);  // S, dP: M queries, N keys
     const uint32_t sb = smem_u32(smem);
-    const uint64_t qdesc = sdesc_sw128(sb + T::B_SM_Q, 16, 1024), odesc = sdesc_sw128(sb + T::B_SM_DO, 16, 1024);
-    uint32_t t = 0, k_it = 0, v_it = 0, qc = 0;
+    uint32_t ts = 0, tp = 0, n = 0, k_it = 0, v_it = 0;  // tiles whose S / dP is issued
     bool ok = true;
-    // S(tile) = Q K^T from K stage `kidx`; the S buffer is free once the
-    // compute warps have read the previous tile's S (right at its start)
-    auto issue_s = [&](uint32_t tile, uint32_t kidx) -> bool {
-      const int ks = kidx % KS;
-      if (!warp_wait(&bars->k_full[ks], (kidx / KS) & 1, wc, 91)) return false;
-      if (tile >= 1 && !warp_wait(&bars->s_free, (tile - 1) & 1, wc, 92)) return false;
+    // S(ts); the first tile of item m also needs the item's Q in TMEM
+    auto issue_s = [&](bool first_of_item, uint32_t m) -> bool {
+      const int ks = k_it % KS, r = ts & 1;
+      if (first_of_item && !warp_wait(&bars->qo_tmem, m & 1, wc, 91)) return false;
+      if (!warp_wait(&bars->k_full[ks], (k_it / KS) & 1, wc, 92)) return false;
+      if (ts >= 2 && !warp_wait(&bars->dq_done[r], ((ts - 2) >> 1) & 1, wc, 93)) return false;
       tc_fence_after();
       const uint64_t kdesc = sdesc_sw128(sb + T::B_SM_K + ks * T::TILE, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * T::SUB + (kk % 4) * 32;
-        mma_f16_ss_warp(tmem + T::B_S, sdesc_add(qdesc, off), sdesc_add(kdesc, off), id_s, kk > 0 ? 1u : 0u);
-      }
-      mma_commit_warp(&bars->s_full);
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_f16_ts_warp(tmem + T::B_R + r * T::BN, tmem + T::B_QT + kk * 8,
+                        sdesc_add(kdesc, (kk / 4) * T::SUB + (kk % 4) * 32), id_s, kk > 0 ? 1u : 0u);
+      mma_commit_warp(&bars->s_full[r]);
+      ++ts;
+      ++k_it;
       return true;
     };
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      int head, ia, ib;
-      bwd2_decode<CAUSAL>(u, nqt, head, ia, ib);
-      for (int half = 0; ok && half < 2; ++half) {
-        const int i = half ? ib : ia;
-        if (i < 0) break;
-        const int nj = num_kv(i);
-        if (!(ok = warp_wait(&bars->q_full, qc & 1, wc, 93))) break;
+    DqItems<CAUSAL> it(units, nqt);
+    if (it.valid()) ok = issue_s(true, 0);
+    for (; ok && it.valid(); ++n) {
+      const int nj = num_kv(it.tile());
+      DqItems<CAUSAL> nx = it;
+      nx.next();
+      for (int j = 0; ok && j < nj; ++j) {
+        // dP(tp) over S in the tile's region, once the compute warps have read S
+        const int vs = v_it % VS, r = tp & 1;
+        if (!(ok = warp_wait(&bars->v_full[vs], (v_it / VS) & 1, wc, 95))) break;
+        if (!(ok = warp_wait(&bars->s_free, tp & 1, wc, 96))) break;
         tc_fence_after();
-        if (!(ok = issue_s(t, k_it))) break;
-        for (int j = 0; j < nj; ++j) {
-          const bool last = (j == nj - 1);
-          const int vs = v_it % VS;
-          // dP = dO V^T into dP buffer t & 1; that buffer holds dS of tile t-2
-          // until tile t-2's dQ MMA has read it
-          const int pb = t & 1;
-          if (!(ok = warp_wait(&bars->v_full[vs], (v_it / VS) & 1, wc, 94))) break;
-          if (t >= 2 && !(ok = warp_wait(&bars->dq_done[pb], ((t - 2) >> 1) & 1, wc, 95))) break;
-          tc_fence_after();
-          const uint64_t vdesc = sdesc_sw128(sb + T::B_SM_V + vs * T::TILE, 16, 1024);
+        const uint64_t vdesc = sdesc_sw128(sb + T::B_SM_V + vs * T::TILE, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * T::SUB + (kk % 4) * 32;
-            mma_f16_ss_warp(tmem + T::B_DP + pb * T::BN, sdesc_add(odesc, off), sdesc_add(vdesc, off), id_s,
-                            kk > 0 ? 1u : 0u);
-          }
-          mma_commit_warp(&bars->dp_full[pb]);
-          mma_commit_warp(&bars->v_empty[vs]);
-          if (last) mma_commit_warp(&bars->q_empty);  // Q_i, dO_i are not read again
-          // next S while the compute warps work on this tile
-          if (!last && !(ok = issue_s(t + 1, k_it + 1))) break;
-          ++t;
-          ++k_it;
-          ++v_it;
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_f16_ts_warp(tmem + T::B_R + r * T::BN, tmem + T::B_OT + kk * 8,
+                          sdesc_add(vdesc, (kk / 4) * T::SUB + (kk % 4) * 32), id_s, kk > 0 ? 1u : 0u);
+        mma_commit_warp(&bars->dp_full);
+        mma_commit_warp(&bars->v_empty[vs]);
+        ++tp;
+        ++v_it;
+        // then S of the next tile: this item's next one, or the next item's first
+        if (j + 1 < nj) {
+          ok = issue_s(false, n);
+        } else if (nx.valid()) {
+          ok = issue_s(true, n + 1);
         }
-        ++qc;
       }
+      it = nx;
     }
     mma_commit_warp(&bars->mma_done[0]);
     bwd2_drain(&bars->mma_done[0], 0);
-  } else if (warp == DQ_MMA_WARP) {
-    // ------------------------------------------------- MMA warp: dQ += dS K
+  } else if (warp == GRAD_MMA_WARP) {
+    // ------------------------------------------------ MMA warp: dQ += dS K
     constexpr uint32_t id_q = idesc_16<BF>(128, D, false, true);  // dQ: N = D, B = K MN-major
     const uint32_t sb = smem_u32(smem);
-    uint32_t t = 0, k_it = 0, qc = 0;
+    uint32_t t = 0, n = 0, k_it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      int head, ia, ib;
-      bwd2_decode<CAUSAL>(u, nqt, head, ia, ib);
-      for (int half = 0; ok && half < 2; ++half) {
-        const int i = half ? ib : ia;
-        if (i < 0) break;
-        const int nj = num_kv(i);
-        for (int j = 0; j < nj; ++j) {
-          const bool first = (j == 0), last = (j == nj - 1);
-          const int ks = k_it % KS, pb = t & 1;
-          // the first tile overwrites dQ, which the previous unit's write-out
-          // must have read; dS of this tile is in TMEM over its dP buffer
-          if (first && qc > 0 && !(ok = warp_wait(&bars->dq_free, (qc - 1) & 1, wc, 96))) break;
-          if (!(ok = warp_wait(&bars->ds_full[pb], (t >> 1) & 1, wc, 97))) break;
-          tc_fence_after();
-          const uint64_t kdesc_mn = sdesc_sw128(sb + T::B_SM_K + ks * T::TILE, T::SUB, 1024);
+    for (DqItems<CAUSAL> it(units, nqt); ok && it.valid(); it.next(), ++n) {
+      const int nj = num_kv(it.tile());
+      for (int j = 0; j < nj; ++j) {
+        const int ks = k_it % KS, r = t & 1;
+        // the item's first tile overwrites dQ, which the previous item's
+        // write-out must have read; dS of the tile is in its region
+        if (j == 0 && n > 0 && !(ok = warp_wait(&bars->dq_free, (n - 1) & 1, wc, 97))) break;
+        if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 98))) break;
+        tc_fence_after();
+        const uint64_t kdesc_mn = sdesc_sw128(sb + T::B_SM_K + ks * T::TILE, T::SUB, 1024);
 #pragma unroll
-          for (int kk = 0; kk < T::BN / 16; ++kk) {
-            const uint32_t a_t = tmem + T::B_DP + pb * T::BN + (kk / 4) * T::QC + (kk % 4) * 8;
-            mma_f16_ts_warp(tmem + T::B_DQ, a_t, sdesc_add(kdesc_mn, kk * 2048), id_q, (first && kk == 0) ? 0u : 1u);
-          }
-          mma_commit_warp(&bars->dq_done[pb]);
-          if (last) {
-            // the K slot of the last tile receives dQ_i; it is released once
-            // dQ_i has been written out
-            mma_commit_warp(&bars->dq_full);
-          } else {
-            // K_j is free: S of this tile completed before the compute warps
-            // could signal ds_full
-            mma_commit_warp(&bars->k_empty[ks]);
-          }
-          ++t;
-          ++k_it;
+        for (int kk = 0; kk < T::BN / 16; ++kk) {
+          const uint32_t a_t = tmem + T::B_R + r * T::BN + (kk / 4) * T::QC + (kk % 4) * 8;
+          mma_f16_ts_warp(tmem + T::B_DQ, a_t, sdesc_add(kdesc_mn, kk * 2048), id_q, (j == 0 && kk == 0) ? 0u : 1u);
         }
-        if (!ok) break;
-        // the compute warps stage dQ_i in the K slot of the last tile; store
-        // it with TMA, then release the slot for the next K load
-        if (!(ok = warp_wait(&bars->epi_full, qc & 1, wc, 98))) break;
-        if (lane == 0) {
-          const int kl = (k_it - 1) % KS;
-          for (int s = 0; s < T::DSUB; ++s)
-            tma_store_3d(&tm_dq, smem + T::B_SM_K + kl * T::TILE + s * T::SUB, s * 64, i * T::BM, head);
-          bulk_commit();
-          bulk_wait_read<0>();
-          mbar_arrive(&bars->k_empty[kl]);
-        }
-        __syncwarp();
-        ++qc;
+        // the region is free and K_t read (S of this tile completed before
+        // the compute warps could signal ds_full)
+        mma_commit_warp(&bars->dq_done[r]);
+        mma_commit_warp(&bars->k_empty[ks]);
+        if (j == nj - 1) mma_commit_warp(&bars->dq_full);
+        ++t;
+        ++k_it;
       }
     }
-    if (lane == 0) bulk_wait<0>();  // all stores complete before the CTA exits
-    __syncwarp();
     mma_commit_warp(&bars->mma_done[1]);
     bwd2_drain(&bars->mma_done[1], 0);
   } else {
@@ -873,193 +897,264 @@ __global__ void __launch_bounds__(384, 1)
     const int row = quad * 32 + lane;  // TMEM lane = query row of the tile
     const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const float sl2 = prm.scale_log2;
-    uint32_t t = 0, qc = 0;
+    constexpr int CH = D / 16;  // 16-byte chunks of this warpgroup's half of a row
+    uint32_t t = 0, n = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      int head, ia, ib;
-      bwd2_decode<CAUSAL>(u, nqt, head, ia, ib);
-      for (int half = 0; ok && half < 2; ++half) {
-        const int i = half ? ib : ia;
-        if (i < 0) break;
-        const int query = i * T::BM + row;
-        const size_t grow = static_cast<size_t>(head) * Nq_pad + query;  // padded: lse2 = +inf past Nq
-        // last key this row sees; key tiles past the tile's smallest limit
-        // (the causal diagonal, or the ragged end of the keys) are masked
-        const int lim = CAUSAL ? min(query + coff, Nk - 1) : Nk - 1;
-        const int lim_lo = CAUSAL ? min(i * T::BM + coff, Nk - 1) : Nk - 1;
-        // ---- Delta_i = rowsum(O_i * dO_i) and lse2 = lse * log2(e) of this
-        // row.  O_i is read here (its line was prefetched into L2 during the
-        // previous item); the sum is formed after P of the item's first key
-        // tile, so the load hides behind S of that tile.
-        const bool live = query < prm.Nq;
-        const size_t src = static_cast<size_t>(head) * prm.Nq + query;  // row of O, dO and lse
-        constexpr int NV = D / 16;  // 16-byte vectors in half a row
-        uint4 ov[NV];
-        if (T::kFuseDelta && live) {
-          const __half* orow = prm.o + src * D + wg * (D / 2);
+    // Delta and lse2 of this thread's row of the current item, packed for
+    // the f32x2 arithmetic (negated)
+    uint64_t nd2 = 0ull, nl2 = 0ull;
+
+    // Item `nx` (index m) begins: Q_m and dO_m are copied from the staging
+    // buffers into TMEM, and this warpgroup's half of rowsum(O * dO) is
+    // formed: with O staged beside them, from the dO words just read; else
+    // with O read coalesced from global memory (CH lanes per row, 32 / CH rows
+    // per load, the sum gathered by the row's owner) and dO re-read from the
+    // staging buffer in the same pattern.  `lse_raw` is the row's
+    // natural-log lse, requested an item earlier.
+    auto load_item = [&](const DqItems<CAUSAL>& nx, uint32_t m, float lse_raw, float& lse2, float& part) -> bool {
+      const bool live = nx.tile() * T::BM + row < prm.Nq;
+      lse2 = live ? lse_raw * 1.4426950408889634f : INFINITY;
+      constexpr int RPL = 32 / CH;  // rows per coalesced load
+      uint4 ov[T::kStageO ? 1 : CH];
+      if constexpr (!T::kStageO) {
 #pragma unroll
-          for (int e = 0; e < NV; ++e) ov[e] = ldg_nc_v4(orow + e * 8);
+        for (int k = 0; k < CH; ++k) {
+          const int qr = nx.tile() * T::BM + quad * 32 + RPL * k + lane / CH;
+          ov[k] = qr < prm.Nq ? ldg_nc_v4(prm.o + (static_cast<size_t>(nx.head) * prm.Nq + qr) * D + wg * (D / 2) +
+                                          (lane % CH) * 8)
+                              : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      const bool got = mbar_wait(&bars->qo_full, m & 1, wc, 104);
+      if (!__all_sync(0xffffffffu, got)) return false;
+      // chunk c of row r's half wg * D / 2 .. of a 128-byte-swizzled tile
+      auto chunk = [&](int buf, int r, int c) {
+        const int g = wg * CH + c;
+        return ld_shared_v4(smem_u32(smem + buf) + (g / 8) * T::SUB + r * 128 + (((g % 8) ^ (r & 7)) << 4));
+      };
+      uint32_t w[4 * CH];
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const uint4 x = chunk(which == 0 ? T::B_SM_Q : T::B_SM_DO, row, c);
+          w[4 * c] = x.x;
+          w[4 * c + 1] = x.y;
+          w[4 * c + 2] = x.z;
+          w[4 * c + 3] = x.w;
+        }
+        const uint32_t col = (which == 0 ? T::B_QT : T::B_OT) + wg * (D / 4);
+        if constexpr (D == 128) {
+          tmem_st32(lb + col, w);
         } else {
-#pragma unroll
-          for (int e = 0; e < NV; ++e) ov[e] = make_uint4(0u, 0u, 0u, 0u);
+          tmem_st16(lb + col, w);
         }
-        const float lse2 = !T::kFuseDelta ? __ldg(prm.lse2 + grow)
-                           : live ? __ldg(prm.lse + src) * 1.4426950408889634f : INFINITY;
-        if (T::kFuseDelta) {
-          // the next item's O rows into L2
-          int nh = head, ni = -1;
-          if (half == 0 && ib >= 0) {
-            ni = ib;
-          } else if (u + static_cast<int>(gridDim.x) < units) {
-            int nb;
-            bwd2_decode<CAUSAL>(u + gridDim.x, nqt, nh, ni, nb);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->qo_tmem);  // Q_m, dO_m are in TMEM: the item's S can start
+      if constexpr (T::kStageO) {
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const uint4 o4 = chunk(T::B_SM_O, row, c);
+          const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 x = unpack2<BF>(ow[q]), y = unpack2<BF>(w[4 * c + q]);
+            acc0 = fmaf(x.x, y.x, acc0);
+            acc1 = fmaf(x.y, y.y, acc1);
           }
-          const int nq = ni * T::BM + row;
-          if (ni >= 0 && nq < prm.Nq) prefetch_l2(prm.o + (static_cast<size_t>(nh) * prm.Nq + nq) * D + wg * (D / 2));
         }
-        uint64_t nd2 = 0ull;
-        if (!T::kFuseDelta) {
-          const float delta = __ldg(prm.delta + grow);
-          nd2 = f2_pack(-delta, -delta);
-        }
-        const uint64_t c2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2);
-        for (int j = 0; j < num_kv(i); ++j) {
-          const int pb = t & 1;
-          const int k0 = j * T::BN + wg * T::QC;  // first key column of this warpgroup
-          // ---- P = exp2(S * c - lse2)
-          ok = mbar_wait(&bars->s_full, t & 1, wc, 101);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          tc_fence_after();
-          uint32_t sr[T::QC];
-          tmem_ld32(lb + T::B_S + wg * T::QC, sr);
-          tmem_ld32(lb + T::B_S + wg * T::QC + 32, sr + 32);
-          tmem_wait_ld();
-          reg_fence<T::QC>(sr);
-          tc_fence_before();
-          mbar_arrive(&bars->s_free);
-          // x = S * c - lse2 in packed fp32 pairs, P = exp2(x)
-          uint64_t p2[T::QC / 2];
-          const bool masked = (j + 1) * T::BN - 1 > lim_lo;
-          // causal: the row's visible columns of this warpgroup's half as one
-          // bit per column of each 32-column word
-          uint32_t keep[T::QC / 32];
-          if constexpr (CAUSAL) {
-            const int nv = lim - k0 + 1;
+        part = acc0 + acc1;
+      } else {
 #pragma unroll
-            for (int w = 0; w < T::QC / 32; ++w) {
-              const int n = min(max(nv - 32 * w, 0), 32);
-              keep[w] = n == 32 ? 0xffffffffu : ((1u << n) - 1u);
-            }
+        for (int k = 0; k < CH; ++k) {
+          const uint4 d4 = chunk(T::B_SM_DO, quad * 32 + RPL * k + lane / CH, lane % CH);
+          const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
+          const uint32_t ow[4] = {ov[k].x, ov[k].y, ov[k].z, ov[k].w};
+          float acc = 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 x = unpack2<BF>(ow[q]), y = unpack2<BF>(dw[q]);
+            acc = fmaf(x.x, y.x, acc);
+            acc = fmaf(x.y, y.y, acc);
           }
 #pragma unroll
-          for (int c = 0; c < T::QC; c += 2) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nl2), x0, x1);
-            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            if constexpr (CAUSAL) {
-              if (masked) {
-                p0 = ((keep[c / 32] >> (c % 32)) & 1u) ? p0 : 0.f;
-                p1 = ((keep[c / 32] >> ((c + 1) % 32)) & 1u) ? p1 : 0.f;
-              }
-            } else if (masked) {
-              if (k0 + c > lim) p0 = 0.f;
-              if (k0 + c + 1 > lim) p1 = 0.f;
-            }
-            p2[c / 2] = f2_pack(p0, p1);
-          }
-          if (T::kFuseDelta && j == 0) {
-            // Delta: this warpgroup's half of the columns (dO_i from the tile
-            // in shared memory), the two halves summed through shared memory
-            ok = mbar_wait(&bars->q_full, qc & 1, wc, 104);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            float dacc[2] = {0.f, 0.f};
-#pragma unroll
-            for (int e = 0; e < NV; ++e) {
-              const int col = wg * (D / 2) + e * 8;
-              const uint32_t a = smem_u32(smem + T::B_SM_DO) + (col / 64) * T::SUB + row * 128 +
-                                 ((((col % 64) / 8) ^ (row & 7)) << 4);
-              const uint4 dv4 = ld_shared_v4(a);
-              const uint32_t dw[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
-              const uint32_t ow[4] = {ov[e].x, ov[e].y, ov[e].z, ov[e].w};
-#pragma unroll
-              for (int w = 0; w < 4; ++w) {
-                const float2 x = unpack2<BF>(ow[w]), y = unpack2<BF>(dw[w]);
-                dacc[w & 1] = fmaf(x.x, y.x, dacc[w & 1]);
-                dacc[w & 1] = fmaf(x.y, y.y, dacc[w & 1]);
-              }
-            }
-            mbar_arrive(&bars->q_empty);  // dO_i read
-            float* dx = reinterpret_cast<float*>(smem + T::B_SM_DX) + (qc & 1) * 2 * T::BM;
-            dx[wg * T::BM + row] = dacc[0] + dacc[1];
-            mbar_arrive(&bars->dx_full[qc & 1]);
-            ok = mbar_wait(&bars->dx_full[qc & 1], (qc >> 1) & 1, wc, 105);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            const float delta = dx[row] + dx[T::BM + row];  // the same sum in both warpgroups
-            nd2 = f2_pack(-delta, -delta);
-            if (wg == 0) {
-              prm.delta[grow] = delta;
-              prm.lse2[grow] = lse2;
-            }
-          }
-          // ---- dS = P * (dP - Delta), fp16 into TMEM over dP
-          ok = mbar_wait(&bars->dp_full[pb], (t >> 1) & 1, wc, 102);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t dpc = T::B_DP + pb * T::BN + wg * T::QC;
-          tmem_ld32(lb + dpc, sr);
-          tmem_ld32(lb + dpc + 32, sr + 32);
-          tmem_wait_ld();
-          reg_fence<T::QC>(sr);
-          uint32_t pk[T::QC / 2];
-#pragma unroll
-          for (int c = 0; c < T::QC; c += 2)
-            pk[c / 2] = f2_to_pack2<BF>(f2_mul(p2[c / 2], f2_add(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), nd2)));
-          tmem_st32(lb + dpc, pk);
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(&bars->ds_full[pb]);
-          ++t;
+          for (int o = 1; o < CH; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+          // row RPL * k + lane / CH of the warp; its owner is lane RPL * k + that
+          const float v = __shfl_sync(0xffffffffu, acc, (lane % RPL) * CH);
+          if (lane / RPL == k) part = v;
         }
-        if (!ok) break;
-        // ---- dQ_i (times scale) -> fp16, staged in the K slot of the last
-        // tile (no longer read); the dQ MMA warp stores it
-        ok = mbar_wait(&bars->dq_full, qc & 1, wc, 103);
+      }
+      mbar_arrive(&bars->qo_empty);  // the staging buffers are no longer read
+      return true;
+    };
+    // Delta of item m's rows: both warpgroups' halves through shared memory;
+    // written to the workspace (with lse2) for the dK/dV kernel
+    auto finish_delta = [&](const DqItems<CAUSAL>& nx, uint32_t m, float lse2, float part) -> bool {
+      float* dx = reinterpret_cast<float*>(smem + T::B_SM_DX) + (m & 1) * 2 * T::BM;
+      dx[wg * T::BM + row] = part;
+      mbar_arrive(&bars->dx_full[m & 1]);
+      const bool got = mbar_wait(&bars->dx_full[m & 1], (m >> 1) & 1, wc, 105);
+      if (!__all_sync(0xffffffffu, got)) return false;
+      const float delta = dx[row] + dx[T::BM + row];  // the same sum in both warpgroups
+      if (wg == 0) {
+        const size_t grow = static_cast<size_t>(nx.head) * Nq_pad + nx.tile() * T::BM + row;
+        prm.delta[grow] = delta;
+        prm.lse2[grow] = lse2;
+      }
+      nd2 = f2_pack(-delta, -delta);
+      return true;
+    };
+
+    // The current item's lse2 and this warpgroup's half of its Delta, until
+    // the halves are combined in its first key tile (after S is read, so that
+    // dP of that tile is already queued)
+    float lse2 = 0.f, part = 0.f;
+    // this row's lse of an item, requested an item before it is needed (a
+    // volatile load, so that it is issued here and not next to its use); at
+    // D = 128 also the row's O half into L2 for the coalesced reads
+    auto lse_of = [&](const DqItems<CAUSAL>& x) {
+      const int q = x.tile() * T::BM + row;
+      if (!x.valid() || q >= prm.Nq) return 0.f;
+      const size_t src = static_cast<size_t>(x.head) * prm.Nq + q;
+      if (!T::kStageO) prefetch_l2(prm.o + src * D + wg * (D / 2));
+      return ldg_nc_f32(prm.lse + src);
+    };
+    DqItems<CAUSAL> it(units, nqt);
+    if (it.valid()) {
+      ok = load_item(it, 0, lse_of(it), lse2, part);
+      ok = __all_sync(0xffffffffu, ok);
+      nl2 = f2_pack(-lse2, -lse2);
+    }
+    for (; ok && it.valid(); ++n) {
+      const int head = it.head, i = it.tile();
+      const int query = i * T::BM + row;
+      DqItems<CAUSAL> nx = it;
+      nx.next();
+      const float lse_next = lse_of(nx);
+      // last key this row sees; key tiles past the tile's smallest limit
+      // (the causal diagonal, or the ragged end of the keys) are masked
+      const int lim = CAUSAL ? min(query + coff, Nk - 1) : Nk - 1;
+      const int lim_lo = CAUSAL ? min(i * T::BM + coff, Nk - 1) : Nk - 1;
+      const uint64_t c2 = f2_pack(sl2, sl2);
+      for (int j = 0; j < num_kv(i); ++j) {
+        const int r = t & 1;
+        const int k0 = j * T::BN + wg * T::QC;  // first key column of this warpgroup
+        const uint32_t rb = lb + T::B_R + r * T::BN + wg * T::QC;  // this warpgroup's columns of the region
+        // ---- P = exp2(S * c - lse2)
+        ok = mbar_wait(&bars->s_full[r], (t >> 1) & 1, wc, 101);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tile = smem_u32(smem + T::B_SM_K + ((t - 1) % KS) * T::TILE);
-#pragma unroll
-        for (int c = 0; c < D / 2; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(lb + T::B_DQ + wg * (D / 2) + c, v);
-          tmem_wait_ld();
-          reg_fence<32>(v);
-          const float sc = prm.scale;
-          uint32_t h[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) h[e] = pack2<BF>(__uint_as_float(v[2 * e]) * sc, __uint_as_float(v[2 * e + 1]) * sc);
-          stage_row32(tile, row, wg * (D / 2) + c, h);
-        }
-        fence_proxy_async_smem();
+        uint32_t sr[T::QC];
+        tmem_ld32(rb, sr);
+        tmem_ld32(rb + 32, sr + 32);
+        tmem_wait_ld();
+        reg_fence<T::QC>(sr);
         tc_fence_before();
-        mbar_arrive(&bars->dq_free);
-        mbar_arrive(&bars->epi_full);
-        ++qc;
+        mbar_arrive(&bars->s_free);  // the region takes dP
+        if (j == 0) {
+          ok = finish_delta(it, n, lse2, part);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        }
+        uint64_t p2[T::QC / 2];
+        const bool masked = (j + 1) * T::BN - 1 > lim_lo;
+        // causal: the row's visible columns of this warpgroup's half as one
+        // bit per column of each 32-column word
+        uint32_t keep[T::QC / 32];
+        if constexpr (CAUSAL) {
+          const int nv = lim - k0 + 1;
+#pragma unroll
+          for (int w = 0; w < T::QC / 32; ++w) {
+            const int nvis = min(max(nv - 32 * w, 0), 32);
+            keep[w] = nvis == 32 ? 0xffffffffu : ((1u << nvis) - 1u);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < T::QC; c += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nl2), x0, x1);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          if constexpr (CAUSAL) {
+            if (masked) {
+              p0 = ((keep[c / 32] >> (c % 32)) & 1u) ? p0 : 0.f;
+              p1 = ((keep[c / 32] >> ((c + 1) % 32)) & 1u) ? p1 : 0.f;
+            }
+          } else if (masked) {
+            if (k0 + c > lim) p0 = 0.f;
+            if (k0 + c + 1 > lim) p1 = 0.f;
+          }
+          p2[c / 2] = f2_pack(p0, p1);
+        }
+        // ---- dS = P * (dP - Delta), 16-bit over the first half of this
+        // warpgroup's dP columns
+        ok = mbar_wait(&bars->dp_full, t & 1, wc, 102);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        tmem_ld32(rb, sr);
+        tmem_ld32(rb + 32, sr + 32);
+        tmem_wait_ld();
+        reg_fence<T::QC>(sr);
+        uint32_t pk[T::QC / 2];
+#pragma unroll
+        for (int c = 0; c < T::QC; c += 2)
+          pk[c / 2] = f2_to_pack2<BF>(
+              f2_mul(p2[c / 2], f2_add(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), nd2)));
+        tmem_st32(rb, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->ds_full);
+        ++t;
       }
+      if (!ok) break;
+      // ---- item boundary: the next item's Q, dO into TMEM first (its S can
+      // start) and its Delta halves, then this item's dQ out
+      const bool has_next = nx.valid();
+      if (has_next) {
+        ok = load_item(nx, n + 1, lse_next, lse2, part);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        nl2 = f2_pack(-lse2, -lse2);
+      }
+      // dQ_i (times scale) -> 16-bit, staged in the Q staging buffer (just
+      // emptied by this thread's own reads of the same row and columns), or
+      // in the dO buffer after the CTA's last item; the producer stores it
+      ok = mbar_wait(&bars->dq_full, n & 1, wc, 103);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t tile = smem_u32(smem + (has_next ? T::B_SM_Q : T::B_SM_DO));
+#pragma unroll
+      for (int c = 0; c < D / 2; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(lb + T::B_DQ + wg * (D / 2) + c, v);
+        tmem_wait_ld();
+        reg_fence<32>(v);
+        const float sc = prm.scale;
+        uint32_t h[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) h[e] = pack2<BF>(__uint_as_float(v[2 * e]) * sc, __uint_as_float(v[2 * e + 1]) * sc);
+        stage_row32(tile, row, wg * (D / 2) + c, h);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);
+      mbar_arrive(&bars->epi_full[n & 1]);
+      it = nx;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == MMA_WARP) {
+  if (warp == S_MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
-// The dQ kernel (for D = 128 it also writes Delta and lse2 of every query
-// row; for D = 64 the preprocess kernel runs first), then the dK/dV kernel,
-// on the same stream.  `max_ctas` caps each persistent
-// grid (normally the SM count).
+// The dQ kernel (which also writes Delta and lse2 of every query row), then
+// the dK/dV kernel, on the same stream.  `max_ctas` caps each persistent
+// grid (normally the SM count).  maps: [0] q, [1] k, [2] v, [3] dout, [4] dq,
+// [5] dk, [6] dv, [9] o.
 template <int D, bool CAUSAL, bool BF>
 int launch_bwd2(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, cudaStream_t stream) {
   using T = Bwd2Traits<D>;
@@ -1073,16 +1168,13 @@ int launch_bwd2(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, cud
                    : -1;
       }) != 0)
     return -1;
-  if constexpr (!T::kFuseDelta) {
-    if (launch_prep<D, BF>(prm, stream) != 0) return -1;
-  }
   auto grid_for = [&](int heads, int tiles) {
     const long long units = CAUSAL ? static_cast<long long>(heads) * ((tiles + 1) / 2) : static_cast<long long>(heads) * tiles;
     return static_cast<int>(units < max_ctas ? units : max_ctas);
   };
   const int nqt = (prm.Nq + T::BM - 1) / T::BM, nkv = (prm.Nk + T::BN - 1) / T::BN;
   fa_bwd_dq_kernel<D, CAUSAL, BF><<<grid_for(prm.heads, nqt), 384, T::B_SMEM, stream>>>(maps[0], maps[1], maps[2],
-                                                                                       maps[3], maps[4], prm);
+                                                                                       maps[3], maps[4], maps[9], prm);
   if (cudaGetLastError() != cudaSuccess) return -1;
   fa_bwd_dkdv_kernel<D, CAUSAL, BF><<<grid_for(prm.heads / prm.group, nkv), 384, T::A_SMEM, stream>>>(
       maps[0], maps[1], maps[2], maps[3], maps[5], maps[6], prm);

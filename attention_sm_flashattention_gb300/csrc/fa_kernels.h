@@ -88,7 +88,7 @@ struct BwdParams {
 #define FA_DECLARE_LAUNCHERS(D)                                                                      \
   int launch_fwd_d##D(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm,       \
                       int num_sms, cudaStream_t stream);                                              \
-  /* bwd maps: q, k, v, dout, dq, dk, dv, q and k with the D = 256 dQ kernel's boxes */                                                         \
+  /* bwd maps: q, k, v, dout, dq, dk, dv, q and k with the D = 256 dQ kernel's boxes, o */                     \
   int launch_bwd_d##D(bool causal, bool bf16, const CUtensorMap* maps, const BwdParams& prm,       \
                       int grid, cudaStream_t stream);
 
