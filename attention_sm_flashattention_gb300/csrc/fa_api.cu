@@ -143,7 +143,7 @@ const char* fa_error_string(int code) {
 
 long long fa_fwd_tile_count(int N, int D, int causal) {
   if (N <= 0 || (D != 64 && D != 128 && D != 256) || (causal != 0 && causal != 1)) return -1;
-  const long long bm = 128, bn = fa::fwd_block_n(D);
+  const long long bm = 128, bn = fa::fwd_dense_block_n(D);
   const long long nqt = (N + bm - 1) / bm, nkv = (N + bn - 1) / bn;
   if (!causal) return nqt * nkv;
   long long n = 0;
@@ -184,7 +184,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, c
   if ((rc = current_device_info(&dev)) != FA_OK) return rc;
 
   const int D = sh.D;
-  const int bn = fa::fwd_block_n(D);
+  const int bn = fa::fwd_dense_block_n(D);
+  const int bv = D == 256 ? 64 : bn;  // D = 256: V in halves of the keys
   // Few queries per head (decode): the G query heads of a K/V head run as one
   // head of G * Nq rows (consecutive in q, o and lse), so K/V tiles are read
   // once per K/V head and the 128-row query tiles are filled.
@@ -193,7 +194,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, c
   const int rows = pack ? sh.group() * sh.Nq : sh.Nq;
   CUtensorMap maps[4];  // q, k, v, o
   if (!map16(&maps[0], q, qh, rows, D, 128, bf16) || !map16(&maps[1], k, sh.kv_heads(), sh.Nk, D, bn, bf16) ||
-      !map16(&maps[2], v, sh.kv_heads(), sh.Nk, D, bn, bf16) || !map16(&maps[3], o, qh, rows, D, 128, bf16))
+      !map16(&maps[2], v, sh.kv_heads(), sh.Nk, D, bv, bf16) || !map16(&maps[3], o, qh, rows, D, 128, bf16))
     return FA_ERR_CUDA;
   fa::FwdParams prm{};
   prm.o = static_cast<__half*>(o);

@@ -85,6 +85,7 @@ struct BwdParams {
 // fp16 inputs and outputs) select the instantiation.  Return 0 on success.
 // For the backward, `grid` caps each persistent grid (the SM count).  The
 // tensor maps carry the element type.
+// Dense forward maps: q, k, v, o (D = 256: v with 64-row boxes; o unused).
 #define FA_DECLARE_LAUNCHERS(D)                                                                      \
   int launch_fwd_d##D(bool causal, bool bf16, const CUtensorMap* maps, const FwdParams& prm,       \
                       int num_sms, cudaStream_t stream);                                              \
@@ -139,7 +140,11 @@ inline int current_device_index() {
   return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
 }
 
-// Tile sizes the host needs to build tensor maps and size grids.
+// Tile sizes the host needs to build tensor maps and size grids: keys per
+// tile of the paged, selected-block and split forward, and of the dense one
+// (which at D = 256 moves each 128-key tile as two halves: K by halves of
+// the contraction, 128-row boxes; V by halves of the keys, 64-row boxes).
 inline int fwd_block_n(int D) { return D == 256 ? 64 : 128; }
+inline int fwd_dense_block_n(int) { return 128; }
 
 }  // namespace fa

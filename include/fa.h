@@ -355,8 +355,8 @@ FA_API const char* fa_error_string(int code);
 
 /*
  * Number of (query tile, key tile) pairs one head's pass visits with the
- * library's forward tiling (128-row query tiles, 128- or 64-key tiles, the
- * last of each possibly partial): the causal loop bound of §八 (T*T tiles
+ * dense forward's tiling (128-row query tiles and 128-key tiles for every D,
+ * the last of each possibly partial): the causal loop bound of §八 (T*T tiles
  * non-causal, 1+2+...+T causal for square tiles).  Host-only helper used
  * for the FLOP model; -1 on bad arguments.
  */
