@@ -64,7 +64,7 @@ struct Bwd2Traits {
   static constexpr int A_SM_L2 = A_SM_DO + A_OS * TILE;       // lse2[128] per Q stage
   static constexpr int A_SM_DL = A_SM_L2 + A_QS * BM * 4;     // Delta[128] per dO stage
   static constexpr int A_SM_BAR = A_SM_DL + A_OS * BM * 4;
-  static constexpr int A_SM_BYTES = A_SM_BAR + 256;
+  static constexpr int A_SM_BYTES = A_SM_BAR + 512;
   static constexpr int A_SMEM = A_SM_BYTES > MIN_SMEM ? A_SM_BYTES : MIN_SMEM;
   static_assert(A_SMEM <= 232448, "dK/dV kernel shared memory budget");
   static_assert(A_R + 2 * BM <= 512, "dK/dV kernel TMEM budget");
@@ -149,12 +149,15 @@ constexpr int kSiteSmemAlign = 99;
 struct DkdvBars {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[4], q_empty[4], o_full[4], o_empty[4];
-  uint64_t s_full, s_free, dp_full, p_full, ds_full, dk_done[2];
+  uint64_t s_full, s_free, dp_full;
+  // per TMEM region (phase = the region's use count): P^T written, dS^T
+  // written, the tile's dK MMA (and the dV MMA before it) read the region
+  uint64_t p_full[2], ds_full[2], dk_done[2];
   uint64_t dkv_full, dkv_free, epi_full, mma_done[2];
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(DkdvBars) <= 256, "barrier area");
+static_assert(sizeof(DkdvBars) <= 512, "barrier area");
 
 // TMEM use per key tile j: the dV_j and dK_j accumulators and two 128-column
 // regions that the query tiles use in turn.  Query tile t works in region
@@ -201,10 +204,11 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, NCOMPUTE);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_full, NCOMPUTE);
-    mbar_init(&bars->ds_full, NCOMPUTE);
-    mbar_init(&bars->dk_done[0], 1);
-    mbar_init(&bars->dk_done[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->p_full[i], NCOMPUTE);
+      mbar_init(&bars->ds_full[i], NCOMPUTE);
+      mbar_init(&bars->dk_done[i], 1);
+    }
     mbar_init(&bars->dkv_full, 1);
     mbar_init(&bars->dkv_free, NCOMPUTE);
     mbar_init(&bars->epi_full, NCOMPUTE);
@@ -372,7 +376,7 @@ __global__ void __launch_bounds__(384, 1)
           // previous unit's write-out must have read
           if (first && kc > 0 && !(ok = warp_wait(&bars->dkv_free, (kc - 1) & 1, wc, 67))) break;
           if (!(ok = warp_wait(&bars->o_full[os], (t / OS) & 1, wc, 60))) break;
-          if (!(ok = warp_wait(&bars->p_full, t & 1, wc, 68))) break;
+          if (!(ok = warp_wait(&bars->p_full[t & 1], (t >> 1) & 1, wc, 68))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < T::BM / 16; ++kk) {
@@ -384,7 +388,7 @@ __global__ void __launch_bounds__(384, 1)
           // last tile's slot receives dV_j and is released by the store warp
           if (!last) mma_commit_warp(&bars->o_empty[os]);
           if (!(ok = warp_wait(&bars->q_full[qs], (t / QS) & 1, wc, 59))) break;
-          if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 69))) break;
+          if (!(ok = warp_wait(&bars->ds_full[t & 1], (t >> 1) & 1, wc, 69))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < T::BM / 16; ++kk) {
@@ -522,7 +526,7 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st32(rb, pk);
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(&bars->p_full);
+          mbar_arrive(&bars->p_full[t & 1]);
           const float4* d4 = reinterpret_cast<const float4*>(smem + T::A_SM_DL + os * 512) + wg * (T::QC / 4);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -544,7 +548,7 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st32(rb + T::QC / 2, pk);
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(&bars->ds_full);
+          mbar_arrive(&bars->ds_full[t & 1]);
           ++t;
         }
         if (!ok) break;
@@ -618,8 +622,10 @@ struct DqBars {
   // them (copied into TMEM, Delta formed); Q_n and dO_n are in TMEM
   uint64_t qo_full, qo_empty, qo_tmem;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], dq_done[2];  // [2]: per TMEM region
-  uint64_t s_free, dp_full, ds_full;
+  // per TMEM region (phase = the region's use count): S landed; dS written;
+  // the dQ MMA has read the region
+  uint64_t s_full[2], ds_full[2], dq_done[2];
+  uint64_t s_free, dp_full;
   uint64_t dq_full, dq_free, mma_done[2];
   uint64_t epi_full[2];  // dQ of item n staged for its store (barrier n % 2)
   uint64_t dx_full[2];   // both Delta halves of an item's rows are in shared memory
@@ -675,6 +681,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->ds_full[i], NCOMPUTE);
       mbar_init(&bars->dq_done[i], 1);
       mbar_init(&bars->epi_full[i], NCOMPUTE);
       mbar_init(&bars->dx_full[i], NCOMPUTE);
@@ -682,7 +689,6 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(&bars->s_free, NCOMPUTE);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->ds_full, NCOMPUTE);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, NCOMPUTE);
     bars->abort_flag = 0;
@@ -872,7 +878,7 @@ __global__ void __launch_bounds__(384, 1)
         // the item's first tile overwrites dQ, which the previous item's
         // write-out must have read; dS of the tile is in its region
         if (j == 0 && n > 0 && !(ok = warp_wait(&bars->dq_free, (n - 1) & 1, wc, 97))) break;
-        if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 98))) break;
+        if (!(ok = warp_wait(&bars->ds_full[r], (t >> 1) & 1, wc, 98))) break;
         tc_fence_after();
         const uint64_t kdesc_mn = sdesc_sw128(sb + T::B_SM_K + ks * T::TILE, T::SUB, 1024);
 #pragma unroll
@@ -1104,7 +1110,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_st32(rb, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->ds_full);
+        mbar_arrive(&bars->ds_full[r]);
         ++t;
       }
       if (!ok) break;

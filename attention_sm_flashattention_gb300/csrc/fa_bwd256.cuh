@@ -17,17 +17,20 @@
 //
 //  fa_bwd256_dkdv_kernel: one work unit per (K/V head, key tile j of 128
 //    keys); the unit sweeps the 64-row query tiles of the G query heads that
-//    read its K/V head twice, once per 128-wide half h of D (§七's halves):
-//      S^T  = K_j Q_i^T                (K in shared memory, full-D contraction)
-//      P^T  = exp2(S^T * c - lse2)     -> fp16, TMEM (over S^T)
-//      dP^T = V_j dO_i^T               (V_j in TMEM, loaded once per unit)
-//      dS^T = P^T * (dP^T - Delta)     -> fp16, TMEM (over dP^T)
-//      dV_j[:, h] += P^T dO_i[:, h],  dK_j[:, h] += dS^T Q_i[:, h]
-//    S^T and dP^T are recomputed in the second half (six 64 x 128 x 128 GEMM
-//    blocks per tile and half instead of four).  TMEM: V_j (128 columns),
-//    dV half, dK half, two 64-column regions that the query tiles use in
-//    turn.  Shared memory: K_j (64 KB), three Q stages and two dO stages of
-//    32 KB.
+//    read its K/V head twice, once per gradient:
+//      dV pass:  S^T  = K_j Q_i^T               (K in shared memory)
+//                P^T  = exp2(S^T * c - lse2)    -> 16-bit, TMEM (over S^T)
+//                dV_j += P^T dO_i               (N = 256: all of D)
+//      dK pass:  S^T as above, P^T in registers
+//                dP^T = V_j dO_i^T              (V_j in TMEM, loaded once per unit)
+//                dS^T = P^T * (dP^T - Delta)    -> 16-bit, TMEM (over dP^T)
+//                dK_j += dS^T Q_i               (N = 256)
+//    S^T is computed in both passes (five 128 x 64 x 256 GEMM blocks per
+//    query tile instead of four): the 256-wide dV and dK accumulators do not
+//    fit in TMEM together (§七 splits D for the same reason), one at a time
+//    they do.  TMEM: the pass's accumulator (256 columns), V_j (128), two
+//    64-column regions that the query tiles use in turn.  Shared memory:
+//    K_j (64 KB), three Q stages and two dO stages of 32 KB.
 //  fa_bwd256_dq_kernel: one work unit per (query head, 128-row query tile
 //    i); 64-key tiles of K and V stream through rings:
 //      S = Q_i K_j^T, P = exp2(S * c - lse2), dP = dO_i V_j^T (dO_i in TMEM),
@@ -57,7 +60,9 @@ struct B256 {
   static constexpr int A_QTILE = 4 * A_QSUB;    // 32 KB
   static constexpr int A_KTILE = 4 * A_KSUB;    // 64 KB
   static constexpr int A_QS = 3, A_OS = 2;
-  static constexpr int A_V = 0, A_DV = 128, A_DK = 256, A_R = 384;  // TMEM columns; region r at A_R + 64 r
+  // TMEM columns: the pass's gradient accumulator (dV, then dK; N = 256),
+  // V_j as an MMA A operand, region r at A_R + 64 r
+  static constexpr int A_ACC = 0, A_V = 256, A_R = 384;
   static constexpr int A_SM_K = 0, A_SM_Q = A_KTILE, A_SM_DO = A_SM_Q + A_QS * A_QTILE;
   static constexpr int A_SM_L2 = A_SM_DO + A_OS * A_QTILE;  // lse2[64] per Q stage
   static constexpr int A_SM_DL = A_SM_L2 + A_QS * 256;      // Delta[64] per dO stage
@@ -140,9 +145,13 @@ __device__ __forceinline__ void stage_tmem32(uint32_t taddr, float mul, uint32_t
 struct Bwd256ABars {
   uint64_t k_full, k_empty, v_full, v_free;
   uint64_t q_full[3], q_empty[3], o_full[2], o_empty[2];
-  uint64_t s_full[2], s_free, dp_full[2], p_full, ds_full, dk_done[2];  // [2]: per TMEM region
+  // per TMEM region (phase = the region's use count): S^T landed; the
+  // tile's gradient A operand (P^T in the dV pass, dS^T in the dK pass) is
+  // written; the tile's gradient MMA has read the region
+  uint64_t s_full[2], a_full[2], dk_done[2];
+  uint64_t s_free, dp_full;  // dK pass only, one use per dK-pass tile
   uint64_t dkv_full, dkv_free, mma_done[3];
-  uint64_t epi_full;  // dK and dV halves staged in the last tile's Q and dO slots
+  uint64_t epi_full;  // the pass's gradient staged in the last tile's Q and dO slots
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -178,12 +187,11 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bars->o_empty[i], 1);
       mbar_init(&bars->dk_done[i], 1);
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->dp_full[i], 1);
+      mbar_init(&bars->a_full[i], T::NCOMPUTE);
     }
     for (int i = 0; i < 3; ++i) mbar_init(&bars->mma_done[i], 1);
+    mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->s_free, T::NCOMPUTE);
-    mbar_init(&bars->p_full, T::NCOMPUTE);
-    mbar_init(&bars->ds_full, T::NCOMPUTE);
     mbar_init(&bars->dkv_full, 1);
     mbar_init(&bars->epi_full, T::NCOMPUTE);
     mbar_init(&bars->dkv_free, T::NCOMPUTE);
@@ -301,11 +309,11 @@ __global__ void __launch_bounds__(384, 1)
     bwd2_drain(&bars->mma_done[0], 0);
   } else if (warp == DP_MMA_WARP) {
     // ----------------------------------------- MMA warp: dP^T = V dO^T
-    // over S^T in the tile's region once the compute warps have read S^T;
-    // V_j must be in TMEM (first tile of the unit)
+    // dK pass only: over S^T in the tile's region once the compute warps have
+    // read S^T; V_j must be in TMEM (written at the start of the unit)
     constexpr uint32_t id_s = idesc_16<BF>(128, T::A_BM, false, false);
     const uint32_t sb = smem_u32(smem);
-    uint32_t t = 0, kc = 0;
+    uint32_t t = 0, t1 = 0, kc = 0;  // tiles, dK-pass tiles
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
       int kvh, ja, jb;
@@ -314,22 +322,22 @@ __global__ void __launch_bounds__(384, 1)
         const int j = half ? jb : ja;
         if (j < 0) break;
         const int nx = G * (nqt - first_q(j));
-        for (int h = 0; ok && h < 2; ++h) {
-          for (int x = 0; x < nx; ++x) {
-            const int os = t % OS;
-            if (!(ok = warp_wait(&bars->o_full[os], (t / OS) & 1, wc, 164))) break;
-            if (!(ok = warp_wait(&bars->s_free, t & 1, wc, 165))) break;
-            if (h == 0 && x == 0 && !(ok = warp_wait(&bars->v_full, kc & 1, wc, 166))) break;
-            tc_fence_after();
-            const uint64_t odesc = sdesc_sw128(sb + T::A_SM_DO + os * T::A_QTILE, 16, 1024);
+        t += nx;  // the dV pass
+        for (int x = 0; x < nx; ++x) {
+          const int os = t % OS;
+          if (!(ok = warp_wait(&bars->o_full[os], (t / OS) & 1, wc, 164))) break;
+          if (!(ok = warp_wait(&bars->s_free, t1 & 1, wc, 165))) break;
+          if (x == 0 && !(ok = warp_wait(&bars->v_full, kc & 1, wc, 166))) break;
+          tc_fence_after();
+          const uint64_t odesc = sdesc_sw128(sb + T::A_SM_DO + os * T::A_QTILE, 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk)
-              mma_f16_ts_warp(tmem + T::A_R + (t & 1) * T::A_BM, tmem + T::A_V + kk * 8,
-                              sdesc_add(odesc, (kk / 4) * T::A_QSUB + (kk % 4) * 32), id_s, kk > 0 ? 1u : 0u);
-            mma_commit_warp(&bars->dp_full[t & 1]);
-            if (h == 1 && x == nx - 1) mma_commit_warp(&bars->v_free);  // V_j is not read again
-            ++t;
-          }
+          for (int kk = 0; kk < 16; ++kk)
+            mma_f16_ts_warp(tmem + T::A_R + (t & 1) * T::A_BM, tmem + T::A_V + kk * 8,
+                            sdesc_add(odesc, (kk / 4) * T::A_QSUB + (kk % 4) * 32), id_s, kk > 0 ? 1u : 0u);
+          mma_commit_warp(&bars->dp_full);
+          if (x == nx - 1) mma_commit_warp(&bars->v_free);  // V_j is not read again
+          ++t;
+          ++t1;
         }
         ++kc;
       }
@@ -337,26 +345,25 @@ __global__ void __launch_bounds__(384, 1)
     mma_commit_warp(&bars->mma_done[2]);
     bwd2_drain(&bars->mma_done[2], 0);
   } else if (warp == GRAD_MMA_WARP) {
-    // ------------------------- MMA warp: dV[:, h] += P^T dO, dK[:, h] += dS^T Q
-    // It also writes out each half's dK and dV, which the compute warps stage
-    // in the Q and dO slots of the half's last tile: before the first MMA of
-    // the next half (which needs the compute warps' next P^T anyway) and at
-    // the end.
-    constexpr uint32_t id_g = idesc_16<BF>(128, 128, false, true);  // N = 128 columns of D, B MN-major
+    // ------------------- MMA warp: dV += P^T dO (dV pass), dK += dS^T Q (dK pass)
+    // N = 256: the whole of D in one accumulator.  It also writes out each
+    // pass's gradient, which the compute warps stage in the Q and dO slots of
+    // the pass's last tile: before the first MMA of the next pass (which
+    // needs the compute warps' next P^T or dS^T anyway) and at the end.
+    constexpr uint32_t id_g = idesc_16<BF>(128, 256, false, true);  // N = D, B MN-major
     const uint32_t sb = smem_u32(smem);
-    uint32_t t = 0, sc = 0;
-    int p_kvh = 0, p_j = 0, p_h = 0;  // the previous half (kvh, key tile, D half)
+    uint32_t t = 0, sc = 0;  // tiles, passes
+    int p_kvh = 0, p_j = 0, p_pass = 0;  // the previous pass (kvh, key tile, dV or dK)
     bool ok = true;
-    // store the staged tiles of half `sc - 1` (last tile t - 1), then release its slots
+    // store the staged tile of pass `sc - 1` (last tile t - 1), then release its slots
     auto store_prev = [&]() -> bool {
       if (!warp_wait(&bars->epi_full, (sc - 1) & 1, wc, 158)) return false;
       if (lane == 0) {
         const int qs = (t - 1) % QS, os = (t - 1) % OS;
+        const CUtensorMap* map = p_pass == 0 ? &tm_dv : &tm_dk;
         for (int s2 = 0; s2 < 2; ++s2) {
-          tma_store_3d(&tm_dk, smem + T::A_SM_Q + qs * T::A_QTILE + s2 * 16384, p_h * 128 + s2 * 64, p_j * T::A_BN,
-                       p_kvh);
-          tma_store_3d(&tm_dv, smem + T::A_SM_DO + os * T::A_QTILE + s2 * 16384, p_h * 128 + s2 * 64, p_j * T::A_BN,
-                       p_kvh);
+          tma_store_3d(map, smem + T::A_SM_Q + qs * T::A_QTILE + s2 * 16384, s2 * 64, p_j * T::A_BN, p_kvh);
+          tma_store_3d(map, smem + T::A_SM_DO + os * T::A_QTILE + s2 * 16384, 128 + s2 * 64, p_j * T::A_BN, p_kvh);
         }
         bulk_commit();
         bulk_wait_read<0>();
@@ -373,49 +380,43 @@ __global__ void __launch_bounds__(384, 1)
         const int j = half ? jb : ja;
         if (j < 0) break;
         const int nx = G * (nqt - first_q(j));
-        for (int h = 0; ok && h < 2; ++h) {
+        for (int pass = 0; ok && pass < 2; ++pass) {
           for (int x = 0; x < nx; ++x) {
             const bool first = (x == 0), last = (x == nx - 1);
-            // the first tile of a half overwrites the accumulators, which the
-            // previous half's write-out must have read
+            // the first tile of a pass overwrites the accumulator, which the
+            // previous pass's write-out must have read
             if (first && sc > 0) {
               if (!(ok = warp_wait(&bars->dkv_free, (sc - 1) & 1, wc, 167))) break;
               if (!(ok = store_prev())) break;
             }
             const int qs = t % QS, os = t % OS;
-            // columns [128 h, 128 h + 128) of the Q / dO tile: sub-tiles 2h, 2h + 1
-            const uint64_t qdesc_mn = sdesc_sw128(sb + T::A_SM_Q + qs * T::A_QTILE + 2 * h * T::A_QSUB, T::A_QSUB, 1024);
-            const uint64_t odesc_mn = sdesc_sw128(sb + T::A_SM_DO + os * T::A_QTILE + 2 * h * T::A_QSUB, T::A_QSUB, 1024);
-            if (!(ok = warp_wait(&bars->o_full[os], (t / OS) & 1, wc, 160))) break;
-            if (!(ok = warp_wait(&bars->p_full, t & 1, wc, 168))) break;
+            // dV pass: B = dO_i (all 256 columns), A = P^T; dK pass: B = Q_i, A = dS^T
+            const uint64_t bdesc = pass == 0 ? sdesc_sw128(sb + T::A_SM_DO + os * T::A_QTILE, T::A_QSUB, 1024)
+                                             : sdesc_sw128(sb + T::A_SM_Q + qs * T::A_QTILE, T::A_QSUB, 1024);
+            if (!(ok = pass == 0 ? warp_wait(&bars->o_full[os], (t / OS) & 1, wc, 160)
+                                 : warp_wait(&bars->q_full[qs], (t / QS) & 1, wc, 159)))
+              break;
+            if (!(ok = warp_wait(&bars->a_full[t & 1], (t >> 1) & 1, wc, 168))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < T::A_BM / 16; ++kk) {
               const uint32_t a_t = tmem + T::A_R + (t & 1) * T::A_BM + (kk / 2) * T::A_QC + (kk % 2) * 8;
-              mma_f16_ts_warp(tmem + T::A_DV, a_t, sdesc_add(odesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
+              mma_f16_ts_warp(tmem + T::A_ACC, a_t, sdesc_add(bdesc, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
             }
-            // dO_i is free: dP^T of the tile completed before p_full (the
-            // half's last slot receives dV and is released after its store)
-            if (!last) mma_commit_warp(&bars->o_empty[os]);
-            if (!(ok = warp_wait(&bars->q_full[qs], (t / QS) & 1, wc, 159))) break;
-            if (!(ok = warp_wait(&bars->ds_full, t & 1, wc, 169))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < T::A_BM / 16; ++kk) {
-              const uint32_t a_t = tmem + T::A_R + (t & 1) * T::A_BM + T::A_QC / 2 + (kk / 2) * T::A_QC + (kk % 2) * 8;
-              mma_f16_ts_warp(tmem + T::A_DK, a_t, sdesc_add(qdesc_mn, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
-            }
-            mma_commit_warp(&bars->dk_done[t & 1]);
+            mma_commit_warp(&bars->dk_done[t & 1]);  // the region is free again
             if (last) {
-              mma_commit_warp(&bars->dkv_full);  // the Q slot receives dK; released after its store
+              mma_commit_warp(&bars->dkv_full);  // the Q and dO slots receive the gradient; released after its store
             } else {
-              mma_commit_warp(&bars->q_empty[qs]);  // S^T of the tile completed before p_full
+              // S^T (and in the dK pass dP^T) of the tile completed before the
+              // compute warps could signal a_full
+              mma_commit_warp(&bars->q_empty[qs]);
+              mma_commit_warp(&bars->o_empty[os]);
             }
             ++t;
           }
           p_kvh = kvh;
           p_j = j;
-          p_h = h;
+          p_pass = pass;
           ++sc;
         }
       }
@@ -431,7 +432,7 @@ __global__ void __launch_bounds__(384, 1)
     const int row = quad * 32 + lane;  // TMEM lane = key row of the tile
     const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const float sl2 = prm.scale_log2;
-    uint32_t t = 0, kc = 0, sc = 0;
+    uint32_t t = 0, t1 = 0, kc = 0, sc = 0;  // tiles, dK-pass tiles, unit halves, passes
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
       int kvh, ja, jb;
@@ -469,7 +470,9 @@ __global__ void __launch_bounds__(384, 1)
           if (nj >= 0 && nj * T::A_BN + row < Nk)
             prefetch_row128(prm.v + (static_cast<size_t>(nkvh) * Nk + nj * T::A_BN + row) * T::D + wg * 128);
         }
-        for (int h = 0; ok && h < 2; ++h) {
+        // two passes over the query tiles: dV (S^T, P^T), then dK (S^T,
+        // dP^T, dS^T); each ends with its gradient written out
+        for (int pass = 0; ok && pass < 2; ++pass) {
           for (int x = 0; x < G * nqi; ++x) {
             const int i = i0 + x % nqi;
             const int qs = t % QS, os = t % OS;
@@ -485,8 +488,10 @@ __global__ void __launch_bounds__(384, 1)
             tmem_ld32(rb, sr);
             tmem_wait_ld();
             reg_fence<T::A_QC>(sr);
-            tc_fence_before();
-            mbar_arrive(&bars->s_free);
+            if (pass == 1) {
+              tc_fence_before();
+              mbar_arrive(&bars->s_free);  // the region takes dP^T
+            }
             // P^T = exp2(S^T * c - lse2) in packed fp32 pairs
             const float4* l4 = reinterpret_cast<const float4*>(smem + T::A_SM_L2 + qs * 256) + wg * (T::A_QC / 4);
             const uint64_t nc2 = f2_pack(-sl2, -sl2);
@@ -516,51 +521,56 @@ __global__ void __launch_bounds__(384, 1)
               p2[c / 2 + 1] = f2_pack(pv[2], pv[3]);
             }
             uint32_t pk[T::A_QC / 2];
+            if (pass == 0) {
+              // ---- P^T (16-bit) over the first half of this warpgroup's S^T
+              // columns (only this warpgroup reads them)
 #pragma unroll
-            for (int c = 0; c < T::A_QC / 2; ++c) pk[c] = f2_to_pack2<BF>(p2[c]);
-            // ---- P^T (16-bit) over the first half of this warpgroup's dP^T
-            // columns, dS^T = P^T * (dP^T - Delta) over the second half
-            ok = mbar_wait(&bars->o_full[os], (t / OS) & 1, wc, 173) &&
-                 mbar_wait(&bars->dp_full[t & 1], (t >> 1) & 1, wc, 174);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            tc_fence_after();
-            tmem_ld32(rb, sr);
-            tmem_wait_ld();
-            reg_fence<T::A_QC>(sr);
-            tmem_st16(rb, pk);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&bars->p_full);
-            const float4* d4 = reinterpret_cast<const float4*>(smem + T::A_SM_DL + os * 256) + wg * (T::A_QC / 4);
+              for (int c = 0; c < T::A_QC / 2; ++c) pk[c] = f2_to_pack2<BF>(p2[c]);
+              tmem_st16(rb, pk);
+              tmem_wait_st();
+              tc_fence_before();
+              mbar_arrive(&bars->a_full[t & 1]);
+            } else {
+              // ---- dS^T = P^T * (dP^T - Delta) (16-bit) over the first half
+              // of this warpgroup's dP^T columns
+              ok = mbar_wait(&bars->o_full[os], (t / OS) & 1, wc, 173) && mbar_wait(&bars->dp_full, t1 & 1, wc, 174);
+              if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+              tc_fence_after();
+              tmem_ld32(rb, sr);
+              tmem_wait_ld();
+              reg_fence<T::A_QC>(sr);
+              const float4* d4 = reinterpret_cast<const float4*>(smem + T::A_SM_DL + os * 256) + wg * (T::A_QC / 4);
 #pragma unroll
-            for (int c = 0; c < T::A_QC; c += 4) {
-              const float4 Dl = d4[c / 4];
-              const uint64_t d01 = f2_sub(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), f2_pack(Dl.x, Dl.y));
-              const uint64_t d23 =
-                  f2_sub(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), f2_pack(Dl.z, Dl.w));
-              pk[c / 2] = f2_to_pack2<BF>(f2_mul(p2[c / 2], d01));
-              pk[c / 2 + 1] = f2_to_pack2<BF>(f2_mul(p2[c / 2 + 1], d23));
+              for (int c = 0; c < T::A_QC; c += 4) {
+                const float4 Dl = d4[c / 4];
+                const uint64_t d01 =
+                    f2_sub(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), f2_pack(Dl.x, Dl.y));
+                const uint64_t d23 =
+                    f2_sub(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), f2_pack(Dl.z, Dl.w));
+                pk[c / 2] = f2_to_pack2<BF>(f2_mul(p2[c / 2], d01));
+                pk[c / 2 + 1] = f2_to_pack2<BF>(f2_mul(p2[c / 2 + 1], d23));
+              }
+              tmem_st16(rb, pk);
+              tmem_wait_st();
+              tc_fence_before();
+              mbar_arrive(&bars->a_full[t & 1]);
+              ++t1;
             }
-            tmem_st16(rb + T::A_QC / 2, pk);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&bars->ds_full);
             ++t;
           }
           if (!ok) break;
-          // ---- dV_j[:, h] and dK_j[:, h] (times scale) -> 16-bit, staged in
-          // the dO and Q slots of the half's last tile; the store warp writes
-          // them out (rows past Nk are dropped by the TMA store)
+          // ---- the pass's gradient, dV_j or dK_j (times scale), -> 16-bit:
+          // columns 0-127 staged in the Q slot and 128-255 in the dO slot of
+          // the pass's last tile; the gradient MMA warp writes them out (rows
+          // past Nk are dropped by the TMA store)
           ok = mbar_wait(&bars->dkv_full, sc & 1, wc, 175);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t st_dv = smem_u32(smem + T::A_SM_DO + ((t - 1) % OS) * T::A_QTILE);
-          const uint32_t st_dk = smem_u32(smem + T::A_SM_Q + ((t - 1) % QS) * T::A_QTILE);
+          const uint32_t st = wg == 0 ? smem_u32(smem + T::A_SM_Q + ((t - 1) % QS) * T::A_QTILE)
+                                      : smem_u32(smem + T::A_SM_DO + ((t - 1) % OS) * T::A_QTILE);
+          const float mul = pass == 0 ? 1.f : prm.scale;
 #pragma unroll 1
-          for (int c = 0; c < 64; c += 32) {
-            stage_tmem32<BF>(lb + T::A_DV + wg * 64 + c, 1.f, st_dv, row, wg * 64 + c);
-            stage_tmem32<BF>(lb + T::A_DK + wg * 64 + c, prm.scale, st_dk, row, wg * 64 + c);
-          }
+          for (int c = 0; c < 128; c += 32) stage_tmem32<BF>(lb + T::A_ACC + wg * 128 + c, mul, st, row, c);
           fence_proxy_async_smem();
           tc_fence_before();
           mbar_arrive(&bars->dkv_free);
