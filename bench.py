@@ -100,18 +100,49 @@ def oracle_sample(budget_s=12.0, max_heads=256):
 
     q, k, v, do = make_inputs(1, max_heads, N, D, seed=SEED)
     scale = 1.0 / math.sqrt(D)
-    done, t0 = 0, time.perf_counter()
+    done, t_fwd, t_bwd, t0 = 0, 0.0, 0.0, time.perf_counter()
     while done < max_heads and (done < 2 or time.perf_counter() - t0 < budget_s):
         qh, kh, vh, dh = (t[0, done] for t in (q, k, v, do))
+        a = time.perf_counter()
         orc.attn_fwd_head(qh, kh, vh, CAUSAL, scale)
+        b = time.perf_counter()
         orc.attn_bwd_head(qh, kh, vh, dh, CAUSAL, scale)
+        t_fwd += b - a
+        t_bwd += time.perf_counter() - b
         done += 1
-    el = time.perf_counter() - t0
+    el = t_fwd + t_bwd
     fl = flops_step(1, done, N, D, CAUSAL)
     return {"value": fl / el / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
             "sample": f"{done} of the {Z * H} heads (N{N} D{D} {'causal' if CAUSAL else 'non-causal'}), "
                       f"fp64 numpy forward+backward, "
-                      f"{el:.1f} s wall"}
+                      f"{el:.1f} s wall",
+            "fwd_s_per_head": t_fwd / done, "bwd_s_per_head": t_bwd / done}
+
+
+def oracle_configs(budget_s=1.5):
+    """The oracle on a few heads of every benchmark shape (forward and
+    backward timed apart), with its time for all heads of the shape by
+    proportion."""
+    from attention_sm_flashattention_gb300.inputs import WORKLOADS, make_inputs
+    from oracle import attention as orc
+
+    out = {}
+    for name, w in WORKLOADS.items():
+        nh = min(w.heads, 64)
+        q, k, v, do = make_inputs(1, nh, w.N, w.D, seed=w.seed)
+        done, t_fwd, t_bwd = 0, 0.0, 0.0
+        while done < nh and (done < 2 or t_fwd + t_bwd < budget_s):
+            qh, kh, vh, dh = (t[0, done] for t in (q, k, v, do))
+            a = time.perf_counter()
+            orc.attn_fwd_head(qh, kh, vh, w.causal, w.scale)
+            b = time.perf_counter()
+            orc.attn_bwd_head(qh, kh, vh, dh, w.causal, w.scale)
+            t_fwd += b - a
+            t_bwd += time.perf_counter() - b
+            done += 1
+        out[name] = {"heads_timed": done, "fwd_s_all_heads": t_fwd / done * w.heads,
+                     "bwd_s_all_heads": t_bwd / done * w.heads, "cores": cpu_threads()}
+    return out
 
 
 # -------------------------------------------------------------- clock sampler
@@ -306,10 +337,10 @@ def call_stats(ms):
 
 
 # The other benchmark shapes, reported beside the headline in the same line:
-# (workload, flush L2 before every timed call).  The Z4 D64 shape's inputs
-# (17 MB) fit in L2, so a 256 MB buffer is written before each call.
-SIDE_CONFIGS = (("z4h8n1024d64", True), ("z128h8n1024d128c", False), ("z128h8n1024d256", False),
-                ("z128h8n1024d256c", False))
+# (workload, flush L2 before every timed call).  The two D64 shapes' inputs
+# (0.1 and 17 MB) fit in L2, so a 256 MB buffer is written before each call.
+SIDE_CONFIGS = (("z1h2n128d64", True), ("z4h8n1024d64", True), ("z128h8n1024d128c", False),
+                ("z128h8n1024d256", False), ("z128h8n1024d256c", False))
 
 
 def config_bench(name, flush, dev, calls=50, warmup=10):
@@ -692,6 +723,8 @@ def main():
         line["sustained"] = sustained_bench(r["step"], ms_per_step, smi_index(local_rank))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample()
+        if not args.no_side:
+            line["cpu_configs"] = oracle_configs()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -1,6 +1,7 @@
 /*
  * fa.h -- C ABI of libfa.so: exact FlashAttention forward and backward for
- * one NVIDIA GB300 (sm_103a), fp16 inputs/outputs, fp32 accumulation.
+ * one NVIDIA GB300 (sm_103a): fp16 inputs and outputs (fa_fwd, fa_bwd; bf16
+ * through fa_fwd_bf16, fa_bwd_bf16 and the _ex calls), fp32 accumulation.
  *
  * What is computed (source: «把 FlashAttention 搬上昇腾：Triton-Ascend CV
  * Pipeline 优化实战»):
@@ -15,7 +16,7 @@
  *                   dQ = dS K, dK = dS^T Q, dV = P^T dO, with every gradient
  *                   tile written by exactly one CTA and a workspace that does
  *                   not grow with the number of heads times N^2 (§二's three
- *                   rules, §五).
+ *                   rules).
  *
  * Layout and types (all calls):
  *   q, k, v, o, dout, dq, dk, dv : fp16 (IEEE binary16), contiguous
@@ -72,7 +73,8 @@ extern "C" {
 /*
  * Forward pass.  Source: «把 FlashAttention 搬上昇腾» §一 (tiled online
  * softmax, exp2, fp32 m/l/acc, fp16 P into the matrix unit, causal loop
- * bound + diagonal-only mask, D256 as two D128 halves).
+ * bound + diagonal-only mask), §七 (D256: the key and value tiles move in
+ * halves; the 256-column accumulator fits whole).
  *   q, k, v : inputs [Z,H,N,D] fp16.
  *   o       : output [Z,H,N,D] fp16, O = softmax(Q K^T scale) V, rounded to
  *             nearest from the fp32 accumulator divided by l.
@@ -99,8 +101,10 @@ FA_API size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal);
 
 /*
  * Backward pass.  Source: «把 FlashAttention 搬上昇腾» §二 (equations and
- * the three rules), §五 (persistent programs that each own whole heads, so
- * every dQ/dK/dV tile has one writer), §七 (D256 as two D128 halves).
+ * the three rules), §五 (persistent programs: here one per SM, each taking
+ * (head, tile) work units in turn, and every dQ/dK/dV tile has one writer),
+ * §七 (D256: the accumulators split so that they fit; here one gradient at a
+ * time).
  *   q, k, v, o, dout : inputs [Z,H,N,D] fp16; o must be fa_fwd's output for
  *                      the same q, k, v, causal and scale.
  *   lse              : input [Z,H,N] fp32 from the same fa_fwd call.
@@ -111,10 +115,9 @@ FA_API size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal);
  *                      undefined.  Must not be used by another call that runs
  *                      concurrently on the GPU.
  *   other arguments  : as for fa_fwd.
- * Enqueues a persistent dQ kernel and a persistent dK/dV kernel: at D = 128
- * the dQ kernel runs first and also forms Delta = rowsum(O * dO) into the
- * workspace; at D = 64 a Delta kernel runs first, then dQ, then dK/dV; at
- * D = 256 a Delta kernel, then dK/dV, then dQ.
+ * Enqueues a persistent dQ kernel and a persistent dK/dV kernel: at D = 64
+ * and 128 the dQ kernel runs first and also forms Delta = rowsum(O * dO)
+ * into the workspace; at D = 256 a Delta kernel, then dK/dV, then dQ.
  * Returns FA_OK or a negative FA_ERR_* code.
  */
 FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -298,8 +301,7 @@ FA_API int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o,
  * The attention pages have no counterpart to this call; it exists for
  * callers that cannot allocate device memory when they run the backward --
  * for example code that runs inside a fixed memory pool or arena it does not
- * own, a stream that is being recorded where allocation calls are not
- * allowed, or an embedding host whose allocator must not be re-entered.
+ * own, or an embedding host whose allocator must not be re-entered.
  *
  * It computes exactly what fa_bwd computes (same kernels, same arguments
  * without workspace/workspace_bytes, same outputs bit for bit), but the
