@@ -44,7 +44,6 @@
 // needs, which a TMA store writes out.
 #pragma once
 
-#include "fa_bwd.cuh"
 #include "fa_bwd2.cuh"
 
 namespace fa {
@@ -82,7 +81,8 @@ struct B256 {
   static constexpr int B_DO = 0, B_DQ = 128, B_R = 384;  // TMEM columns; region r (S, then dP, then dS) at B_R + 64 r
   static constexpr int B_SM_Q = 0, B_SM_K = B_QTILE, B_SM_V = B_SM_K + B_KS * B_KTILE;
   static constexpr int B_SM_BAR = B_SM_V + B_VS * B_KTILE;
-  static constexpr int B_SMEM = B_SM_BAR + 256;
+  static constexpr int B_SM_DX = B_SM_BAR + 256;   // Delta halves: [item parity][warpgroup][B_BM] fp32
+  static constexpr int B_SMEM = B_SM_DX + 2 * 2 * B_BM * 4;
   static constexpr int B_THREADS = 416;  // 8 compute warps, two producers, three MMA warps
   static_assert(B_SMEM <= 232448, "dQ kernel shared memory budget");
   static_assert(B_R + 2 * B_BN <= 512, "dQ kernel TMEM budget");
@@ -599,6 +599,7 @@ struct Bwd256BBars {
   uint64_t s_full[2], s_free, dp_full[2], ds_full[2], dq_done[2];  // [2]: per TMEM region
   uint64_t dq_full, dq_free, mma_done[3];
   uint64_t epi_full;  // dQ_i staged in the last tile's K and V slots
+  uint64_t dx_full[2];  // both Delta halves of an item's rows are in shared memory
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -638,6 +639,8 @@ __global__ void __launch_bounds__(416, 1)
     for (int i = 0; i < 3; ++i) mbar_init(&bars->mma_done[i], 1);
     mbar_init(&bars->do_full, T::NCOMPUTE);
     mbar_init(&bars->do_free, 1);
+    mbar_init(&bars->dx_full[0], T::NCOMPUTE);
+    mbar_init(&bars->dx_full[1], T::NCOMPUTE);
     mbar_init(&bars->s_free, T::NCOMPUTE);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->epi_full, T::NCOMPUTE);
@@ -888,9 +891,7 @@ __global__ void __launch_bounds__(416, 1)
         const bool q_live = query < Nq;
         const size_t q_row = static_cast<size_t>(head) * Nq + query;
         const size_t grow = static_cast<size_t>(head) * Nq_pad + query;  // padded: lse2 = +inf past Nq
-        const float lse2 = __ldg(prm.lse2 + grow);
-        const float delta = __ldg(prm.delta + grow);
-        const uint64_t c2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2), nd2 = f2_pack(-delta, -delta);
+        const float lse2 = q_live ? __ldg(prm.lse + q_row) * 1.4426950408889634f : INFINITY;
         // last key this row sees; key tiles past the tile's smallest limit are masked
         const int lim = CAUSAL ? min(query + coff, Nk - 1) : Nk - 1;
         const int lim_lo = CAUSAL ? min(i * T::B_BM + coff, Nk - 1) : Nk - 1;
@@ -907,7 +908,48 @@ __global__ void __launch_bounds__(416, 1)
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->do_full);
+          // Delta_i = rowsum(O_i * dO_i): this warpgroup's 128 columns, O read
+          // in 16-word chunks (the next chunk requested before this one is
+          // used), dO from the words just written to TMEM
+          const uint4* orow = reinterpret_cast<const uint4*>(prm.o + q_row * T::D + wg * 128);
+          uint4 oc[2][4];
+          float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) oc[0][e] = q_live ? ldg_nc_v4(orow + e) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if (c + 1 < 4) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                oc[(c + 1) & 1][e] = q_live ? ldg_nc_v4(orow + 4 * (c + 1) + e) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t ow[4] = {oc[c & 1][e].x, oc[c & 1][e].y, oc[c & 1][e].z, oc[c & 1][e].w};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float2 x = unpack2<BF>(ow[q]), y = unpack2<BF>(w[16 * c + 4 * e + q]);
+                acc0 = fmaf(x.x, y.x, acc0);
+                acc1 = fmaf(x.y, y.y, acc1);
+              }
+            }
+          }
+          float* dx = reinterpret_cast<float*>(smem + T::B_SM_DX) + (qc & 1) * 2 * T::B_BM;
+          dx[wg * T::B_BM + row] = acc0 + acc1;
+          mbar_arrive(&bars->dx_full[qc & 1]);
         }
+        float delta;
+        {
+          ok = mbar_wait(&bars->dx_full[qc & 1], (qc >> 1) & 1, wc, 205);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          const float* dx = reinterpret_cast<const float*>(smem + T::B_SM_DX) + (qc & 1) * 2 * T::B_BM;
+          delta = dx[row] + dx[T::B_BM + row];  // the same sum in both warpgroups
+          if (wg == 0) {  // for the dK/dV kernel, launched after this one
+            prm.delta[grow] = delta;
+            prm.lse2[grow] = lse2;
+          }
+        }
+        const uint64_t c2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2), nd2 = f2_pack(-delta, -delta);
         {
           // the CTA's next item: its dO rows into L2 while this one runs
           int nhead = head, ni = -1;
@@ -918,12 +960,11 @@ __global__ void __launch_bounds__(416, 1)
             bwd2_decode<CAUSAL>(u + gridDim.x, nqt, nhead, ni, nb);
           }
           if (ni >= 0 && ni * T::B_BM + row < Nq) {
-            prefetch_row128(prm.dout + (static_cast<size_t>(nhead) * Nq + ni * T::B_BM + row) * T::D + wg * 128);
-            if (wg == 0 && lane == 0) {  // one line of lse2 and of Delta covers this warp's 32 rows
-              const size_t nrow = static_cast<size_t>(nhead) * Nq_pad + ni * T::B_BM + row;
-              asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(prm.lse2 + nrow));
-              asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(prm.delta + nrow));
-            }
+            const size_t nrow = static_cast<size_t>(nhead) * Nq + ni * T::B_BM + row;
+            prefetch_row128(prm.dout + nrow * T::D + wg * 128);
+            prefetch_row128(prm.o + nrow * T::D + wg * 128);
+            if (wg == 0 && lane == 0)  // one line of lse covers this warp's 32 rows
+              asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(prm.lse + nrow));
           }
         }
         for (int j = 0; j < num_kv(i); ++j) {
@@ -1009,10 +1050,11 @@ __global__ void __launch_bounds__(416, 1)
   }
 }
 
-// Delta/lse2 preprocess, then the dK/dV and dQ kernels on the same stream.
-// maps: [0] q (64-row boxes), [1] k (128-row boxes), [3] dout (64-row
-// boxes) for the dK/dV kernel; [7] q (128-row boxes), [8] k (64-row boxes),
-// [2] v (64-row boxes) for the dQ kernel.
+// The dQ kernel (which also writes Delta and lse2 of every query row), then
+// the dK/dV kernel, on the same stream.  maps: [0] q (64-row boxes), [1] k
+// (128-row boxes), [3] dout (64-row boxes) for the dK/dV kernel; [7] q
+// (128-row boxes), [8] k (64-row boxes), [2] v (64-row boxes) for the dQ
+// kernel.
 template <bool CAUSAL, bool BF>
 int launch_bwd256(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, cudaStream_t stream) {
   using T = B256;
@@ -1026,17 +1068,16 @@ int launch_bwd256(const CUtensorMap* maps, const BwdParams& prm, int max_ctas, c
                    : -1;
       }) != 0)
     return -1;
-  if (launch_prep<256, BF>(prm, stream) != 0) return -1;
   auto grid_for = [&](int heads, int tiles) {
     const long long units = CAUSAL ? static_cast<long long>(heads) * ((tiles + 1) / 2) : static_cast<long long>(heads) * tiles;
     return static_cast<int>(units < max_ctas ? units : max_ctas);
   };
   const int nkv = (prm.Nk + T::A_BN - 1) / T::A_BN, nqt = (prm.Nq + T::B_BM - 1) / T::B_BM;
-  fa_bwd256_dkdv_kernel<CAUSAL, BF><<<grid_for(prm.heads / prm.group, nkv), T::A_THREADS, T::A_SMEM, stream>>>(
-      maps[0], maps[1], maps[3], maps[5], maps[6], prm);
-  if (cudaGetLastError() != cudaSuccess) return -1;
   fa_bwd256_dq_kernel<CAUSAL, BF><<<grid_for(prm.heads, nqt), T::B_THREADS, T::B_SMEM, stream>>>(
       maps[7], maps[8], maps[2], maps[4], prm);
+  if (cudaGetLastError() != cudaSuccess) return -1;
+  fa_bwd256_dkdv_kernel<CAUSAL, BF><<<grid_for(prm.heads / prm.group, nkv), T::A_THREADS, T::A_SMEM, stream>>>(
+      maps[0], maps[1], maps[3], maps[5], maps[6], prm);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -1,9 +1,8 @@
 """Benchmark: attention fwd + bwd TFLOP/s on one GB300 (Z128 H8 N1024 D128).
 
 One step = one pass of the whole hot path over one batch: fa_fwd (O, lse)
-then fa_bwd (D128: dQ kernel with Delta, dK/dV kernel; D64 and D256 add a
-Delta preprocess kernel), fp16 in, fp32
-accumulate.  FLOPs are the algorithmic count (forward 4 N^2 D per head, the
+then fa_bwd (a dQ kernel that also forms Delta, then a dK/dV kernel), fp16
+in, fp32 accumulate.  FLOPs are the algorithmic count (forward 4 N^2 D per head, the
 backward 2.5x that); the work the method avoids is not counted.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -462,17 +461,14 @@ def job_throughput(flops_per_step_per_rank, world, steps, max_total_ms):
 def bwd_kernel_names(d, causal):
     c = str(bool(causal)).lower()
     if d == 256:
-        return f"fa_bwd call: fa_bwd_prep_kernel<{d}> + fa_bwd256_dkdv_kernel<{c}> + fa_bwd256_dq_kernel<{c}>"
-    if d == 64:
-        return f"fa_bwd call: fa_bwd_prep_kernel<{d}> + fa_bwd_dq_kernel<{d},{c}> + fa_bwd_dkdv_kernel<{d},{c}>"
+        return f"fa_bwd call: fa_bwd256_dq_kernel<{c}> (with Delta) + fa_bwd256_dkdv_kernel<{c}>"
     return f"fa_bwd call: fa_bwd_dq_kernel<{d},{c}> (with Delta) + fa_bwd_dkdv_kernel<{d},{c}>"
 
 
 def bwd_launches(d):
-    """Kernels one fa_bwd call launches: D = 64 and 256 run a Delta
-    preprocess, a dK/dV and a dQ kernel; D = 128 a dQ kernel that also forms
-    Delta, then a dK/dV kernel."""
-    return 2 if d == 128 else 3
+    """Kernels one fa_bwd call launches: a dQ kernel that also forms Delta,
+    then a dK/dV kernel (every D)."""
+    return 2
 
 
 def load_traffic():
