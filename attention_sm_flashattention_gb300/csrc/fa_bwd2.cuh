@@ -1018,15 +1018,20 @@ __global__ void __launch_bounds__(384, 1)
     // the halves are combined in its first key tile (after S is read, so that
     // dP of that tile is already queued)
     float lse2 = 0.f, part = 0.f;
-    // this row's lse of an item, requested an item before it is needed (a
-    // volatile load, so that it is issued here and not next to its use); at
-    // D = 128 also the row's O half into L2 for the coalesced reads
-    auto lse_of = [&](const DqItems<CAUSAL>& x) {
+    // an item ahead: this row's lse (and, at D = 128, its O half for the
+    // coalesced reads) into L2.  No load into a register here: a warp's
+    // tcgen05.wait::ld also waits for its global loads in flight, so a load
+    // issued an item ahead would stall the item's first TMEM read.
+    auto prefetch_item = [&](const DqItems<CAUSAL>& x) {
       const int q = x.tile() * T::BM + row;
-      if (!x.valid() || q >= prm.Nq) return 0.f;
+      if (!x.valid() || q >= prm.Nq) return;
       const size_t src = static_cast<size_t>(x.head) * prm.Nq + q;
       if (!T::kStageO) prefetch_l2(prm.o + src * D + wg * (D / 2));
-      return ldg_nc_f32(prm.lse + src);
+      prefetch_l2(prm.lse + src);
+    };
+    auto lse_of = [&](const DqItems<CAUSAL>& x) {
+      const int q = x.tile() * T::BM + row;
+      return x.valid() && q < prm.Nq ? __ldg(prm.lse + static_cast<size_t>(x.head) * prm.Nq + q) : 0.f;
     };
     DqItems<CAUSAL> it(units, nqt);
     if (it.valid()) {
@@ -1039,7 +1044,7 @@ __global__ void __launch_bounds__(384, 1)
       const int query = i * T::BM + row;
       DqItems<CAUSAL> nx = it;
       nx.next();
-      const float lse_next = lse_of(nx);
+      prefetch_item(nx);
       // last key this row sees; key tiles past the tile's smallest limit
       // (the causal diagonal, or the ragged end of the keys) are masked
       const int lim = CAUSAL ? min(query + coff, Nk - 1) : Nk - 1;
@@ -1118,7 +1123,7 @@ __global__ void __launch_bounds__(384, 1)
       // start) and its Delta halves, then this item's dQ out
       const bool has_next = nx.valid();
       if (has_next) {
-        ok = load_item(nx, n + 1, lse_next, lse2, part);
+        ok = load_item(nx, n + 1, lse_of(nx), lse2, part);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         nl2 = f2_pack(-lse2, -lse2);
       }
