@@ -338,8 +338,8 @@ def call_stats(ms):
 # The other benchmark shapes, reported beside the headline in the same line:
 # (workload, flush L2 before every timed call).  The two D64 shapes' inputs
 # (0.1 and 17 MB) fit in L2, so a 256 MB buffer is written before each call.
-SIDE_CONFIGS = (("z1h2n128d64", True), ("z4h8n1024d64", True), ("z128h8n1024d128c", False),
-                ("z128h8n1024d256", False), ("z128h8n1024d256c", False))
+SIDE_CONFIGS = (("z1h2n128d64", True), ("z4h8n1024d64", True), ("z128h8n1024d128", False),
+                ("z128h8n1024d128c", False), ("z128h8n1024d256", False), ("z128h8n1024d256c", False))
 
 
 def config_bench(name, flush, dev, calls=50, warmup=10):

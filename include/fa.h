@@ -115,9 +115,9 @@ FA_API size_t fa_bwd_workspace_size(int Z, int H, int N, int D, int causal);
  *                      undefined.  Must not be used by another call that runs
  *                      concurrently on the GPU.
  *   other arguments  : as for fa_fwd.
- * Enqueues a persistent dQ kernel and a persistent dK/dV kernel: at D = 64
- * and 128 the dQ kernel runs first and also forms Delta = rowsum(O * dO)
- * into the workspace; at D = 256 a Delta kernel, then dK/dV, then dQ.
+ * Enqueues two persistent kernels on `stream`: first the dQ kernel, which
+ * also forms Delta = rowsum(O * dO) and the log2-scaled lse of every query
+ * row into the workspace, then the dK/dV kernel, which reads them.
  * Returns FA_OK or a negative FA_ERR_* code.
  */
 FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
