@@ -202,16 +202,16 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bars->o_empty[i], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, NCOMPUTE);
+    mbar_init(&bars->s_free, NCOMPUTE / 32);
     mbar_init(&bars->dp_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->p_full[i], NCOMPUTE);
-      mbar_init(&bars->ds_full[i], NCOMPUTE);
+      mbar_init(&bars->p_full[i], NCOMPUTE / 32);
+      mbar_init(&bars->ds_full[i], NCOMPUTE / 32);
       mbar_init(&bars->dk_done[i], 1);
     }
     mbar_init(&bars->dkv_full, 1);
-    mbar_init(&bars->dkv_free, NCOMPUTE);
-    mbar_init(&bars->epi_full, NCOMPUTE);
+    mbar_init(&bars->dkv_free, NCOMPUTE / 32);
+    mbar_init(&bars->epi_full, NCOMPUTE / 32);
     mbar_init(&bars->mma_done[0], 1);
     mbar_init(&bars->mma_done[1], 1);
     bars->abort_flag = 0;
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(384, 1)
           tmem_wait_ld();
           reg_fence<T::QC>(sr);
           tc_fence_before();
-          mbar_arrive(&bars->s_free);
+          mbar_arrive_warp(&bars->s_free);
           // y = lse2 - S^T * c in packed fp32 pairs, P^T = exp2(-y)
           const float4* l4 = reinterpret_cast<const float4*>(smem + T::A_SM_L2 + qs * 512) + wg * (T::QC / 4);
           const uint64_t nc2 = f2_pack(-sl2, -sl2);
@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st32(rb, pk);
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(&bars->p_full[t & 1]);
+          mbar_arrive_warp(&bars->p_full[t & 1]);
           const float4* d4 = reinterpret_cast<const float4*>(smem + T::A_SM_DL + os * 512) + wg * (T::QC / 4);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st32(rb + T::QC / 2, pk);
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(&bars->ds_full[t & 1]);
+          mbar_arrive_warp(&bars->ds_full[t & 1]);
           ++t;
         }
         if (!ok) break;
@@ -578,8 +578,8 @@ __global__ void __launch_bounds__(384, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&bars->dkv_free);
-        mbar_arrive(&bars->epi_full);
+        mbar_arrive_warp(&bars->dkv_free);
+        mbar_arrive_warp(&bars->epi_full);
         ++kc;
       }
     }
@@ -671,8 +671,8 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->qo_full, 1);
-    mbar_init(&bars->qo_empty, NCOMPUTE);
-    mbar_init(&bars->qo_tmem, NCOMPUTE);
+    mbar_init(&bars->qo_empty, NCOMPUTE / 32);
+    mbar_init(&bars->qo_tmem, NCOMPUTE / 32);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
@@ -681,16 +681,16 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->ds_full[i], NCOMPUTE);
+      mbar_init(&bars->ds_full[i], NCOMPUTE / 32);
       mbar_init(&bars->dq_done[i], 1);
-      mbar_init(&bars->epi_full[i], NCOMPUTE);
-      mbar_init(&bars->dx_full[i], NCOMPUTE);
+      mbar_init(&bars->epi_full[i], NCOMPUTE / 32);
+      mbar_init(&bars->dx_full[i], NCOMPUTE / 32);
       mbar_init(&bars->mma_done[i], 1);
     }
-    mbar_init(&bars->s_free, NCOMPUTE);
+    mbar_init(&bars->s_free, NCOMPUTE / 32);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, NCOMPUTE);
+    mbar_init(&bars->dq_free, NCOMPUTE / 32);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -958,7 +958,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars->qo_tmem);  // Q_m, dO_m are in TMEM: the item's S can start
+      mbar_arrive_warp(&bars->qo_tmem);  // Q_m, dO_m are in TMEM: the item's S can start
       if constexpr (T::kStageO) {
         float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
@@ -993,7 +993,7 @@ __global__ void __launch_bounds__(384, 1)
           if (lane / RPL == k) part = v;
         }
       }
-      mbar_arrive(&bars->qo_empty);  // the staging buffers are no longer read
+      mbar_arrive_warp(&bars->qo_empty);  // the staging buffers are no longer read
       return true;
     };
     // Delta of item m's rows: both warpgroups' halves through shared memory;
@@ -1001,7 +1001,7 @@ __global__ void __launch_bounds__(384, 1)
     auto finish_delta = [&](const DqItems<CAUSAL>& nx, uint32_t m, float lse2, float part) -> bool {
       float* dx = reinterpret_cast<float*>(smem + T::B_SM_DX) + (m & 1) * 2 * T::BM;
       dx[wg * T::BM + row] = part;
-      mbar_arrive(&bars->dx_full[m & 1]);
+      mbar_arrive_warp(&bars->dx_full[m & 1]);
       const bool got = mbar_wait(&bars->dx_full[m & 1], (m >> 1) & 1, wc, 105);
       if (!__all_sync(0xffffffffu, got)) return false;
       const float delta = dx[row] + dx[T::BM + row];  // the same sum in both warpgroups
@@ -1064,7 +1064,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_wait_ld();
         reg_fence<T::QC>(sr);
         tc_fence_before();
-        mbar_arrive(&bars->s_free);  // the region takes dP
+        mbar_arrive_warp(&bars->s_free);  // the region takes dP
         if (j == 0) {
           ok = finish_delta(it, n, lse2, part);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -1115,7 +1115,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_st32(rb, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->ds_full[r]);
+        mbar_arrive_warp(&bars->ds_full[r]);
         ++t;
       }
       if (!ok) break;
@@ -1148,8 +1148,8 @@ __global__ void __launch_bounds__(384, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars->dq_free);
-      mbar_arrive(&bars->epi_full[n & 1]);
+      mbar_arrive_warp(&bars->dq_free);
+      mbar_arrive_warp(&bars->epi_full[n & 1]);
       it = nx;
     }
   }

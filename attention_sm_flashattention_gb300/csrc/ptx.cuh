@@ -63,6 +63,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One arrive for a whole warp, on a barrier counted in warps: the lanes meet
+// first (a warp barrier also orders their earlier memory writes, and, after
+// tcgen05.wait and tcgen05.fence::before_thread_sync, their tensor-memory
+// accesses), then lane 0's arrive releases them all.  Replaces 32 separate
+// arrives on the same shared-memory word.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
