@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->k_full, 1);
     mbar_init(&bars->k_empty, 1);
-    mbar_init(&bars->v_full, T::NCOMPUTE / 32);
+    mbar_init(&bars->v_full, T::NCOMPUTE);
     mbar_init(&bars->v_free, 1);
     for (int i = 0; i < 3; ++i) {
       mbar_init(&bars->q_full[i], 1);
@@ -187,14 +187,14 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bars->o_empty[i], 1);
       mbar_init(&bars->dk_done[i], 1);
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->a_full[i], T::NCOMPUTE / 32);
+      mbar_init(&bars->a_full[i], T::NCOMPUTE);
     }
     for (int i = 0; i < 3; ++i) mbar_init(&bars->mma_done[i], 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->s_free, T::NCOMPUTE / 32);
+    mbar_init(&bars->s_free, T::NCOMPUTE);
     mbar_init(&bars->dkv_full, 1);
-    mbar_init(&bars->epi_full, T::NCOMPUTE / 32);
-    mbar_init(&bars->dkv_free, T::NCOMPUTE / 32);
+    mbar_init(&bars->epi_full, T::NCOMPUTE);
+    mbar_init(&bars->dkv_free, T::NCOMPUTE);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st32(lb + T::A_V + wg * 64 + 32, w + 32);
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive_warp(&bars->v_full);
+          mbar_arrive(&bars->v_full);
         }
         const int i0 = first_q(j), nqi = nqt - i0;
         {
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(384, 1)
             reg_fence<T::A_QC>(sr);
             if (pass == 1) {
               tc_fence_before();
-              mbar_arrive_warp(&bars->s_free);  // the region takes dP^T
+              mbar_arrive(&bars->s_free);  // the region takes dP^T
             }
             // P^T = exp2(S^T * c - lse2) in packed fp32 pairs
             const float4* l4 = reinterpret_cast<const float4*>(smem + T::A_SM_L2 + qs * 256) + wg * (T::A_QC / 4);
@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(384, 1)
               tmem_st16(rb, pk);
               tmem_wait_st();
               tc_fence_before();
-              mbar_arrive_warp(&bars->a_full[t & 1]);
+              mbar_arrive(&bars->a_full[t & 1]);
             } else {
               // ---- dS^T = P^T * (dP^T - Delta) (16-bit) over the first half
               // of this warpgroup's dP^T columns
@@ -553,7 +553,7 @@ __global__ void __launch_bounds__(384, 1)
               tmem_st16(rb, pk);
               tmem_wait_st();
               tc_fence_before();
-              mbar_arrive_warp(&bars->a_full[t & 1]);
+              mbar_arrive(&bars->a_full[t & 1]);
               ++t1;
             }
             ++t;
@@ -573,8 +573,8 @@ __global__ void __launch_bounds__(384, 1)
           for (int c = 0; c < 128; c += 32) stage_tmem32<BF>(lb + T::A_ACC + wg * 128 + c, mul, st, row, c);
           fence_proxy_async_smem();
           tc_fence_before();
-          mbar_arrive_warp(&bars->dkv_free);
-          mbar_arrive_warp(&bars->epi_full);
+          mbar_arrive(&bars->dkv_free);
+          mbar_arrive(&bars->epi_full);
           ++sc;
         }
         ++kc;
@@ -633,18 +633,18 @@ __global__ void __launch_bounds__(416, 1)
       mbar_init(&bars->v_empty[i], 1);
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->dp_full[i], 1);
-      mbar_init(&bars->ds_full[i], T::NCOMPUTE / 32);
+      mbar_init(&bars->ds_full[i], T::NCOMPUTE);
       mbar_init(&bars->dq_done[i], 1);
     }
     for (int i = 0; i < 3; ++i) mbar_init(&bars->mma_done[i], 1);
-    mbar_init(&bars->do_full, T::NCOMPUTE / 32);
+    mbar_init(&bars->do_full, T::NCOMPUTE);
     mbar_init(&bars->do_free, 1);
-    mbar_init(&bars->dx_full[0], T::NCOMPUTE / 32);
-    mbar_init(&bars->dx_full[1], T::NCOMPUTE / 32);
-    mbar_init(&bars->s_free, T::NCOMPUTE / 32);
+    mbar_init(&bars->dx_full[0], T::NCOMPUTE);
+    mbar_init(&bars->dx_full[1], T::NCOMPUTE);
+    mbar_init(&bars->s_free, T::NCOMPUTE);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->epi_full, T::NCOMPUTE / 32);
-    mbar_init(&bars->dq_free, T::NCOMPUTE / 32);
+    mbar_init(&bars->epi_full, T::NCOMPUTE);
+    mbar_init(&bars->dq_free, T::NCOMPUTE);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -907,7 +907,7 @@ __global__ void __launch_bounds__(416, 1)
           tmem_st32(lb + T::B_DO + wg * 64 + 32, w + 32);
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive_warp(&bars->do_full);
+          mbar_arrive(&bars->do_full);
           // Delta_i = rowsum(O_i * dO_i): this warpgroup's 128 columns, O read
           // in 16-word chunks (the next chunk requested before this one is
           // used), dO from the words just written to TMEM
@@ -936,7 +936,7 @@ __global__ void __launch_bounds__(416, 1)
           }
           float* dx = reinterpret_cast<float*>(smem + T::B_SM_DX) + (qc & 1) * 2 * T::B_BM;
           dx[wg * T::B_BM + row] = acc0 + acc1;
-          mbar_arrive_warp(&bars->dx_full[qc & 1]);
+          mbar_arrive(&bars->dx_full[qc & 1]);
         }
         float delta;
         {
@@ -978,7 +978,7 @@ __global__ void __launch_bounds__(416, 1)
           tmem_wait_ld();
           reg_fence<T::B_KC>(sr);
           tc_fence_before();
-          mbar_arrive_warp(&bars->s_free);
+          mbar_arrive(&bars->s_free);
           // P = exp2(S * c - lse2) in packed fp32 pairs
           uint64_t p2[T::B_KC / 2];
           const bool masked = (j + 1) * T::B_BN - 1 > lim_lo;
@@ -1018,7 +1018,7 @@ __global__ void __launch_bounds__(416, 1)
           tmem_st16(rb, pk);
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive_warp(&bars->ds_full[t & 1]);
+          mbar_arrive(&bars->ds_full[t & 1]);
           ++t;
         }
         if (!ok) break;
@@ -1035,8 +1035,8 @@ __global__ void __launch_bounds__(416, 1)
         for (int c = 0; c < 128; c += 32) stage_tmem32<BF>(lb + T::B_DQ + wg * 128 + c, prm.scale, st_q, row, c);
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive_warp(&bars->dq_free);
-        mbar_arrive_warp(&bars->epi_full);
+        mbar_arrive(&bars->dq_free);
+        mbar_arrive(&bars->epi_full);
         ++qc;
       }
     }
