@@ -470,14 +470,6 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
 }
 
-// 4 bytes from global memory through the read-only path, issued where it
-// stands in the program (volatile: the compiler does not move it to its use).
-__device__ __forceinline__ float ldg_nc_f32(const float* p) {
-  float v;
-  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
-
 // 16 bytes from global memory through the read-only path.
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
